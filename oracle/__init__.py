@@ -1,0 +1,29 @@
+"""Oracle: a plain, slow, float64 CPU statement of the paged-attention hot path.
+
+TEST INFRASTRUCTURE ONLY. It exists to check the CUDA library, and only the
+tests, the smoke check and the benchmark's CPU-baseline leg may import it. It
+shares no code with the CUDA path: not a kernel, a header, a helper, a table
+or a constant generator. The seeded inputs both sides consume come from the
+separate ``workloads`` package, which holds none of the method's arithmetic.
+
+Contents, each citing the page passage it follows:
+- block_manager.BlockAllocator: blocks, tables, ref counts, fork, copy-on-write.
+- attention.kv_write_ref / copy_blocks_ref / paged_attention_ref /
+  dense_causal_ref: the byte moves and the float64 attention.
+- runner.run_workload: a seeded workload, phase by phase.
+
+Every function is pinned by the CPU tests (the pages' worked examples, closed
+forms, invariants, brute force and a library cross-check); none is unpinned.
+"""
+from .attention import (  # noqa: F401
+    BlockStore,
+    attend,
+    copy_blocks_ref,
+    dense_causal_ref,
+    gather_kv,
+    kv_write_ref,
+    paged_attention_ref,
+    to_f64,
+)
+from .block_manager import BlockAllocator, NoFreeBlocks, TooLarge  # noqa: F401
+from .runner import OracleResult, batch_metadata, run_allocator, run_workload  # noqa: F401
