@@ -1,0 +1,401 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV-cache hot path on the GQA decode batch.
+
+Workload: 256 requests, 32 query / 8 KV heads, head_dim 128, block size 16, bf16, context
+lengths lognormal (median 1024, sigma 1, clipped to [16, 8192]), physical blocks handed
+out in a seeded random order from a pool 1.25x the blocks needed. One step = one KV write
+of the new token of every request plus one paged decode attention over all of them.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line. `value` is K/V bytes read by attention per second over the whole
+step (device-resident inputs); `e2e` is the same metric through the public API with host
+buffers (host block accounting, host->device copies of the step's inputs, the kernels,
+device->host copy of the output, all inside the timed region). With --gpus N > 1 (under
+torchrun) every rank runs its own batch of 256 requests (weak scaling, no collective on
+the data path); `value` is all ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: K/V GB/s (% of GB300 HBM peak) and tokens/s, batch 256"
+FALLBACK_HBM_GBS = 6800.0
+CONFIG_ID = 3
+
+
+def _args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    a = ap.parse_args(argv)
+    a.warmup = max(3, a.warmup)
+    return a
+
+
+def _workload_config(wl, l2_note):
+    lens = [n for n in wl.meta["final_lens"]]
+    sp = wl.spec
+    return {
+        "workload": "gqa_bf16_decode_b256: 256 requests, 32 q / 8 kv heads, head_dim 128, block 16, "
+                    "lognormal context (median 1024, sigma 1, clip [16, 8192]), random block placement, "
+                    "1 KV write + 1 decode attention per request",
+        "global_batch": len(lens),
+        "num_heads": sp.num_heads, "num_kv_heads": sp.num_kv_heads, "head_dim": sp.head_dim,
+        "block_size": sp.block_size, "num_blocks": wl.num_blocks,
+        "kv_tokens": int(sum(lens)), "kv_bytes_per_step": int(sum(lens)) * sp.kv_token_bytes,
+        "seed": wl.seed, "l2": l2_note,
+    }
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        self.dev = self._smi_id(device_index)
+
+    @staticmethod
+    def _smi_id(i):
+        try:
+            import torch
+
+            u = getattr(torch.cuda.get_device_properties(i), "uuid", None)
+            if u is not None:
+                s = str(u)
+                return s if s.startswith("GPU-") else "GPU-" + s
+        except Exception:
+            pass
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[i] if vis else str(i)
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.dev, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def _oracle_state(wl, eval_seqs):
+    """Oracle caches after the untimed phases, plus the step's inputs (not timed)."""
+    import numpy as np
+
+    from oracle import BlockStore, copy_blocks_ref, kv_write_ref, run_allocator, batch_metadata
+    from workloads import relevant_seqs
+
+    sp = wl.spec
+    alloc, slots_pp, copies_pp = run_allocator(wl)
+    dt = np.float32 if sp.dtype == "f32" else np.uint16
+    kc = BlockStore(sp.block_size, sp.num_kv_heads, sp.head_dim, dt)
+    vc = BlockStore(sp.block_size, sp.num_kv_heads, sp.head_dim, dt)
+    batch = wl.step.batch
+    rel = relevant_seqs(wl, [batch[i][0] for i in eval_seqs])
+    lens = {}
+    phases = wl.phases()
+    for ph, slots, copies in list(zip(phases, slots_pp, copies_pp))[:-1]:
+        apps = wl.appends(ph, lens)
+        copy_blocks_ref(kc, vc, copies)
+        t0 = 0
+        reqs = [a for a in apps if a[0] in rel]
+        vals = dict(zip(reqs, wl.kv_many(reqs)))
+        for a in apps:
+            if a in vals:
+                kv_write_ref(kc, vc, vals[a][0], vals[a][1], slots[t0:t0 + a[2]], sp.block_size)
+            t0 += a[2]
+    step_apps = wl.appends(wl.step, lens)
+    step_vals = wl.kv_many(step_apps)
+    k_new = np.concatenate([v[0] for v in step_vals])
+    v_new = np.concatenate([v[1] for v in step_vals])
+    bt, seq_lens, qsl, seqs = batch_metadata(wl, alloc)
+    q = np.concatenate([wl.q(s, a, n) for s, a, n in wl.step_queries()])
+    return dict(kc=kc, vc=vc, k_new=k_new, v_new=v_new, slots=slots_pp[-1], copies=copies_pp[-1], bt=bt,
+                seq_lens=seq_lens, qsl=qsl, q=q)
+
+
+def _oracle_step(wl, st, eval_seqs):
+    """One oracle step over ``eval_seqs`` (copies, writes, attention); returns seconds."""
+    from oracle import copy_blocks_ref, kv_write_ref, paged_attention_ref
+
+    sp = wl.spec
+    t = time.perf_counter()
+    copy_blocks_ref(st["kc"], st["vc"], st["copies"])
+    keep = set()
+    for i in eval_seqs:  # the evaluated requests' new tokens
+        keep.update(range(int(st["qsl"][i]), int(st["qsl"][i + 1])))
+    kv_write_ref(st["kc"], st["vc"], st["k_new"], st["v_new"], st["slots"], sp.block_size, keep=keep)
+    paged_attention_ref(st["q"], st["kc"], st["vc"], st["bt"], st["seq_lens"], st["qsl"], sp.scale,
+                        sp.block_size, seqs=eval_seqs)
+    return time.perf_counter() - t
+
+
+def _cpu_sample_bytes(wl, st, eval_seqs):
+    return int(sum(int(st["seq_lens"][i]) for i in eval_seqs)) * wl.spec.kv_token_bytes
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(a):
+    import workloads
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    wl = workloads.build(CONFIG_ID)
+    sample = list(range(0, len(wl.step.batch), 8))  # 32 of the 256 requests per step
+    st = _oracle_state(wl, sample)
+    for _ in range(a.warmup):
+        _oracle_step(wl, st, sample)
+    secs = [_oracle_step(wl, st, sample) for _ in range(a.steps)]
+    total = sum(secs)
+    nbytes = _cpu_sample_bytes(wl, st, sample)
+    value = nbytes * a.steps / total / 1e9
+    desc = f"{len(sample)} of the 256 requests (every 8th) per step: their copies, KV writes and attention"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": a.gpus,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * total / a.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _workload_config(wl, "CPU run (no L2 rule)"),
+        "tokens_per_s": len(sample) * a.steps / total,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(a):
+    import numpy as np
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import paged_kv_cache_161_gb300 as pa
+    import workloads
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload
+
+    wl = workloads.build(CONFIG_ID)
+    sp = wl.spec
+    dw = DeviceWorkload(wl, device=dev, table_width=(8192 + 2 * (a.steps + a.warmup) + 64) // 16 + 1)
+    dw.run_setup()
+    st = dw.prepare_step()
+    torch.cuda.synchronize()
+    kv_bytes = int(st.seq_lens.sum().item()) * sp.kv_token_bytes
+    n_req = int(st.seq_lens.shape[0])
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-resident timing: K steps of (KV write + attention)
+    for _ in range(a.warmup):
+        dw.run_step(st)
+    pa.read_device_errors(clear=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index)
+    barrier()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    t_start.record(stream)
+    for i in range(a.steps):
+        pa.kv_write(st.k_new, st.v_new, dw.k_cache, dw.v_cache, st.slot_mapping, stream=stream)
+        ev[i][0].record(stream)
+        pa.attention(st.out, st.q, dw.k_cache, dw.v_cache, st.block_table, st.seq_lens, st.query_start_loc,
+                     max_query_len=st.max_query_len, max_seq_len=st.max_seq_len, scale=sp.scale,
+                     workspace=st.workspace, stream=stream)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    flags = pa.read_device_errors(clear=True)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x}")
+    step_ms = t_start.elapsed_time(t_end) / a.steps
+    attn_ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / a.steps
+    if dist is not None:
+        tt = torch.tensor([step_ms, attn_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        step_ms, attn_ms = tt.tolist()
+    value = world * kv_bytes / (step_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not a.no_e2e:
+        e2e = _e2e(a, pa, dw, st, wl, dev, stream, world, dist)
+
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        peak, peak_src = json.load(open(peaks_path))["hbm_gbs"], "measured (MEASURED_PEAKS.json hbm_gbs)"
+    else:
+        peak, peak_src = FALLBACK_HBM_GBS, "fallback"
+    achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "pa_attention decode (split-K kernel + merge kernel)",
+                "peak_source": peak_src, "attention_ms": attn_ms,
+                "frac_of_nominal_8TBs": achieved / 8000.0}
+
+    cpu = None
+    if rank == 0 and not a.no_cpu_baseline and world == 1:
+        sample = list(range(n_req))
+        ost = _oracle_state(wl, sample)
+        secs = _oracle_step(wl, ost, sample)
+        cpu = {"value": _cpu_sample_bytes(wl, ost, sample) / secs / 1e9, "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "seconds": secs,
+               "sample": "the whole step (all 256 requests: their KV writes and attention), one pass"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": _workload_config(wl, f"inputs ({kv_bytes / 1e9:.2f} GB of K/V per step) larger than the "
+                                            "129 MB L2; no flush"),
+            "tokens_per_s": world * n_req / (step_ms * 1e-3),
+            "hbm_frac_of_measured": value / peak,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": a.steps * 3, "clocks": clk,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
+    """Decode steps as a user runs them: host block accounting (C++), pinned host inputs
+    copied in, write + attention, output copied back; host wall time per step."""
+    import numpy as np
+    import torch
+
+    sp = wl.spec
+    seqs = [s for s, _ in wl.step.batch]
+    S = len(seqs)
+    width = int(st.block_table.shape[1])
+    q_h = st.q.cpu().pin_memory()
+    k_h = st.k_new.cpu().pin_memory()
+    v_h = st.v_new.cpu().pin_memory()
+    out_h = torch.empty_like(q_h).pin_memory()
+    slots_h = torch.empty(S, dtype=torch.int64).pin_memory()
+    table_h = torch.empty((S, width), dtype=torch.int32).pin_memory()
+    lens_h = torch.empty(S, dtype=torch.int32).pin_memory()
+    qsl_h = torch.arange(S + 1, dtype=torch.int32).pin_memory()
+    q_d, k_d, v_d = torch.empty_like(st.q), torch.empty_like(st.k_new), torch.empty_like(st.v_new)
+    slots_d = torch.empty(S, dtype=torch.int64, device=dev)
+    table_d = torch.empty((S, width), dtype=torch.int32, device=dev)
+    lens_d = torch.empty(S, dtype=torch.int32, device=dev)
+    qsl_d = torch.empty(S + 1, dtype=torch.int32, device=dev)
+    out_d = torch.empty_like(st.q)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, slots_h, table_h, lens_h, qsl_h))
+    d2h = out_h.numel() * out_h.element_size()
+    bm = dw.bm
+    kv_bytes_steps = []
+
+    def one_step():
+        slots = np.concatenate([bm.append(s, 1) for s in seqs])
+        table, lens = bm.batch_tables(seqs, width)
+        slots_h.numpy()[:] = slots
+        table_h.numpy()[:] = table
+        lens_h.numpy()[:] = lens
+        with torch.cuda.stream(stream):
+            for dst, src in ((q_d, q_h), (k_d, k_h), (v_d, v_h), (slots_d, slots_h), (table_d, table_h),
+                             (lens_d, lens_h), (qsl_d, qsl_h)):
+                dst.copy_(src, non_blocking=True)
+            pa.kv_write(k_d, v_d, dw.k_cache, dw.v_cache, slots_d, stream=stream)
+            pa.attention(out_d, q_d, dw.k_cache, dw.v_cache, table_d, lens_d, qsl_d, max_query_len=1,
+                         max_seq_len=int(lens.max()), scale=sp.scale, workspace=st.workspace, stream=stream)
+            out_h.copy_(out_d, non_blocking=True)
+        stream.synchronize()
+        return int(lens.astype(np.int64).sum()) * sp.kv_token_bytes
+
+    for _ in range(a.warmup):
+        one_step()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        kv_bytes_steps.append(one_step())
+    secs = (time.perf_counter() - t0) / a.steps
+    if dist is not None:
+        t = torch.tensor([secs], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        secs = t.item()
+    if pa.read_device_errors(clear=True):
+        raise RuntimeError("device error flags set during the end-to-end run")
+    mean_bytes = sum(kv_bytes_steps) / len(kv_bytes_steps)
+    return {"value": world * mean_bytes / secs / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": secs * 1e3,
+            "includes": "host block accounting (pa_bm_append, pa_bm_batch_tables), H2D of q/k/v/slots/"
+                        "table/lens/query_start_loc from pinned memory, pa_kv_write, pa_attention, D2H of out"}
+
+
+def main(argv=None):
+    a = _args(argv)
+    if a.impl == "reference":
+        return run_reference(a)
+    return run_ours(a)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

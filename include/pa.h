@@ -1,0 +1,210 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged-KV-cache hot path.
+ *
+ * Three device operations and a host block manager:
+ *   pa_kv_write     scatter new tokens' K/V into physical cache blocks through slot_mapping
+ *   pa_attention    paged decode and chunked-prefill attention through block_table
+ *   pa_copy_blocks  copy whole physical blocks (the copy step of copy-on-write)
+ *   pa_bm_*         host-side block accounting: free queue, block tables, ref counts, CoW
+ *
+ * Conventions shared by every entry point:
+ *  - Cache layout: k_cache and v_cache are each [num_blocks, block_size, num_kv_heads,
+ *    head_dim], row-major and contiguous, element type `dtype`. A "slot" is one token
+ *    position in the pool: slot = block * block_size + offset, i.e. the row index of
+ *    the cache viewed as [num_blocks * block_size, num_kv_heads * head_dim].
+ *  - Pointers marked "device" must point to device memory of the current CUDA device,
+ *    owned by the caller and 16-byte aligned; the library never allocates, frees or
+ *    synchronises (except pa_read_device_errors, which synchronises by design). Work is
+ *    enqueued on `stream` (0 = legacy default stream) and the call returns before it runs.
+ *  - Return value: a pa_status. Argument checks happen before anything is launched; a
+ *    call that returns an error has enqueued nothing. PA_ERR_CUDA means a launch
+ *    failed; pa_last_cuda_error() gives the cudaError_t of the calling thread's last one.
+ *  - Index values inside device arrays (slots, block ids, lengths) cannot be checked on
+ *    the host. Kernels check them against the sizes passed in and skip any access that
+ *    would leave the buffers; such a skip sets a bit in a per-device error word that
+ *    pa_read_device_errors() returns. Results are then unspecified but no memory outside
+ *    the arguments is touched.
+ *
+ * Sources (the pages this library restates):
+ *  [docs]  "vLLM", docs.acceleratez.fun/llm/model-inference/vllm.html -- PagedAttention
+ *          (blocks, block table, algorithm flow), memory-utilisation arithmetic,
+ *          Copy-on-Write (reference counting, copy before a divergent write).
+ *  [flow]  vLLM 0.10.0 flow analysis, ascendai.csdn.net/69ac14cf54b52172bc5fa372.html --
+ *          3.2 Scheduler (prefill compute-bound, decode memory-bound, chunked prefill
+ *          mixed with decodes), 3.3 KV Manager (slot, block, pool, slot_mapping),
+ *          3.5 Attention (q is the flattened token batch; metadata block_table,
+ *          slot_mapping, query_start_loc).
+ *  [read]  vLLM code reading, sourceaix.com/community/post/7301643446391930880 --
+ *          5.1.1 single request (logical vs physical blocks, '# filled'),
+ *          5.2.1 parallel sampling (shared blocks, ref count, copy-on-write).
+ *  [intro] VLLM overview, dn008.com.cn/news/553482 -- 2.1 KV cache (causal mask).
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, misaligned pointer, bad shape */
+  PA_ERR_UNSUPPORTED = 2,  /* a valid shape this build has no kernel for */
+  PA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than pa_attention_workspace_size */
+  PA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  PA_ERR_NO_BLOCKS = 5,    /* block manager: not enough free blocks now */
+  PA_ERR_TOO_LARGE = 6,    /* block manager: the sequence can never fit the pool */
+  PA_ERR_NOT_FOUND = 7,    /* block manager: unknown sequence id, or id already in use */
+} pa_status;
+
+/* Bits of the per-device error word (see pa_read_device_errors). */
+#define PA_DEVERR_SLOT_RANGE   0x1u  /* a slot >= num_blocks * block_size was skipped */
+#define PA_DEVERR_BLOCK_RANGE  0x2u  /* a block id outside [0, num_blocks) was skipped */
+#define PA_DEVERR_SEQ_RANGE    0x4u  /* seq_len > max_blocks_per_seq * block_size, or q_len > seq_len */
+#define PA_DEVERR_TIMEOUT      0x8u  /* a pipeline wait gave up (the kernel returned early) */
+
+const char* pa_status_string(int status);
+int pa_last_cuda_error(void);
+
+/* Reads the current device's error word (synchronising the device) and clears it if
+ * `clear` is non-zero. Returns PA_OK or PA_ERR_CUDA. */
+int pa_read_device_errors(unsigned int* flags_out, int clear);
+
+/* ------------------------------------------------------------------------------
+ * pa_kv_write -- [docs] PagedAttention, algorithm flow (prefill step c, decode step d:
+ * store each new token's KV in its physical block); [flow] 3.3 KV Manager (the model
+ * runner builds slot_mapping; attention finds each token's KV through it).
+ *
+ * For every t in [0, num_tokens) with s = slot_mapping[t] >= 0:
+ *     k_cache[s / block_size, s % block_size, :, :] = k[t, :, :]   (same for v)
+ * A negative slot marks a padding token: nothing is written for it.
+ *
+ * k, v          device, [num_tokens, num_kv_heads, head_dim], contiguous, `dtype`
+ * k_cache, ...  device, cache layout above (written in place)
+ * slot_mapping  device, int64 [num_tokens]; slots must be distinct (no two tokens
+ *               written to one slot in a call -- which one would win is unspecified)
+ * num_tokens    >= 0 (0 enqueues nothing)
+ * Byte-exact copy; no arithmetic on the values.
+ * --------------------------------------------------------------------------- */
+int pa_kv_write(const void* k, const void* v, void* k_cache, void* v_cache,
+                const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                int block_size, int num_kv_heads, int head_dim, pa_dtype dtype,
+                pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------
+ * pa_copy_blocks -- [docs] Copy-on-Write (copy the old block's content into the newly
+ * allocated block before the divergent write); [read] 5.2.1 (A1's block 1 copied to 3).
+ *
+ * For each i in [0, num_pairs): src = block_mapping[2i], dst = block_mapping[2i+1]:
+ *     k_cache[dst] = k_cache[src]; v_cache[dst] = v_cache[src]   (all block_size slots)
+ * block_mapping  device, int64 [num_pairs, 2]
+ * Pairs are applied concurrently: no dst may repeat or appear as another pair's src
+ * (pairs emitted by the block manager below always satisfy this: every dst is a block
+ * just taken from the free queue and every src is a block still held by others).
+ * Byte-exact copy.
+ * --------------------------------------------------------------------------- */
+int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
+                   int64_t num_pairs, int64_t num_blocks, int block_size, int num_kv_heads,
+                   int head_dim, pa_dtype dtype, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------
+ * pa_attention -- [flow] 3.5 Attention (q = flattened tokens of the batch, requests
+ * delimited by query_start_loc; K/V read from the whole cache through block_table);
+ * [docs] PagedAttention (block table: logical block -> physical block); [read] 5.1.1
+ * (attention runs over the logical blocks, as if contiguous); [intro] 2.1 (causal);
+ * [flow] 3.2 (chunked prefill mixed with decodes in one batch).
+ *
+ * For request s with q_len = query_start_loc[s+1] - query_start_loc[s] and
+ * L = seq_lens[s] (keys, including the request's new tokens), query row j (token
+ * t = query_start_loc[s] + j) sits at position p = L - q_len + j and, for each query
+ * head h with KV head g = h / (num_heads / num_kv_heads):
+ *     K_i = k_cache[block_table[s, i / block_size], i % block_size, g, :]   (V alike)
+ *     out[t, h, :] = sum_{i<=p} softmax_i(scale * <q[t, h, :], K_i>) * V_i
+ * Softmax and accumulation in fp32; out is written in `dtype` (bf16 rounded to nearest
+ * even). Requests with q_len == 1 run the split-K decode kernel; q_len >= 2 the prefill
+ * kernel; q_len == 0 produces no rows. Requires q_len <= L.
+ * The result does not depend on which physical blocks hold the tokens: the reduction
+ * order is fixed by positions only, so relabelling block ids gives identical bits.
+ *
+ * out           device, [num_tokens, num_heads, head_dim], `dtype` (written)
+ * q             device, [num_tokens, num_heads, head_dim], `dtype`
+ * block_table   device, int32 [num_seqs, max_blocks_per_seq] (entries past a request's
+ *               ceil(L / block_size) blocks are never read)
+ * seq_lens      device, int32 [num_seqs]
+ * query_start_loc device, int32 [num_seqs + 1], non-decreasing, [0] = 0, [num_seqs] =
+ *               num_tokens
+ * max_query_len host: an upper bound of every q_len (sizes the prefill grid)
+ * max_seq_len   host: an upper bound of every L (validated against the table width)
+ * workspace     device scratch of at least pa_attention_workspace_size() bytes (may be
+ *               NULL only when that size is 0); no initial contents needed; must not be
+ *               used by another call that may run concurrently.
+ * Supported: dtype PA_F32 / PA_BF16; head_dim 64 / 128; num_heads / num_kv_heads in
+ * {1, 2, 4, 8}; block_size a divisor of 16 (1, 2, 4, 8, 16) or a multiple of 16.
+ * --------------------------------------------------------------------------- */
+int pa_attention_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                int head_dim, size_t* bytes_out);
+
+int pa_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                 const int32_t* query_start_loc, int num_seqs, int num_tokens,
+                 int max_query_len, int max_seq_len, int num_heads, int num_kv_heads,
+                 int head_dim, int block_size, int64_t num_blocks, float scale,
+                 pa_dtype dtype, void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------
+ * Host block manager -- [docs] PagedAttention algorithm flow and Copy-on-Write
+ * (reference counting); [read] 5.1.1 and 5.2.1; [flow] 3.3 (pool of blocks, slots).
+ *
+ * Free blocks are handed out first-in first-out, starting from `free_order` (a
+ * permutation of [0, num_blocks)); a released block rejoins the tail. Appending a
+ * token takes a new block only when the sequence's last block is full (or it has none),
+ * so a sequence of n tokens holds ceil(n / block_size) blocks. Writing into a last
+ * block whose reference count is > 1 first moves the writer to a fresh block and
+ * records a (src, dst) copy pair; the old block's count drops by 1. An append that
+ * cannot be satisfied changes nothing. Not thread-safe: one manager per thread.
+ * All arrays are host memory.
+ * --------------------------------------------------------------------------- */
+typedef struct pa_bm pa_bm;
+
+/* NULL on invalid arguments (free_order not a permutation, sizes < 1) or no memory. */
+pa_bm* pa_bm_create(int64_t num_blocks, int block_size, const int32_t* free_order);
+void pa_bm_destroy(pa_bm* bm);
+
+int pa_bm_add_seq(pa_bm* bm, int64_t seq);               /* PA_ERR_NOT_FOUND if id in use */
+/* Appends n >= 0 tokens; writes their n slots to slots_out (may be NULL when n == 0).
+ * PA_ERR_NO_BLOCKS: the free queue is too short now; PA_ERR_TOO_LARGE: the sequence
+ * would need more blocks than the pool has. */
+int pa_bm_append(pa_bm* bm, int64_t seq, int64_t n, int64_t* slots_out);
+int pa_bm_fork(pa_bm* bm, int64_t parent, int64_t child); /* child shares parent's blocks */
+int pa_bm_free_seq(pa_bm* bm, int64_t seq);               /* counts - 1, release at 0 */
+int64_t pa_bm_seq_len(const pa_bm* bm, int64_t seq);      /* -1 if unknown */
+int64_t pa_bm_num_seq_blocks(const pa_bm* bm, int64_t seq);/* -1 if unknown */
+int pa_bm_ref_count(const pa_bm* bm, int64_t block);      /* -1 if out of range */
+int64_t pa_bm_num_free(const pa_bm* bm);
+/* Copies the free queue, head first, into out (capacity >= pa_bm_num_free). */
+int pa_bm_free_queue(const pa_bm* bm, int32_t* out, int64_t capacity);
+/* Copies seq's block table (logical order) into out (capacity >= its block count). */
+int pa_bm_block_table(const pa_bm* bm, int64_t seq, int32_t* out, int64_t capacity);
+/* Fills a batch's metadata: row i of table_out [n, width] gets seqs[i]'s block table
+ * (unused entries 0) and seq_lens_out[i] its length. PA_ERR_INVALID_ARG if a table is
+ * wider than `width`. */
+int pa_bm_batch_tables(const pa_bm* bm, const int64_t* seqs, int64_t n, int32_t* table_out,
+                       int64_t width, int32_t* seq_lens_out);
+int64_t pa_bm_num_pending_copies(const pa_bm* bm);
+/* Moves up to `capacity` pending (src, dst) pairs, oldest first, into pairs_out
+ * [capacity, 2]; returns how many were moved (or -1 on a bad argument). */
+int64_t pa_bm_take_copies(pa_bm* bm, int64_t* pairs_out, int64_t capacity);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

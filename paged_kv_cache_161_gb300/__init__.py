@@ -1,0 +1,275 @@
+"""GB300 (sm_103a) paged-KV-cache hot path: a thin ctypes binding over libpa_gb300.so.
+
+Names follow the C ABI in include/pa.h (pa_kv_write -> kv_write, ...). The binding only
+checks tensors and marshals pointers, sizes and the current CUDA stream; every step of
+the path runs in the library's kernels. PyTorch provides device memory and streams.
+
+The library is built in-tree by ``python -m paged_kv_cache_161_gb300.build`` (or the
+repository's ``__graft_entry__.build()``). Importing this package without it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+__all__ = [
+    "PAError",
+    "BlockManager",
+    "kv_write",
+    "copy_blocks",
+    "attention",
+    "attention_workspace_size",
+    "read_device_errors",
+    "lib",
+    "LIB_PATH",
+]
+
+PA_F32, PA_BF16 = 0, 1
+PA_DEVERR = {"slot_range": 0x1, "block_range": 0x2, "seq_range": 0x4, "timeout": 0x8}
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m paged_kv_cache_161_gb300.build` "
+        "(there is no fallback path)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_p, _i, _i64, _sz, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+_sig = {
+    "pa_status_string": (ctypes.c_char_p, [_i]),
+    "pa_last_cuda_error": (_i, []),
+    "pa_read_device_errors": (_i, [ctypes.POINTER(ctypes.c_uint), _i]),
+    "pa_kv_write": (_i, [_p, _p, _p, _p, _p, _i64, _i64, _i, _i, _i, _i, _p]),
+    "pa_copy_blocks": (_i, [_p, _p, _p, _i64, _i64, _i, _i, _i, _i, _p]),
+    "pa_attention_workspace_size": (_i, [_i, _i, _i, _i, ctypes.POINTER(_sz)]),
+    "pa_attention": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i64, _f, _i, _p,
+                          _sz, _p]),
+    "pa_bm_create": (_p, [_i64, _i, _p]),
+    "pa_bm_destroy": (None, [_p]),
+    "pa_bm_add_seq": (_i, [_p, _i64]),
+    "pa_bm_append": (_i, [_p, _i64, _i64, _p]),
+    "pa_bm_fork": (_i, [_p, _i64, _i64]),
+    "pa_bm_free_seq": (_i, [_p, _i64]),
+    "pa_bm_seq_len": (_i64, [_p, _i64]),
+    "pa_bm_num_seq_blocks": (_i64, [_p, _i64]),
+    "pa_bm_ref_count": (_i, [_p, _i64]),
+    "pa_bm_num_free": (_i64, [_p]),
+    "pa_bm_free_queue": (_i, [_p, _p, _i64]),
+    "pa_bm_block_table": (_i, [_p, _i64, _p, _i64]),
+    "pa_bm_batch_tables": (_i, [_p, _p, _i64, _p, _i64, _p]),
+    "pa_bm_num_pending_copies": (_i64, [_p]),
+    "pa_bm_take_copies": (_i64, [_p, _p, _i64]),
+}
+for _name, (_res, _args) in _sig.items():
+    _fn = getattr(lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        msg = lib.pa_status_string(status).decode()
+        if status == 4:
+            msg += f" (cudaError {lib.pa_last_cuda_error()})"
+        super().__init__(f"{what}: {msg} [status {status}]")
+        self.status = status
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise PAError(status, what)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return PA_F32
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _stream(stream, device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _cache_geometry(k_cache: torch.Tensor, v_cache: torch.Tensor):
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype or k_cache.dim() != 4:
+        raise ValueError("k_cache and v_cache must both be [num_blocks, block_size, num_kv_heads, head_dim]")
+    return tuple(int(x) for x in k_cache.shape)
+
+
+def kv_write(k, v, k_cache, v_cache, slot_mapping, stream=None):
+    """pa_kv_write: k_cache[slot // B, slot % B] = k[t] (and v) for every slot >= 0."""
+    NB, B, Hkv, D = _cache_geometry(k_cache, v_cache)
+    T = int(k.shape[0])
+    if tuple(k.shape) != (T, Hkv, D) or tuple(v.shape) != (T, Hkv, D) or k.dtype != k_cache.dtype or \
+            v.dtype != k_cache.dtype:
+        raise ValueError("k, v must be [num_tokens, num_kv_heads, head_dim] in the cache dtype")
+    if tuple(slot_mapping.shape) != (T,):
+        raise ValueError("slot_mapping must be [num_tokens]")
+    st = lib.pa_kv_write(_dev(k, "k"), _dev(v, "v"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                         _dev(slot_mapping, "slot_mapping", torch.int64), T, NB, B, Hkv, D,
+                         _dtype_code(k_cache), _stream(stream, k_cache.device))
+    _check(st, "pa_kv_write")
+
+
+def copy_blocks(k_cache, v_cache, block_mapping, stream=None):
+    """pa_copy_blocks: for each (src, dst) row of block_mapping [n, 2], cache[dst] = cache[src]."""
+    NB, B, Hkv, D = _cache_geometry(k_cache, v_cache)
+    if block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
+        raise ValueError("block_mapping must be [num_pairs, 2]")
+    n = int(block_mapping.shape[0])
+    ptr = _dev(block_mapping, "block_mapping", torch.int64) if n > 0 else 0
+    st = lib.pa_copy_blocks(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ptr, n, NB, B, Hkv, D,
+                            _dtype_code(k_cache), _stream(stream, k_cache.device))
+    _check(st, "pa_copy_blocks")
+
+
+def attention_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int) -> int:
+    """pa_attention_workspace_size for the current device."""
+    out = ctypes.c_size_t(0)
+    _check(lib.pa_attention_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, ctypes.byref(out)),
+           "pa_attention_workspace_size")
+    return int(out.value)
+
+
+def attention(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, *, max_query_len: int,
+              max_seq_len: int, scale: float, workspace=None, stream=None):
+    """pa_attention: paged decode + chunked-prefill attention of one varlen batch.
+
+    out, q: [num_tokens, num_heads, head_dim]; block_table int32 [num_seqs, max_blocks];
+    seq_lens int32 [num_seqs]; query_start_loc int32 [num_seqs + 1]. ``max_query_len`` and
+    ``max_seq_len`` are host-side upper bounds. ``workspace`` is a uint8 CUDA tensor of at
+    least attention_workspace_size(...) bytes; when None one is allocated with torch.
+    """
+    NB, B, Hkv, D = _cache_geometry(k_cache, v_cache)
+    T, Hq = int(q.shape[0]), int(q.shape[1])
+    if q.dim() != 3 or tuple(out.shape) != tuple(q.shape) or int(q.shape[2]) != D:
+        raise ValueError("q and out must be [num_tokens, num_heads, head_dim]")
+    if q.dtype != k_cache.dtype or out.dtype != k_cache.dtype:
+        raise TypeError("q, out and the caches must share one dtype")
+    S = int(seq_lens.shape[0])
+    if block_table.dim() != 2 or int(block_table.shape[0]) != S or tuple(query_start_loc.shape) != (S + 1,):
+        raise ValueError("block_table [S, W], seq_lens [S], query_start_loc [S + 1]")
+    if workspace is None:
+        workspace = torch.empty(attention_workspace_size(S, Hq, Hkv, D), dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace.numel() > 0 else 0
+    st = lib.pa_attention(_dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                          _dev(block_table, "block_table", torch.int32, 2), int(block_table.shape[1]),
+                          _dev(seq_lens, "seq_lens", torch.int32, 1),
+                          _dev(query_start_loc, "query_start_loc", torch.int32, 1), S, T, int(max_query_len),
+                          int(max_seq_len), Hq, Hkv, D, B, NB, float(scale), _dtype_code(q), ws_ptr,
+                          workspace.numel(), _stream(stream, q.device))
+    _check(st, "pa_attention")
+    return out
+
+
+def read_device_errors(clear: bool = True) -> int:
+    """The current device's error word (PA_DEVERR bits); synchronises the device."""
+    flags = ctypes.c_uint(0)
+    _check(lib.pa_read_device_errors(ctypes.byref(flags), 1 if clear else 0), "pa_read_device_errors")
+    return int(flags.value)
+
+
+class BlockManager:
+    """pa_bm_*: host block accounting (free queue, tables, ref counts, copy-on-write)."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order):
+        import numpy as np
+
+        order = np.ascontiguousarray(np.asarray(free_order, dtype=np.int32))
+        if order.shape != (num_blocks,):
+            raise ValueError("free_order must have num_blocks entries")
+        self._h = lib.pa_bm_create(num_blocks, block_size, order.ctypes.data)
+        if not self._h:
+            raise ValueError("pa_bm_create: free_order must be a permutation of range(num_blocks)")
+        self.num_blocks, self.block_size = num_blocks, block_size
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            lib.pa_bm_destroy(h)
+            self._h = None
+
+    def add_seq(self, seq: int):
+        _check(lib.pa_bm_add_seq(self._h, seq), "pa_bm_add_seq")
+
+    def append(self, seq: int, n: int):
+        """Returns the slots of the n new tokens (numpy int64)."""
+        import numpy as np
+
+        out = np.empty(max(n, 0), np.int64)
+        _check(lib.pa_bm_append(self._h, seq, n, out.ctypes.data if n > 0 else None), "pa_bm_append")
+        return out
+
+    def fork(self, parent: int, child: int):
+        _check(lib.pa_bm_fork(self._h, parent, child), "pa_bm_fork")
+
+    def free_seq(self, seq: int):
+        _check(lib.pa_bm_free_seq(self._h, seq), "pa_bm_free_seq")
+
+    def seq_len(self, seq: int) -> int:
+        return int(lib.pa_bm_seq_len(self._h, seq))
+
+    def ref_count(self, block: int) -> int:
+        return int(lib.pa_bm_ref_count(self._h, block))
+
+    def num_free(self) -> int:
+        return int(lib.pa_bm_num_free(self._h))
+
+    def free_queue(self):
+        import numpy as np
+
+        out = np.empty(self.num_free(), np.int32)
+        _check(lib.pa_bm_free_queue(self._h, out.ctypes.data if out.size else None, out.size), "pa_bm_free_queue")
+        return out
+
+    def block_table(self, seq: int):
+        import numpy as np
+
+        n = int(lib.pa_bm_num_seq_blocks(self._h, seq))
+        if n < 0:
+            raise PAError(7, "pa_bm_block_table")
+        out = np.empty(n, np.int32)
+        _check(lib.pa_bm_block_table(self._h, seq, out.ctypes.data if n else None, n), "pa_bm_block_table")
+        return out
+
+    def batch_tables(self, seqs, width: int):
+        """(block_table int32 [n, width], seq_lens int32 [n]) for the sequences ``seqs``."""
+        import numpy as np
+
+        s = np.ascontiguousarray(np.asarray(seqs, np.int64))
+        table = np.empty((len(s), width), np.int32)
+        lens = np.empty(len(s), np.int32)
+        _check(lib.pa_bm_batch_tables(self._h, s.ctypes.data if len(s) else None, len(s),
+                                      table.ctypes.data if len(s) else None, width,
+                                      lens.ctypes.data if len(s) else None), "pa_bm_batch_tables")
+        return table, lens
+
+    def take_copies(self):
+        """Pending copy-on-write pairs, oldest first: int64 [n, 2] (src, dst)."""
+        import numpy as np
+
+        n = int(lib.pa_bm_num_pending_copies(self._h))
+        out = np.empty((n, 2), np.int64)
+        got = lib.pa_bm_take_copies(self._h, out.ctypes.data if n else None, n)
+        if got != n:
+            raise PAError(1, "pa_bm_take_copies")
+        return out

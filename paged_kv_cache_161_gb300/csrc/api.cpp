@@ -1,0 +1,197 @@
+// C ABI of include/pa.h: argument validation, then dispatch to the kernel launchers.
+// Nothing here allocates device memory or synchronises (except pa_read_device_errors).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "launch.h"
+#include "pa.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return PA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(pa_dtype dt) {
+  switch (dt) {
+    case PA_F32: return 4;
+    case PA_BF16: return 2;
+  }
+  return 0;
+}
+
+bool pow2_le8(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+// Cache geometry shared by the three device entry points.
+int check_cache(const void* k_cache, const void* v_cache, int64_t num_blocks, int block_size,
+                int num_kv_heads, int head_dim, pa_dtype dtype) {
+  if (!k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+  if (num_blocks < 1 || block_size < 1 || num_kv_heads < 1 || head_dim < 1) return PA_ERR_INVALID_ARG;
+  if (elem_bytes(dtype) == 0) return PA_ERR_INVALID_ARG;
+  if ((int64_t(num_kv_heads) * head_dim * elem_bytes(dtype)) % 16 != 0) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_NO_BLOCKS: return "not enough free blocks";
+    case PA_ERR_TOO_LARGE: return "sequence larger than the block pool";
+    case PA_ERR_NOT_FOUND: return "unknown or duplicate sequence id";
+  }
+  return "unknown status";
+}
+
+int pa_last_cuda_error(void) { return g_last_cuda_error; }
+
+int pa_read_device_errors(unsigned int* flags_out, int clear) {
+  if (!flags_out) return PA_ERR_INVALID_ARG;
+  cudaError_t e;
+  unsigned int* w = pa::device_error_word(&e);
+  if (!w) return cuda_fail(e);
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaMemcpy(flags_out, w, sizeof(unsigned int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (clear) {
+    e = cudaMemset(w, 0, sizeof(unsigned int));
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return PA_OK;
+}
+
+int pa_kv_write(const void* k, const void* v, void* k_cache, void* v_cache,
+                const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                int block_size, int num_kv_heads, int head_dim, pa_dtype dtype,
+                pa_stream_t stream) {
+  int st = check_cache(k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !aligned16(k) || !aligned16(v)) return PA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(slot_mapping) % 8 != 0) return PA_ERR_INVALID_ARG;
+  cudaError_t e;
+  unsigned int* err = pa::device_error_word(&e);
+  if (!err) return cuda_fail(e);
+  const int64_t row_bytes = int64_t(num_kv_heads) * head_dim * elem_bytes(dtype);
+  e = pa::launch_kv_write(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_blocks * block_size,
+                          row_bytes, err, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping, int64_t num_pairs,
+                   int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
+                   pa_dtype dtype, pa_stream_t stream) {
+  int st = check_cache(k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_pairs < 0 || num_pairs > 0x7fffffff) return PA_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (!block_mapping || reinterpret_cast<uintptr_t>(block_mapping) % 8 != 0) return PA_ERR_INVALID_ARG;
+  cudaError_t e;
+  unsigned int* err = pa::device_error_word(&e);
+  if (!err) return cuda_fail(e);
+  const int64_t block_bytes = int64_t(block_size) * num_kv_heads * head_dim * elem_bytes(dtype);
+  e = pa::launch_copy_blocks(k_cache, v_cache, block_mapping, num_pairs, num_blocks, block_bytes, err,
+                             reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int pa_attention_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                size_t* bytes_out) {
+  if (!bytes_out || num_seqs < 0 || num_heads < 1 || num_kv_heads < 1) return PA_ERR_INVALID_ARG;
+  if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+  if (!pa::decode_supported(PA_BF16, head_dim, num_heads / num_kv_heads)) return PA_ERR_UNSUPPORTED;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int ctas = pa::decode_num_ctas(dev, &e);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // The larger of the two element types' layouts, so one size serves both.
+  const size_t a = pa::decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, ctas, PA_BF16);
+  const size_t b = pa::decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, ctas, PA_F32);
+  *bytes_out = a > b ? a : b;
+  return PA_OK;
+}
+
+int pa_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                 const int32_t* query_start_loc, int num_seqs, int num_tokens, int max_query_len,
+                 int max_seq_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                 int64_t num_blocks, float scale, pa_dtype dtype, void* workspace,
+                 size_t workspace_bytes, pa_stream_t stream) {
+  int st = check_cache(k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || max_seq_len < 0) return PA_ERR_INVALID_ARG;
+  if (num_heads < 1 || num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || scale != scale) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0 || num_tokens == 0) return PA_OK;
+  if (!out || !q || !block_table || !seq_lens || !query_start_loc) return PA_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q)) return PA_ERR_INVALID_ARG;
+  if (max_blocks_per_seq < 1) return PA_ERR_INVALID_ARG;
+  if (int64_t(max_blocks_per_seq) * block_size > 0x7fffffff) return PA_ERR_INVALID_ARG;
+  if (int64_t(max_blocks_per_seq) * block_size < max_seq_len) return PA_ERR_INVALID_ARG;
+  if (max_query_len > max_seq_len) return PA_ERR_INVALID_ARG;
+  const int G = num_heads / num_kv_heads;
+  if (!pow2_le8(G) || (head_dim != 64 && head_dim != 128)) return PA_ERR_UNSUPPORTED;
+  if (!(16 % block_size == 0 || block_size % 16 == 0)) return PA_ERR_UNSUPPORTED;
+  if (!pa::decode_supported(dtype, head_dim, G) || !pa::prefill_supported(dtype, head_dim, G))
+    return PA_ERR_UNSUPPORTED;
+  if (num_seqs > 0x7fffffff / 8) return PA_ERR_INVALID_ARG;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int ctas = pa::decode_num_ctas(dev, &e);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const size_t need = pa::decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, ctas, dtype);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PA_ERR_WORKSPACE;
+  unsigned int* err = pa::device_error_word(&e);
+  if (!err) return cuda_fail(e);
+
+  pa::AttnArgs a;
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.query_start_loc = query_start_loc;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.num_tokens = num_tokens;
+  a.max_query_len = max_query_len;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.workspace = workspace;
+  a.err = err;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  e = pa::launch_decode(a, ctas, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = pa::launch_prefill(a, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,848 @@
+// Paged decode attention (requests with q_len == 1): split-K over a balanced partition of
+// all K/V pages, then a log-sum-exp merge of the pieces.
+//
+// What it computes: vLLM 0.10.0 flow page, 3.5 Attention -- the query of each request
+// attends to all of its cached K/V, which attention finds through block_table;
+// "vLLM" docs page, PagedAttention -- logical block i of a request lives in physical
+// block block_table[s, i]; code-reading page 5.1.1 -- the computation runs over the
+// logical blocks as if the tokens were contiguous. Decode is memory-bound (flow page,
+// 3.2 Scheduler), so the kernel is built around streaming K/V once at HBM speed.
+//
+// Design (sm_103a):
+//  * Work unit = 16 consecutive logical tokens of one request for one group of HG KV
+//    heads ("stage"): 16 x HG x D elements of K and the same of V (64 KiB for bf16,
+//    HG = 8, D = 128). Units are numbered head-group-major, then request, then
+//    position; the grid (one CTA per SM) splits that numbering into equal contiguous
+//    ranges, so every SM streams the same number of bytes whatever the length mix.
+//    A request cut by a range boundary leaves one partial result per CTA; the merge
+//    kernel combines them in CTA order. The cut points depend only on seq_lens, so
+//    results do not depend on which physical blocks hold the tokens.
+//  * One producer warp walks the CTA's units and moves each stage into shared memory
+//    with bulk copies (cp.async.bulk, the TMA engine): one copy per physical block
+//    when the CTA covers all KV heads (the block's rows are contiguous), one per token
+//    row otherwise. A 3-deep ring of stages with full/empty mbarriers keeps two stages
+//    in flight while one is consumed. Every wait is bounded (common.cuh).
+//  * Two consumer warps per KV head split each stage's 16 tokens 8/8. A lane owns VEC
+//    consecutive dims of a row; q of the head's G query heads sits in registers (fp32,
+//    pre-scaled by scale * log2 e). Dot products are packed fp32 FMAs; the per-lane
+//    partial dots of (token, head) pairs are summed across the row's lanes by a
+//    halving butterfly (each step trades half the values with the partner lane), so a
+//    lane ends with whole logits of its own (token, head) pairs. Online softmax in
+//    fp32 (exp2 domain) with warp-shuffle max/sum; P goes through a 128-byte shared
+//    buffer to the P.V product, accumulated in fp32 registers.
+//  * At a request's last unit in the CTA the two warps of a head merge their (m, l, O)
+//    through shared memory; the result is written to `out` directly when the CTA
+//    covered the whole request, else to the workspace as (O / l, m + log2 l).
+#include <float.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace pa {
+namespace {
+
+constexpr int kTPS = 16;    // tokens per stage
+constexpr int kStages = 3;  // ring depth
+constexpr int kSmemLimit = 227 * 1024;
+
+enum : int { kFirst = 1, kLast = 2, kSeqStart = 4, kSeqEnd = 8, kBad = 16 };
+
+struct __align__(16) StageDesc {
+  int s, hg, j, valid, flags, pad0, pad1, pad2;
+};
+
+struct DecodeParams {
+  void* out;
+  const void* q;
+  const char* k_cache;
+  const char* v_cache;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  float* ws_o;
+  float* ws_lse;
+  int4* ws_meta;  // per (head group, request): first CTA, last CTA, units per head group
+  unsigned int* err;
+  int64_t num_blocks;
+  int max_blocks_per_seq;
+  int num_seqs;
+  int num_heads;
+  int num_kv_heads;
+  int block_size;
+  int hg_size;  // KV heads per CTA (HG)
+  int num_hg;   // num_kv_heads / HG
+  int group;    // query heads per KV head
+  int qg;       // warp pairs per KV head = group / (query heads per warp)
+  int num_ctas; // grid of the split-K kernel
+  float scale_log2;
+};
+
+// Keys of request s if it is a decode request (q_len == 1), else 0.
+__device__ __forceinline__ int decode_len(const DecodeParams& p, int s) {
+  const int q_len = __ldg(p.qsl + s + 1) - __ldg(p.qsl + s);
+  if (q_len != 1) return 0;
+  int L = __ldg(p.seq_lens + s);
+  const int cap = p.max_blocks_per_seq * p.block_size;
+  if (L > cap) {
+    raise_error(p.err, PA_DEVERR_SEQ_RANGE);
+    L = cap;
+  }
+  return L > 0 ? L : 0;
+}
+
+__device__ __forceinline__ int units_of(int L) { return (L + kTPS - 1) / kTPS; }
+
+// ---------------------------------------------------------------- block-wide helpers
+__device__ __forceinline__ int warp_sum_i(int x) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+  return x;
+}
+
+// Sum over the block; `red` holds >= 33 ints of shared memory.
+__device__ int block_sum(int x, int* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  x = warp_sum_i(x);
+  if (lane == 0) red[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int y = lane < nw ? red[lane] : 0;
+    y = warp_sum_i(y);
+    if (lane == 0) red[32] = y;
+  }
+  __syncthreads();
+  const int r = red[32];
+  __syncthreads();
+  return r;
+}
+
+// Exclusive prefix over the block (thread order); returns it and the block total.
+__device__ int block_exclusive_scan(int x, int* red, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc = x;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, d);
+    if (lane >= d) inc += y;
+  }
+  if (lane == 31) red[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < nw ? red[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, d);
+      if (lane >= d) wi += y;
+    }
+    if (lane < nw) red[lane] = wi - w;  // exclusive warp offsets
+    if (lane == 31) red[32] = wi;
+  }
+  __syncthreads();
+  const int r = red[warp] + inc - x;
+  *total = red[32];
+  __syncthreads();
+  return r;
+}
+
+// ---------------------------------------------------------------- register tile helpers
+template <typename T, int VEC>
+struct RowVec;
+
+// VEC elements of a row -> fp32, from shared or global memory.
+template <int VEC>
+struct RowVec<__nv_bfloat16, VEC> {
+  static_assert(VEC == 4 || VEC == 8, "bf16 rows move 8 or 16 bytes per lane");
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float* f) {
+    if constexpr (VEC == 8) {
+      Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(p), f);
+    } else {
+      const uint2 u = *reinterpret_cast<const uint2*>(p);
+      f[0] = __uint_as_float(u.x << 16);
+      f[1] = __uint_as_float(u.x & 0xffff0000u);
+      f[2] = __uint_as_float(u.y << 16);
+      f[3] = __uint_as_float(u.y & 0xffff0000u);
+    }
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float* f) {
+    uint32_t w[VEC / 2];
+#pragma unroll
+    for (int i = 0; i < VEC / 2; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    if constexpr (VEC == 8)
+      *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    else
+      *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+  }
+};
+
+template <int VEC>
+struct RowVec<float, VEC> {
+  static_assert(VEC == 4, "fp32 rows move 16 bytes per lane");
+  static __device__ __forceinline__ void load(const float* p, float* f) {
+    const float4 u = *reinterpret_cast<const float4*>(p);
+    f[0] = u.x;
+    f[1] = u.y;
+    f[2] = u.z;
+    f[3] = u.w;
+  }
+  static __device__ __forceinline__ void store(float* p, const float* f) {
+    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+  }
+};
+
+template <int G>
+__device__ __forceinline__ float pick(const float (&a)[G], int g) {
+  float r = a[0];
+#pragma unroll
+  for (int i = 1; i < G; ++i) r = (g == i) ? a[i] : r;
+  return r;
+}
+
+// ---------------------------------------------------------------- compile-time layout
+// G here is the number of query heads one warp serves (at most 4; a KV head with more
+// query heads is split across several warp pairs).
+template <typename T, int D, int G>
+struct Cfg {
+  static constexpr int EL = sizeof(T);
+  static constexpr int VEC = 4;  // dims per lane: q and O take 4 * G registers each
+  static constexpr int LPR = D / VEC;  // lanes per token row
+  static_assert(LPR >= 1 && LPR <= 32 && (32 % LPR) == 0, "row must map onto a warp");
+  static constexpr int RPI = 32 / LPR;  // token rows per warp instruction
+  static constexpr int TPW = kTPS / 2;  // tokens per warp per stage
+  static_assert(TPW % RPI == 0, "tokens per warp must fill whole row groups");
+  static constexpr int TPL = TPW / RPI;  // tokens per lane per stage
+  static constexpr int NV = TPL * G;     // partial dots per lane before the reduction
+  static constexpr int LOG_LPR = LPR == 1 ? 0 : LPR == 2 ? 1 : LPR == 4 ? 2 : LPR == 8 ? 3 : LPR == 16 ? 4 : 5;
+  static constexpr int LOG_NV = NV == 1 ? 0 : NV == 2 ? 1 : NV == 4 ? 2 : NV == 8 ? 3 : NV == 16 ? 4 : NV == 32 ? 5 : 6;
+  static_assert((1 << LOG_NV) == NV, "NV must be a power of two");
+  static constexpr int NVF = NV > LPR ? NV / LPR : 1;  // whole logits per lane after it
+  // Low lane bits that hold duplicates after the reduction (NV < LPR).
+  static constexpr int SH = LOG_LPR > LOG_NV ? LOG_LPR - LOG_NV : 0;
+  // Lane mask bit b reduces over tokens (not heads, not duplicates)?
+  static constexpr __host__ __device__ bool token_bit(int b) {
+    return b >= LOG_LPR || (b >= SH && (((1 << (b - SH)) * NVF) % G) == 0);
+  }
+};
+
+template <typename T, int D, int G>
+struct Smem {
+  using C = Cfg<T, D, G>;
+  // Byte offsets inside the dynamic shared memory of one CTA with HG KV heads.
+  static __host__ __device__ size_t stage_bytes(int hg) { return size_t(kTPS) * hg * D * C::EL; }
+  static __host__ __device__ size_t k_off(int) { return 0; }
+  static __host__ __device__ size_t v_off(int hg) { return kStages * stage_bytes(hg); }
+  // `pairs` = consumer warp pairs = HG * (query heads per KV head / G)
+  static __host__ __device__ size_t merge_off(int hg) { return 2 * kStages * stage_bytes(hg); }
+  static __host__ __device__ size_t merge_bytes_per_pair() { return size_t(G) * D * 4 + 2 * G * 4; }
+  static __host__ __device__ size_t pbuf_off(int hg, int pairs) { return merge_off(hg) + pairs * merge_bytes_per_pair(); }
+  static __host__ __device__ size_t pbuf_floats_per_warp() { return size_t(C::RPI) * C::NV; }
+  static __host__ __device__ size_t desc_off(int hg, int pairs) {
+    return (pbuf_off(hg, pairs) + 2 * pairs * pbuf_floats_per_warp() * 4 + 15) / 16 * 16;
+  }
+  static __host__ __device__ size_t bar_off(int hg, int pairs) { return desc_off(hg, pairs) + kStages * sizeof(StageDesc); }
+  static __host__ __device__ size_t red_off(int hg, int pairs) { return bar_off(hg, pairs) + 2 * kStages * 8; }
+  static __host__ __device__ size_t total(int hg, int pairs) { return red_off(hg, pairs) + 40 * 4; }
+};
+
+// ---------------------------------------------------------------- the split-K kernel
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_constant__ DecodeParams p) {
+  using C = Cfg<T, D, G>;
+  using SM = Smem<T, D, G>;
+  constexpr int VEC = C::VEC, LPR = C::LPR, RPI = C::RPI, TPL = C::TPL, NV = C::NV, NVF = C::NVF;
+  constexpr int SH = C::SH;
+  const int HG = p.hg_size, QG = p.qg, GF = p.group;
+  const int S = p.num_seqs;
+  const int pairs = HG * QG;
+  const int num_consumers = 2 * pairs;
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  StageDesc* desc = reinterpret_cast<StageDesc*>(smem + SM::desc_off(HG, pairs));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::bar_off(HG, pairs));
+  int* red = reinterpret_cast<int*>(smem + SM::red_off(HG, pairs));
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- plan: this CTA's range of units [u_begin, u_end) and where it starts
+  int my_units = 0;
+  for (int s = threadIdx.x; s < S; s += blockDim.x) my_units += units_of(decode_len(p, s));
+  const int units_per_hg = block_sum(my_units, red);
+  const int64_t U = int64_t(units_per_hg) * p.num_hg;
+  const int64_t c = blockIdx.x, C_ = gridDim.x;
+  const int64_t u_begin = c * U / C_, u_end = (c + 1) * U / C_;
+  if (u_begin >= u_end) return;
+  const int start_hg = int(u_begin / units_per_hg);
+  const int rem = int(u_begin % units_per_hg);
+  int run = 0;
+  for (int base = 0; base < S; base += blockDim.x) {
+    const int s = base + threadIdx.x;
+    const int us = s < S ? units_of(decode_len(p, s)) : 0;
+    int total;
+    const int ex = block_exclusive_scan(us, red, &total);
+    if (us > 0 && run + ex <= rem && rem < run + ex + us) {
+      red[34] = s;
+      red[35] = rem - (run + ex);
+    }
+    __syncthreads();
+    run += total;
+    if (run > rem) break;
+  }
+  const int start_s = red[34], start_j = red[35];
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, num_consumers);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const size_t sbytes = SM::stage_bytes(HG);
+  const int Hkv = p.num_kv_heads, B = p.block_size;
+  const int64_t kv_row_bytes = int64_t(Hkv) * D * C::EL;  // one token, all KV heads
+
+  if (warp == num_consumers) {
+    // =========================== producer warp ===========================
+    int s = start_s, j = start_j, hg = start_hg;
+    int L = decode_len(p, s);
+    int units_s = units_of(L);
+    int stage = 0;
+    uint32_t phase = 0;
+    const bool whole_rows = (HG == Hkv);
+    const int kv = lane >> 4, idx = lane & 15;
+    const char* cache = kv ? p.v_cache : p.k_cache;
+    const uint32_t buf0 = smem_u32(smem + (kv ? SM::v_off(HG) : SM::k_off(HG)));
+    for (int64_t u = u_begin; u < u_end; ++u) {
+      const int64_t u0 = u - j, u1 = u0 + units_s;
+      int flags = 0;
+      if (u == u_begin || j == 0) flags |= kFirst;
+      if (u == u_end - 1 || j == units_s - 1) flags |= kLast;
+      if (u0 >= u_begin) flags |= kSeqStart;
+      if (u1 <= u_end) flags |= kSeqEnd;
+      const int valid = min(kTPS, L - j * kTPS);
+      // ---- this lane's copy (at most one per lane: 16 for K, 16 for V)
+      const int32_t* bt = p.block_table + int64_t(s) * p.max_blocks_per_seq;
+      const int pos0 = j * kTPS;
+      bool have = false, bad = false;
+      const char* src = nullptr;
+      uint32_t dst = 0, bytes = 0;
+      if (whole_rows) {
+        if (B >= kTPS) {
+          if (idx == 0) {
+            const int64_t blk = __ldg(bt + pos0 / B);
+            bad = blk < 0 || blk >= p.num_blocks;
+            have = !bad;
+            src = cache + (blk * B + pos0 % B) * kv_row_bytes;
+            bytes = uint32_t(valid * kv_row_bytes);
+            dst = buf0 + stage * sbytes;
+          }
+        } else {
+          const int nblk = (valid + B - 1) / B;
+          if (idx < nblk) {
+            const int64_t blk = __ldg(bt + pos0 / B + idx);
+            bad = blk < 0 || blk >= p.num_blocks;
+            have = !bad;
+            src = cache + blk * B * kv_row_bytes;
+            bytes = uint32_t(min(B, valid - idx * B) * kv_row_bytes);
+            dst = buf0 + stage * sbytes + uint32_t(idx * B * kv_row_bytes);
+          }
+        }
+      } else if (idx < valid) {
+        const int pos = pos0 + idx;
+        const int64_t blk = __ldg(bt + pos / B);
+        bad = blk < 0 || blk >= p.num_blocks;
+        have = !bad;
+        const int64_t hg_row = int64_t(HG) * D * C::EL;
+        src = cache + (blk * B + pos % B) * kv_row_bytes + hg * hg_row;
+        bytes = uint32_t(hg_row);
+        dst = buf0 + stage * sbytes + uint32_t(idx * hg_row);
+      }
+      const int total_bytes = warp_sum_i(have ? int(bytes) : 0);
+      const bool any_bad = __any_sync(0xffffffffu, bad);
+      if (any_bad) flags |= kBad;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(empty0 + 8 * stage, phase ^ 1) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        raise_error(p.err, PA_DEVERR_TIMEOUT);
+        break;
+      }
+      if (lane == 0) {
+        if (any_bad) raise_error(p.err, PA_DEVERR_BLOCK_RANGE);
+        StageDesc d;
+        d.s = s;
+        d.hg = hg;
+        d.j = j;
+        d.valid = valid;
+        d.flags = flags;
+        d.pad0 = d.pad1 = d.pad2 = 0;
+        desc[stage] = d;
+        mbar_arrive_expect_tx(full0 + 8 * stage, uint32_t(total_bytes));
+      }
+      __syncwarp();
+      if (have) bulk_g2s(dst, src, bytes, full0 + 8 * stage);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+      if (++j == units_s && u + 1 < u_end) {
+        j = 0;
+        do {
+          if (++s == S) {
+            s = 0;
+            ++hg;
+          }
+          L = decode_len(p, s);
+          units_s = units_of(L);
+        } while (units_s == 0);
+      }
+    }
+    return;
+  }
+
+  // =========================== consumer warps ===========================
+  const int pair = warp >> 1, half = warp & 1;
+  const int hk = pair / QG, qg = pair % QG;
+  const int lir = lane & (LPR - 1), r = lane / LPR;
+  const int Hq = p.num_heads;
+  float* pbuf = reinterpret_cast<float*>(smem + SM::pbuf_off(HG, pairs)) + warp * SM::pbuf_floats_per_warp();
+  float* merge = reinterpret_cast<float*>(smem + SM::merge_off(HG) + pair * SM::merge_bytes_per_pair());
+  const T* kbase = reinterpret_cast<const T*>(smem + SM::k_off(HG));
+  const T* vbase = reinterpret_cast<const T*>(smem + SM::v_off(HG));
+  const size_t stage_elems = sbytes / C::EL;
+
+  // value i of this lane after the reduction: index = (lir >> SH) * NVF + i = ti * G + g
+  int my_g[NVF], my_ti[NVF];
+#pragma unroll
+  for (int i = 0; i < NVF; ++i) {
+    const int id = (lir >> SH) * NVF + i;
+    my_g[i] = id % G;
+    my_ti[i] = id / G;
+  }
+  const bool p_writer = (lir & ((1 << SH) - 1)) == 0;
+
+  float2 qf[G][VEC / 2];
+  float2 acc[G][VEC / 2];
+  float mrun[G];
+  float lpart[NVF];
+
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int64_t u = u_begin; u < u_end; ++u) {
+    if (!mbar_wait(full0 + 8 * stage, phase)) {
+      raise_error(p.err, PA_DEVERR_TIMEOUT);
+      return;
+    }
+    const StageDesc d = desc[stage];
+    if (d.flags & kFirst) {
+      const int qrow = __ldg(p.qsl + d.s);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int hq = (d.hg * HG + hk) * GF + qg * G + g;
+        float f[VEC];
+        RowVec<T, VEC>::load(reinterpret_cast<const T*>(p.q) + (int64_t(qrow) * Hq + hq) * D + lir * VEC, f);
+#pragma unroll
+        for (int e = 0; e < VEC / 2; ++e) {
+          qf[g][e] = make_float2(f[2 * e] * p.scale_log2, f[2 * e + 1] * p.scale_log2);
+          acc[g][e] = make_float2(0.f, 0.f);
+        }
+        mrun[g] = -INFINITY;
+      }
+#pragma unroll
+      for (int i = 0; i < NVF; ++i) lpart[i] = 0.f;
+    }
+    const int valid = (d.flags & kBad) ? 0 : d.valid;
+
+    // ---- S = q . K for this warp's 8 tokens
+    const T* ks = kbase + stage * stage_elems;
+    float sv[NV];
+#pragma unroll
+    for (int ti = 0; ti < TPL; ++ti) {
+      const int t = half * C::TPW + r + RPI * ti;
+      float kf[VEC];
+      RowVec<T, VEC>::load(ks + (size_t(t) * HG + hk) * D + lir * VEC, kf);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < VEC / 2; ++e) ffma2(a, qf[g][e], make_float2(kf[2 * e], kf[2 * e + 1]));
+        sv[ti * G + g] = a.x + a.y;
+      }
+    }
+    // ---- halving butterfly across the row's lanes: lane keeps whole dots of its pairs
+    {
+      int cur = NV;
+#pragma unroll
+      for (int m = LPR / 2; m >= 1; m >>= 1) {
+        if (cur > 1) {
+          const int h = cur / 2;
+          const bool up = (lir & m) != 0;
+#pragma unroll
+          for (int i = 0; i < NV / 2; ++i) {
+            if (i < h) {
+              const float send = up ? sv[i] : sv[i + h];
+              const float keep = up ? sv[i + h] : sv[i];
+              sv[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+            }
+          }
+          cur = h;
+        } else {
+          sv[0] += __shfl_xor_sync(0xffffffffu, sv[0], m);
+        }
+      }
+    }
+    // ---- online softmax (log2 domain)
+    float x[NVF], bm[NVF];
+#pragma unroll
+    for (int i = 0; i < NVF; ++i) {
+      const int t = half * C::TPW + r + RPI * my_ti[i];
+      x[i] = (t < valid) ? sv[i] : -INFINITY;
+      bm[i] = x[i];
+    }
+#pragma unroll
+    for (int b = 0; b < 5; ++b) {
+      if (C::token_bit(b)) {
+#pragma unroll
+        for (int i = 0; i < NVF; ++i) bm[i] = fmaxf(bm[i], __shfl_xor_sync(0xffffffffu, bm[i], 1 << b));
+      }
+    }
+    float mnew[G], msafe[G], alpha[G];
+    bool rescale = false;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float mb = __shfl_sync(0xffffffffu, bm[g % NVF], (g / NVF) << SH);
+      mnew[g] = fmaxf(mrun[g], mb);
+      msafe[g] = (mnew[g] == -INFINITY) ? 0.f : mnew[g];
+      alpha[g] = exp2f(mrun[g] - msafe[g]);
+      rescale |= (alpha[g] != 1.f);
+    }
+    if (rescale) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < VEC / 2; ++e) {
+          acc[g][e].x *= alpha[g];
+          acc[g][e].y *= alpha[g];
+        }
+#pragma unroll
+      for (int i = 0; i < NVF; ++i) lpart[i] *= pick(alpha, my_g[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < NVF; ++i) {
+      const float pv = exp2f(x[i] - pick(msafe, my_g[i]));
+      lpart[i] += pv;
+      if (p_writer) pbuf[r * NV + (lir >> SH) * NVF + i] = pv;
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) mrun[g] = mnew[g];
+    __syncwarp();
+
+    // ---- O += P . V
+    const T* vs = vbase + stage * stage_elems;
+#pragma unroll
+    for (int ti = 0; ti < TPL; ++ti) {
+      const int t = half * C::TPW + r + RPI * ti;
+      if (t < valid) {
+        float vf[VEC];
+        RowVec<T, VEC>::load(vs + (size_t(t) * HG + hk) * D + lir * VEC, vf);
+        float pw[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) pw[g] = pbuf[r * NV + ti * G + g];
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int e = 0; e < VEC / 2; ++e)
+            ffma2(acc[g][e], make_float2(pw[g], pw[g]), make_float2(vf[2 * e], vf[2 * e + 1]));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1;
+    }
+
+    if (!(d.flags & kLast)) continue;
+
+    // ================= finalize this request's piece =================
+    const int qrow = __ldg(p.qsl + d.s);
+    float lsum[NVF];
+#pragma unroll
+    for (int i = 0; i < NVF; ++i) lsum[i] = lpart[i];
+#pragma unroll
+    for (int b = 0; b < 5; ++b) {
+      if (C::token_bit(b)) {
+#pragma unroll
+        for (int i = 0; i < NVF; ++i) lsum[i] += __shfl_xor_sync(0xffffffffu, lsum[i], 1 << b);
+      }
+    }
+    float lh[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) lh[g] = __shfl_sync(0xffffffffu, lsum[g % NVF], (g / NVF) << SH);
+    // O partials of the row groups -> every lane
+#pragma unroll
+    for (int m = LPR; m < 32; m <<= 1)
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < VEC / 2; ++e) {
+          acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, m);
+          acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, m);
+        }
+    // the two warps of this KV head meet in shared memory
+    float* mo = merge;               // [G][D]
+    float* mm = merge + G * D;       // [G] m
+    float* ml = merge + G * D + G;   // [G] l
+    if (half == 1) {
+      if (r == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int e = 0; e < VEC / 2; ++e)
+            *reinterpret_cast<float2*>(mo + g * D + lir * VEC + 2 * e) = acc[g][e];
+      }
+      if (lane < G) {
+        mm[lane] = pick(mrun, lane);
+        ml[lane] = pick(lh, lane);
+      }
+    }
+    named_bar_sync(1 + pair, 64);
+    if (half == 0) {
+      float o[G][VEC];
+      float lt[G], mt[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float m1 = mm[g], l1 = ml[g];
+        const float M = fmaxf(mrun[g], m1);
+        const float Ms = (M == -INFINITY) ? 0.f : M;
+        const float a0 = exp2f(mrun[g] - Ms), a1 = exp2f(m1 - Ms);
+        lt[g] = lh[g] * a0 + l1 * a1;
+        mt[g] = M;
+#pragma unroll
+        for (int e = 0; e < VEC / 2; ++e) {
+          const float2 o1 = *reinterpret_cast<const float2*>(mo + g * D + lir * VEC + 2 * e);
+          o[g][2 * e] = acc[g][e].x * a0 + o1.x * a1;
+          o[g][2 * e + 1] = acc[g][e].y * a0 + o1.y * a1;
+        }
+      }
+      named_bar_sync(1 + pair, 64);
+      const bool whole = (d.flags & kSeqStart) && (d.flags & kSeqEnd);
+      if (r == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float inv = lt[g] > 0.f ? 1.f / lt[g] : 0.f;
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) o[g][e] *= inv;
+          const int hq = (d.hg * HG + hk) * GF + qg * G + g;
+          if (whole) {
+            RowVec<T, VEC>::store(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + lir * VEC, o[g]);
+          } else {
+            const int64_t slot = c + int64_t(d.hg) * S + d.s;
+            const int64_t hrow = slot * (HG * GF) + hk * GF + qg * G + g;
+            float* dst = p.ws_o + hrow * D + lir * VEC;
+#pragma unroll
+            for (int e = 0; e < VEC; e += 4)
+              *reinterpret_cast<float4*>(dst + e) = make_float4(o[g][e], o[g][e + 1], o[g][e + 2], o[g][e + 3]);
+            if (lir == 0) p.ws_lse[hrow] = (lt[g] > 0.f) ? mt[g] + __log2f(lt[g]) : -INFINITY;
+          }
+        }
+      }
+      if (pair == 0 && lane == 0) {
+        const int64_t v = int64_t(d.hg) * S + d.s;
+        if (d.flags & kSeqStart) {
+          p.ws_meta[v].x = int(c);
+          p.ws_meta[v].z = units_per_hg;
+        }
+        if (d.flags & kSeqEnd) p.ws_meta[v].y = int(c);
+      }
+    } else {
+      named_bar_sync(1 + pair, 64);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- merge of the pieces
+template <typename T, int D>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant__ DecodeParams p, int group) {
+  const int S = p.num_seqs;
+  const int v = blockIdx.x;
+  const int s = v % S, hg = v / S;
+  const int q_len = __ldg(p.qsl + s + 1) - __ldg(p.qsl + s);
+  if (q_len != 1) return;
+  const int L = decode_len(p, s);
+  const int HGG = p.hg_size * group;
+  const int qrow = __ldg(p.qsl + s);
+  T* out = reinterpret_cast<T*>(p.out);
+  const int D4 = D / 4;
+  if (L == 0) {  // no keys: a query without context gets zeros
+    if (threadIdx.x == 0) raise_error(p.err, PA_DEVERR_SEQ_RANGE);
+    for (int i = threadIdx.x; i < HGG * D4; i += blockDim.x) {
+      const int hq = hg * HGG + i / D4;
+      const float z[4] = {0.f, 0.f, 0.f, 0.f};
+      RowVec<T, 4>::store(out + (int64_t(qrow) * p.num_heads + hq) * D + (i % D4) * 4, z);
+    }
+    return;
+  }
+  const int4 meta = p.ws_meta[v];
+  if (meta.x == meta.y) return;  // one CTA covered the request and wrote `out` itself
+  // CTAs whose range is empty (fewer units than CTAs) left no piece: skip them.
+  const int64_t U = int64_t(meta.z) * p.num_hg, C = p.num_ctas;
+  for (int i = threadIdx.x; i < HGG * D4; i += blockDim.x) {
+    const int head = i / D4, d4 = i % D4;
+    float M = -INFINITY;
+    for (int cc = meta.x; cc <= meta.y; ++cc) {
+      if (cc * U / C == (cc + 1) * U / C) continue;
+      M = fmaxf(M, p.ws_lse[(int64_t(cc) + v) * HGG + head]);
+    }
+    const float Ms = (M == -INFINITY) ? 0.f : M;
+    float a[4] = {0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
+    for (int cc = meta.x; cc <= meta.y; ++cc) {
+      if (cc * U / C == (cc + 1) * U / C) continue;
+      const int64_t hrow = (int64_t(cc) + v) * HGG + head;
+      const float w = exp2f(p.ws_lse[hrow] - Ms);
+      const float4 o = *reinterpret_cast<const float4*>(p.ws_o + hrow * D + d4 * 4);
+      a[0] += w * o.x;
+      a[1] += w * o.y;
+      a[2] += w * o.z;
+      a[3] += w * o.w;
+      wsum += w;
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) a[e] *= inv;
+    const int hq = hg * HGG + head;
+    RowVec<T, 4>::store(out + (int64_t(qrow) * p.num_heads + hq) * D + d4 * 4, a);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+// GW = query heads per warp (<= 4), QG = G / GW warp pairs per KV head, HG = KV heads per
+// CTA: the largest power of two dividing num_kv_heads with HG * QG <= 8 warp pairs whose
+// stages fit in shared memory.
+template <typename T, int D, int GW>
+int pick_hg(int num_kv_heads, int qg) {
+  for (int hg = 8; hg >= 1; hg >>= 1)
+    if (num_kv_heads % hg == 0 && hg * qg <= 8 && Smem<T, D, GW>::total(hg, hg * qg) <= size_t(kSmemLimit))
+      return hg;
+  return 0;
+}
+
+int gw_of(int G) { return G < 4 ? G : 4; }
+
+int hg_for(pa_dtype dt, int D, int G, int num_kv_heads) {
+  const int GW = gw_of(G), QG = G / GW;
+#define PA_HG_CASE(TT, DD, WW) \
+  if (D == DD && GW == WW) return pick_hg<TT, DD, WW>(num_kv_heads, QG);
+  if (dt == PA_BF16) {
+    PA_HG_CASE(__nv_bfloat16, 64, 1) PA_HG_CASE(__nv_bfloat16, 64, 2) PA_HG_CASE(__nv_bfloat16, 64, 4)
+    PA_HG_CASE(__nv_bfloat16, 128, 1) PA_HG_CASE(__nv_bfloat16, 128, 2) PA_HG_CASE(__nv_bfloat16, 128, 4)
+  } else {
+    PA_HG_CASE(float, 64, 1) PA_HG_CASE(float, 64, 2) PA_HG_CASE(float, 64, 4)
+    PA_HG_CASE(float, 128, 1) PA_HG_CASE(float, 128, 2) PA_HG_CASE(float, 128, 4)
+  }
+#undef PA_HG_CASE
+  return 0;
+}
+
+template <typename T, int D, int GW>
+cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
+  using SM = Smem<T, D, GW>;
+  const int G = a.num_heads / a.num_kv_heads;
+  const int QG = G / GW;
+  const int hg = pick_hg<T, D, GW>(a.num_kv_heads, QG);
+  if (hg == 0) return cudaErrorInvalidValue;
+  DecodeParams p;
+  p.out = a.out;
+  p.q = a.q;
+  p.k_cache = static_cast<const char*>(a.k_cache);
+  p.v_cache = static_cast<const char*>(a.v_cache);
+  p.block_table = a.block_table;
+  p.seq_lens = a.seq_lens;
+  p.qsl = a.query_start_loc;
+  const int num_hg = a.num_kv_heads / hg;
+  const int64_t slots = int64_t(num_ctas) + int64_t(a.num_seqs) * num_hg;
+  const int64_t HGG = int64_t(hg) * G;
+  char* ws = static_cast<char*>(a.workspace);
+  p.ws_o = reinterpret_cast<float*>(ws);
+  p.ws_lse = reinterpret_cast<float*>(ws + slots * HGG * D * 4);
+  p.ws_meta = reinterpret_cast<int4*>(ws + slots * HGG * D * 4 + ((slots * HGG * 4 + 15) / 16) * 16);
+  p.err = a.err;
+  p.num_blocks = a.num_blocks;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_seqs = a.num_seqs;
+  p.num_heads = a.num_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.block_size = a.block_size;
+  p.hg_size = hg;
+  p.num_hg = num_hg;
+  p.group = G;
+  p.qg = QG;
+  p.num_ctas = num_ctas;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  const int pairs = hg * QG;
+  const size_t smem = SM::total(hg, pairs);
+  auto kern = decode_splitk_kernel<T, D, GW>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<num_ctas, (2 * pairs + 1) * 32, smem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_merge_kernel<T, D><<<unsigned(int64_t(a.num_seqs) * num_hg), 256, 0, stream>>>(p, G);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t run_g(const AttnArgs& a, int G, int num_ctas, cudaStream_t stream) {
+  switch (gw_of(G)) {
+    case 1: return run<T, D, 1>(a, num_ctas, stream);
+    case 2: return run<T, D, 2>(a, num_ctas, stream);
+    case 4: return run<T, D, 4>(a, num_ctas, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool decode_supported(pa_dtype dtype, int head_dim, int group) {
+  if (head_dim != 64 && head_dim != 128) return false;
+  if (group != 1 && group != 2 && group != 4 && group != 8) return false;
+  return dtype == PA_F32 || dtype == PA_BF16;
+}
+
+int decode_num_ctas(int device, cudaError_t* err) {
+  int sms = 0;
+  *err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  return sms;
+}
+
+size_t decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                              int num_ctas, pa_dtype dtype) {
+  const int G = num_heads / num_kv_heads;
+  const int hg = hg_for(dtype, head_dim, G, num_kv_heads);
+  if (hg == 0) return 0;
+  const int num_hg = num_kv_heads / hg;
+  const int64_t slots = int64_t(num_ctas) + int64_t(num_seqs) * num_hg;
+  const int64_t HGG = int64_t(hg) * G;
+  const int64_t o_bytes = slots * HGG * head_dim * 4;
+  const int64_t lse_bytes = ((slots * HGG * 4 + 15) / 16) * 16;
+  const int64_t meta_bytes = int64_t(num_seqs) * num_hg * 16;
+  return size_t(o_bytes + lse_bytes + meta_bytes);
+}
+
+cudaError_t launch_decode(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
+  const int G = a.num_heads / a.num_kv_heads;
+  if (a.num_seqs == 0) return cudaSuccess;
+  if (a.dtype == PA_BF16) {
+    if (a.head_dim == 64) return run_g<__nv_bfloat16, 64>(a, G, num_ctas, stream);
+    return run_g<__nv_bfloat16, 128>(a, G, num_ctas, stream);
+  }
+  if (a.head_dim == 64) return run_g<float, 64>(a, G, num_ctas, stream);
+  return run_g<float, 128>(a, G, num_ctas, stream);
+}
+
+}  // namespace pa

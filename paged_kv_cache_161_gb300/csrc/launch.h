@@ -1,0 +1,58 @@
+// Internal launchers behind the C ABI (include/pa.h). Arguments are validated by the
+// caller (api.cpp); these only pick a kernel instantiation and enqueue it.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// Device address of the per-device error word (set up once per device).
+unsigned int* device_error_word(cudaError_t* err);
+
+cudaError_t launch_kv_write(const void* k, const void* v, void* k_cache, void* v_cache,
+                            const int64_t* slot_mapping, int64_t num_tokens, int64_t num_slots,
+                            int64_t row_bytes, unsigned int* err, cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
+                               int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
+                               unsigned int* err, cudaStream_t stream);
+
+struct AttnArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  int max_blocks_per_seq;
+  int num_seqs;
+  int num_tokens;
+  int max_query_len;
+  int num_heads;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int64_t num_blocks;
+  float scale;
+  pa_dtype dtype;
+  void* workspace;
+  unsigned int* err;
+};
+
+// Decode (q_len == 1 requests): workspace bytes needed, and the launch (split-K + merge).
+size_t decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                              int num_ctas, pa_dtype dtype);
+int decode_num_ctas(int device, cudaError_t* err);
+bool decode_supported(pa_dtype dtype, int head_dim, int group);
+cudaError_t launch_decode(const AttnArgs& a, int num_ctas, cudaStream_t stream);
+
+// Prefill (q_len >= 2 requests).
+bool prefill_supported(pa_dtype dtype, int head_dim, int group);
+cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream);
+
+}  // namespace pa

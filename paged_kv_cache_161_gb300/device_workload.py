@@ -1,0 +1,148 @@
+"""Execute a seeded workload on the GPU through the C ABI.
+
+The block manager is the library's C++ one (pa_bm_*), the copies, writes and attention
+are its kernels; this module only moves the generator's values to the device and hands
+the library's outputs from one call to the next. A phase runs as the workload script
+defines: block-manager operations, then pa_copy_blocks of the emitted pairs, then
+pa_kv_write of the appended tokens, then (for the step) pa_attention over the batch.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import BlockManager, attention, attention_workspace_size, copy_blocks, kv_write
+
+
+def storage_to_torch(a: np.ndarray) -> torch.Tensor:
+    """float32 arrays stay float32; uint16 arrays hold bfloat16 bit patterns."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a))
+
+
+def torch_to_storage(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+@dataclass
+class StepInputs:
+    """Device tensors of one timed step (write + copies + attention)."""
+    slot_mapping: torch.Tensor
+    k_new: torch.Tensor
+    v_new: torch.Tensor
+    block_mapping: torch.Tensor
+    q: torch.Tensor
+    out: torch.Tensor
+    block_table: torch.Tensor
+    seq_lens: torch.Tensor
+    query_start_loc: torch.Tensor
+    max_query_len: int
+    max_seq_len: int
+    workspace: torch.Tensor
+
+
+class DeviceWorkload:
+    def __init__(self, wl, device="cuda", table_width: int | None = None):
+        self.wl = wl
+        sp = wl.spec
+        self.device = torch.device(device)
+        self.bm = BlockManager(wl.num_blocks, sp.block_size, wl.free_order)
+        self.dtype = torch.float32 if sp.dtype == "f32" else torch.bfloat16
+        shape = (wl.num_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
+        self.k_cache = torch.zeros(shape, dtype=self.dtype, device=self.device)
+        self.v_cache = torch.zeros(shape, dtype=self.dtype, device=self.device)
+        self.lens: dict = {}
+        self.table_width = table_width
+        self.phase_slots: list = []
+        self.phase_copies: list = []
+
+    # -- block manager side ------------------------------------------------------
+    def _ops(self, phase):
+        slots = []
+        for op in phase.ops:
+            if op[0] == "add":
+                self.bm.add_seq(op[1])
+            elif op[0] == "fork":
+                self.bm.fork(op[1], op[2])
+            elif op[0] == "append":
+                slots.append(self.bm.append(op[1], op[2]))
+        slots = np.concatenate(slots) if slots else np.zeros(0, np.int64)
+        copies = self.bm.take_copies()
+        self.phase_slots.append(slots)
+        self.phase_copies.append(copies)
+        return slots, copies
+
+    def _values(self, phase):
+        apps = self.wl.appends(phase, self.lens)
+        if not apps:
+            sp = self.wl.spec
+            z = torch.zeros((0, sp.num_kv_heads, sp.head_dim), dtype=self.dtype)
+            return z, z
+        vals = self.wl.kv_many(apps)
+        k = np.concatenate([kv[0] for kv in vals])
+        v = np.concatenate([kv[1] for kv in vals])
+        return storage_to_torch(k), storage_to_torch(v)
+
+    # -- phases --------------------------------------------------------------------
+    def run_setup(self):
+        """All untimed phases: operations, copies, writes."""
+        for ph in self.wl.setup:
+            slots, copies = self._ops(ph)
+            k, v = self._values(ph)
+            if len(copies):
+                copy_blocks(self.k_cache, self.v_cache, torch.from_numpy(copies).to(self.device))
+            if len(slots):
+                kv_write(k.to(self.device), v.to(self.device), self.k_cache, self.v_cache,
+                         torch.from_numpy(slots).to(self.device))
+
+    def prepare_step(self) -> StepInputs:
+        """Run the step's block-manager operations and stage its inputs on the device."""
+        wl = self.wl
+        sp = wl.spec
+        slots, copies = self._ops(wl.step)
+        k, v = self._values(wl.step)
+        batch = wl.step.batch or []
+        seqs = [s for s, _ in batch]
+        nblk = [int(np.ceil(self.bm.seq_len(s) / sp.block_size)) for s in seqs]
+        width = self.table_width or max(nblk + [1])
+        table, lens = self.bm.batch_tables(seqs, width)
+        qranges = wl.step_queries()
+        q = np.concatenate([wl.q(s, a, n) for s, a, n in qranges]) if qranges else \
+            np.zeros((0, sp.num_heads, sp.head_dim), np.float32 if sp.dtype == "f32" else np.uint16)
+        qsl = np.zeros(len(batch) + 1, np.int32)
+        qsl[1:] = np.cumsum([n for _, n in batch])
+        dev = self.device
+        qt = storage_to_torch(q).to(dev)
+        ws = torch.empty(attention_workspace_size(len(batch), sp.num_heads, sp.num_kv_heads, sp.head_dim),
+                         dtype=torch.uint8, device=dev)
+        return StepInputs(
+            slot_mapping=torch.from_numpy(slots).to(dev),
+            k_new=k.to(dev), v_new=v.to(dev),
+            block_mapping=torch.from_numpy(copies.reshape(-1, 2)).to(dev),
+            q=qt, out=torch.empty_like(qt),
+            block_table=torch.from_numpy(table).to(dev),
+            seq_lens=torch.from_numpy(lens).to(dev),
+            query_start_loc=torch.from_numpy(qsl).to(dev),
+            max_query_len=int(max([n for _, n in batch] + [0])),
+            max_seq_len=int(lens.max()) if len(lens) else 0,
+            workspace=ws,
+        )
+
+    def run_step(self, st: StepInputs, stream=None):
+        """The hot path of one step: copies, write, attention (all on the device)."""
+        sp = self.wl.spec
+        if st.block_mapping.shape[0]:
+            copy_blocks(self.k_cache, self.v_cache, st.block_mapping, stream=stream)
+        if st.slot_mapping.shape[0]:
+            kv_write(st.k_new, st.v_new, self.k_cache, self.v_cache, st.slot_mapping, stream=stream)
+        if st.q.shape[0]:
+            attention(st.out, st.q, self.k_cache, self.v_cache, st.block_table, st.seq_lens,
+                      st.query_start_loc, max_query_len=st.max_query_len, max_seq_len=st.max_seq_len,
+                      scale=sp.scale, workspace=st.workspace, stream=stream)
+        return st.out
