@@ -154,6 +154,7 @@ int pa_attention(void* out, const void* q, const void* k_cache, const void* v_ca
   if (!pa::decode_supported(dtype, head_dim, G) || !pa::prefill_supported(dtype, head_dim, G))
     return PA_ERR_UNSUPPORTED;
   if (num_seqs > 0x7fffffff / 8) return PA_ERR_INVALID_ARG;
+  if (num_kv_heads > 65535 || (max_query_len + 7) / 8 > 65535) return PA_ERR_UNSUPPORTED;  // prefill grid
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

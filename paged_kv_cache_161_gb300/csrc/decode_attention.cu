@@ -243,7 +243,8 @@ struct Smem {
     return (pbuf_off(hg, pairs) + 2 * pairs * pbuf_floats_per_warp() * 4 + 15) / 16 * 16;
   }
   static __host__ __device__ size_t bar_off(int hg, int pairs) { return desc_off(hg, pairs) + kStages * sizeof(StageDesc); }
-  static __host__ __device__ size_t red_off(int hg, int pairs) { return bar_off(hg, pairs) + 2 * kStages * 8; }
+  // barriers: kStages full, kStages empty, one per consumer warp pair (<= 8)
+  static __host__ __device__ size_t red_off(int hg, int pairs) { return bar_off(hg, pairs) + (2 * kStages + 8) * 8; }
   static __host__ __device__ size_t total(int hg, int pairs) { return red_off(hg, pairs) + 40 * 4; }
 };
 
@@ -264,6 +265,7 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::bar_off(HG, pairs));
   int* red = reinterpret_cast<int*>(smem + SM::red_off(HG, pairs));
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
+  const uint32_t pair0 = smem_u32(bars + 2 * kStages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -298,6 +300,7 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
       mbar_init(full0 + 8 * i, 1);
       mbar_init(empty0 + 8 * i, num_consumers);
     }
+    for (int i = 0; i < pairs; ++i) mbar_init(pair0 + 8 * i, 64);
     fence_mbar_init();
   }
   __syncthreads();
@@ -395,11 +398,15 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
         do {
           if (++s == S) {
             s = 0;
-            ++hg;
+            if (++hg >= p.num_hg) break;  // cannot happen: the plan counted these units
           }
           L = decode_len(p, s);
           units_s = units_of(L);
         } while (units_s == 0);
+        if (hg >= p.num_hg) {
+          raise_error(p.err, PA_DEVERR_TIMEOUT);
+          break;
+        }
       }
     }
     return;
@@ -430,6 +437,15 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
   float2 acc[G][VEC / 2];
   float mrun[G];
   float lpart[NVF];
+  // The two warps of a pair meet on an mbarrier (64 arrivals) with a bounded wait.
+  const uint32_t pbar = pair0 + 8 * pair;
+  uint32_t pphase = 0;
+  auto pair_sync = [&]() -> bool {
+    mbar_arrive(pbar);
+    const bool ok = mbar_wait(pbar, pphase);
+    pphase ^= 1;
+    return ok;
+  };
 
   int stage = 0;
   uint32_t phase = 0;
@@ -611,7 +627,10 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
         ml[lane] = pick(lh, lane);
       }
     }
-    named_bar_sync(1 + pair, 64);
+    if (!pair_sync()) {
+      raise_error(p.err, PA_DEVERR_TIMEOUT);
+      return;
+    }
     if (half == 0) {
       float o[G][VEC];
       float lt[G], mt[G];
@@ -630,7 +649,10 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
           o[g][2 * e + 1] = acc[g][e].y * a0 + o1.y * a1;
         }
       }
-      named_bar_sync(1 + pair, 64);
+      if (!pair_sync()) {
+        raise_error(p.err, PA_DEVERR_TIMEOUT);
+        return;
+      }
       const bool whole = (d.flags & kSeqStart) && (d.flags & kSeqEnd);
       if (r == 0) {
 #pragma unroll
@@ -660,8 +682,9 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
         }
         if (d.flags & kSeqEnd) p.ws_meta[v].y = int(c);
       }
-    } else {
-      named_bar_sync(1 + pair, 64);
+    } else if (!pair_sync()) {
+      raise_error(p.err, PA_DEVERR_TIMEOUT);
+      return;
     }
   }
 }
@@ -690,6 +713,11 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
   }
   const int4 meta = p.ws_meta[v];
   if (meta.x == meta.y) return;  // one CTA covered the request and wrote `out` itself
+  if (meta.x < 0 || meta.y >= p.num_ctas || meta.x > meta.y || meta.z <= 0) {
+    // only if the split-K kernel gave up early: leave `out` alone, report it
+    if (threadIdx.x == 0) raise_error(p.err, PA_DEVERR_TIMEOUT);
+    return;
+  }
   // CTAs whose range is empty (fewer units than CTAs) left no piece: skip them.
   const int64_t U = int64_t(meta.z) * p.num_hg, C = p.num_ctas;
   for (int i = threadIdx.x; i < HGG * D4; i += blockDim.x) {
