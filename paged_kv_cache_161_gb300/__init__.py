@@ -4,7 +4,7 @@ Names follow the C ABI in include/pa.h (pa_kv_write -> kv_write, ...). The bindi
 checks tensors and marshals pointers, sizes and the current CUDA stream; every step of
 the path runs in the library's kernels. PyTorch provides device memory and streams.
 
-The library is built in-tree by ``python -m paged_kv_cache_161_gb300.build`` (or the
+The library is built in-tree by ``python paged_kv_cache_161_gb300/build.py`` (or the
 repository's ``__graft_entry__.build()``). Importing this package without it raises.
 """
 from __future__ import annotations
@@ -14,7 +14,7 @@ import os
 
 import torch
 
-from .build import LIB_PATH
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libpa_gb300.so")
 
 __all__ = [
     "PAError",
@@ -33,7 +33,7 @@ PA_DEVERR = {"slot_range": 0x1, "block_range": 0x2, "seq_range": 0x4, "timeout":
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m paged_kv_cache_161_gb300.build` "
+        f"{LIB_PATH} is missing: build it with `python paged_kv_cache_161_gb300/build.py` "
         "(there is no fallback path)")
 
 lib = ctypes.CDLL(LIB_PATH)

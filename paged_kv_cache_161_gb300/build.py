@@ -1,6 +1,8 @@
 """Build the C-ABI shared library libpa_gb300.so in-tree (sm_103a only).
 
-    python -m paged_kv_cache_161_gb300.build [--force] [--verbose]
+    python paged_kv_cache_161_gb300/build.py [--force] [--verbose] [--ptxas]
+
+(run as a script: importing the package itself requires the built library)
 
 Each CUDA translation unit is compiled by nvcc in parallel, the host units by g++, and
 nvcc links them with the static CUDA runtime, so the library needs only the driver at
