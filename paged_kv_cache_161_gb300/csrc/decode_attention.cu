@@ -22,17 +22,18 @@
 //    when the CTA covers all KV heads (the block's rows are contiguous), one per token
 //    row otherwise. A 3-deep ring of stages with full/empty mbarriers keeps two stages
 //    in flight while one is consumed. Every wait is bounded (common.cuh).
-//  * Two consumer warps per KV head split each stage's 16 tokens 8/8. A lane owns VEC
-//    consecutive dims of a row; q of the head's G query heads sits in registers (fp32,
-//    pre-scaled by scale * log2 e). Dot products are packed fp32 FMAs; the per-lane
-//    partial dots of (token, head) pairs are summed across the row's lanes by a
-//    halving butterfly (each step trades half the values with the partner lane), so a
-//    lane ends with whole logits of its own (token, head) pairs. Online softmax in
-//    fp32 (exp2 domain) with warp-shuffle max/sum; P goes through a 128-byte shared
-//    buffer to the P.V product, accumulated in fp32 registers.
-//  * At a request's last unit in the CTA the two warps of a head merge their (m, l, O)
-//    through shared memory; the result is written to `out` directly when the CTA
-//    covered the whole request, else to the workspace as (O / l, m + log2 l).
+//  * One consumer warp per KV head (two when it has 8 query heads) takes all 16 tokens
+//    of a stage. A lane owns one 16-byte vector of a row (8 bf16 / 4 fp32 dims); q of
+//    the warp's query heads sits in registers (fp32, pre-scaled by scale * log2 e). Dot
+//    products are packed fp32 FMAs; the per-lane partial dots of (token, head) pairs are
+//    summed across the row's lanes by a halving butterfly in which each lane's register
+//    slots are pre-permuted by its lane bits, so every step is one shuffle and one add
+//    (no selects) and a lane ends with whole logits of its own pairs. Online softmax in
+//    fp32 (exp2 domain) with warp-shuffle max/sum; P goes through a small shared buffer
+//    to the P.V product, accumulated in fp32 registers.
+//  * At a request's last unit in the CTA the warp writes its heads' result to `out`
+//    directly when the CTA covered the whole request, else to the workspace as
+//    (O / l, m + log2 l).
 #include <float.h>
 
 #include "common.cuh"
@@ -72,7 +73,7 @@ struct DecodeParams {
   int hg_size;  // KV heads per CTA (HG)
   int num_hg;   // num_kv_heads / HG
   int group;    // query heads per KV head
-  int qg;       // warp pairs per KV head = group / (query heads per warp)
+  int qg;       // consumer warps per KV head = group / (query heads per warp)
   int num_ctas; // grid of the split-K kernel
   float scale_log2;
 };
@@ -202,22 +203,22 @@ __device__ __forceinline__ float pick(const float (&a)[G], int g) {
 }
 
 // ---------------------------------------------------------------- compile-time layout
-// G here is the number of query heads one warp serves (at most 4; a KV head with more
-// query heads is split across several warp pairs).
+// G here is the number of query heads one warp serves (at most 4; a KV head with 8 query
+// heads is served by two warps). One warp covers all 16 tokens of a stage for its heads.
 template <typename T, int D, int G>
 struct Cfg {
   static constexpr int EL = sizeof(T);
-  static constexpr int VEC = 4;  // dims per lane: q and O take 4 * G registers each
+  static constexpr int VEC = 16 / EL;  // dims per lane: one 16-byte vector of a row
   static constexpr int LPR = D / VEC;  // lanes per token row
   static_assert(LPR >= 1 && LPR <= 32 && (32 % LPR) == 0, "row must map onto a warp");
   static constexpr int RPI = 32 / LPR;  // token rows per warp instruction
-  static constexpr int TPW = kTPS / 2;  // tokens per warp per stage
-  static_assert(TPW % RPI == 0, "tokens per warp must fill whole row groups");
-  static constexpr int TPL = TPW / RPI;  // tokens per lane per stage
-  static constexpr int NV = TPL * G;     // partial dots per lane before the reduction
+  static_assert(kTPS % RPI == 0, "a stage must fill whole row groups");
+  static constexpr int TPL = kTPS / RPI;  // tokens per lane per stage
+  static constexpr int NV = TPL * G;      // partial dots per lane before the reduction
   static constexpr int LOG_LPR = LPR == 1 ? 0 : LPR == 2 ? 1 : LPR == 4 ? 2 : LPR == 8 ? 3 : LPR == 16 ? 4 : 5;
-  static constexpr int LOG_NV = NV == 1 ? 0 : NV == 2 ? 1 : NV == 4 ? 2 : NV == 8 ? 3 : NV == 16 ? 4 : NV == 32 ? 5 : 6;
+  static constexpr int LOG_NV = NV == 1 ? 0 : NV == 2 ? 1 : NV == 4 ? 2 : NV == 8 ? 3 : NV == 16 ? 4 : NV == 32 ? 5 : NV == 64 ? 6 : 7;
   static_assert((1 << LOG_NV) == NV, "NV must be a power of two");
+  static constexpr int LOG_G = G == 1 ? 0 : G == 2 ? 1 : 2;
   static constexpr int NVF = NV > LPR ? NV / LPR : 1;  // whole logits per lane after it
   // Low lane bits that hold duplicates after the reduction (NV < LPR).
   static constexpr int SH = LOG_LPR > LOG_NV ? LOG_LPR - LOG_NV : 0;
@@ -230,42 +231,38 @@ struct Cfg {
 template <typename T, int D, int G>
 struct Smem {
   using C = Cfg<T, D, G>;
-  // Byte offsets inside the dynamic shared memory of one CTA with HG KV heads.
+  // Byte offsets inside the dynamic shared memory of one CTA with HG KV heads served by
+  // `warps` consumer warps.
   static __host__ __device__ size_t stage_bytes(int hg) { return size_t(kTPS) * hg * D * C::EL; }
   static __host__ __device__ size_t k_off(int) { return 0; }
   static __host__ __device__ size_t v_off(int hg) { return kStages * stage_bytes(hg); }
-  // `pairs` = consumer warp pairs = HG * (query heads per KV head / G)
-  static __host__ __device__ size_t merge_off(int hg) { return 2 * kStages * stage_bytes(hg); }
-  static __host__ __device__ size_t merge_bytes_per_pair() { return size_t(G) * D * 4 + 2 * G * 4; }
-  static __host__ __device__ size_t pbuf_off(int hg, int pairs) { return merge_off(hg) + pairs * merge_bytes_per_pair(); }
+  static __host__ __device__ size_t pbuf_off(int hg) { return 2 * kStages * stage_bytes(hg); }
   static __host__ __device__ size_t pbuf_floats_per_warp() { return size_t(C::RPI) * C::NV; }
-  static __host__ __device__ size_t desc_off(int hg, int pairs) {
-    return (pbuf_off(hg, pairs) + 2 * pairs * pbuf_floats_per_warp() * 4 + 15) / 16 * 16;
+  static __host__ __device__ size_t desc_off(int hg, int warps) {
+    return (pbuf_off(hg) + warps * pbuf_floats_per_warp() * 4 + 15) / 16 * 16;
   }
-  static __host__ __device__ size_t bar_off(int hg, int pairs) { return desc_off(hg, pairs) + kStages * sizeof(StageDesc); }
-  // barriers: kStages full, kStages empty, one per consumer warp pair (<= 8)
-  static __host__ __device__ size_t red_off(int hg, int pairs) { return bar_off(hg, pairs) + (2 * kStages + 8) * 8; }
-  static __host__ __device__ size_t total(int hg, int pairs) { return red_off(hg, pairs) + 40 * 4; }
+  static __host__ __device__ size_t bar_off(int hg, int warps) { return desc_off(hg, warps) + kStages * sizeof(StageDesc); }
+  // barriers: kStages full, kStages empty
+  static __host__ __device__ size_t red_off(int hg, int warps) { return bar_off(hg, warps) + 2 * kStages * 8; }
+  static __host__ __device__ size_t total(int hg, int warps) { return red_off(hg, warps) + 40 * 4; }
 };
 
 // ---------------------------------------------------------------- the split-K kernel
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_constant__ DecodeParams p) {
   using C = Cfg<T, D, G>;
   using SM = Smem<T, D, G>;
   constexpr int VEC = C::VEC, LPR = C::LPR, RPI = C::RPI, TPL = C::TPL, NV = C::NV, NVF = C::NVF;
-  constexpr int SH = C::SH;
+  constexpr int SH = C::SH, LOG_G = C::LOG_G;
   const int HG = p.hg_size, QG = p.qg, GF = p.group;
   const int S = p.num_seqs;
-  const int pairs = HG * QG;
-  const int num_consumers = 2 * pairs;
+  const int num_consumers = HG * QG;
 
   extern __shared__ __align__(128) unsigned char smem[];
-  StageDesc* desc = reinterpret_cast<StageDesc*>(smem + SM::desc_off(HG, pairs));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::bar_off(HG, pairs));
-  int* red = reinterpret_cast<int*>(smem + SM::red_off(HG, pairs));
+  StageDesc* desc = reinterpret_cast<StageDesc*>(smem + SM::desc_off(HG, num_consumers));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::bar_off(HG, num_consumers));
+  int* red = reinterpret_cast<int*>(smem + SM::red_off(HG, num_consumers));
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
-  const uint32_t pair0 = smem_u32(bars + 2 * kStages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -300,7 +297,6 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
       mbar_init(full0 + 8 * i, 1);
       mbar_init(empty0 + 8 * i, num_consumers);
     }
-    for (int i = 0; i < pairs; ++i) mbar_init(pair0 + 8 * i, 64);
     fence_mbar_init();
   }
   __syncthreads();
@@ -413,17 +409,26 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
   }
 
   // =========================== consumer warps ===========================
-  const int pair = warp >> 1, half = warp & 1;
-  const int hk = pair / QG, qg = pair % QG;
+  // warp -> (KV head hk within the CTA's group, query-head group qg); lane -> (row group
+  // r, lane-in-row lir owning dims [lir * VEC, lir * VEC + VEC)).
+  const int hk = warp / QG, qg = warp % QG;
   const int lir = lane & (LPR - 1), r = lane / LPR;
   const int Hq = p.num_heads;
-  float* pbuf = reinterpret_cast<float*>(smem + SM::pbuf_off(HG, pairs)) + warp * SM::pbuf_floats_per_warp();
-  float* merge = reinterpret_cast<float*>(smem + SM::merge_off(HG) + pair * SM::merge_bytes_per_pair());
+  float* pbuf = reinterpret_cast<float*>(smem + SM::pbuf_off(HG)) + warp * SM::pbuf_floats_per_warp();
   const T* kbase = reinterpret_cast<const T*>(smem + SM::k_off(HG));
   const T* vbase = reinterpret_cast<const T*>(smem + SM::v_off(HG));
   const size_t stage_elems = sbytes / C::EL;
 
-  // value i of this lane after the reduction: index = (lir >> SH) * NVF + i = ti * G + g
+  // Butterfly without selects: slot s of this lane holds the partial dot of value
+  // (s ^ P), value = token * G + head, where P collects the lane bits the halving steps
+  // test. Each step then keeps the low half of the slots and adds the partner's high half.
+  int P = 0;
+#pragma unroll
+  for (int k = 1; k <= C::LOG_LPR; ++k)
+    if ((NV >> k) >= 1 && (lir & (LPR >> k))) P |= (NV >> k);
+  const int Pt = P >> LOG_G;        // token part of the permutation
+  const int Pg = P & (G - 1);       // head part
+  // After the reduction slot i (< NVF) holds value (lir >> SH) * NVF + i.
   int my_g[NVF], my_ti[NVF];
 #pragma unroll
   for (int i = 0; i < NVF; ++i) {
@@ -433,19 +438,13 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
   }
   const bool p_writer = (lir & ((1 << SH) - 1)) == 0;
 
-  float2 qf[G][VEC / 2];
-  float2 acc[G][VEC / 2];
+  float2 qf[G][VEC / 2];   // q of head (g ^ Pg), scaled to the log2 domain
+  float2 acc[G][VEC / 2];  // unnormalised O of head g, this lane's dims, this row group
   float mrun[G];
   float lpart[NVF];
-  // The two warps of a pair meet on an mbarrier (64 arrivals) with a bounded wait.
-  const uint32_t pbar = pair0 + 8 * pair;
-  uint32_t pphase = 0;
-  auto pair_sync = [&]() -> bool {
-    mbar_arrive(pbar);
-    const bool ok = mbar_wait(pbar, pphase);
-    pphase ^= 1;
-    return ok;
-  };
+  const T* kw = kbase + hk * D + lir * VEC;  // this lane's column in every K / V row
+  const T* vw = vbase + hk * D + lir * VEC;
+  const int row_stride = HG * D;
 
   int stage = 0;
   uint32_t phase = 0;
@@ -457,11 +456,12 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
     const StageDesc d = desc[stage];
     if (d.flags & kFirst) {
       const int qrow = __ldg(p.qsl + d.s);
+      const T* qb = reinterpret_cast<const T*>(p.q) + (int64_t(qrow) * Hq + (d.hg * HG + hk) * GF + qg * G) * D +
+                    lir * VEC;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const int hq = (d.hg * HG + hk) * GF + qg * G + g;
         float f[VEC];
-        RowVec<T, VEC>::load(reinterpret_cast<const T*>(p.q) + (int64_t(qrow) * Hq + hq) * D + lir * VEC, f);
+        RowVec<T, VEC>::load(qb + (g ^ Pg) * D, f);
 #pragma unroll
         for (int e = 0; e < VEC / 2; ++e) {
           qf[g][e] = make_float2(f[2 * e] * p.scale_log2, f[2 * e + 1] * p.scale_log2);
@@ -473,50 +473,40 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
       for (int i = 0; i < NVF; ++i) lpart[i] = 0.f;
     }
     const int valid = (d.flags & kBad) ? 0 : d.valid;
+    const T* ks = kw + stage * stage_elems;
 
-    // ---- S = q . K for this warp's 8 tokens
-    const T* ks = kbase + stage * stage_elems;
+    // ---- S = q . K: slot (tj, gj) holds token r + RPI * (tj ^ Pt), head gj ^ Pg
     float sv[NV];
 #pragma unroll
-    for (int ti = 0; ti < TPL; ++ti) {
-      const int t = half * C::TPW + r + RPI * ti;
+    for (int tj = 0; tj < TPL; ++tj) {
+      const int t = r + RPI * (tj ^ Pt);
       float kf[VEC];
-      RowVec<T, VEC>::load(ks + (size_t(t) * HG + hk) * D + lir * VEC, kf);
+      RowVec<T, VEC>::load(ks + t * row_stride, kf);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float2 a = make_float2(0.f, 0.f);
 #pragma unroll
         for (int e = 0; e < VEC / 2; ++e) ffma2(a, qf[g][e], make_float2(kf[2 * e], kf[2 * e + 1]));
-        sv[ti * G + g] = a.x + a.y;
+        sv[tj * G + g] = a.x + a.y;
       }
     }
-    // ---- halving butterfly across the row's lanes: lane keeps whole dots of its pairs
-    {
-      int cur = NV;
+    // ---- butterfly across the row's lanes
 #pragma unroll
-      for (int m = LPR / 2; m >= 1; m >>= 1) {
-        if (cur > 1) {
-          const int h = cur / 2;
-          const bool up = (lir & m) != 0;
+    for (int k = 1; k <= C::LOG_LPR; ++k) {
+      const int m = LPR >> k;
+      if ((NV >> k) >= 1) {
 #pragma unroll
-          for (int i = 0; i < NV / 2; ++i) {
-            if (i < h) {
-              const float send = up ? sv[i] : sv[i + h];
-              const float keep = up ? sv[i + h] : sv[i];
-              sv[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-            }
-          }
-          cur = h;
-        } else {
-          sv[0] += __shfl_xor_sync(0xffffffffu, sv[0], m);
-        }
+        for (int i = 0; i < NV / 2; ++i)
+          if (i < (NV >> k)) sv[i] += __shfl_xor_sync(0xffffffffu, sv[i + (NV >> k)], m);
+      } else {
+        sv[0] += __shfl_xor_sync(0xffffffffu, sv[0], m);
       }
     }
     // ---- online softmax (log2 domain)
     float x[NVF], bm[NVF];
 #pragma unroll
     for (int i = 0; i < NVF; ++i) {
-      const int t = half * C::TPW + r + RPI * my_ti[i];
+      const int t = r + RPI * my_ti[i];
       x[i] = (t < valid) ? sv[i] : -INFINITY;
       bm[i] = x[i];
     }
@@ -558,14 +548,14 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
     for (int g = 0; g < G; ++g) mrun[g] = mnew[g];
     __syncwarp();
 
-    // ---- O += P . V
-    const T* vs = vbase + stage * stage_elems;
+    // ---- O += P . V over this lane's tokens r + RPI * ti
+    const T* vs = vw + stage * stage_elems;
+    if (valid == kTPS) {
 #pragma unroll
-    for (int ti = 0; ti < TPL; ++ti) {
-      const int t = half * C::TPW + r + RPI * ti;
-      if (t < valid) {
+      for (int ti = 0; ti < TPL; ++ti) {
+        const int t = r + RPI * ti;
         float vf[VEC];
-        RowVec<T, VEC>::load(vs + (size_t(t) * HG + hk) * D + lir * VEC, vf);
+        RowVec<T, VEC>::load(vs + t * row_stride, vf);
         float pw[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) pw[g] = pbuf[r * NV + ti * G + g];
@@ -574,6 +564,23 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
 #pragma unroll
           for (int e = 0; e < VEC / 2; ++e)
             ffma2(acc[g][e], make_float2(pw[g], pw[g]), make_float2(vf[2 * e], vf[2 * e + 1]));
+      }
+    } else {
+#pragma unroll
+      for (int ti = 0; ti < TPL; ++ti) {
+        const int t = r + RPI * ti;
+        if (t < valid) {  // rows past the request's end hold stale data: skip, never multiply
+          float vf[VEC];
+          RowVec<T, VEC>::load(vs + t * row_stride, vf);
+          float pw[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) pw[g] = pbuf[r * NV + ti * G + g];
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < VEC / 2; ++e)
+              ffma2(acc[g][e], make_float2(pw[g], pw[g]), make_float2(vf[2 * e], vf[2 * e + 1]));
+        }
       }
     }
     __syncwarp();
@@ -586,7 +593,6 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
     if (!(d.flags & kLast)) continue;
 
     // ================= finalize this request's piece =================
-    const int qrow = __ldg(p.qsl + d.s);
     float lsum[NVF];
 #pragma unroll
     for (int i = 0; i < NVF; ++i) lsum[i] = lpart[i];
@@ -610,81 +616,39 @@ __global__ void __launch_bounds__(17 * 32, 1) decode_splitk_kernel(const __grid_
           acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, m);
           acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, m);
         }
-    // the two warps of this KV head meet in shared memory
-    float* mo = merge;               // [G][D]
-    float* mm = merge + G * D;       // [G] m
-    float* ml = merge + G * D + G;   // [G] l
-    if (half == 1) {
-      if (r == 0) {
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-          for (int e = 0; e < VEC / 2; ++e)
-            *reinterpret_cast<float2*>(mo + g * D + lir * VEC + 2 * e) = acc[g][e];
-      }
-      if (lane < G) {
-        mm[lane] = pick(mrun, lane);
-        ml[lane] = pick(lh, lane);
-      }
-    }
-    if (!pair_sync()) {
-      raise_error(p.err, PA_DEVERR_TIMEOUT);
-      return;
-    }
-    if (half == 0) {
-      float o[G][VEC];
-      float lt[G], mt[G];
+    const bool whole = (d.flags & kSeqStart) && (d.flags & kSeqEnd);
+    const int qrow = __ldg(p.qsl + d.s);
+    if (r == 0) {
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float m1 = mm[g], l1 = ml[g];
-        const float M = fmaxf(mrun[g], m1);
-        const float Ms = (M == -INFINITY) ? 0.f : M;
-        const float a0 = exp2f(mrun[g] - Ms), a1 = exp2f(m1 - Ms);
-        lt[g] = lh[g] * a0 + l1 * a1;
-        mt[g] = M;
+        const float inv = lh[g] > 0.f ? 1.f / lh[g] : 0.f;
+        float o[VEC];
 #pragma unroll
         for (int e = 0; e < VEC / 2; ++e) {
-          const float2 o1 = *reinterpret_cast<const float2*>(mo + g * D + lir * VEC + 2 * e);
-          o[g][2 * e] = acc[g][e].x * a0 + o1.x * a1;
-          o[g][2 * e + 1] = acc[g][e].y * a0 + o1.y * a1;
+          o[2 * e] = acc[g][e].x * inv;
+          o[2 * e + 1] = acc[g][e].y * inv;
+        }
+        const int hq = (d.hg * HG + hk) * GF + qg * G + g;
+        if (whole) {
+          RowVec<T, VEC>::store(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + lir * VEC, o);
+        } else {
+          const int64_t slot = c + int64_t(d.hg) * S + d.s;
+          const int64_t hrow = slot * (HG * GF) + hk * GF + qg * G + g;
+          float* dst = p.ws_o + hrow * D + lir * VEC;
+#pragma unroll
+          for (int e = 0; e < VEC; e += 4)
+            *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+          if (lir == 0) p.ws_lse[hrow] = (lh[g] > 0.f) ? mrun[g] + __log2f(lh[g]) : -INFINITY;
         }
       }
-      if (!pair_sync()) {
-        raise_error(p.err, PA_DEVERR_TIMEOUT);
-        return;
+    }
+    if (warp == 0 && lane == 0) {
+      const int64_t v = int64_t(d.hg) * S + d.s;
+      if (d.flags & kSeqStart) {
+        p.ws_meta[v].x = int(c);
+        p.ws_meta[v].z = units_per_hg;
       }
-      const bool whole = (d.flags & kSeqStart) && (d.flags & kSeqEnd);
-      if (r == 0) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float inv = lt[g] > 0.f ? 1.f / lt[g] : 0.f;
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) o[g][e] *= inv;
-          const int hq = (d.hg * HG + hk) * GF + qg * G + g;
-          if (whole) {
-            RowVec<T, VEC>::store(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + lir * VEC, o[g]);
-          } else {
-            const int64_t slot = c + int64_t(d.hg) * S + d.s;
-            const int64_t hrow = slot * (HG * GF) + hk * GF + qg * G + g;
-            float* dst = p.ws_o + hrow * D + lir * VEC;
-#pragma unroll
-            for (int e = 0; e < VEC; e += 4)
-              *reinterpret_cast<float4*>(dst + e) = make_float4(o[g][e], o[g][e + 1], o[g][e + 2], o[g][e + 3]);
-            if (lir == 0) p.ws_lse[hrow] = (lt[g] > 0.f) ? mt[g] + __log2f(lt[g]) : -INFINITY;
-          }
-        }
-      }
-      if (pair == 0 && lane == 0) {
-        const int64_t v = int64_t(d.hg) * S + d.s;
-        if (d.flags & kSeqStart) {
-          p.ws_meta[v].x = int(c);
-          p.ws_meta[v].z = units_per_hg;
-        }
-        if (d.flags & kSeqEnd) p.ws_meta[v].y = int(c);
-      }
-    } else if (!pair_sync()) {
-      raise_error(p.err, PA_DEVERR_TIMEOUT);
-      return;
+      if (d.flags & kSeqEnd) p.ws_meta[v].y = int(c);
     }
   }
 }
@@ -749,9 +713,9 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
 }
 
 // ---------------------------------------------------------------- host side
-// GW = query heads per warp (<= 4), QG = G / GW warp pairs per KV head, HG = KV heads per
-// CTA: the largest power of two dividing num_kv_heads with HG * QG <= 8 warp pairs whose
-// stages fit in shared memory.
+// GW = query heads per warp (<= 4), QG = G / GW consumer warps per KV head, HG = KV heads
+// per CTA: the largest power of two dividing num_kv_heads with HG * QG <= 8 consumer warps
+// whose stages fit in shared memory.
 template <typename T, int D, int GW>
 int pick_hg(int num_kv_heads, int qg) {
   for (int hg = 8; hg >= 1; hg >>= 1)
@@ -812,12 +776,12 @@ cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   p.qg = QG;
   p.num_ctas = num_ctas;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  const int pairs = hg * QG;
-  const size_t smem = SM::total(hg, pairs);
+  const int warps = hg * QG;
+  const size_t smem = SM::total(hg, warps);
   auto kern = decode_splitk_kernel<T, D, GW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  kern<<<num_ctas, (2 * pairs + 1) * 32, smem, stream>>>(p);
+  kern<<<num_ctas, (warps + 1) * 32, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_merge_kernel<T, D><<<unsigned(int64_t(a.num_seqs) * num_hg), 256, 0, stream>>>(p, G);
