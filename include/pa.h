@@ -160,6 +160,35 @@ int pa_attention(void* out, const void* q, const void* k_cache, const void* v_ca
                  pa_dtype dtype, void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------------
+ * pa_attention_fixed_scratch -- no counterpart in the pages: an addition for callers that
+ * cannot allocate device memory, so cannot provide pa_attention's workspace. Examples: a
+ * serving loop that reserved the GPU's free memory for its KV pool at start-up and must not
+ * call cudaMalloc again (the call synchronises the device and fails once the pool owns the
+ * memory); a plugin inside a host framework whose allocator it cannot reach; a binding from
+ * a language with no device allocator.
+ *
+ * Same arguments and result as pa_attention, minus workspace / workspace_bytes. The split-K
+ * scratch is instead a fixed 16 MiB array inside the library, which every GPU that loads
+ * the library holds until the process exits. Allocates nothing (no cudaMalloc / cudaFree,
+ * no allocating library call).
+ *  - Limit: returns PA_ERR_WORKSPACE, enqueuing nothing, when the batch needs more scratch
+ *    than 16 MiB (pa_attention_workspace_size gives the need; e.g. up to ~850 requests of
+ *    32 query / 8 KV heads at head_dim 128 on a 152-SM GPU).
+ *  - The first call on each device looks up the array's device address (once, with that
+ *    device current); make that first call before any stream capture.
+ *  - All calls on a device share the one array, which keeps the last call's contents; no
+ *    part of it needs to start at zero. Calls whose work may overlap on the GPU (different
+ *    streams without ordering between them) race on it and give wrong results: order them.
+ * --------------------------------------------------------------------------- */
+int pa_attention_fixed_scratch(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, int max_blocks_per_seq,
+                               const int32_t* seq_lens, const int32_t* query_start_loc,
+                               int num_seqs, int num_tokens, int max_query_len, int max_seq_len,
+                               int num_heads, int num_kv_heads, int head_dim, int block_size,
+                               int64_t num_blocks, float scale, pa_dtype dtype,
+                               pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------
  * Host block manager -- [docs] PagedAttention algorithm flow and Copy-on-Write
  * (reference counting); [read] 5.1.1 and 5.2.1; [flow] 3.3 (pool of blocks, slots).
  *
