@@ -266,6 +266,12 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // Programmatic dependent launch: inputs may come from the previous kernel in the stream
+  // (e.g. the KV write), so wait for it before reading anything; the merge kernel may be
+  // scheduled now and waits for this grid itself.
+  griddep_wait();
+  griddep_launch_dependents();
+
   // ---- plan: this CTA's range of units [u_begin, u_end) and where it starts
   int my_units = 0;
   for (int s = threadIdx.x; s < S; s += blockDim.x) my_units += units_of(decode_len(p, s));
@@ -654,8 +660,12 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
 }
 
 // ---------------------------------------------------------------- merge of the pieces
+// One CTA per (head group, request); requests one CTA covered whole leave at once. Warp w
+// merges heads w, w + 8, ...: lanes read the pieces' log-sum-exps in parallel for the
+// max, then each lane accumulates its 4 dims over the pieces (float4 loads, independent).
 template <typename T, int D>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant__ DecodeParams p, int group) {
+  griddep_wait();  // the split-K grid's pieces must be complete and visible
   const int S = p.num_seqs;
   const int v = blockIdx.x;
   const int s = v % S, hg = v / S;
@@ -684,31 +694,37 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
   }
   // CTAs whose range is empty (fewer units than CTAs) left no piece: skip them.
   const int64_t U = int64_t(meta.z) * p.num_hg, C = p.num_ctas;
-  for (int i = threadIdx.x; i < HGG * D4; i += blockDim.x) {
-    const int head = i / D4, d4 = i % D4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int npieces = meta.y - meta.x + 1;
+  for (int head = warp; head < HGG; head += nwarps) {
     float M = -INFINITY;
-    for (int cc = meta.x; cc <= meta.y; ++cc) {
-      if (cc * U / C == (cc + 1) * U / C) continue;
-      M = fmaxf(M, p.ws_lse[(int64_t(cc) + v) * HGG + head]);
+    for (int i = lane; i < npieces; i += 32) {
+      const int64_t cc = meta.x + i;
+      if (cc * U / C != (cc + 1) * U / C) M = fmaxf(M, p.ws_lse[(cc + v) * HGG + head]);
     }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
     const float Ms = (M == -INFINITY) ? 0.f : M;
     float a[4] = {0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
-    for (int cc = meta.x; cc <= meta.y; ++cc) {
-      if (cc * U / C == (cc + 1) * U / C) continue;
-      const int64_t hrow = (int64_t(cc) + v) * HGG + head;
-      const float w = exp2f(p.ws_lse[hrow] - Ms);
-      const float4 o = *reinterpret_cast<const float4*>(p.ws_o + hrow * D + d4 * 4);
-      a[0] += w * o.x;
-      a[1] += w * o.y;
-      a[2] += w * o.z;
-      a[3] += w * o.w;
-      wsum += w;
-    }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    if (lane < D4) {
+#pragma unroll 4
+      for (int i = 0; i < npieces; ++i) {
+        const int64_t cc = meta.x + i;
+        if (cc * U / C == (cc + 1) * U / C) continue;
+        const int64_t hrow = (cc + v) * HGG + head;
+        const float w = exp2f(p.ws_lse[hrow] - Ms);
+        const float4 o = *reinterpret_cast<const float4*>(p.ws_o + hrow * D + lane * 4);
+        a[0] += w * o.x;
+        a[1] += w * o.y;
+        a[2] += w * o.z;
+        a[3] += w * o.w;
+        wsum += w;
+      }
+      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) a[e] *= inv;
-    const int hq = hg * HGG + head;
-    RowVec<T, 4>::store(out + (int64_t(qrow) * p.num_heads + hq) * D + d4 * 4, a);
+      for (int e = 0; e < 4; ++e) a[e] *= inv;
+      RowVec<T, 4>::store(out + (int64_t(qrow) * p.num_heads + hg * HGG + head) * D + lane * 4, a);
+    }
   }
 }
 
@@ -781,11 +797,10 @@ cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   auto kern = decode_splitk_kernel<T, D, GW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  kern<<<num_ctas, (warps + 1) * 32, smem, stream>>>(p);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, dim3(num_ctas), dim3((warps + 1) * 32), smem, stream, p);
   if (e != cudaSuccess) return e;
-  decode_merge_kernel<T, D><<<unsigned(int64_t(a.num_seqs) * num_hg), 256, 0, stream>>>(p, G);
-  return cudaGetLastError();
+  return launch_pdl(decode_merge_kernel<T, D>, dim3(unsigned(int64_t(a.num_seqs) * num_hg)), dim3(256), 0, stream,
+                    p, G);
 }
 
 template <typename T, int D>

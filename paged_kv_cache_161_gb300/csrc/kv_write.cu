@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4* __restrict__
                                                        const int64_t* __restrict__ slot_mapping,
                                                        int64_t num_tokens, int64_t num_slots,
                                                        int vec_per_row, unsigned int* err) {
+  griddep_launch_dependents();  // a following attention launch may be scheduled early
   const int64_t per_token = 2 * static_cast<int64_t>(vec_per_row);
   const int64_t total = num_tokens * per_token;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
