@@ -62,7 +62,8 @@ struct DecodeParams {
   const int32_t* qsl;
   float* ws_o;
   float* ws_lse;
-  int4* ws_meta;  // per (head group, request): first CTA, last CTA, units per head group
+  int4* ws_meta;  // per (head group, request): first CTA (-1: nothing to merge), last CTA,
+                  // units per head group, output row
   unsigned int* err;
   int64_t num_blocks;
   int max_blocks_per_seq;
@@ -278,6 +279,20 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
   const int units_per_hg = block_sum(my_units, red);
   const int64_t U = int64_t(units_per_hg) * p.num_hg;
   const int64_t c = blockIdx.x, C_ = gridDim.x;
+  if (c == 0) {
+    // Requests no CTA will touch: tell the merge kernel to skip them (meta.x = -1), and
+    // give a decode query without keys a zero output.
+    for (int s = threadIdx.x; s < S; s += blockDim.x) {
+      if (units_of(decode_len(p, s)) > 0) continue;
+      for (int hg = 0; hg < p.num_hg; ++hg) p.ws_meta[int64_t(hg) * S + s] = make_int4(-1, -1, 0, 0);
+      const int q0 = __ldg(p.qsl + s);
+      if (__ldg(p.qsl + s + 1) - q0 == 1) {
+        raise_error(p.err, PA_DEVERR_SEQ_RANGE);
+        T* o = reinterpret_cast<T*>(p.out) + int64_t(q0) * p.num_heads * D;
+        for (int i = 0; i < p.num_heads * D; ++i) o[i] = T(0.f);
+      }
+    }
+  }
   const int64_t u_begin = c * U / C_, u_end = (c + 1) * U / C_;
   if (u_begin >= u_end) return;
   const int start_hg = int(u_begin / units_per_hg);
@@ -653,6 +668,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
       if (d.flags & kSeqStart) {
         p.ws_meta[v].x = int(c);
         p.ws_meta[v].z = units_per_hg;
+        p.ws_meta[v].w = qrow;
       }
       if (d.flags & kSeqEnd) p.ws_meta[v].y = int(c);
     }
@@ -660,38 +676,27 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
 }
 
 // ---------------------------------------------------------------- merge of the pieces
-// One CTA per (head group, request); requests one CTA covered whole leave at once. Warp w
-// merges heads w, w + 8, ...: lanes read the pieces' log-sum-exps in parallel for the
-// max, then each lane accumulates its 4 dims over the pieces (float4 loads, independent).
+// One CTA per (head group, request). It reads the request's descriptor written by the
+// split-K kernel and leaves at once unless the request was cut into pieces; then warp w
+// merges heads w, w + nwarps, ...: lanes read the pieces' log-sum-exps in parallel for the
+// max, and each lane accumulates its 4 dims over the pieces with independent float4 loads.
 template <typename T, int D>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant__ DecodeParams p, int group) {
-  griddep_wait();  // the split-K grid's pieces must be complete and visible
+__global__ void __launch_bounds__(1024) decode_merge_kernel(const __grid_constant__ DecodeParams p, int group) {
+  griddep_wait();  // the split-K grid's pieces and descriptors must be complete and visible
   const int S = p.num_seqs;
   const int v = blockIdx.x;
-  const int s = v % S, hg = v / S;
-  const int q_len = __ldg(p.qsl + s + 1) - __ldg(p.qsl + s);
-  if (q_len != 1) return;
-  const int L = decode_len(p, s);
-  const int HGG = p.hg_size * group;
-  const int qrow = __ldg(p.qsl + s);
-  T* out = reinterpret_cast<T*>(p.out);
-  const int D4 = D / 4;
-  if (L == 0) {  // no keys: a query without context gets zeros
-    if (threadIdx.x == 0) raise_error(p.err, PA_DEVERR_SEQ_RANGE);
-    for (int i = threadIdx.x; i < HGG * D4; i += blockDim.x) {
-      const int hq = hg * HGG + i / D4;
-      const float z[4] = {0.f, 0.f, 0.f, 0.f};
-      RowVec<T, 4>::store(out + (int64_t(qrow) * p.num_heads + hq) * D + (i % D4) * 4, z);
-    }
-    return;
-  }
+  const int hg = v / S;
   const int4 meta = p.ws_meta[v];
-  if (meta.x == meta.y) return;  // one CTA covered the request and wrote `out` itself
-  if (meta.x < 0 || meta.y >= p.num_ctas || meta.x > meta.y || meta.z <= 0) {
+  if (meta.x < 0 || meta.x == meta.y) return;  // nothing to merge / one CTA wrote `out` itself
+  if (meta.y >= p.num_ctas || meta.x > meta.y || meta.z <= 0) {
     // only if the split-K kernel gave up early: leave `out` alone, report it
     if (threadIdx.x == 0) raise_error(p.err, PA_DEVERR_TIMEOUT);
     return;
   }
+  const int HGG = p.hg_size * group;
+  const int qrow = meta.w;
+  T* out = reinterpret_cast<T*>(p.out);
+  constexpr int D4 = D / 4;
   // CTAs whose range is empty (fewer units than CTAs) left no piece: skip them.
   const int64_t U = int64_t(meta.z) * p.num_hg, C = p.num_ctas;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
@@ -705,8 +710,8 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
     const float Ms = (M == -INFINITY) ? 0.f : M;
-    float a[4] = {0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
     if (lane < D4) {
+      float a[4] = {0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
 #pragma unroll 4
       for (int i = 0; i < npieces; ++i) {
         const int64_t cc = meta.x + i;
@@ -799,8 +804,9 @@ cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_ctas), dim3((warps + 1) * 32), smem, stream, p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_merge_kernel<T, D>, dim3(unsigned(int64_t(a.num_seqs) * num_hg)), dim3(256), 0, stream,
-                    p, G);
+  const int merge_threads = 32 * (HGG < 32 ? int(HGG) : 32);
+  return launch_pdl(decode_merge_kernel<T, D>, dim3(unsigned(int64_t(a.num_seqs) * num_hg)), dim3(merge_threads), 0,
+                    stream, p, G);
 }
 
 template <typename T, int D>
