@@ -190,8 +190,10 @@ int pa_attention(void* out, const void* q, const void* k_cache, const void* v_ca
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   e = pa::launch_decode(a, ctas, s);
   if (e != cudaSuccess) return cuda_fail(e);
-  e = pa::launch_prefill(a, s);
-  if (e != cudaSuccess) return cuda_fail(e);
+  if (max_query_len >= 2) {
+    e = pa::prefill_tc_supported(a) ? pa::launch_prefill_tc(a, ctas, s) : pa::launch_prefill(a, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   return PA_OK;
 }
 

@@ -51,8 +51,11 @@ int decode_num_ctas(int device, cudaError_t* err);
 bool decode_supported(pa_dtype dtype, int head_dim, int group);
 cudaError_t launch_decode(const AttnArgs& a, int num_ctas, cudaStream_t stream);
 
-// Prefill (q_len >= 2 requests).
+// Prefill (q_len >= 2 requests): the tcgen05 tensor-core kernel where it applies (bf16,
+// block size 8..128 dividing 128, <= 4096 requests), else the CUDA-core tile kernel.
 bool prefill_supported(pa_dtype dtype, int head_dim, int group);
 cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream);
+bool prefill_tc_supported(const AttnArgs& a);
+cudaError_t launch_prefill_tc(const AttnArgs& a, int num_ctas, cudaStream_t stream);
 
 }  // namespace pa

@@ -1,0 +1,502 @@
+// Chunked-prefill attention on the tensor cores (tcgen05, TMEM accumulators, TMA).
+//
+// What it computes: vLLM 0.10.0 flow page, 3.2 Scheduler (a long prefill is cut into
+// chunks that run in one batch with decodes; prefill is compute-bound) and 3.5 Attention
+// (requests delimited by query_start_loc, K/V found through block_table); VLLM overview
+// page, 2.1 (causal mask). Query j of a request with q_len queries and L keys sits at
+// position L - q_len + j and sees keys 0..L - q_len + j; its chunk's own K/V are already
+// in the cache (written by pa_kv_write).
+//
+// Tile: 128 rows = (128 / G) query tokens x the G query heads that share one KV head, so
+// each K/V tile feeds all of them. Per 128-key tile: S = Q.K^T (8 x tcgen05.mma
+// 128x128x16, bf16 in, f32 accumulate in TMEM), online softmax in registers (one thread
+// per row, exp2 domain, lazy rescaling of O only when the row max grows by more than
+// 2^8), P as bf16 into 128-byte-swizzled shared memory, O += P.V (8 x tcgen05.mma
+// 128xDx16, V as an MN-major operand), O in TMEM.
+//
+// Roles (192 threads, one CTA per SM, persistent over a static round-robin of tiles):
+//   warps 0-3  softmax + epilogue: thread r owns row r = TMEM lane r;
+//   warp 4     TMA producer: Q tile once per tile, K and V tiles of 128 keys by physical
+//              block through the block table (one 3-D box per block and 64-dim half),
+//              into a 2-deep ring;
+//   warp 5     allocates 512 TMEM columns (S double buffer 2 x 128, O 128) and one
+//              thread issues the MMAs, tracking completion with tcgen05.commit.
+// Every wait is bounded; on a timeout the kernel sets an error bit and leaves after its
+// copies and MMAs in flight have landed, freeing TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tcgen05.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kBM = 128;             // rows per tile
+constexpr int kBN = 128;             // keys per tile
+constexpr int kMaxSeqs = 4096;       // requests per call this kernel accepts
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kHalf = 128 * 128;  // bytes of a 128-row x 64-element bf16 half tile
+
+struct PrefillParams {
+  void* out;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  unsigned int* err;
+  int64_t num_blocks;
+  int max_blocks_per_seq;
+  int num_seqs;
+  int num_heads;
+  int num_kv_heads;
+  int block_size;
+  float scale_log2;
+};
+
+template <int D>
+struct Layout {
+  static constexpr int NH = D / 64;  // 64-element halves of the head dim
+  static constexpr uint32_t Q = 0;
+  static constexpr uint32_t K = Q + NH * kHalf;             // 2 stages
+  static constexpr uint32_t V = K + 2 * NH * kHalf;         // 2 stages
+  static constexpr uint32_t P = V + 2 * NH * kHalf;         // 2 halves of 64 keys
+  static constexpr uint32_t PFX = P + 2 * kHalf;            // int[kMaxSeqs + 1]
+  static constexpr uint32_t BAR = PFX + (kMaxSeqs + 8) * 4;  // mbarriers
+  static constexpr int NBAR = 16;
+  static constexpr uint32_t MISC = BAR + NBAR * 8;           // tmem base, abort flag
+  static constexpr uint32_t BYTES = MISC + 16;
+  static constexpr uint32_t SMEM = BYTES + 1024;             // + alignment slack
+};
+
+// barrier indices
+enum : int {
+  bQFull = 0, bQEmpty, bKVFull0, bKVFull1, bKVEmpty0, bKVEmpty1, bSFull0, bSFull1,
+  bSEmpty0, bSEmpty1, bPFull, bPVDone, bOEmpty, bMmaDone
+};
+
+struct Tile {
+  int s, hk, qs, L, q0, nq, pos0, leff, nt;
+};
+
+// Tile t of the batch: binary search of the per-request tile prefix in shared memory.
+template <int G>
+__device__ __forceinline__ void tile_info(const PrefillParams& p, const int* pfx, int S, int t, Tile& tl) {
+  int lo = 0, hi = S;  // find s with pfx[s] <= t < pfx[s + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pfx[mid] <= t) lo = mid; else hi = mid;
+  }
+  constexpr int TOK = kBM / G;
+  const int s = lo;
+  const int r = t - pfx[s];
+  const int Hkv = p.num_kv_heads;
+  tl.s = s;
+  tl.hk = r % Hkv;
+  const int qt = r / Hkv;
+  tl.qs = __ldg(p.qsl + s);
+  const int q_len = __ldg(p.qsl + s + 1) - tl.qs;
+  int L = __ldg(p.seq_lens + s);
+  const int cap = p.max_blocks_per_seq * p.block_size;
+  if (L > cap) L = cap;
+  tl.L = L;
+  tl.q0 = qt * TOK;
+  tl.nq = min(TOK, q_len - tl.q0);
+  tl.pos0 = L - q_len + tl.q0;
+  tl.leff = tl.pos0 + tl.nq;  // keys this tile needs: 0 .. leff - 1
+  if (q_len > L) raise_error(p.err, PA_DEVERR_SEQ_RANGE);
+  tl.nt = (q_len > L || tl.nq <= 0) ? 0 : (tl.leff + kBN - 1) / kBN;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillParams p,
+                                                                 const __grid_constant__ CUtensorMap qmap,
+                                                                 const __grid_constant__ CUtensorMap kmap,
+                                                                 const __grid_constant__ CUtensorMap vmap) {
+  using LY = Layout<D>;
+  constexpr int NH = LY::NH;
+  constexpr int TOK = kBM / G;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1024-byte alignment
+  unsigned char* sm = smem_raw + (base - raw);
+  int* pfx = reinterpret_cast<int*>(sm + LY::PFX);
+  const uint32_t bar0 = base + LY::BAR;
+  auto bar = [&](int i) { return bar0 + 8u * uint32_t(i); };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + LY::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + LY::MISC + 4);
+
+  griddep_wait();  // inputs (e.g. this step's KV writes) come from earlier kernels
+
+  const int S = p.num_seqs;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- per-request tile prefix (tiles = ceil(q_len / TOK) x num_kv_heads for q_len >= 2)
+  int run = 0;
+  for (int b0 = 0; b0 <= S; b0 += kThreads) {
+    const int s = b0 + threadIdx.x;
+    int cnt = 0;
+    if (s < S) {
+      const int q_len = __ldg(p.qsl + s + 1) - __ldg(p.qsl + s);
+      if (q_len >= 2) cnt = ((q_len + TOK - 1) / TOK) * p.num_kv_heads;
+    }
+    // inclusive warp scan, then across the 6 warps
+    int inc = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, d);
+      if (lane >= d) inc += y;
+    }
+    __shared__ int wsum[kThreads / 32];
+    if (lane == 31) wsum[warp] = inc;
+    __syncthreads();
+    int off = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      if (w < warp) off += wsum[w];
+      tot += wsum[w];
+    }
+    if (s <= S) pfx[s] = run + off + inc - cnt;  // exclusive prefix; pfx[S] = total
+    run += tot;
+    __syncthreads();
+  }
+  const int total = pfx[S];
+  if (int(blockIdx.x) >= total) return;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < LY::NBAR; ++i) {
+      uint32_t cnt = 1;
+      if (i == bSEmpty0 || i == bSEmpty1 || i == bPFull || i == bOEmpty) cnt = 4;
+      mbar_init(bar(i), cnt);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tc::tmem_alloc(base + LY::MISC, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    raise_error(p.err, PA_DEVERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 4) {
+    // =========================== TMA producer ===========================
+    if (lane == 0) {
+      tc::prefetch_tensormap(&qmap);
+      tc::prefetch_tensormap(&kmap);
+      tc::prefetch_tensormap(&vmap);
+      const int B = p.block_size;
+      int n = 0, tt = 0;
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        Tile tl;
+        tile_info<G>(p, pfx, S, t, tl);
+        if (tl.nt == 0) continue;
+        if (!mbar_wait(bar(bQEmpty), (tt & 1) ^ 1)) { fail(); break; }
+        mbar_arrive_expect_tx(bar(bQFull), uint32_t(kBM * D * 2));
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          tc::tma_load_3d(base + LY::Q + h * kHalf, &qmap, 64 * h, tl.hk * G, tl.qs + tl.q0, bar(bQFull));
+        const int32_t* bt = p.block_table + int64_t(tl.s) * p.max_blocks_per_seq;
+        for (int kb = 0; kb < tl.nt; ++kb, ++n) {
+          const int stage = n & 1;
+          if (!mbar_wait(bar(bKVEmpty0 + stage), ((n >> 1) & 1) ^ 1)) { fail(); break; }
+          const int key0 = kb * kBN;
+          int nload = 0;
+          for (int b = 0; b < kBN / B && key0 + b * B < tl.leff; ++b) {
+            const int64_t blk = __ldg(bt + (key0 + b * B) / B);
+            if (blk >= 0 && blk < p.num_blocks) ++nload;
+          }
+          mbar_arrive_expect_tx(bar(bKVFull0 + stage), uint32_t(nload * B * 128 * NH * 2));
+          for (int b = 0; b < kBN / B && key0 + b * B < tl.leff; ++b) {
+            const int64_t blk = __ldg(bt + (key0 + b * B) / B);
+            if (blk < 0 || blk >= p.num_blocks) {
+              raise_error(p.err, PA_DEVERR_BLOCK_RANGE);
+              continue;
+            }
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+              const uint32_t off = uint32_t(stage * NH + h) * kHalf + uint32_t(b * B * 128);
+              tc::tma_load_3d(base + LY::K + off, &kmap, 64 * h, tl.hk, int(blk * B), bar(bKVFull0 + stage));
+              tc::tma_load_3d(base + LY::V + off, &vmap, 64 * h, tl.hk, int(blk * B), bar(bKVFull0 + stage));
+            }
+          }
+        }
+        ++tt;
+      }
+    }
+  } else if (warp == 5) {
+    // =========================== MMA issuer ===========================
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kBM, kBN, 0);
+      constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kBM, D, 1);
+      int n = 0, tt = 0;
+      auto issue_qk = [&](int nn) -> bool {
+        const int stage = nn & 1, sb = nn & 1;
+        if (!mbar_wait(bar(bKVFull0 + stage), (nn >> 1) & 1)) return false;
+        if (!mbar_wait(bar(bSEmpty0 + sb), ((nn >> 1) & 1) ^ 1)) return false;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t koff = uint32_t(k / 4) * kHalf + uint32_t(k % 4) * 32;
+          const uint64_t a = tc::smem_desc_sw128(base + LY::Q + koff, 16, 1024);
+          const uint64_t b = tc::smem_desc_sw128(base + LY::K + uint32_t(stage * NH) * kHalf + koff, 16, 1024);
+          tc::mma_f16(tmem + uint32_t(sb * kBN), a, b, idesc_qk, k > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(bar(bSFull0 + sb));
+        return true;
+      };
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        Tile tl;
+        tile_info<G>(p, pfx, S, t, tl);
+        if (tl.nt == 0) continue;
+        if (!mbar_wait(bar(bQFull), tt & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        if (!issue_qk(n)) { ok = false; break; }
+        if (tl.nt == 1) tc::mma_commit(bar(bQEmpty));
+        for (int kb = 0; kb < tl.nt; ++kb, ++n) {
+          if (kb + 1 < tl.nt) {
+            if (!issue_qk(n + 1)) { ok = false; break; }
+            if (kb + 2 == tl.nt) tc::mma_commit(bar(bQEmpty));  // last QK of the tile issued
+          }
+          if (!mbar_wait(bar(bPFull), n & 1)) { ok = false; break; }
+          if (kb == 0 && !mbar_wait(bar(bOEmpty), (tt & 1) ^ 1)) { ok = false; break; }
+          tc::fence_after_sync();
+          const int stage = n & 1;
+#pragma unroll
+          for (int k = 0; k < kBN / 16; ++k) {
+            const uint64_t a =
+                tc::smem_desc_sw128(base + LY::P + uint32_t(k / 4) * kHalf + uint32_t(k % 4) * 32, 16, 1024);
+            const uint64_t b = tc::smem_desc_sw128(base + LY::V + uint32_t(stage * NH) * kHalf + uint32_t(k) * 2048,
+                                                   kHalf, 1024);
+            tc::mma_f16(tmem + 256u, a, b, idesc_pv, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(bar(bKVEmpty0 + stage));
+          tc::mma_commit(bar(bPVDone));
+        }
+        ++tt;
+      }
+      if (!ok) fail();
+      // let every MMA issued by this thread land before TMEM is released
+      tc::mma_commit(bar(bMmaDone));
+      mbar_wait(bar(bMmaDone), 0);
+    }
+  } else {
+    // =========================== softmax + epilogue (rows) ===========================
+    const int r = threadIdx.x;  // tile row == TMEM lane
+    const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
+    int n = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      Tile tl;
+      tile_info<G>(p, pfx, S, t, tl);
+      if (tl.nt == 0) continue;
+      const int i = r / G, g = r % G;
+      const bool active = i < tl.nq;
+      const int mypos = tl.pos0 + (active ? i : tl.nq - 1);
+      float m_used = -INFINITY, l = 0.f;
+      for (int kb = 0; kb < tl.nt; ++kb, ++n) {
+        const int sb = n & 1;
+        if (!mbar_wait(bar(bSFull0 + sb), (n >> 1) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        float s[kBN];
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) tc::tmem_ld32(trow + uint32_t(sb * kBN + c * 32), *reinterpret_cast<float(*)[32]>(s + c * 32));
+        tc::tmem_wait_ld();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bSEmpty0 + sb));
+        // mask (causal; keys past the request's end) and scale into the log2 domain
+        const int key0 = kb * kBN;
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          s[c] = (key0 + c <= mypos) ? s[c] * p.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, s[c]);
+        }
+        const float m_new = fmaxf(m_used, mt);
+        const bool grow = m_new > m_used + 8.f;  // also true on the first tile
+        const float m_use = grow ? m_new : m_used;
+        const float alpha = exp2f(m_used - m_use);
+        float rs = 0.f;
+        uint32_t pk[kBN / 2];
+#pragma unroll
+        for (int c = 0; c < kBN; c += 2) {
+          const float p0 = exp2f(s[c] - m_use), p1 = exp2f(s[c + 1] - m_use);
+          rs += p0 + p1;
+          __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+          pk[c / 2] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        l = l * alpha + rs;
+        m_used = m_use;
+        // the previous P.V must be done before P is overwritten or O rescaled
+        if (kb > 0) {
+          if (!mbar_wait(bar(bPVDone), (n - 1) & 1)) { ok = false; break; }
+          tc::fence_after_sync();
+          if (__any_sync(0xffffffffu, grow)) {
+            const float a = grow ? alpha : 1.f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              float o[32];
+              tc::tmem_ld32(trow + 256u + uint32_t(c * 32), o);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] *= a;
+              tc::tmem_st32(trow + 256u + uint32_t(c * 32), o);
+            }
+            tc::tmem_wait_st();
+          }
+        }
+        // P row -> shared memory (K-major, 128-byte swizzle: 16-byte chunk index ^ row % 8)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint32_t addr = LY::P + uint32_t(h) * kHalf + uint32_t(r) * 128 + (uint32_t(ch ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(sm + addr) =
+                make_uint4(pk[h * 32 + ch * 4], pk[h * 32 + ch * 4 + 1], pk[h * 32 + ch * 4 + 2], pk[h * 32 + ch * 4 + 3]);
+          }
+        // last tile: V rows past the keys this tile needs may hold stale or invalid data;
+        // P is 0 there, but 0 * NaN is NaN in the MMA: zero them
+        if (kb == tl.nt - 1 && tl.leff - key0 < kBN) {
+          if (!mbar_wait(bar(bKVFull0 + (n & 1)), (n >> 1) & 1)) { ok = false; break; }
+          if (r >= tl.leff - key0) {
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+#pragma unroll
+              for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4*>(sm + LY::V + uint32_t((n & 1) * NH + h) * kHalf + uint32_t(r) * 128 + ch * 16) =
+                    make_uint4(0, 0, 0, 0);
+          }
+        }
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bPFull));
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l -> out
+      if (!mbar_wait(bar(bPVDone), (n - 1) & 1)) { ok = false; break; }
+      tc::fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
+                           (int64_t(tl.qs + tl.q0 + i) * p.num_heads + tl.hk * G + g) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tc::tmem_ld32(trow + 256u + uint32_t(c * 32), o);
+        tc::tmem_wait_ld();
+        if (active) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            float f[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) f[x] = o[e + x] * inv;
+            *reinterpret_cast<uint4*>(out + c * 32 + e) = Elem<__nv_bfloat16>::pack(f);
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(bOEmpty));
+    }
+    if (!ok) fail();
+  }
+
+  // ---- teardown: everyone done with TMEM, then the allocating warp frees it
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// 3-D bf16 map over [d2][d1][d0] (d0 contiguous), box {64, b1, b2}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1, uint32_t b2) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const cuuint32_t box[3] = {64, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int G>
+cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
+  CUtensorMap qm, km, vm;
+  const int B = a.block_size;
+  if (!make_map(&qm, a.q, D, uint64_t(a.num_heads), uint64_t(a.num_tokens), G, kBM / G) ||
+      !make_map(&km, a.k_cache, D, uint64_t(a.num_kv_heads), uint64_t(a.num_blocks) * B, 1, B) ||
+      !make_map(&vm, a.v_cache, D, uint64_t(a.num_kv_heads), uint64_t(a.num_blocks) * B, 1, B))
+    return cudaErrorInvalidValue;
+  PrefillParams p;
+  p.out = a.out;
+  p.block_table = a.block_table;
+  p.seq_lens = a.seq_lens;
+  p.qsl = a.query_start_loc;
+  p.err = a.err;
+  p.num_blocks = a.num_blocks;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_seqs = a.num_seqs;
+  p.num_heads = a.num_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.block_size = a.block_size;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  auto kern = prefill_tc_kernel<D, G>;
+  const size_t smem = Layout<D>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(num_ctas), dim3(kThreads), smem, stream, p, qm, km, vm);
+}
+
+template <int D>
+cudaError_t run_g(const AttnArgs& a, int G, int num_ctas, cudaStream_t stream) {
+  switch (G) {
+    case 1: return run<D, 1>(a, num_ctas, stream);
+    case 2: return run<D, 2>(a, num_ctas, stream);
+    case 4: return run<D, 4>(a, num_ctas, stream);
+    case 8: return run<D, 8>(a, num_ctas, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const AttnArgs& a) {
+  const int B = a.block_size;
+  return a.dtype == PA_BF16 && (a.head_dim == 64 || a.head_dim == 128) && B >= 8 && B <= kBN && kBN % B == 0 &&
+         a.num_seqs <= kMaxSeqs && encode_fn() != nullptr;
+}
+
+cudaError_t launch_prefill_tc(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
+  const int G = a.num_heads / a.num_kv_heads;
+  if (a.head_dim == 64) return run_g<64>(a, G, num_ctas, stream);
+  return run_g<128>(a, G, num_ctas, stream);
+}
+
+}  // namespace pa

@@ -129,6 +129,12 @@ EDGE = [
     ("fp32_b1_g1", workloads.Spec("f32", 2, 2, 64, 1, 0.125), [9, 17], [1, 2]),
     ("bf16_b8_mqa", workloads.Spec("bf16", 4, 1, 128, 8, 0.088), [23, 8, 70], [1, 1, 1]),
     ("many_short", workloads.Spec("bf16", 32, 8, 128, 16, 0.088), list(range(1, 300)), [1] * 299),
+    # chunked prefill on the tensor cores (bf16): group sizes, head dims, block sizes
+    ("prefill_g4_b16", workloads.Spec("bf16", 32, 8, 128, 16, 0.088), [0, 100, 300, 7], [200, 77, 5, 1]),
+    ("prefill_g1_b64", workloads.Spec("bf16", 8, 8, 128, 64, 0.088), [50, 0], [130, 300]),
+    ("prefill_g2_d64_b128", workloads.Spec("bf16", 8, 4, 64, 128, 0.125), [129, 0], [40, 256]),
+    ("prefill_g8_b8", workloads.Spec("bf16", 32, 4, 128, 8, 0.088), [17, 0], [60, 2]),
+    ("prefill_long_prior", workloads.Spec("bf16", 32, 8, 128, 16, 0.088), [3000], [300]),
 ]
 
 
