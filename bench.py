@@ -42,6 +42,9 @@ def _args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", choices=["gqa_decode", "mixed"], default="gqa_decode",
+                    help="gqa_decode: the headline line (default); mixed: the chunked-prefill + decode "
+                         "batch, timed whole and as its prefill-only and decode-only sub-batches")
     a = ap.parse_args(argv)
     a.warmup = max(3, a.warmup)
     return a
@@ -393,10 +396,118 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
                         "table/lens/query_start_loc from pinned memory, pa_kv_write, pa_attention, D2H of out"}
 
 
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        pk = json.load(open(path))
+        return pk["hbm_gbs"], pk["bf16_tflops"], "measured (MEASURED_PEAKS.json)"
+    return FALLBACK_HBM_GBS, 1900.0, "fallback"
+
+
+def _sub_batch(st, rows_of, idx, dev):
+    """Requests `idx` of a step's batch as a batch of their own (device tensors)."""
+    import torch
+
+    qsl = st.query_start_loc.cpu()
+    sel_rows = torch.cat([torch.arange(int(qsl[i]), int(qsl[i + 1])) for i in idx]).to(dev)
+    q = st.q.index_select(0, sel_rows).contiguous()
+    lens_q = torch.tensor([int(qsl[i + 1] - qsl[i]) for i in idx])
+    new_qsl = torch.zeros(len(idx) + 1, dtype=torch.int32)
+    new_qsl[1:] = torch.cumsum(lens_q, 0)
+    idx_t = torch.tensor(idx, device=dev)
+    return dict(q=q, out=torch.empty_like(q), block_table=st.block_table.index_select(0, idx_t).contiguous(),
+                seq_lens=st.seq_lens.index_select(0, idx_t).contiguous(), query_start_loc=new_qsl.to(dev),
+                max_query_len=int(lens_q.max()), max_seq_len=int(st.seq_lens.index_select(0, idx_t).max()))
+
+
+def run_mixed(a):
+    """The mixed chunked-prefill + decode batch (8 chunks of 512 queries with prior context
+    U[0, 4096] + 248 decodes with L ~ U[256, 4096]): whole step, and each part alone."""
+    import torch
+
+    import paged_kv_cache_161_gb300 as pa
+    import workloads
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    wl = workloads.build(5)
+    sp = wl.spec
+    dw = DeviceWorkload(wl, device=dev)
+    dw.run_setup()
+    st = dw.prepare_step()
+    stream = torch.cuda.current_stream(dev)
+    C = wl.meta["chunks"]
+    lens = st.seq_lens.cpu().tolist()
+    qlens = torch.diff(st.query_start_loc.cpu()).tolist()
+    # algorithmic work: prefill flops (4 * D per query-key pair per query head), decode K/V bytes
+    pf_flops = sum(4.0 * sp.head_dim * sp.num_heads * sum(lens[i] - qlens[i] + j + 1 for j in range(qlens[i]))
+                   for i in range(C))
+    dec_bytes = sum(lens[i] for i in range(C, len(lens))) * sp.kv_token_bytes
+    pf_kv_bytes = sum(lens[i] for i in range(C)) * sp.kv_token_bytes
+
+    def timed(fn, steps, warm):
+        for _ in range(warm):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    def attn(b):
+        return lambda: pa.attention(b["out"], b["q"], dw.k_cache, dw.v_cache, b["block_table"], b["seq_lens"],
+                                    b["query_start_loc"], max_query_len=b["max_query_len"],
+                                    max_seq_len=b["max_seq_len"], scale=sp.scale, workspace=st.workspace,
+                                    stream=stream)
+
+    whole = dict(q=st.q, out=st.out, block_table=st.block_table, seq_lens=st.seq_lens,
+                 query_start_loc=st.query_start_loc, max_query_len=st.max_query_len, max_seq_len=st.max_seq_len)
+    pre = _sub_batch(st, None, list(range(C)), dev)
+    dec = _sub_batch(st, None, list(range(C, len(lens))), dev)
+    steps = max(10, a.steps // 10)
+    pa.read_device_errors(clear=True)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    step_ms = timed(lambda: dw.run_step(st, stream=stream), steps, a.warmup)
+    attn_ms = timed(attn(whole), steps, a.warmup)
+    pre_ms = timed(attn(pre), steps, a.warmup)
+    dec_ms = timed(attn(dec), steps, a.warmup)
+    clk = clocks.stop()
+    if pa.read_device_errors(clear=True):
+        raise RuntimeError("device error flags set")
+    hbm, tflops_peak, src = _peaks()
+    pre_tf = pf_flops / (pre_ms * 1e-3) / 1e12
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    t_star = max(pf_flops / (tflops_peak * 1e12), (dec_bytes + pf_kv_bytes) / (hbm * 1e9)) * 1e3
+    line = {
+        "metric": "mixed chunked-prefill + decode attention (8 x 512-query chunks + 248 decodes)",
+        "value": t_star / attn_ms, "unit": "fraction of max(flops / tensor peak, bytes / HBM peak) roofline time",
+        "n_gpus": 1, "steps": steps, "warmup": a.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "mixed_prefill_decode_bf16: 8 chunks x 512 queries, prior context U[0, 4096]; "
+                               "248 decodes, L ~ U[256, 4096]; 32 q / 8 kv heads, head_dim 128, block 16",
+                   "prefill_gflop": pf_flops / 1e9, "decode_kv_bytes": dec_bytes, "seed": wl.seed},
+        "attention_ms": attn_ms, "roofline_time_ms": t_star,
+        "prefill": {"ms": pre_ms, "tflops": pre_tf, "peak_tflops": tflops_peak, "frac": pre_tf / tflops_peak,
+                    "bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05)"},
+        "decode": {"ms": dec_ms, "gbs": dec_gbs, "peak_gbs": hbm, "frac": dec_gbs / hbm, "bound": "hbm"},
+        "peak_source": src, "clocks": clk,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main(argv=None):
     a = _args(argv)
     if a.impl == "reference":
         return run_reference(a)
+    if a.workload == "mixed":
+        return run_mixed(a)
     return run_ours(a)
 
 
