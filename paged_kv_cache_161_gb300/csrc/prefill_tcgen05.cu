@@ -9,18 +9,21 @@
 //
 // Tile: 128 rows = (128 / G) query tokens x the G query heads that share one KV head, so
 // each K/V tile feeds all of them. Per 128-key tile: S = Q.K^T (8 x tcgen05.mma
-// 128x128x16, bf16 in, f32 accumulate in TMEM), online softmax in registers (one thread
-// per row, exp2 domain, lazy rescaling of O only when the row max grows by more than
-// 2^8), P as bf16 into 128-byte-swizzled shared memory, O += P.V (8 x tcgen05.mma
-// 128xDx16, V as an MN-major operand), O in TMEM.
+// 128x128x16, bf16 in, f32 accumulate in TMEM), online softmax in registers (exp2
+// domain, the scale folded into one FMA per score, lazy rescaling of O only when the row
+// max grows by more than 2^8), P as bf16 back into TMEM, O += P.V (8 x tcgen05.mma
+// 128xDx16, A = P from TMEM, B = V as an MN-major shared-memory operand), O in TMEM.
 //
-// Roles (192 threads, one CTA per SM, persistent over a static round-robin of tiles):
-//   warps 0-3  softmax + epilogue: thread r owns row r = TMEM lane r;
-//   warp 4     TMA producer: Q tile once per tile, K and V tiles of 128 keys by physical
+// Roles (320 threads, one CTA per SM, persistent over a static round-robin of tiles):
+//   warps 0-7  softmax + epilogue: two threads per row (TMEM lane r), one per 64-key half
+//              of S and 64-dim half of O; the row max (and the final sum) cross halves
+//              through shared memory on a bounded mbarrier;
+//   warp 8     TMA producer: Q tile once per tile, K and V tiles of 128 keys by physical
 //              block through the block table (one 3-D box per block and 64-dim half),
-//              into a 2-deep ring;
-//   warp 5     allocates 512 TMEM columns (S double buffer 2 x 128, O 128) and one
-//              thread issues the MMAs, tracking completion with tcgen05.commit.
+//              into separate 2-deep K and V rings (a K stage frees as soon as its QK is done);
+//   warp 9     allocates 512 TMEM columns (S triple buffer 3 x 128, O 128) and one thread
+//              issues the MMAs, tracking completion with tcgen05.commit. P is written back
+//              into its S buffer as packed bf16 and read from TMEM by the P.V MMA.
 // Every wait is bounded; on a timeout the kernel sets an error bit and leaves after its
 // copies and MMAs in flight have landed, freeing TMEM.
 #include <cuda.h>
@@ -36,8 +39,10 @@ namespace {
 constexpr int kBM = 128;             // rows per tile
 constexpr int kBN = 128;             // keys per tile
 constexpr int kMaxSeqs = 4096;       // requests per call this kernel accepts
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;
+constexpr int kSoftmaxWarps = 8;     // two threads per row: column halves
+constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+constexpr uint32_t kTmemCols = 512;  // S buffers 3 x 128 columns, O 128 columns
+constexpr uint32_t kOCol = 384;
 constexpr uint32_t kHalf = 128 * 128;  // bytes of a 128-row x 64-element bf16 half tile
 
 struct PrefillParams {
@@ -61,10 +66,10 @@ struct Layout {
   static constexpr uint32_t Q = 0;
   static constexpr uint32_t K = Q + NH * kHalf;             // 2 stages
   static constexpr uint32_t V = K + 2 * NH * kHalf;         // 2 stages
-  static constexpr uint32_t P = V + 2 * NH * kHalf;         // 2 halves of 64 keys
-  static constexpr uint32_t PFX = P + 2 * kHalf;            // int[kMaxSeqs + 1]
-  static constexpr uint32_t BAR = PFX + (kMaxSeqs + 8) * 4;  // mbarriers
-  static constexpr int NBAR = 16;
+  static constexpr uint32_t PFX = V + 2 * NH * kHalf;       // int[kMaxSeqs + 8]
+  static constexpr uint32_t XCH = PFX + (kMaxSeqs + 8) * 4;  // float[2 slots][2 halves][128 rows]
+  static constexpr uint32_t BAR = XCH + 2 * 2 * 128 * 4;     // mbarriers
+  static constexpr int NBAR = 24;
   static constexpr uint32_t MISC = BAR + NBAR * 8;           // tmem base, abort flag
   static constexpr uint32_t BYTES = MISC + 16;
   static constexpr uint32_t SMEM = BYTES + 1024;             // + alignment slack
@@ -72,8 +77,11 @@ struct Layout {
 
 // barrier indices
 enum : int {
-  bQFull = 0, bQEmpty, bKVFull0, bKVFull1, bKVEmpty0, bKVEmpty1, bSFull0, bSFull1,
-  bSEmpty0, bSEmpty1, bPFull, bPVDone, bOEmpty, bMmaDone
+  bQFull = 0, bQEmpty,
+  bKFull0, bKFull1, bKEmpty0, bKEmpty1,
+  bVFull0, bVFull1, bVEmpty0, bVEmpty1,
+  bSFull0, bSFull1, bSFull2, bSFree0, bSFree1, bSFree2,
+  bPFull, bPVDone, bOEmpty, bXch, bMmaDone
 };
 
 struct Tile {
@@ -117,11 +125,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   using LY = Layout<D>;
   constexpr int NH = LY::NH;
   constexpr int TOK = kBM / G;
+  constexpr int DH = D / 2;  // O dims per softmax thread
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1024-byte alignment
   unsigned char* sm = smem_raw + (base - raw);
   int* pfx = reinterpret_cast<int*>(sm + LY::PFX);
+  float* xch = reinterpret_cast<float*>(sm + LY::XCH);
   const uint32_t bar0 = base + LY::BAR;
   auto bar = [&](int i) { return bar0 + 8u * uint32_t(i); };
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + LY::MISC);
@@ -141,7 +151,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const int q_len = __ldg(p.qsl + s + 1) - __ldg(p.qsl + s);
       if (q_len >= 2) cnt = ((q_len + TOK - 1) / TOK) * p.num_kv_heads;
     }
-    // inclusive warp scan, then across the 6 warps
     int inc = cnt;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -167,13 +176,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   if (threadIdx.x == 0) {
     for (int i = 0; i < LY::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i == bSEmpty0 || i == bSEmpty1 || i == bPFull || i == bOEmpty) cnt = 4;
+      if (i == bPFull || i == bOEmpty || i == bXch) cnt = kSoftmaxWarps;
       mbar_init(bar(i), cnt);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kSoftmaxWarps + 1) {
     tc::tmem_alloc(base + LY::MISC, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -187,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     *abort_flag = 1;
   };
 
-  if (warp == 4) {
+  if (warp == kSoftmaxWarps) {
     // =========================== TMA producer ===========================
     if (lane == 0) {
       tc::prefetch_tensormap(&qmap);
@@ -195,11 +204,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       tc::prefetch_tensormap(&vmap);
       const int B = p.block_size;
       int n = 0, tt = 0;
-      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         Tile tl;
         tile_info<G>(p, pfx, S, t, tl);
         if (tl.nt == 0) continue;
-        if (!mbar_wait(bar(bQEmpty), (tt & 1) ^ 1)) { fail(); break; }
+        if (!mbar_wait(bar(bQEmpty), (tt & 1) ^ 1)) { ok = false; break; }
         mbar_arrive_expect_tx(bar(bQFull), uint32_t(kBM * D * 2));
 #pragma unroll
         for (int h = 0; h < NH; ++h)
@@ -207,41 +217,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int32_t* bt = p.block_table + int64_t(tl.s) * p.max_blocks_per_seq;
         for (int kb = 0; kb < tl.nt; ++kb, ++n) {
           const int stage = n & 1;
-          if (!mbar_wait(bar(bKVEmpty0 + stage), ((n >> 1) & 1) ^ 1)) { fail(); break; }
           const int key0 = kb * kBN;
           int nload = 0;
           for (int b = 0; b < kBN / B && key0 + b * B < tl.leff; ++b) {
             const int64_t blk = __ldg(bt + (key0 + b * B) / B);
             if (blk >= 0 && blk < p.num_blocks) ++nload;
           }
-          mbar_arrive_expect_tx(bar(bKVFull0 + stage), uint32_t(nload * B * 128 * NH * 2));
-          for (int b = 0; b < kBN / B && key0 + b * B < tl.leff; ++b) {
-            const int64_t blk = __ldg(bt + (key0 + b * B) / B);
-            if (blk < 0 || blk >= p.num_blocks) {
-              raise_error(p.err, PA_DEVERR_BLOCK_RANGE);
-              continue;
-            }
+          const uint32_t bytes = uint32_t(nload * B * 128 * NH);
+          for (int kv = 0; kv < 2; ++kv) {  // K first (needed first), then V
+            if (!mbar_wait(bar((kv ? bVEmpty0 : bKEmpty0) + stage), ((n >> 1) & 1) ^ 1)) { ok = false; break; }
+            const uint32_t fb = bar((kv ? bVFull0 : bKFull0) + stage);
+            mbar_arrive_expect_tx(fb, bytes);
+            const uint32_t dst0 = base + (kv ? LY::V : LY::K) + uint32_t(stage * NH) * kHalf;
+            for (int b = 0; b < kBN / B && key0 + b * B < tl.leff; ++b) {
+              const int64_t blk = __ldg(bt + (key0 + b * B) / B);
+              if (blk < 0 || blk >= p.num_blocks) {
+                if (kv == 0) raise_error(p.err, PA_DEVERR_BLOCK_RANGE);
+                continue;
+              }
 #pragma unroll
-            for (int h = 0; h < NH; ++h) {
-              const uint32_t off = uint32_t(stage * NH + h) * kHalf + uint32_t(b * B * 128);
-              tc::tma_load_3d(base + LY::K + off, &kmap, 64 * h, tl.hk, int(blk * B), bar(bKVFull0 + stage));
-              tc::tma_load_3d(base + LY::V + off, &vmap, 64 * h, tl.hk, int(blk * B), bar(bKVFull0 + stage));
+              for (int h = 0; h < NH; ++h)
+                tc::tma_load_3d(dst0 + uint32_t(h) * kHalf + uint32_t(b * B * 128), kv ? &vmap : &kmap, 64 * h,
+                                tl.hk, int(blk * B), fb);
             }
           }
+          if (!ok) break;
         }
         ++tt;
       }
+      if (!ok) fail();
     }
-  } else if (warp == 5) {
+  } else if (warp == kSoftmaxWarps + 1) {
     // =========================== MMA issuer ===========================
     if (lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kBM, kBN, 0);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kBM, D, 1);
       int n = 0, tt = 0;
+      // S(nn) = Q . K(nn)^T into S buffer nn % 3
       auto issue_qk = [&](int nn) -> bool {
-        const int stage = nn & 1, sb = nn & 1;
-        if (!mbar_wait(bar(bKVFull0 + stage), (nn >> 1) & 1)) return false;
-        if (!mbar_wait(bar(bSEmpty0 + sb), ((nn >> 1) & 1) ^ 1)) return false;
+        const int stage = nn & 1, sb = nn % 3;
+        if (!mbar_wait(bar(bKFull0 + stage), (nn >> 1) & 1)) return false;
+        if (!mbar_wait(bar(bSFree0 + sb), ((nn / 3) & 1) ^ 1)) return false;
         tc::fence_after_sync();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
@@ -250,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           const uint64_t b = tc::smem_desc_sw128(base + LY::K + uint32_t(stage * NH) * kHalf + koff, 16, 1024);
           tc::mma_f16(tmem + uint32_t(sb * kBN), a, b, idesc_qk, k > 0 ? 1u : 0u);
         }
+        tc::mma_commit(bar(bKEmpty0 + stage));
         tc::mma_commit(bar(bSFull0 + sb));
         return true;
       };
@@ -260,27 +277,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         if (tl.nt == 0) continue;
         if (!mbar_wait(bar(bQFull), tt & 1)) { ok = false; break; }
         tc::fence_after_sync();
-        if (!issue_qk(n)) { ok = false; break; }
-        if (tl.nt == 1) tc::mma_commit(bar(bQEmpty));
+        const int n0 = n;
+        for (int i = 0; i < 2 && i < tl.nt; ++i)
+          if (!issue_qk(n0 + i)) { ok = false; break; }
+        if (!ok) break;
+        if (tl.nt <= 2) tc::mma_commit(bar(bQEmpty));  // every QK of the tile is issued
         for (int kb = 0; kb < tl.nt; ++kb, ++n) {
-          if (kb + 1 < tl.nt) {
-            if (!issue_qk(n + 1)) { ok = false; break; }
-            if (kb + 2 == tl.nt) tc::mma_commit(bar(bQEmpty));  // last QK of the tile issued
-          }
           if (!mbar_wait(bar(bPFull), n & 1)) { ok = false; break; }
           if (kb == 0 && !mbar_wait(bar(bOEmpty), (tt & 1) ^ 1)) { ok = false; break; }
-          tc::fence_after_sync();
           const int stage = n & 1;
+          if (!mbar_wait(bar(bVFull0 + stage), (n >> 1) & 1)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t pcol = tmem + uint32_t((n % 3) * kBN);  // P (bf16 pairs) over S's first 64 columns
 #pragma unroll
           for (int k = 0; k < kBN / 16; ++k) {
-            const uint64_t a =
-                tc::smem_desc_sw128(base + LY::P + uint32_t(k / 4) * kHalf + uint32_t(k % 4) * 32, 16, 1024);
             const uint64_t b = tc::smem_desc_sw128(base + LY::V + uint32_t(stage * NH) * kHalf + uint32_t(k) * 2048,
                                                    kHalf, 1024);
-            tc::mma_f16(tmem + 256u, a, b, idesc_pv, (kb > 0 || k > 0) ? 1u : 0u);
+            tc::mma_f16_ts(tmem + kOCol, pcol + uint32_t(k * 8), b, idesc_pv, (kb > 0 || k > 0) ? 1u : 0u);
           }
-          tc::mma_commit(bar(bKVEmpty0 + stage));
+          tc::mma_commit(bar(bVEmpty0 + stage));
+          tc::mma_commit(bar(bSFree0 + n % 3));
           tc::mma_commit(bar(bPVDone));
+          if (kb + 2 < tl.nt) {
+            if (!issue_qk(n + 2)) { ok = false; break; }
+            if (kb + 3 == tl.nt) tc::mma_commit(bar(bQEmpty));
+          }
         }
         ++tt;
       }
@@ -290,11 +311,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       mbar_wait(bar(bMmaDone), 0);
     }
   } else {
-    // =========================== softmax + epilogue (rows) ===========================
-    const int r = threadIdx.x;  // tile row == TMEM lane
-    const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
-    int n = 0;
+    // =========================== softmax + epilogue ===========================
+    // warp w: rows 32 (w % 4) .. + 31 (its TMEM lane quarter), column half h = w / 4 of S
+    // (keys 64h .. 64h + 63 of each tile) and of O (dims DH h .. DH h + DH - 1).
+    const int h = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;  // tile row == TMEM lane
+    const uint32_t trow = tmem + (uint32_t((warp & 3) * 32) << 16);
+    const float sc = p.scale_log2;
+    int n = 0, xph = 0;
     bool ok = true;
+    // exchange a per-row value with the thread holding the other column half (bounded)
+    auto exchange = [&](float v, float& other) -> bool {
+      float* slot = xch + (xph & 1) * 256;
+      slot[h * 128 + r] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(bXch));
+      const bool done = mbar_wait(bar(bXch), xph & 1);
+      other = slot[(1 - h) * 128 + r];
+      ++xph;
+      return done;
+    };
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       Tile tl;
       tile_info<G>(p, pfx, S, t, tl);
@@ -302,97 +338,98 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const int i = r / G, g = r % G;
       const bool active = i < tl.nq;
       const int mypos = tl.pos0 + (active ? i : tl.nq - 1);
-      float m_used = -INFINITY, l = 0.f;
+      float m_used = -INFINITY, l = 0.f;  // m in raw score units; l: this half's partial sum
       for (int kb = 0; kb < tl.nt; ++kb, ++n) {
-        const int sb = n & 1;
-        if (!mbar_wait(bar(bSFull0 + sb), (n >> 1) & 1)) { ok = false; break; }
+        const int sb = n % 3;
+        if (!mbar_wait(bar(bSFull0 + sb), (n / 3) & 1)) { ok = false; break; }
         tc::fence_after_sync();
-        float s[kBN];
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) tc::tmem_ld32(trow + uint32_t(sb * kBN + c * 32), *reinterpret_cast<float(*)[32]>(s + c * 32));
+        float s[64];
+        tc::tmem_ld32(trow + uint32_t(sb * kBN + h * 64), *reinterpret_cast<float(*)[32]>(s));
+        tc::tmem_ld32(trow + uint32_t(sb * kBN + h * 64 + 32), *reinterpret_cast<float(*)[32]>(s + 32));
         tc::tmem_wait_ld();
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(bSEmpty0 + sb));
-        // mask (causal; keys past the request's end) and scale into the log2 domain
-        const int key0 = kb * kBN;
+        const int key0 = kb * kBN + h * 64;
         float mt = -INFINITY;
+        if (kb * kBN + kBN - 1 > tl.pos0) {  // a diagonal tile: causal mask
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          s[c] = (key0 + c <= mypos) ? s[c] * p.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, s[c]);
+          for (int c = 0; c < 64; ++c) {
+            s[c] = (key0 + c <= mypos) ? s[c] : -INFINITY;
+            mt = fmaxf(mt, s[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) mt = fmaxf(mt, s[c]);
         }
-        const float m_new = fmaxf(m_used, mt);
-        const bool grow = m_new > m_used + 8.f;  // also true on the first tile
+        tc::fence_before_sync();  // S reads done before the other half overwrites S with P
+        float mo;
+        if (!exchange(mt, mo)) { ok = false; break; }
+        tc::fence_after_sync();
+        const float m_new = fmaxf(m_used, fmaxf(mt, mo));
+        const bool grow = (m_new - m_used) * sc > 8.f;  // also true on the first tile
         const float m_use = grow ? m_new : m_used;
-        const float alpha = exp2f(m_used - m_use);
-        float rs = 0.f;
-        uint32_t pk[kBN / 2];
+        const float alpha = exp2f((m_used - m_use) * sc);
+        const float bias = -m_use * sc;
+        float2 rs2 = make_float2(0.f, 0.f);
+        float pk[32];
 #pragma unroll
-        for (int c = 0; c < kBN; c += 2) {
-          const float p0 = exp2f(s[c] - m_use), p1 = exp2f(s[c + 1] - m_use);
-          rs += p0 + p1;
-          __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-          pk[c / 2] = *reinterpret_cast<uint32_t*>(&h);
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = exp2f(fmaf(s[c], sc, bias));
+          const float p1 = exp2f(fmaf(s[c + 1], sc, bias));
+          rs2.x += p0;
+          rs2.y += p1;
+          __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+          pk[c / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&hh));
         }
-        l = l * alpha + rs;
+        l = l * alpha + (rs2.x + rs2.y);
         m_used = m_use;
-        // the previous P.V must be done before P is overwritten or O rescaled
-        if (kb > 0) {
+        // O rescale needs the previous P.V finished (rare with the lazy threshold)
+        if (kb > 0 && __any_sync(0xffffffffu, grow)) {
           if (!mbar_wait(bar(bPVDone), (n - 1) & 1)) { ok = false; break; }
           tc::fence_after_sync();
-          if (__any_sync(0xffffffffu, grow)) {
-            const float a = grow ? alpha : 1.f;
+          const float a = grow ? alpha : 1.f;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              float o[32];
-              tc::tmem_ld32(trow + 256u + uint32_t(c * 32), o);
-              tc::tmem_wait_ld();
+          for (int c = 0; c < DH / 32; ++c) {
+            float o[32];
+            tc::tmem_ld32(trow + kOCol + uint32_t(h * DH + c * 32), o);
+            tc::tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] *= a;
-              tc::tmem_st32(trow + 256u + uint32_t(c * 32), o);
-            }
-            tc::tmem_wait_st();
+            for (int e = 0; e < 32; ++e) o[e] *= a;
+            tc::tmem_st32(trow + kOCol + uint32_t(h * DH + c * 32), o);
           }
         }
-        // P row -> shared memory (K-major, 128-byte swizzle: 16-byte chunk index ^ row % 8)
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint32_t addr = LY::P + uint32_t(h) * kHalf + uint32_t(r) * 128 + (uint32_t(ch ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(sm + addr) =
-                make_uint4(pk[h * 32 + ch * 4], pk[h * 32 + ch * 4 + 1], pk[h * 32 + ch * 4 + 2], pk[h * 32 + ch * 4 + 3]);
-          }
+        // P (bf16 pairs) into the first 64 columns of this S buffer: half h -> 32 columns
+        tc::tmem_st32(trow + uint32_t(sb * kBN + h * 32), pk);
+        tc::tmem_wait_st();
         // last tile: V rows past the keys this tile needs may hold stale or invalid data;
         // P is 0 there, but 0 * NaN is NaN in the MMA: zero them
-        if (kb == tl.nt - 1 && tl.leff - key0 < kBN) {
-          if (!mbar_wait(bar(bKVFull0 + (n & 1)), (n >> 1) & 1)) { ok = false; break; }
-          if (r >= tl.leff - key0) {
+        if (kb == tl.nt - 1 && tl.leff - kb * kBN < kBN) {
+          const int st = n & 1;
+          if (!mbar_wait(bar(bVFull0 + st), (n >> 1) & 1)) { ok = false; break; }
+          if (r >= tl.leff - kb * kBN && h < NH) {  // thread h clears V dim-half h of row r
 #pragma unroll
-            for (int h = 0; h < NH; ++h)
-#pragma unroll
-              for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4*>(sm + LY::V + uint32_t((n & 1) * NH + h) * kHalf + uint32_t(r) * 128 + ch * 16) =
-                    make_uint4(0, 0, 0, 0);
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(sm + LY::V + uint32_t(st * NH + h) * kHalf + uint32_t(r) * 128 + ch * 16) =
+                  make_uint4(0, 0, 0, 0);
           }
+          tc::fence_proxy_async_smem();
         }
-        tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(bPFull));
       }
       if (!ok) break;
       // ---- epilogue: O / l -> out
+      float lo;
+      if (!exchange(l, lo)) { ok = false; break; }
       if (!mbar_wait(bar(bPVDone), (n - 1) & 1)) { ok = false; break; }
       tc::fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float lt = l + lo;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
-                           (int64_t(tl.qs + tl.q0 + i) * p.num_heads + tl.hk * G + g) * D;
+                           (int64_t(tl.qs + tl.q0 + i) * p.num_heads + tl.hk * G + g) * D + h * DH;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DH / 32; ++c) {
         float o[32];
-        tc::tmem_ld32(trow + 256u + uint32_t(c * 32), o);
+        tc::tmem_ld32(trow + kOCol + uint32_t(h * DH + c * 32), o);
         tc::tmem_wait_ld();
         if (active) {
 #pragma unroll
@@ -414,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   // ---- teardown: everyone done with TMEM, then the allocating warp frees it
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kSoftmaxWarps + 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
