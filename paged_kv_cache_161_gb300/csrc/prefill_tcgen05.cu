@@ -14,13 +14,13 @@
 // max grows by more than 2^8), P as bf16 back into TMEM, O += P.V (8 x tcgen05.mma
 // 128xDx16, A = P from TMEM, B = V as an MN-major shared-memory operand), O in TMEM.
 //
-// Roles (320 threads, one CTA per SM, persistent over a static round-robin of tiles):
+// Roles (352 threads, one CTA per SM, persistent over a static round-robin of tiles):
 //   warps 0-7  softmax + epilogue: two threads per row (TMEM lane r), one per 64-key half
 //              of S and 64-dim half of O; the row max (and the final sum) cross halves
 //              through shared memory on a bounded mbarrier;
-//   warp 8     TMA producer: Q tile once per tile, K and V tiles of 128 keys by physical
-//              block through the block table (one 3-D box per block and 64-dim half),
-//              into separate 2-deep K and V rings (a K stage frees as soon as its QK is done);
+//   warps 8/10 TMA producers: Q tile once per tile and K tiles (3-deep ring) on warp 8,
+//              V tiles (2-deep ring) on warp 10, 128 keys at a time by physical block
+//              through the block table (one 3-D box per block and 64-dim half);
 //   warp 9     allocates 512 TMEM columns (S triple buffer 3 x 128, O 128) and one thread
 //              issues the MMAs, tracking completion with tcgen05.commit. P is written back
 //              into its S buffer as packed bf16 and read from TMEM by the P.V MMA.
@@ -40,7 +40,9 @@ constexpr int kBM = 128;             // rows per tile
 constexpr int kBN = 128;             // keys per tile
 constexpr int kMaxSeqs = 4096;       // requests per call this kernel accepts
 constexpr int kSoftmaxWarps = 8;     // two threads per row: column halves
-constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+constexpr int kThreads = (kSoftmaxWarps + 3) * 32;  // + K/Q producer, MMA issuer, V producer
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
 constexpr uint32_t kTmemCols = 512;  // S buffers 3 x 128 columns, O 128 columns
 constexpr uint32_t kOCol = 384;
 constexpr uint32_t kHalf = 128 * 128;  // bytes of a 128-row x 64-element bf16 half tile
@@ -64,12 +66,12 @@ template <int D>
 struct Layout {
   static constexpr int NH = D / 64;  // 64-element halves of the head dim
   static constexpr uint32_t Q = 0;
-  static constexpr uint32_t K = Q + NH * kHalf;             // 2 stages
-  static constexpr uint32_t V = K + 2 * NH * kHalf;         // 2 stages
-  static constexpr uint32_t PFX = V + 2 * NH * kHalf;       // int[kMaxSeqs + 8]
+  static constexpr uint32_t K = Q + NH * kHalf;                  // kKStages stages
+  static constexpr uint32_t V = K + kKStages * NH * kHalf;       // kVStages stages
+  static constexpr uint32_t PFX = V + kVStages * NH * kHalf;     // int[kMaxSeqs + 8]
   static constexpr uint32_t XCH = PFX + (kMaxSeqs + 8) * 4;  // float[2 slots][2 halves][128 rows]
   static constexpr uint32_t BAR = XCH + 2 * 2 * 128 * 4;     // mbarriers
-  static constexpr int NBAR = 24;
+  static constexpr int NBAR = 26;
   static constexpr uint32_t MISC = BAR + NBAR * 8;           // tmem base, abort flag
   static constexpr uint32_t BYTES = MISC + 16;
   static constexpr uint32_t SMEM = BYTES + 1024;             // + alignment slack
@@ -78,7 +80,7 @@ struct Layout {
 // barrier indices
 enum : int {
   bQFull = 0, bQEmpty,
-  bKFull0, bKFull1, bKEmpty0, bKEmpty1,
+  bKFull0, bKFull1, bKFull2, bKEmpty0, bKEmpty1, bKEmpty2,
   bVFull0, bVFull1, bVEmpty0, bVEmpty1,
   bSFull0, bSFull1, bSFull2, bSFree0, bSFree1, bSFree2,
   bPFull, bPVDone, bOEmpty, bXch, bMmaDone
@@ -196,52 +198,53 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     *abort_flag = 1;
   };
 
-  if (warp == kSoftmaxWarps) {
-    // =========================== TMA producer ===========================
+  if (warp == kSoftmaxWarps || warp == kSoftmaxWarps + 2) {
+    // =========================== TMA producers ===========================
+    // warp 8: Q (once per tile) and K (3-deep ring); warp 10: V (2-deep ring). Separate
+    // threads so that a K load never queues behind a V stage that is still in use.
     if (lane == 0) {
-      tc::prefetch_tensormap(&qmap);
-      tc::prefetch_tensormap(&kmap);
-      tc::prefetch_tensormap(&vmap);
+      const bool is_k = (warp == kSoftmaxWarps);
+      const CUtensorMap* map = is_k ? &kmap : &vmap;
+      if (is_k) tc::prefetch_tensormap(&qmap);
+      tc::prefetch_tensormap(map);
       const int B = p.block_size;
+      const int nst = is_k ? kKStages : kVStages;
       int n = 0, tt = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         Tile tl;
         tile_info<G>(p, pfx, S, t, tl);
         if (tl.nt == 0) continue;
-        if (!mbar_wait(bar(bQEmpty), (tt & 1) ^ 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(bQFull), uint32_t(kBM * D * 2));
+        if (is_k) {
+          if (!mbar_wait(bar(bQEmpty), (tt & 1) ^ 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(bQFull), uint32_t(kBM * D * 2));
 #pragma unroll
-        for (int h = 0; h < NH; ++h)
-          tc::tma_load_3d(base + LY::Q + h * kHalf, &qmap, 64 * h, tl.hk * G, tl.qs + tl.q0, bar(bQFull));
+          for (int h = 0; h < NH; ++h)
+            tc::tma_load_3d(base + LY::Q + h * kHalf, &qmap, 64 * h, tl.hk * G, tl.qs + tl.q0, bar(bQFull));
+        }
         const int32_t* bt = p.block_table + int64_t(tl.s) * p.max_blocks_per_seq;
         for (int kb = 0; kb < tl.nt; ++kb, ++n) {
-          const int stage = n & 1;
+          const int stage = n % nst, use = n / nst;
           const int key0 = kb * kBN;
           int nload = 0;
           for (int b = 0; b < kBN / B && key0 + b * B < tl.leff; ++b) {
             const int64_t blk = __ldg(bt + (key0 + b * B) / B);
             if (blk >= 0 && blk < p.num_blocks) ++nload;
           }
-          const uint32_t bytes = uint32_t(nload * B * 128 * NH);
-          for (int kv = 0; kv < 2; ++kv) {  // K first (needed first), then V
-            if (!mbar_wait(bar((kv ? bVEmpty0 : bKEmpty0) + stage), ((n >> 1) & 1) ^ 1)) { ok = false; break; }
-            const uint32_t fb = bar((kv ? bVFull0 : bKFull0) + stage);
-            mbar_arrive_expect_tx(fb, bytes);
-            const uint32_t dst0 = base + (kv ? LY::V : LY::K) + uint32_t(stage * NH) * kHalf;
-            for (int b = 0; b < kBN / B && key0 + b * B < tl.leff; ++b) {
-              const int64_t blk = __ldg(bt + (key0 + b * B) / B);
-              if (blk < 0 || blk >= p.num_blocks) {
-                if (kv == 0) raise_error(p.err, PA_DEVERR_BLOCK_RANGE);
-                continue;
-              }
-#pragma unroll
-              for (int h = 0; h < NH; ++h)
-                tc::tma_load_3d(dst0 + uint32_t(h) * kHalf + uint32_t(b * B * 128), kv ? &vmap : &kmap, 64 * h,
-                                tl.hk, int(blk * B), fb);
+          if (!mbar_wait(bar((is_k ? bKEmpty0 : bVEmpty0) + stage), (use & 1) ^ 1)) { ok = false; break; }
+          const uint32_t fb = bar((is_k ? bKFull0 : bVFull0) + stage);
+          mbar_arrive_expect_tx(fb, uint32_t(nload * B * 128 * NH));
+          const uint32_t dst0 = base + (is_k ? LY::K : LY::V) + uint32_t(stage * NH) * kHalf;
+          for (int b = 0; b < kBN / B && key0 + b * B < tl.leff; ++b) {
+            const int64_t blk = __ldg(bt + (key0 + b * B) / B);
+            if (blk < 0 || blk >= p.num_blocks) {
+              if (is_k) raise_error(p.err, PA_DEVERR_BLOCK_RANGE);
+              continue;
             }
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+              tc::tma_load_3d(dst0 + uint32_t(h) * kHalf + uint32_t(b * B * 128), map, 64 * h, tl.hk, int(blk * B), fb);
           }
-          if (!ok) break;
         }
         ++tt;
       }
@@ -255,8 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       int n = 0, tt = 0;
       // S(nn) = Q . K(nn)^T into S buffer nn % 3
       auto issue_qk = [&](int nn) -> bool {
-        const int stage = nn & 1, sb = nn % 3;
-        if (!mbar_wait(bar(bKFull0 + stage), (nn >> 1) & 1)) return false;
+        const int stage = nn % kKStages, sb = nn % 3;
+        if (!mbar_wait(bar(bKFull0 + stage), (nn / kKStages) & 1)) return false;
         if (!mbar_wait(bar(bSFree0 + sb), ((nn / 3) & 1) ^ 1)) return false;
         tc::fence_after_sync();
 #pragma unroll
@@ -285,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         for (int kb = 0; kb < tl.nt; ++kb, ++n) {
           if (!mbar_wait(bar(bPFull), n & 1)) { ok = false; break; }
           if (kb == 0 && !mbar_wait(bar(bOEmpty), (tt & 1) ^ 1)) { ok = false; break; }
-          const int stage = n & 1;
-          if (!mbar_wait(bar(bVFull0 + stage), (n >> 1) & 1)) { ok = false; break; }
+          const int stage = n % kVStages;
+          if (!mbar_wait(bar(bVFull0 + stage), (n / kVStages) & 1)) { ok = false; break; }
           tc::fence_after_sync();
           const uint32_t pcol = tmem + uint32_t((n % 3) * kBN);  // P (bf16 pairs) over S's first 64 columns
 #pragma unroll
@@ -348,17 +351,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tc::tmem_ld32(trow + uint32_t(sb * kBN + h * 64 + 32), *reinterpret_cast<float(*)[32]>(s + 32));
         tc::tmem_wait_ld();
         const int key0 = kb * kBN + h * 64;
-        float mt = -INFINITY;
         if (kb * kBN + kBN - 1 > tl.pos0) {  // a diagonal tile: causal mask
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            s[c] = (key0 + c <= mypos) ? s[c] : -INFINITY;
-            mt = fmaxf(mt, s[c]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) mt = fmaxf(mt, s[c]);
+          for (int c = 0; c < 64; ++c) s[c] = (key0 + c <= mypos) ? s[c] : -INFINITY;
         }
+        float mx[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) mx[c] = fmaxf(fmaxf(s[c], s[c + 8]), fmaxf(s[c + 16], s[c + 24]));
+#pragma unroll
+        for (int c = 0; c < 8; ++c) mx[c] = fmaxf(mx[c], fmaxf(fmaxf(s[c + 32], s[c + 40]), fmaxf(s[c + 48], s[c + 56])));
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         tc::fence_before_sync();  // S reads done before the other half overwrites S with P
         float mo;
         if (!exchange(mt, mo)) { ok = false; break; }
@@ -368,18 +370,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const float m_use = grow ? m_new : m_used;
         const float alpha = exp2f((m_used - m_use) * sc);
         const float bias = -m_use * sc;
-        float2 rs2 = make_float2(0.f, 0.f);
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};
         float pk[32];
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
           const float p0 = exp2f(fmaf(s[c], sc, bias));
           const float p1 = exp2f(fmaf(s[c + 1], sc, bias));
-          rs2.x += p0;
-          rs2.y += p1;
+          rs[(c >> 1) & 3] += p0 + p1;
           __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
           pk[c / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&hh));
         }
-        l = l * alpha + (rs2.x + rs2.y);
+        l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
         m_used = m_use;
         // O rescale needs the previous P.V finished (rare with the lazy threshold)
         if (kb > 0 && __any_sync(0xffffffffu, grow)) {
@@ -402,8 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         // last tile: V rows past the keys this tile needs may hold stale or invalid data;
         // P is 0 there, but 0 * NaN is NaN in the MMA: zero them
         if (kb == tl.nt - 1 && tl.leff - kb * kBN < kBN) {
-          const int st = n & 1;
-          if (!mbar_wait(bar(bVFull0 + st), (n >> 1) & 1)) { ok = false; break; }
+          const int st = n % kVStages;
+          if (!mbar_wait(bar(bVFull0 + st), (n / kVStages) & 1)) { ok = false; break; }
           if (r >= tl.leff - kb * kBN && h < NH) {  // thread h clears V dim-half h of row r
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
