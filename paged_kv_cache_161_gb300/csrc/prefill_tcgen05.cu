@@ -201,55 +201,68 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   if (warp == kSoftmaxWarps || warp == kSoftmaxWarps + 2) {
     // =========================== TMA producers ===========================
     // warp 8: Q (once per tile) and K (3-deep ring); warp 10: V (2-deep ring). Separate
-    // threads so that a K load never queues behind a V stage that is still in use.
+    // warps so that a K load never queues behind a V stage still in use. Lane j handles
+    // physical block j of a 128-key step: it reads that block-table entry one step ahead
+    // and issues the block's boxes itself.
+    const bool is_k = (warp == kSoftmaxWarps);
+    const CUtensorMap* map = is_k ? &kmap : &vmap;
     if (lane == 0) {
-      const bool is_k = (warp == kSoftmaxWarps);
-      const CUtensorMap* map = is_k ? &kmap : &vmap;
       if (is_k) tc::prefetch_tensormap(&qmap);
       tc::prefetch_tensormap(map);
-      const int B = p.block_size;
-      const int nst = is_k ? kKStages : kVStages;
-      int n = 0, tt = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        Tile tl;
-        tile_info<G>(p, pfx, S, t, tl);
-        if (tl.nt == 0) continue;
-        if (is_k) {
-          if (!mbar_wait(bar(bQEmpty), (tt & 1) ^ 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(bQFull), uint32_t(kBM * D * 2));
-#pragma unroll
-          for (int h = 0; h < NH; ++h)
-            tc::tma_load_3d(base + LY::Q + h * kHalf, &qmap, 64 * h, tl.hk * G, tl.qs + tl.q0, bar(bQFull));
-        }
-        const int32_t* bt = p.block_table + int64_t(tl.s) * p.max_blocks_per_seq;
-        for (int kb = 0; kb < tl.nt; ++kb, ++n) {
-          const int stage = n % nst, use = n / nst;
-          const int key0 = kb * kBN;
-          int nload = 0;
-          for (int b = 0; b < kBN / B && key0 + b * B < tl.leff; ++b) {
-            const int64_t blk = __ldg(bt + (key0 + b * B) / B);
-            if (blk >= 0 && blk < p.num_blocks) ++nload;
-          }
-          if (!mbar_wait(bar((is_k ? bKEmpty0 : bVEmpty0) + stage), (use & 1) ^ 1)) { ok = false; break; }
-          const uint32_t fb = bar((is_k ? bKFull0 : bVFull0) + stage);
-          mbar_arrive_expect_tx(fb, uint32_t(nload * B * 128 * NH));
-          const uint32_t dst0 = base + (is_k ? LY::K : LY::V) + uint32_t(stage * NH) * kHalf;
-          for (int b = 0; b < kBN / B && key0 + b * B < tl.leff; ++b) {
-            const int64_t blk = __ldg(bt + (key0 + b * B) / B);
-            if (blk < 0 || blk >= p.num_blocks) {
-              if (is_k) raise_error(p.err, PA_DEVERR_BLOCK_RANGE);
-              continue;
-            }
+    }
+    const int B = p.block_size;
+    const int nb = kBN / B;  // physical blocks per step (<= 16)
+    const int nst = is_k ? kKStages : kVStages;
+    int n = 0, tt = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      Tile tl;
+      tile_info<G>(p, pfx, S, t, tl);
+      if (tl.nt == 0) continue;
+      if (is_k) {
+        int qok = 1;
+        if (lane == 0) {
+          qok = mbar_wait(bar(bQEmpty), (tt & 1) ^ 1) ? 1 : 0;
+          if (qok) {
+            mbar_arrive_expect_tx(bar(bQFull), uint32_t(kBM * D * 2));
 #pragma unroll
             for (int h = 0; h < NH; ++h)
-              tc::tma_load_3d(dst0 + uint32_t(h) * kHalf + uint32_t(b * B * 128), map, 64 * h, tl.hk, int(blk * B), fb);
+              tc::tma_load_3d(base + LY::Q + h * kHalf, &qmap, 64 * h, tl.hk * G, tl.qs + tl.q0, bar(bQFull));
           }
         }
-        ++tt;
+        if (!__shfl_sync(0xffffffffu, qok, 0)) { ok = false; break; }
       }
-      if (!ok) fail();
+      const int32_t* bt = p.block_table + int64_t(tl.s) * p.max_blocks_per_seq;
+      auto entry = [&](int kb) -> int64_t {  // this lane's block of step kb, or -1
+        const int key = kb * kBN + lane * B;
+        return (lane < nb && key < tl.leff) ? int64_t(__ldg(bt + key / B)) : int64_t(-1);
+      };
+      int64_t ent_next = entry(0);
+      for (int kb = 0; kb < tl.nt; ++kb, ++n) {
+        const int64_t ent = ent_next;
+        if (kb + 1 < tl.nt) ent_next = entry(kb + 1);  // prefetch one step ahead
+        const bool needed = lane < nb && kb * kBN + lane * B < tl.leff;
+        const bool good = needed && ent >= 0 && ent < p.num_blocks;
+        if (is_k && needed && !good) raise_error(p.err, PA_DEVERR_BLOCK_RANGE);
+        const int nload = __popc(__ballot_sync(0xffffffffu, good));
+        const int stage = n % nst, use = n / nst;
+        const uint32_t fb = bar((is_k ? bKFull0 : bVFull0) + stage);
+        int wok = 1;
+        if (lane == 0) {
+          wok = mbar_wait(bar((is_k ? bKEmpty0 : bVEmpty0) + stage), (use & 1) ^ 1) ? 1 : 0;
+          if (wok) mbar_arrive_expect_tx(fb, uint32_t(nload * B * 128 * NH));
+        }
+        if (!__shfl_sync(0xffffffffu, wok, 0)) { ok = false; break; }
+        if (good) {
+          const uint32_t dst = base + (is_k ? LY::K : LY::V) + uint32_t(stage * NH) * kHalf + uint32_t(lane * B * 128);
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+            tc::tma_load_3d(dst + uint32_t(h) * kHalf, map, 64 * h, tl.hk, int(ent * B), fb);
+        }
+      }
+      ++tt;
     }
+    if (!ok && lane == 0) fail();
   } else if (warp == kSoftmaxWarps + 1) {
     // =========================== MMA issuer ===========================
     if (lane == 0) {
