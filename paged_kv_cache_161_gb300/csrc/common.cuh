@@ -142,6 +142,39 @@ __device__ __forceinline__ void ffma2(float2& d, const float2 a, const float2 b)
   d.y = __uint_as_float(static_cast<uint32_t>(dd >> 32));
 }
 
+// Packed fp32 add (sm_100 family): (a.x + b.x, a.y + b.y).
+__device__ __forceinline__ float2 fadd2(const float2 a, const float2 b) {
+  unsigned long long d;
+  const unsigned long long aa = (static_cast<unsigned long long>(__float_as_uint(a.y)) << 32) | __float_as_uint(a.x);
+  const unsigned long long bb = (static_cast<unsigned long long>(__float_as_uint(b.y)) << 32) | __float_as_uint(b.x);
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(aa), "l"(bb));
+  return make_float2(__uint_as_float(static_cast<uint32_t>(d)), __uint_as_float(static_cast<uint32_t>(d >> 32)));
+}
+
+// Packed fp32 fused multiply-add: (a.x * b.x + c.x, a.y * b.y + c.y).
+__device__ __forceinline__ float2 ffma2v(const float2 a, const float2 b, const float2 c) {
+  unsigned long long d;
+  const unsigned long long aa = (static_cast<unsigned long long>(__float_as_uint(a.y)) << 32) | __float_as_uint(a.x);
+  const unsigned long long bb = (static_cast<unsigned long long>(__float_as_uint(b.y)) << 32) | __float_as_uint(b.x);
+  const unsigned long long cc = (static_cast<unsigned long long>(__float_as_uint(c.y)) << 32) | __float_as_uint(c.x);
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(aa), "l"(bb), "l"(cc));
+  return make_float2(__uint_as_float(static_cast<uint32_t>(d)), __uint_as_float(static_cast<uint32_t>(d >> 32)));
+}
+
+// Three-input maximum (sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 2^x with the hardware approximation (subnormal results flushed to zero).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Wait until the preceding grid in the stream has completed and its writes are visible
 // (returns at once when the kernel was launched without the PDL attribute).

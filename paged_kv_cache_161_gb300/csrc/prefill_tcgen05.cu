@@ -368,12 +368,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
           for (int c = 0; c < 64; ++c) s[c] = (key0 + c <= mypos) ? s[c] : -INFINITY;
         }
-        float mx[8];
+        // row max of this half: 3-input max tree (64 -> 22 -> 8 -> 3 -> 1)
+        float m22[22];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) mx[c] = fmaxf(fmaxf(s[c], s[c + 8]), fmaxf(s[c + 16], s[c + 24]));
+        for (int c = 0; c < 21; ++c) m22[c] = fmax3(s[3 * c], s[3 * c + 1], s[3 * c + 2]);
+        m22[21] = s[63];
+        float m8[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) mx[c] = fmaxf(mx[c], fmaxf(fmaxf(s[c + 32], s[c + 40]), fmaxf(s[c + 48], s[c + 56])));
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int c = 0; c < 7; ++c) m8[c] = fmax3(m22[3 * c], m22[3 * c + 1], m22[3 * c + 2]);
+        m8[7] = m22[21];
+        const float mt = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         tc::fence_before_sync();  // S reads done before the other half overwrites S with P
         float mo;
         if (!exchange(mt, mo)) { ok = false; break; }
@@ -383,17 +387,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const float m_use = grow ? m_new : m_used;
         const float alpha = exp2f((m_used - m_use) * sc);
         const float bias = -m_use * sc;
-        float rs[4] = {0.f, 0.f, 0.f, 0.f};
+        // p = 2^(s * scale_log2 - m * scale_log2): one packed FMA per pair, hardware ex2
+        float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         float pk[32];
+        const float2 sc2 = make_float2(sc, sc), bias2 = make_float2(bias, bias);
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          const float p0 = exp2f(fmaf(s[c], sc, bias));
-          const float p1 = exp2f(fmaf(s[c + 1], sc, bias));
-          rs[(c >> 1) & 3] += p0 + p1;
-          __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+          const float2 x = ffma2v(make_float2(s[c], s[c + 1]), sc2, bias2);
+          const float2 pp = make_float2(ex2_ftz(x.x), ex2_ftz(x.y));
+          rs[(c >> 1) & 3] = fadd2(rs[(c >> 1) & 3], pp);
+          __nv_bfloat162 hh = __floats2bfloat162_rn(pp.x, pp.y);
           pk[c / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&hh));
         }
-        l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+        const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
+        l = l * alpha + ((r01.x + r01.y) + (r23.x + r23.y));
         m_used = m_use;
         // O rescale needs the previous P.V finished (rare with the lazy threshold)
         if (kb > 0 && __any_sync(0xffffffffu, grow)) {
