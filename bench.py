@@ -42,9 +42,12 @@ def _args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--workload", choices=["gqa_decode", "mixed"], default="gqa_decode",
+    ap.add_argument("--workload", choices=["gqa_decode", "mixed", "mha_decode", "shared_prefix"],
+                    default="gqa_decode",
                     help="gqa_decode: the headline line (default); mixed: the chunked-prefill + decode "
-                         "batch, timed whole and as its prefill-only and decode-only sub-batches")
+                         "batch, timed whole and as its prefill-only and decode-only sub-batches; "
+                         "mha_decode: 64 requests, 32/32 heads; shared_prefix: 64 prompts x 4 samples with "
+                         "copy-on-write block copies")
     a = ap.parse_args(argv)
     a.warmup = max(3, a.warmup)
     return a
@@ -502,12 +505,100 @@ def run_mixed(a):
     return 0
 
 
+def run_secondary(a):
+    """MHA decode (attention only) or shared-prefix sampling (copy-on-write copies, write,
+    attention): per-operation times and bytes on one GPU, device-resident inputs."""
+    import torch
+
+    import paged_kv_cache_161_gb300 as pa
+    import workloads
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    cfg = 2 if a.workload == "mha_decode" else 4
+    wl = workloads.build(cfg)
+    sp = wl.spec
+    dw = DeviceWorkload(wl, device=dev)
+    dw.run_setup()
+    st = dw.prepare_step()
+    stream = torch.cuda.current_stream(dev)
+    hbm, _, src = _peaks()
+
+    def timed(fn, steps, warm):
+        for _ in range(warm):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    steps = max(20, a.steps // 4)
+    pa.read_device_errors(clear=True)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    attn = lambda: pa.attention(st.out, st.q, dw.k_cache, dw.v_cache, st.block_table, st.seq_lens,  # noqa: E731
+                                st.query_start_loc, max_query_len=st.max_query_len, max_seq_len=st.max_seq_len,
+                                scale=sp.scale, workspace=st.workspace, stream=stream)
+    attn_ms = timed(attn, steps, a.warmup)
+    lens = st.seq_lens.cpu().long()
+    logical = int(lens.sum()) * sp.kv_token_bytes
+    line = {"metric": f"{wl.name}: attention K/V GB/s", "n_gpus": 1, "steps": steps, "warmup": a.warmup,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic", "peak_gbs": hbm, "peak_source": src,
+            "attention_ms": attn_ms, "attention_gbs_logical": logical / (attn_ms * 1e-3) / 1e9,
+            "config": {"workload": wl.name, "requests": int(lens.numel()), "kv_bytes_logical": logical,
+                       "seed": wl.seed}}
+    if cfg == 4:
+        # unique bytes: each physical block read once however many samples share it
+        table = st.block_table.cpu()
+        B = sp.block_size
+        seen = set()
+        uniq_tokens = 0
+        for i in range(table.shape[0]):
+            L = int(lens[i])
+            for j in range((L + B - 1) // B):
+                b = int(table[i, j])
+                if b not in seen:
+                    seen.add(b)
+                    uniq_tokens += B if (j + 1) * B <= L else L - j * B
+        uniq = uniq_tokens * sp.kv_token_bytes
+        pairs = torch.cat([torch.from_numpy(c.reshape(-1, 2)) for c in dw.phase_copies if len(c)]).to(dev)
+        cp_ms = timed(lambda: pa.copy_blocks(dw.k_cache, dw.v_cache, pairs, stream=stream), steps, a.warmup)
+        block_bytes = B * sp.num_kv_heads * sp.head_dim * 2 * 2  # K and V
+        cp_bytes = 2 * int(pairs.shape[0]) * block_bytes  # read + write
+        wr_ms = timed(lambda: pa.kv_write(st.k_new, st.v_new, dw.k_cache, dw.v_cache, st.slot_mapping,
+                                          stream=stream), steps, a.warmup)
+        wr_bytes = 2 * int(st.slot_mapping.shape[0]) * sp.kv_token_bytes
+        line.update({
+            "attention_gbs_unique": uniq / (attn_ms * 1e-3) / 1e9, "frac_unique": uniq / (attn_ms * 1e-3) / 1e9 / hbm,
+            "copy_blocks": {"pairs": int(pairs.shape[0]), "ms": cp_ms, "gbs": cp_bytes / (cp_ms * 1e-3) / 1e9,
+                            "bytes": cp_bytes},
+            "kv_write": {"tokens": int(st.slot_mapping.shape[0]), "ms": wr_ms,
+                         "gbs": wr_bytes / (wr_ms * 1e-3) / 1e9},
+        })
+        line["config"]["kv_bytes_unique"] = uniq
+    else:
+        line["frac_logical"] = line["attention_gbs_logical"] / hbm
+    line["clocks"] = clocks.stop()
+    if pa.read_device_errors(clear=True):
+        raise RuntimeError("device error flags set")
+    print(json.dumps(line))
+    return 0
+
+
 def main(argv=None):
     a = _args(argv)
     if a.impl == "reference":
         return run_reference(a)
     if a.workload == "mixed":
         return run_mixed(a)
+    if a.workload in ("mha_decode", "shared_prefix"):
+        return run_secondary(a)
     return run_ours(a)
 
 
