@@ -212,6 +212,12 @@ int pa_bm_add_seq(pa_bm* bm, int64_t seq);               /* PA_ERR_NOT_FOUND if 
  * PA_ERR_NO_BLOCKS: the free queue is too short now; PA_ERR_TOO_LARGE: the sequence
  * would need more blocks than the pool has. */
 int pa_bm_append(pa_bm* bm, int64_t seq, int64_t n, int64_t* slots_out);
+/* Batched append: for i in [0, n), appends counts[i] >= 0 tokens to seqs[i], in order, writing
+ * all slots concatenated to slots_out (capacity >= sum of counts). Stops at the first append
+ * that fails and returns its status; *done_out (if not NULL) gets the number of entries fully
+ * applied, so those appends stay and the rest are not attempted. */
+int pa_bm_append_batch(pa_bm* bm, const int64_t* seqs, const int64_t* counts, int64_t n,
+                       int64_t* slots_out, int64_t* done_out);
 int pa_bm_fork(pa_bm* bm, int64_t parent, int64_t child); /* child shares parent's blocks */
 int pa_bm_free_seq(pa_bm* bm, int64_t seq);               /* counts - 1, release at 0 */
 int64_t pa_bm_seq_len(const pa_bm* bm, int64_t seq);      /* -1 if unknown */

@@ -52,6 +52,7 @@ _sig = {
     "pa_bm_destroy": (None, [_p]),
     "pa_bm_add_seq": (_i, [_p, _i64]),
     "pa_bm_append": (_i, [_p, _i64, _i64, _p]),
+    "pa_bm_append_batch": (_i, [_p, _p, _p, _i64, _p, _p]),
     "pa_bm_fork": (_i, [_p, _i64, _i64]),
     "pa_bm_free_seq": (_i, [_p, _i64]),
     "pa_bm_seq_len": (_i64, [_p, _i64]),
@@ -219,6 +220,24 @@ class BlockManager:
         _check(lib.pa_bm_append(self._h, seq, n, out.ctypes.data if n > 0 else None), "pa_bm_append")
         return out
 
+    def append_batch(self, seqs, counts, out=None):
+        """Append counts[i] tokens to seqs[i] for every i (one C call); returns the slots,
+        concatenated (numpy int64). ``out`` may be a preallocated int64 array."""
+        import numpy as np
+
+        s = np.ascontiguousarray(np.asarray(seqs, np.int64))
+        c = np.ascontiguousarray(np.asarray(counts, np.int64))
+        total = int(c.sum())
+        if out is None:
+            out = np.empty(total, np.int64)
+        elif out.dtype != np.int64 or not out.flags.c_contiguous or out.size < total:
+            raise ValueError("out must be a contiguous int64 array of at least sum(counts) entries")
+        done = ctypes.c_int64(0)
+        st = lib.pa_bm_append_batch(self._h, s.ctypes.data if len(s) else None, c.ctypes.data if len(c) else None,
+                                    len(s), out.ctypes.data if total else None, ctypes.byref(done))
+        _check(st, f"pa_bm_append_batch (stopped after {done.value} entries)")
+        return out[:total]
+
     def fork(self, parent: int, child: int):
         _check(lib.pa_bm_fork(self._h, parent, child), "pa_bm_fork")
 
@@ -251,13 +270,17 @@ class BlockManager:
         _check(lib.pa_bm_block_table(self._h, seq, out.ctypes.data if n else None, n), "pa_bm_block_table")
         return out
 
-    def batch_tables(self, seqs, width: int):
-        """(block_table int32 [n, width], seq_lens int32 [n]) for the sequences ``seqs``."""
+    def batch_tables(self, seqs, width: int, table_out=None, lens_out=None):
+        """(block_table int32 [n, width], seq_lens int32 [n]) for the sequences ``seqs``,
+        written into ``table_out`` / ``lens_out`` when given (contiguous int32 arrays)."""
         import numpy as np
 
         s = np.ascontiguousarray(np.asarray(seqs, np.int64))
-        table = np.empty((len(s), width), np.int32)
-        lens = np.empty(len(s), np.int32)
+        table = np.empty((len(s), width), np.int32) if table_out is None else table_out
+        lens = np.empty(len(s), np.int32) if lens_out is None else lens_out
+        if table.shape != (len(s), width) or lens.shape != (len(s),) or table.dtype != np.int32 or \
+                lens.dtype != np.int32 or not table.flags.c_contiguous or not lens.flags.c_contiguous:
+            raise ValueError("table_out must be int32 [n, width] and lens_out int32 [n], contiguous")
         _check(lib.pa_bm_batch_tables(self._h, s.ctypes.data if len(s) else None, len(s),
                                       table.ctypes.data if len(s) else None, width,
                                       lens.ctypes.data if len(s) else None), "pa_bm_batch_tables")

@@ -108,6 +108,20 @@ int pa_bm_append(pa_bm* bm, int64_t seq, int64_t n, int64_t* slots_out) {
   return PA_OK;
 }
 
+int pa_bm_append_batch(pa_bm* bm, const int64_t* seqs, const int64_t* counts, int64_t n, int64_t* slots_out,
+                       int64_t* done_out) {
+  if (done_out) *done_out = 0;
+  if (!bm || n < 0 || (n > 0 && (!seqs || !counts))) return PA_ERR_INVALID_ARG;
+  int64_t off = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const int st = pa_bm_append(bm, seqs[i], counts[i], counts[i] > 0 ? slots_out + off : nullptr);
+    if (st != PA_OK) return st;
+    off += counts[i];
+    if (done_out) *done_out = i + 1;
+  }
+  return PA_OK;
+}
+
 int pa_bm_fork(pa_bm* bm, int64_t parent, int64_t child) {
   if (!bm) return PA_ERR_INVALID_ARG;
   auto it = bm->seqs.find(parent);

@@ -162,3 +162,34 @@ def test_workload_accounting_matches_oracle(cfg, size):
         t = ref.block_table(s)
         assert table[i, : len(t)].tolist() == t and not table[i, len(t):].any()
         assert lens[i] == ref.seq_len(s)
+
+
+def test_batched_append_matches_sequential_appends():
+    rng = random.Random(7)
+    order = rng.sample(range(64), 64)
+    ref = BlockAllocator(64, 4, order)
+    bm = pa.BlockManager(64, 4, order)
+    for sq in range(6):
+        ref.add_seq(sq)
+        bm.add_seq(sq)
+    ref.append(0, 5)
+    bm.append(0, 5)
+    ref.fork(0, 6)
+    bm.fork(0, 6)
+    seqs = [0, 6, 1, 2, 3, 6, 4, 5]
+    counts = [3, 2, 0, 9, 1, 4, 7, 2]
+    want = [sl for sq, c in zip(seqs, counts) for sl in ref.append(sq, c)]
+    got = bm.append_batch(seqs, counts)
+    assert got.tolist() == want
+    assert [list(p) for p in ref.take_copies()] == bm.take_copies().tolist()
+    _compare(ref, bm, range(7))
+
+
+def test_batched_append_stops_at_first_failure():
+    bm = pa.BlockManager(4, 4, range(4))
+    for sq in range(3):
+        bm.add_seq(sq)
+    with pytest.raises(pa.PAError) as e:
+        bm.append_batch([0, 1, 2], [8, 8, 1])  # the second needs 2 blocks, only 2 left -> ok; third fails
+    assert e.value.status == 5 and "after 2 entries" in str(e.value)
+    assert bm.seq_len(0) == 8 and bm.seq_len(1) == 8 and bm.seq_len(2) == 0
