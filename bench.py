@@ -68,6 +68,23 @@ def _workload_config(wl, l2_note):
     }
 
 
+# ----------------------------------------------------------------------------- multi-rank
+def max_over_ranks(vals, dist=None, device="cpu"):
+    """Element-wise maximum of ``vals`` over all ranks (the slowest rank's times)."""
+    if dist is None:
+        return [float(v) for v in vals]
+    import torch
+
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_gbs(world, bytes_per_rank, ms_per_step):
+    """Whole-job throughput: every rank's bytes over the slowest rank's step time."""
+    return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -279,11 +296,8 @@ def run_ours(a):
         raise RuntimeError(f"device error flags {flags:#x}")
     step_ms = t_start.elapsed_time(t_end) / a.steps
     attn_ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / a.steps
-    if dist is not None:
-        tt = torch.tensor([step_ms, attn_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        step_ms, attn_ms = tt.tolist()
-    value = world * kv_bytes / (step_ms * 1e-3) / 1e9
+    step_ms, attn_ms = max_over_ranks([step_ms, attn_ms], dist, dev)
+    value = job_gbs(world, kv_bytes, step_ms)
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -399,14 +413,11 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
     for _ in range(steps):
         kv_bytes_steps.append(one_step())
     secs = (time.perf_counter() - t0) / steps
-    if dist is not None:
-        t = torch.tensor([secs], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        secs = t.item()
+    secs = max_over_ranks([secs], dist, dev)[0]
     if pa.read_device_errors(clear=True):
         raise RuntimeError("device error flags set during the end-to-end run")
     mean_bytes = sum(kv_bytes_steps) / len(kv_bytes_steps)
-    return {"value": world * mean_bytes / secs / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+    return {"value": job_gbs(world, mean_bytes, secs * 1e3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": secs * 1e3, "steps": steps, "warmup": warm,
             "includes": "host block accounting (pa_bm_append_batch, pa_bm_batch_tables) into pinned memory, one "
                         "H2D copy of q/k/v/slots/table/lens/query_start_loc, pa_kv_write, pa_attention, D2H of out"}
