@@ -11,7 +11,7 @@
 // Design (sm_103a):
 //  * Work unit = 16 consecutive logical tokens of one request for one group of HG KV
 //    heads ("stage"): 16 x HG x D elements of K and the same of V (64 KiB for bf16,
-//    HG = 8, D = 128). Units are numbered head-group-major, then request, then
+//    HG = 8, D = 128). Units are numbered request-major, then head group, then
 //    position; the grid (one CTA per SM) splits that numbering into equal contiguous
 //    ranges, so every SM streams the same number of bytes whatever the length mix.
 //    A request cut by a range boundary leaves one partial result per CTA; the merge
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
     // give a decode query without keys a zero output.
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
       if (units_of(decode_len(p, s)) > 0) continue;
-      for (int hg = 0; hg < p.num_hg; ++hg) p.ws_meta[int64_t(hg) * S + s] = make_int4(-1, -1, 0, 0);
+      for (int hg = 0; hg < p.num_hg; ++hg) p.ws_meta[int64_t(s) * p.num_hg + hg] = make_int4(-1, -1, 0, 0);
       const int q0 = __ldg(p.qsl + s);
       if (__ldg(p.qsl + s + 1) - q0 == 1) {
         raise_error(p.err, PA_DEVERR_SEQ_RANGE);
@@ -295,23 +295,26 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
   }
   const int64_t u_begin = c * U / C_, u_end = (c + 1) * U / C_;
   if (u_begin >= u_end) return;
-  const int start_hg = int(u_begin / units_per_hg);
-  const int rem = int(u_begin % units_per_hg);
-  int run = 0;
+  // units are numbered request-major: (request, head group, position), so the head groups
+  // of one request (the other slices of the same cache rows) are streamed back to back
+  const int64_t rem = u_begin;
+  int64_t run = 0;
   for (int base = 0; base < S; base += blockDim.x) {
     const int s = base + threadIdx.x;
-    const int us = s < S ? units_of(decode_len(p, s)) : 0;
+    const int us = s < S ? units_of(decode_len(p, s)) * p.num_hg : 0;
     int total;
     const int ex = block_exclusive_scan(us, red, &total);
     if (us > 0 && run + ex <= rem && rem < run + ex + us) {
       red[34] = s;
-      red[35] = rem - (run + ex);
+      red[35] = int(rem - (run + ex));
     }
     __syncthreads();
     run += total;
     if (run > rem) break;
   }
-  const int start_s = red[34], start_j = red[35];
+  const int start_s = red[34];
+  const int start_us = units_of(decode_len(p, start_s));
+  const int start_hg = red[35] / start_us, start_j = red[35] % start_us;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -412,17 +415,17 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
       }
       if (++j == units_s && u + 1 < u_end) {
         j = 0;
-        do {
-          if (++s == S) {
-            s = 0;
-            if (++hg >= p.num_hg) break;  // cannot happen: the plan counted these units
+        if (++hg == p.num_hg) {
+          hg = 0;
+          do {
+            if (++s >= S) break;  // cannot happen: the plan counted these units
+            L = decode_len(p, s);
+            units_s = units_of(L);
+          } while (units_s == 0);
+          if (s >= S) {
+            raise_error(p.err, PA_DEVERR_TIMEOUT);
+            break;
           }
-          L = decode_len(p, s);
-          units_s = units_of(L);
-        } while (units_s == 0);
-        if (hg >= p.num_hg) {
-          raise_error(p.err, PA_DEVERR_TIMEOUT);
-          break;
         }
       }
     }
@@ -653,7 +656,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
         if (whole) {
           RowVec<T, VEC>::store(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + lir * VEC, o);
         } else {
-          const int64_t slot = c + int64_t(d.hg) * S + d.s;
+          const int64_t slot = c + int64_t(d.s) * p.num_hg + d.hg;
           const int64_t hrow = slot * (HG * GF) + hk * GF + qg * G + g;
           float* dst = p.ws_o + hrow * D + lir * VEC;
 #pragma unroll
@@ -664,7 +667,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
       }
     }
     if (warp == 0 && lane == 0) {
-      const int64_t v = int64_t(d.hg) * S + d.s;
+      const int64_t v = int64_t(d.s) * p.num_hg + d.hg;
       if (d.flags & kSeqStart) {
         p.ws_meta[v].x = int(c);
         p.ws_meta[v].z = units_per_hg;
@@ -683,9 +686,8 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
 template <typename T, int D>
 __global__ void __launch_bounds__(1024) decode_merge_kernel(const __grid_constant__ DecodeParams p, int group) {
   griddep_wait();  // the split-K grid's pieces and descriptors must be complete and visible
-  const int S = p.num_seqs;
   const int v = blockIdx.x;
-  const int hg = v / S;
+  const int hg = v % p.num_hg;
   const int4 meta = p.ws_meta[v];
   if (meta.x < 0 || meta.x == meta.y) return;  // nothing to merge / one CTA wrote `out` itself
   if (meta.y >= p.num_ctas || meta.x > meta.y || meta.z <= 0) {
