@@ -30,6 +30,26 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention: K/V GB/s (% of GB300 HBM peak) and tokens/s, batch 256"
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one pa_attention decode call
+# on this workload -- split-K kernel plus merge kernel -- from one ncu capture of
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum \
+#       --clock-control none -k regex:"decode_(splitk|merge)" -s 6 -c 2 \
+#       python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-e2e
+# It holds only for the kernel sources it was measured on (their SHA-256 below); any
+# change to them makes the reported traffic null until it is measured again.
+DECODE_TRAFFIC = {"sources_sha256": "d425c1a0ebca866139d2c7a45a14daaecc877d898b375e7f4d6c4be90cf48c41", "bytes": 1646223616}
+DECODE_SOURCES = ["paged_kv_cache_161_gb300/csrc/decode_attention.cu", "paged_kv_cache_161_gb300/csrc/common.cuh"]
+
+
+def _decode_traffic():
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return DECODE_TRAFFIC["bytes"] if h.hexdigest() == DECODE_TRAFFIC["sources_sha256"] else None
 FALLBACK_HBM_GBS = 6800.0
 CONFIG_ID = 3
 
@@ -311,7 +331,7 @@ def run_ours(a):
         peak, peak_src = FALLBACK_HBM_GBS, "fallback"
     achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": None, "kernel": "pa_attention decode (split-K kernel + merge kernel)",
+                "traffic": _decode_traffic(), "algorithmic_bytes": kv_bytes, "kernel": "pa_attention decode (split-K kernel + merge kernel)",
                 "peak_source": peak_src, "attention_ms": attn_ms,
                 "frac_of_nominal_8TBs": achieved / 8000.0}
 
