@@ -168,28 +168,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// 2^x for a pair, evaluated on the FMA/ALU pipes instead of the MUFU unit (to share the
-// load when a kernel issues more ex2 than MUFU sustains). Cody-Waite split x = n + f with
-// n = round(x) and |f| <= 1/2; 2^f by a degree-3 polynomial fitted for the smallest maximum
-// relative error on [-1/2, 1/2] (1.01e-4, ample for results rounded to bf16); 2^n added
-// to the exponent bits. Valid for x <= 64; x <= -127 (including -inf) gives exactly 0.
-constexpr float kExp2C1 = 0.6932829f, kExp2C2 = 0.24221066f, kExp2C3 = 0.05500871f;
-constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23: x + it holds round(x) in its low mantissa bits
-
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  x.x = fmaxf(x.x, -127.f);
-  x.y = fmaxf(x.y, -127.f);
-  const float2 t = fadd2(x, make_float2(kRoundMagic, kRoundMagic));
-  const float2 n = fadd2(t, make_float2(-kRoundMagic, -kRoundMagic));  // round(x), exact
-  const float2 f = ffma2v(n, make_float2(-1.f, -1.f), x);                 // x - n, exact
-  float2 p = ffma2v(make_float2(kExp2C3, kExp2C3), f, make_float2(kExp2C2, kExp2C2));
-  p = ffma2v(p, f, make_float2(kExp2C1, kExp2C1));
-  p = ffma2v(p, f, make_float2(1.f, 1.f));
-  // bits(t) = bits(magic) + n and bits(magic) << 23 wraps to 0, so bits(t) << 23 = n << 23
-  return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
-                     __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
-}
-
 // 2^x with the hardware approximation (subnormal results flushed to zero).
 __device__ __forceinline__ float ex2_ftz(float x) {
   float y;

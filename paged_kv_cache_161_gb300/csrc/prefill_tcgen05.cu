@@ -423,9 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
             const float2 xv = ffma2v(make_float2(s[c], s[c + 1]), sc2, bias2);
-            // 3 of every 8 pairs on the FMA pipe, the rest on MUFU: the exp pass is
-            // MUFU-bound otherwise
-            const float2 pp = ((c >> 1) & 7) < 3 ? exp2_poly2(xv) : make_float2(ex2_ftz(xv.x), ex2_ftz(xv.y));
+            const float2 pp = make_float2(ex2_ftz(xv.x), ex2_ftz(xv.y));
             rs[(c >> 1) & 3] = fadd2(rs[(c >> 1) & 3], pp);
             __nv_bfloat162 hh = __floats2bfloat162_rn(pp.x, pp.y);
             pk[c / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&hh));
