@@ -31,14 +31,15 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention: K/V GB/s (% of GB300 HBM peak) and tokens/s, batch 256"
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one pa_attention decode call
-# on this workload -- split-K kernel plus merge kernel -- from one ncu capture of
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one pa_write_attention decode
+# call on this workload -- split-K kernel (KV write fused in) plus merge kernel -- from one
+# ncu capture (the first timed step's two launches) of
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum \
-#       --clock-control none -k regex:"decode_(splitk|merge)" -s 6 -c 2 \
+#       --clock-control none --csv --log-file launches.csv \
 #       python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-e2e
 # It holds only for the kernel sources it was measured on (their SHA-256 below); any
 # change to them makes the reported traffic null until it is measured again.
-DECODE_TRAFFIC = {"sources_sha256": "d425c1a0ebca866139d2c7a45a14daaecc877d898b375e7f4d6c4be90cf48c41", "bytes": 1646223616}
+DECODE_TRAFFIC = {"sources_sha256": "26c642349bb987f141491e3d9c786561bc684e21c921e75a482fb41b04234d3e", "bytes": 1644220416}
 DECODE_SOURCES = ["paged_kv_cache_161_gb300/csrc/decode_attention.cu", "paged_kv_cache_161_gb300/csrc/common.cuh"]
 
 
@@ -290,9 +291,23 @@ def run_ours(a):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # ---- device-resident timing: K steps of (KV write + attention)
+    # ---- device-resident timing: K steps of (KV write + attention), the write fused into
+    # the decode kernel (pa_write_attention: split-K kernel + merge kernel per step)
+    def fused_step():
+        pa.write_attention(st.out, st.q, st.k_new, st.v_new, st.slot_mapping, dw.k_cache, dw.v_cache,
+                           st.block_table, st.seq_lens, st.query_start_loc, max_query_len=st.max_query_len,
+                           max_seq_len=st.max_seq_len, scale=sp.scale, workspace=st.workspace, stream=stream)
+
+    def unfused_write():
+        pa.kv_write(st.k_new, st.v_new, dw.k_cache, dw.v_cache, st.slot_mapping, stream=stream)
+
+    def unfused_attention():
+        pa.attention(st.out, st.q, dw.k_cache, dw.v_cache, st.block_table, st.seq_lens, st.query_start_loc,
+                     max_query_len=st.max_query_len, max_seq_len=st.max_seq_len, scale=sp.scale,
+                     workspace=st.workspace, stream=stream)
+
     for _ in range(a.warmup):
-        dw.run_step(st)
+        fused_step()
     pa.read_device_errors(clear=True)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -302,11 +317,8 @@ def run_ours(a):
     time.sleep(0.3)  # let the sampler take its first reading
     t_start.record(stream)
     for i in range(a.steps):
-        pa.kv_write(st.k_new, st.v_new, dw.k_cache, dw.v_cache, st.slot_mapping, stream=stream)
         ev[i][0].record(stream)
-        pa.attention(st.out, st.q, dw.k_cache, dw.v_cache, st.block_table, st.seq_lens, st.query_start_loc,
-                     max_query_len=st.max_query_len, max_seq_len=st.max_seq_len, scale=sp.scale,
-                     workspace=st.workspace, stream=stream)
+        fused_step()
         ev[i][1].record(stream)
     t_end.record(stream)
     barrier()
@@ -318,6 +330,26 @@ def run_ours(a):
     attn_ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / a.steps
     step_ms, attn_ms = max_over_ranks([step_ms, attn_ms], dist, dev)
     value = job_gbs(world, kv_bytes, step_ms)
+
+    # ---- the same step as two calls (pa_kv_write, then pa_attention), for comparison
+    for _ in range(a.warmup):
+        unfused_write()
+        unfused_attention()
+    uev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    barrier()
+    t_start.record(stream)
+    for i in range(a.steps):
+        unfused_write()
+        uev[i][0].record(stream)
+        unfused_attention()
+        uev[i][1].record(stream)
+    t_end.record(stream)
+    barrier()
+    if pa.read_device_errors(clear=True):
+        raise RuntimeError("device error flags set during the two-call comparison")
+    u_step_ms = t_start.elapsed_time(t_end) / a.steps
+    u_attn_ms = sum(e0.elapsed_time(e1) for e0, e1 in uev) / a.steps
+    u_step_ms, u_attn_ms = max_over_ranks([u_step_ms, u_attn_ms], dist, dev)
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -331,7 +363,8 @@ def run_ours(a):
         peak, peak_src = FALLBACK_HBM_GBS, "fallback"
     achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": _decode_traffic(), "algorithmic_bytes": kv_bytes, "kernel": "pa_attention decode (split-K kernel + merge kernel)",
+                "traffic": _decode_traffic(), "algorithmic_bytes": kv_bytes,
+                "kernel": "pa_write_attention decode (split-K kernel with the KV write fused in + merge kernel)",
                 "peak_source": peak_src, "attention_ms": attn_ms,
                 "frac_of_nominal_8TBs": achieved / 8000.0}
 
@@ -354,7 +387,10 @@ def run_ours(a):
             "tokens_per_s": world * n_req / (step_ms * 1e-3),
             "hbm_frac_of_measured": value / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": a.steps * 3, "clocks": clk,
+            "gpu_launches": a.steps * 2, "clocks": clk,
+            "two_call_step": {"ms_per_step": u_step_ms, "attention_ms": u_attn_ms,
+                              "value": job_gbs(world, kv_bytes, u_step_ms), "unit": "GB/s",
+                              "calls": "pa_kv_write then pa_attention (3 launches), timed after the fused steps"},
         }
         print(json.dumps(line))
     if dist is not None:
@@ -414,9 +450,9 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
         bm.batch_tables(seqs, width, table_out=table_h, lens_out=lens_h)
         with torch.cuda.stream(stream):
             d_buf.copy_(h_buf, non_blocking=True)
-            pa.kv_write(k_d, v_d, dw.k_cache, dw.v_cache, slots_d, stream=stream)
-            pa.attention(out_d, q_d, dw.k_cache, dw.v_cache, table_d, lens_d, qsl_d, max_query_len=1,
-                         max_seq_len=int(lens_h.max()), scale=sp.scale, workspace=st.workspace, stream=stream)
+            pa.write_attention(out_d, q_d, k_d, v_d, slots_d, dw.k_cache, dw.v_cache, table_d, lens_d, qsl_d,
+                               max_query_len=1, max_seq_len=int(lens_h.max()), scale=sp.scale,
+                               workspace=st.workspace, stream=stream)
             out_h.copy_(out_d, non_blocking=True)
         stream.synchronize()
         return int(lens_h.astype(np.int64).sum()) * sp.kv_token_bytes
@@ -440,7 +476,7 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
     return {"value": job_gbs(world, mean_bytes, secs * 1e3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": secs * 1e3, "steps": steps, "warmup": warm,
             "includes": "host block accounting (pa_bm_append_batch, pa_bm_batch_tables) into pinned memory, one "
-                        "H2D copy of q/k/v/slots/table/lens/query_start_loc, pa_kv_write, pa_attention, D2H of out"}
+                        "H2D copy of q/k/v/slots/table/lens/query_start_loc, pa_write_attention, D2H of out"}
 
 
 def _peaks():

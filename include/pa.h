@@ -1,9 +1,10 @@
 /*
  * pa.h -- C ABI of the GB300 (sm_103a) paged-KV-cache hot path.
  *
- * Three device operations and a host block manager:
+ * Device operations and a host block manager:
  *   pa_kv_write     scatter new tokens' K/V into physical cache blocks through slot_mapping
  *   pa_attention    paged decode and chunked-prefill attention through block_table
+ *   pa_write_attention  the two above in one call (the write fused into decode)
  *   pa_copy_blocks  copy whole physical blocks (the copy step of copy-on-write)
  *   pa_bm_*         host-side block accounting: free queue, block tables, ref counts, CoW
  *
@@ -70,6 +71,7 @@ typedef enum {
 #define PA_DEVERR_BLOCK_RANGE  0x2u  /* a block id outside [0, num_blocks) was skipped */
 #define PA_DEVERR_SEQ_RANGE    0x4u  /* seq_len > max_blocks_per_seq * block_size, or q_len > seq_len */
 #define PA_DEVERR_TIMEOUT      0x8u  /* a pipeline wait gave up (the kernel returned early) */
+#define PA_DEVERR_SLOT_MISMATCH 0x10u /* pa_write_attention: a decode token's slot is not its position's slot */
 
 const char* pa_status_string(int status);
 int pa_last_cuda_error(void);
@@ -158,6 +160,38 @@ int pa_attention(void* out, const void* q, const void* k_cache, const void* v_ca
                  int max_query_len, int max_seq_len, int num_heads, int num_kv_heads,
                  int head_dim, int block_size, int64_t num_blocks, float scale,
                  pa_dtype dtype, void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------
+ * pa_write_attention -- pa_kv_write followed by pa_attention, in one call:
+ * [docs] PagedAttention algorithm flow (decode step d stores the new token's KV in its
+ * block, then attends over all of the request's blocks); [flow] 3.3 / 3.5 (slot_mapping
+ * feeds the cache write that precedes attention in the same forward pass).
+ *
+ * Result (cache and out) identical to pa_kv_write(k_new, v_new, ..., slot_mapping,
+ * num_tokens, ...) then pa_attention(...) on one stream, under one extra contract: for
+ * a request with q_len == 1 at length L, slot_mapping of its token is the slot of
+ * position L - 1, block_table[s, (L-1) / block_size] * block_size + (L-1) % block_size
+ * (or negative: a padding token, nothing written). A token breaking this sets
+ * PA_DEVERR_SLOT_MISMATCH; its KV is still written, its request's output is then
+ * unspecified.
+ *  - max_query_len <= 1 (a decode-only batch): one launch pair. The split-K CTA that
+ *    streams a request's last 16 positions for a KV-head group first copies that group's
+ *    slice of the new K/V row into the cache, then reads it back with the rest, so the
+ *    new token costs one write and no separate kernel.
+ *  - max_query_len >= 2: the cache write is a separate kernel ahead of the attention
+ *    kernels (prefill rows read their new tokens through many CTAs).
+ * k_new, v_new  device, [num_tokens, num_kv_heads, head_dim], `dtype`, 16-byte aligned
+ * slot_mapping  device, int64 [num_tokens], distinct non-negative slots
+ * Other arguments, validation, workspace and errors as pa_kv_write and pa_attention;
+ * validation happens before anything is enqueued.
+ * --------------------------------------------------------------------------- */
+int pa_write_attention(void* out, const void* q, const void* k_new, const void* v_new,
+                       const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                       const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                       const int32_t* query_start_loc, int num_seqs, int num_tokens,
+                       int max_query_len, int max_seq_len, int num_heads, int num_kv_heads,
+                       int head_dim, int block_size, int64_t num_blocks, float scale,
+                       pa_dtype dtype, void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------------
  * pa_attention_fixed_scratch -- no counterpart in the pages: an addition for callers that

@@ -22,6 +22,7 @@ __all__ = [
     "kv_write",
     "copy_blocks",
     "attention",
+    "write_attention",
     "attention_workspace_size",
     "read_device_errors",
     "lib",
@@ -29,7 +30,7 @@ __all__ = [
 ]
 
 PA_F32, PA_BF16 = 0, 1
-PA_DEVERR = {"slot_range": 0x1, "block_range": 0x2, "seq_range": 0x4, "timeout": 0x8}
+PA_DEVERR = {"slot_range": 0x1, "block_range": 0x2, "seq_range": 0x4, "timeout": 0x8, "slot_mismatch": 0x10}
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -48,6 +49,8 @@ _sig = {
     "pa_attention_workspace_size": (_i, [_i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "pa_attention": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i64, _f, _i, _p,
                           _sz, _p]),
+    "pa_write_attention": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i,
+                                _i64, _f, _i, _p, _sz, _p]),
     "pa_bm_create": (_p, [_i64, _i, _p]),
     "pa_bm_destroy": (None, [_p]),
     "pa_bm_add_seq": (_i, [_p, _i64]),
@@ -179,6 +182,42 @@ def attention(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, 
                           int(max_seq_len), Hq, Hkv, D, B, NB, float(scale), _dtype_code(q), ws_ptr,
                           workspace.numel(), _stream(stream, q.device))
     _check(st, "pa_attention")
+    return out
+
+
+def write_attention(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_table, seq_lens,
+                    query_start_loc, *, max_query_len: int, max_seq_len: int, scale: float, workspace=None,
+                    stream=None):
+    """pa_write_attention: kv_write(k_new, v_new, ..., slot_mapping) then attention(...), in one call.
+
+    For a decode request (q_len 1, length L) slot_mapping of its token must be the slot of
+    position L - 1 in its block table; the decode kernel then writes it itself.
+    """
+    NB, B, Hkv, D = _cache_geometry(k_cache, v_cache)
+    T, Hq = int(q.shape[0]), int(q.shape[1])
+    if q.dim() != 3 or tuple(out.shape) != tuple(q.shape) or int(q.shape[2]) != D:
+        raise ValueError("q and out must be [num_tokens, num_heads, head_dim]")
+    if q.dtype != k_cache.dtype or out.dtype != k_cache.dtype:
+        raise TypeError("q, out and the caches must share one dtype")
+    if tuple(k_new.shape) != (T, Hkv, D) or tuple(v_new.shape) != (T, Hkv, D) or \
+            k_new.dtype != k_cache.dtype or v_new.dtype != k_cache.dtype:
+        raise ValueError("k_new, v_new must be [num_tokens, num_kv_heads, head_dim] in the cache dtype")
+    if tuple(slot_mapping.shape) != (T,):
+        raise ValueError("slot_mapping must be [num_tokens]")
+    S = int(seq_lens.shape[0])
+    if block_table.dim() != 2 or int(block_table.shape[0]) != S or tuple(query_start_loc.shape) != (S + 1,):
+        raise ValueError("block_table [S, W], seq_lens [S], query_start_loc [S + 1]")
+    if workspace is None:
+        workspace = torch.empty(attention_workspace_size(S, Hq, Hkv, D), dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace.numel() > 0 else 0
+    st = lib.pa_write_attention(_dev(out, "out"), _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+                                _dev(slot_mapping, "slot_mapping", torch.int64), _dev(k_cache, "k_cache"),
+                                _dev(v_cache, "v_cache"), _dev(block_table, "block_table", torch.int32, 2),
+                                int(block_table.shape[1]), _dev(seq_lens, "seq_lens", torch.int32, 1),
+                                _dev(query_start_loc, "query_start_loc", torch.int32, 1), S, T, int(max_query_len),
+                                int(max_seq_len), Hq, Hkv, D, B, NB, float(scale), _dtype_code(q), ws_ptr,
+                                workspace.numel(), _stream(stream, q.device))
+    _check(st, "pa_write_attention")
     return out
 
 

@@ -130,18 +130,28 @@ int pa_attention_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
   return PA_OK;
 }
 
-int pa_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
-                 const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
-                 const int32_t* query_start_loc, int num_seqs, int num_tokens, int max_query_len,
-                 int max_seq_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                 int64_t num_blocks, float scale, pa_dtype dtype, void* workspace,
-                 size_t workspace_bytes, pa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Validation and argument packing shared by pa_attention and pa_write_attention; nothing
+// is launched. On success `a` and `ctas` are ready for run_attention.
+int prepare_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                      const int32_t* query_start_loc, int num_seqs, int num_tokens, int max_query_len,
+                      int max_seq_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                      int64_t num_blocks, float scale, pa_dtype dtype, void* workspace,
+                      size_t workspace_bytes, pa::AttnArgs& a, int& ctas, bool& nothing) {
+  nothing = false;
   int st = check_cache(k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim, dtype);
   if (st != PA_OK) return st;
   if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || max_seq_len < 0) return PA_ERR_INVALID_ARG;
   if (num_heads < 1 || num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || scale != scale) return PA_ERR_INVALID_ARG;
-  if (num_seqs == 0 || num_tokens == 0) return PA_OK;
+  if (num_seqs == 0 || num_tokens == 0) {
+    nothing = true;
+    return PA_OK;
+  }
   if (!out || !q || !block_table || !seq_lens || !query_start_loc) return PA_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q)) return PA_ERR_INVALID_ARG;
   if (max_blocks_per_seq < 1) return PA_ERR_INVALID_ARG;
@@ -159,14 +169,13 @@ int pa_attention(void* out, const void* q, const void* k_cache, const void* v_ca
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
-  const int ctas = pa::decode_num_ctas(dev, &e);
+  ctas = pa::decode_num_ctas(dev, &e);
   if (e != cudaSuccess) return cuda_fail(e);
   const size_t need = pa::decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, ctas, dtype);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PA_ERR_WORKSPACE;
   unsigned int* err = pa::device_error_word(&e);
   if (!err) return cuda_fail(e);
 
-  pa::AttnArgs a;
   a.out = out;
   a.q = q;
   a.k_cache = k_cache;
@@ -187,14 +196,73 @@ int pa_attention(void* out, const void* q, const void* k_cache, const void* v_ca
   a.dtype = dtype;
   a.workspace = workspace;
   a.err = err;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  e = pa::launch_decode(a, ctas, s);
+  return PA_OK;
+}
+
+int run_attention(const pa::AttnArgs& a, int ctas, cudaStream_t s) {
+  cudaError_t e = pa::launch_decode(a, ctas, s);
   if (e != cudaSuccess) return cuda_fail(e);
-  if (max_query_len >= 2) {
+  if (a.max_query_len >= 2) {
     e = pa::prefill_tc_supported(a) ? pa::launch_prefill_tc(a, ctas, s) : pa::launch_prefill(a, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                 const int32_t* query_start_loc, int num_seqs, int num_tokens, int max_query_len,
+                 int max_seq_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                 int64_t num_blocks, float scale, pa_dtype dtype, void* workspace,
+                 size_t workspace_bytes, pa_stream_t stream) {
+  pa::AttnArgs a;
+  int ctas = 0;
+  bool nothing = false;
+  const int st = prepare_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
+                                   query_start_loc, num_seqs, num_tokens, max_query_len, max_seq_len, num_heads,
+                                   num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace,
+                                   workspace_bytes, a, ctas, nothing);
+  if (st != PA_OK || nothing) return st;
+  return run_attention(a, ctas, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_write_attention(void* out, const void* q, const void* k_new, const void* v_new,
+                       const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                       const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                       const int32_t* query_start_loc, int num_seqs, int num_tokens, int max_query_len,
+                       int max_seq_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                       int64_t num_blocks, float scale, pa_dtype dtype, void* workspace,
+                       size_t workspace_bytes, pa_stream_t stream) {
+  if (num_seqs > 0 && num_tokens > 0) {
+    if (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new)) return PA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(slot_mapping) % 8 != 0) return PA_ERR_INVALID_ARG;
+  }
+  pa::AttnArgs a;
+  int ctas = 0;
+  bool nothing = false;
+  const int st = prepare_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
+                                   query_start_loc, num_seqs, num_tokens, max_query_len, max_seq_len, num_heads,
+                                   num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace,
+                                   workspace_bytes, a, ctas, nothing);
+  if (st != PA_OK || nothing) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (max_query_len >= 2) {
+    // prefill rows read their own new tokens from the cache through many CTAs: write every
+    // new token first, then attend
+    const int64_t row_bytes = int64_t(num_kv_heads) * head_dim * elem_bytes(dtype);
+    cudaError_t e = pa::launch_kv_write(k_new, v_new, k_cache, v_cache, slot_mapping, num_tokens,
+                                        num_blocks * block_size, row_bytes, a.err, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return run_attention(a, ctas, s);
+  }
+  a.k_new = k_new;  // a decode-only batch: the decode kernel writes each new token itself
+  a.v_new = v_new;
+  a.slot_mapping = slot_mapping;
+  return run_attention(a, ctas, s);
 }
 
 }  // extern "C"

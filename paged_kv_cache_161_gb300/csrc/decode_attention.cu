@@ -49,7 +49,8 @@ constexpr int kSmemLimit = 227 * 1024;
 enum : int { kFirst = 1, kLast = 2, kSeqStart = 4, kSeqEnd = 8, kBad = 16 };
 
 struct __align__(16) StageDesc {
-  int s, hg, j, valid, flags, pad0, pad1, pad2;
+  int s, hg, j, valid, flags, pad;
+  int64_t wslot;  // >= 0: row valid - 1 came from the new token's K/V; store it to this slot
 };
 
 struct DecodeParams {
@@ -57,6 +58,11 @@ struct DecodeParams {
   const void* q;
   const char* k_cache;
   const char* v_cache;
+  char* k_cache_w;  // the same caches, for the fused write of new tokens
+  char* v_cache_w;
+  const char* k_new;  // fused write inputs (null: no write); [num_tokens, Hkv, D]
+  const char* v_new;
+  const int64_t* slot_mapping;
   const int32_t* block_table;
   const int32_t* seq_lens;
   const int32_t* qsl;
@@ -341,6 +347,39 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
     const char* cache = kv ? p.v_cache : p.k_cache;
     const uint32_t buf0 = smem_u32(smem + (kv ? SM::v_off(HG) : SM::k_off(HG)));
     for (int64_t u = u_begin; u < u_end; ++u) {
+      // Fused KV write (decode-only batches): at a request's last unit the new token's row
+      // (position L - 1) is taken from k_new / v_new instead of the cache, and the consumer
+      // warps store it from shared memory to its slot. Only this CTA reads position L - 1
+      // of (request s, head group hg), so nothing reads the slot back within the grid.
+      int64_t wslot = -1;
+      int qrow_new = 0;
+      if (p.k_new && j == units_s - 1) {
+        qrow_new = __ldg(p.qsl + s);
+        const int64_t slot = __ldg(p.slot_mapping + qrow_new);
+        const int64_t at =
+            int64_t(__ldg(p.block_table + int64_t(s) * p.max_blocks_per_seq + (L - 1) / B)) * B + (L - 1) % B;
+        if (slot >= 0 && slot == at && slot < p.num_blocks * B) {
+          wslot = slot;
+        } else if (slot >= 0) {
+          // not the slot of position L - 1 (or out of range): flag it, and write the row
+          // where slot_mapping says (as pa_kv_write would); position L - 1 is read from
+          // the cache as it stands
+          if (lane == 0 && slot != at) raise_error(p.err, PA_DEVERR_SLOT_MISMATCH);
+          if (slot < p.num_blocks * B) {
+            const int64_t slice = int64_t(HG) * D * C::EL;
+            const int64_t src_off = int64_t(qrow_new) * kv_row_bytes + hg * slice;
+            const int64_t dst_off = slot * kv_row_bytes + hg * slice;
+            for (int64_t o = int64_t(lane) * 16; o < slice; o += 32 * 16) {
+              const uint4 kx = __ldg(reinterpret_cast<const uint4*>(p.k_new + src_off + o));
+              const uint4 vx = __ldg(reinterpret_cast<const uint4*>(p.v_new + src_off + o));
+              *reinterpret_cast<uint4*>(p.k_cache_w + dst_off + o) = kx;
+              *reinterpret_cast<uint4*>(p.v_cache_w + dst_off + o) = vx;
+            }
+          } else if (lane == 0) {
+            raise_error(p.err, PA_DEVERR_SLOT_RANGE);
+          }
+        }
+      }
       const int64_t u0 = u - j, u1 = u0 + units_s;
       int flags = 0;
       if (u == u_begin || j == 0) flags |= kFirst;
@@ -351,17 +390,22 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
       // ---- this lane's copy (at most one per lane: 16 for K, 16 for V)
       const int32_t* bt = p.block_table + int64_t(s) * p.max_blocks_per_seq;
       const int pos0 = j * kTPS;
-      bool have = false, bad = false;
+      bool have = false, bad = false, have2 = false;
       const char* src = nullptr;
-      uint32_t dst = 0, bytes = 0;
+      const char* src2 = nullptr;
+      uint32_t dst = 0, bytes = 0, dst2 = 0;
+      const char* fresh = (kv ? p.v_new : p.k_new) + int64_t(qrow_new) * kv_row_bytes;  // used iff wslot >= 0
       if (whole_rows) {
+        // the lane whose copy ends at row valid - 1 leaves that row to a second copy from
+        // the new token's K/V when the write is fused
         if (B >= kTPS) {
           if (idx == 0) {
             const int64_t blk = __ldg(bt + pos0 / B);
             bad = blk < 0 || blk >= p.num_blocks;
-            have = !bad;
+            const int rows = valid - (wslot >= 0 ? 1 : 0);
+            have = !bad && rows > 0;
             src = cache + (blk * B + pos0 % B) * kv_row_bytes;
-            bytes = uint32_t(valid * kv_row_bytes);
+            bytes = uint32_t(rows * kv_row_bytes);
             dst = buf0 + stage * sbytes;
           }
         } else {
@@ -369,23 +413,39 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
           if (idx < nblk) {
             const int64_t blk = __ldg(bt + pos0 / B + idx);
             bad = blk < 0 || blk >= p.num_blocks;
-            have = !bad;
+            const int rows = min(B, valid - idx * B) - ((wslot >= 0 && idx == nblk - 1) ? 1 : 0);
+            have = !bad && rows > 0;
             src = cache + blk * B * kv_row_bytes;
-            bytes = uint32_t(min(B, valid - idx * B) * kv_row_bytes);
+            bytes = uint32_t(rows * kv_row_bytes);
             dst = buf0 + stage * sbytes + uint32_t(idx * B * kv_row_bytes);
           }
+          if (wslot >= 0 && idx == nblk - 1) {
+            have2 = true;
+            src2 = fresh;
+            dst2 = buf0 + stage * sbytes + uint32_t((valid - 1) * kv_row_bytes);
+          }
+        }
+        if (B >= kTPS && wslot >= 0 && idx == 1) {
+          have2 = true;
+          src2 = fresh;
+          dst2 = buf0 + stage * sbytes + uint32_t((valid - 1) * kv_row_bytes);
         }
       } else if (idx < valid) {
         const int pos = pos0 + idx;
-        const int64_t blk = __ldg(bt + pos / B);
-        bad = blk < 0 || blk >= p.num_blocks;
-        have = !bad;
         const int64_t hg_row = int64_t(HG) * D * C::EL;
-        src = cache + (blk * B + pos % B) * kv_row_bytes + hg * hg_row;
+        if (wslot >= 0 && idx == valid - 1) {
+          have = true;
+          src = fresh + hg * hg_row;
+        } else {
+          const int64_t blk = __ldg(bt + pos / B);
+          bad = blk < 0 || blk >= p.num_blocks;
+          have = !bad;
+          src = cache + (blk * B + pos % B) * kv_row_bytes + hg * hg_row;
+        }
         bytes = uint32_t(hg_row);
         dst = buf0 + stage * sbytes + uint32_t(idx * hg_row);
       }
-      const int total_bytes = warp_sum_i(have ? int(bytes) : 0);
+      const int total_bytes = warp_sum_i((have ? int(bytes) : 0) + (have2 ? int(kv_row_bytes) : 0));
       const bool any_bad = __any_sync(0xffffffffu, bad);
       if (any_bad) flags |= kBad;
       int ok = 1;
@@ -403,12 +463,14 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
         d.j = j;
         d.valid = valid;
         d.flags = flags;
-        d.pad0 = d.pad1 = d.pad2 = 0;
+        d.pad = 0;
+        d.wslot = wslot;
         desc[stage] = d;
         mbar_arrive_expect_tx(full0 + 8 * stage, uint32_t(total_bytes));
       }
       __syncwarp();
       if (have) bulk_g2s(dst, src, bytes, full0 + 8 * stage);
+      if (have2) bulk_g2s(dst2, src2, uint32_t(kv_row_bytes), full0 + 8 * stage);
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1;
@@ -498,6 +560,14 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
     }
     const int valid = (d.flags & kBad) ? 0 : d.valid;
     const T* ks = kw + stage * stage_elems;
+    if (d.wslot >= 0 && qg == 0 && r == (d.valid - 1) % RPI) {
+      // fused KV write: this warp's KV head of the new token's row, shared -> cache
+      const int64_t off = d.wslot * kv_row_bytes + (int64_t(d.hg * HG + hk) * D + lir * VEC) * C::EL;
+      const int t = d.valid - 1;
+      *reinterpret_cast<uint4*>(p.k_cache_w + off) = *reinterpret_cast<const uint4*>(ks + t * row_stride);
+      *reinterpret_cast<uint4*>(p.v_cache_w + off) =
+          *reinterpret_cast<const uint4*>(vw + stage * stage_elems + t * row_stride);
+    }
 
     // ---- S = q . K: slot (tj, gj) holds token r + RPI * (tj ^ Pt), head gj ^ Pg
     float sv[NV];
@@ -776,6 +846,11 @@ cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   p.q = a.q;
   p.k_cache = static_cast<const char*>(a.k_cache);
   p.v_cache = static_cast<const char*>(a.v_cache);
+  p.k_cache_w = static_cast<char*>(const_cast<void*>(a.k_cache));
+  p.v_cache_w = static_cast<char*>(const_cast<void*>(a.v_cache));
+  p.k_new = static_cast<const char*>(a.k_new);
+  p.v_new = static_cast<const char*>(a.v_new);
+  p.slot_mapping = a.slot_mapping;
   p.block_table = a.block_table;
   p.seq_lens = a.seq_lens;
   p.qsl = a.query_start_loc;

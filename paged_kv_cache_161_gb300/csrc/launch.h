@@ -42,6 +42,11 @@ struct AttnArgs {
   pa_dtype dtype;
   void* workspace;
   unsigned int* err;
+  // Fused KV write (decode requests only; all three null otherwise): row t of k_new / v_new
+  // [num_tokens, num_kv_heads, head_dim] goes to cache slot slot_mapping[t].
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  const int64_t* slot_mapping = nullptr;
 };
 
 // Decode (q_len == 1 requests): workspace bytes needed, and the launch (split-K + merge).

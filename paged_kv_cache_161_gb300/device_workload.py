@@ -4,7 +4,8 @@ The block manager is the library's C++ one (pa_bm_*), the copies, writes and att
 are its kernels; this module only moves the generator's values to the device and hands
 the library's outputs from one call to the next. A phase runs as the workload script
 defines: block-manager operations, then pa_copy_blocks of the emitted pairs, then
-pa_kv_write of the appended tokens, then (for the step) pa_attention over the batch.
+pa_kv_write of the appended tokens, then (for the step) pa_attention over the batch --
+or, for a step whose appended tokens are exactly its query tokens, pa_write_attention.
 """
 from __future__ import annotations
 
@@ -13,7 +14,7 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from . import BlockManager, attention, attention_workspace_size, copy_blocks, kv_write
+from . import BlockManager, attention, attention_workspace_size, copy_blocks, kv_write, write_attention
 
 
 def storage_to_torch(a: np.ndarray) -> torch.Tensor:
@@ -134,11 +135,25 @@ class DeviceWorkload:
             workspace=ws,
         )
 
-    def run_step(self, st: StepInputs, stream=None):
-        """The hot path of one step: copies, write, attention (all on the device)."""
+    def fusable(self, st: StepInputs) -> bool:
+        """The step appends exactly its query tokens (row t of k_new belongs to query row t)."""
+        return st.q.shape[0] > 0 and st.slot_mapping.shape[0] == st.q.shape[0]
+
+    def run_step(self, st: StepInputs, stream=None, fused: bool = False):
+        """The hot path of one step: copies, write, attention (all on the device).
+
+        ``fused``: the write and the attention as one pa_write_attention call (the step
+        must be fusable)."""
         sp = self.wl.spec
         if st.block_mapping.shape[0]:
             copy_blocks(self.k_cache, self.v_cache, st.block_mapping, stream=stream)
+        if fused:
+            if not self.fusable(st):
+                raise ValueError("this step's appended tokens are not its query tokens")
+            write_attention(st.out, st.q, st.k_new, st.v_new, st.slot_mapping, self.k_cache, self.v_cache,
+                            st.block_table, st.seq_lens, st.query_start_loc, max_query_len=st.max_query_len,
+                            max_seq_len=st.max_seq_len, scale=sp.scale, workspace=st.workspace, stream=stream)
+            return st.out
         if st.slot_mapping.shape[0]:
             kv_write(st.k_new, st.v_new, self.k_cache, self.v_cache, st.slot_mapping, stream=stream)
         if st.q.shape[0]:

@@ -1,0 +1,218 @@
+"""pa_write_attention (the cache write fused into the attention call) vs the oracle.
+
+The fused call must leave the same cache bytes as pa_kv_write and give the outputs the
+oracle gives for write-then-attend (same bars as the unfused path), and its decode
+outputs must be bit-identical to pa_kv_write + pa_attention on the same inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import paged_attention_ref, run_workload, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import paged_kv_cache_161_gb300 as m
+
+    m.read_device_errors(clear=True)
+    return m
+
+
+def _close(got, ref, dtype, what):
+    err = np.abs(to_f64(got) - ref)
+    if dtype == "f32":
+        assert np.max(err) <= 2e-5, f"{what}: max err {np.max(err)}"
+    else:
+        bad = err > 1.5e-2 + 1e-2 * np.abs(ref)
+        assert not bad.any(), f"{what}: {bad.sum()} elements out of tolerance"
+
+
+def _fused_step(pa, wl, eval_seqs=None):
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload, torch_to_storage
+
+    dw = DeviceWorkload(wl)
+    dw.run_setup()
+    st = dw.prepare_step()
+    assert dw.fusable(st)
+    dw.run_step(st, fused=True)
+    torch.cuda.synchronize()
+    assert pa.read_device_errors(clear=True) == 0
+    return dw, st, torch_to_storage(st.out), run_workload(wl, eval_seqs=eval_seqs), torch_to_storage
+
+
+@pytest.mark.parametrize("cfg", [1, 3, 4, 5])
+def test_fused_small_workload_matches_oracle(pa, cfg):
+    wl = workloads.build(cfg, "small")
+    dw, st, out, ref, t2s = _fused_step(pa, wl)
+    assert np.array_equal(t2s(dw.k_cache), ref.k_cache)
+    assert np.array_equal(t2s(dw.v_cache), ref.v_cache)
+    _close(out, ref.out, wl.spec.dtype, wl.name)
+
+
+def test_fused_full_size_gqa_decode_batch(pa):
+    """The 256-request GQA decode batch: the new token of every request is in the cache and
+    sampled requests' outputs match the oracle."""
+    wl = workloads.build(3)
+    lens = np.array(wl.meta["final_lens"])
+    rng = np.random.default_rng(7)
+    pick = sorted({0, len(lens) - 1, int(np.argmax(lens)), int(np.argmin(lens))}
+                  | set(int(i) for i in rng.choice(len(lens), 8, replace=False)))
+    dw, st, out, ref, t2s = _fused_step(pa, wl, eval_seqs=pick)
+    kc, vc = t2s(dw.k_cache), t2s(dw.v_cache)
+    slots = st.slot_mapping.cpu().numpy()
+    B = wl.spec.block_size
+    k_new, v_new = t2s(st.k_new), t2s(st.v_new)
+    for t, slot in enumerate(slots):  # every request's new row, bit-exact
+        assert np.array_equal(kc[slot // B, slot % B], k_new[t])
+        assert np.array_equal(vc[slot // B, slot % B], v_new[t])
+    for i in pick:
+        table = ref.block_table[i]
+        for pos in range(int(ref.seq_lens[i])):
+            blk, off = int(table[pos // B]), pos % B
+            assert np.array_equal(kc[blk, off], ref.k_cache[blk][off]), (i, pos)
+    _close(out[pick], ref.out[pick], wl.spec.dtype, wl.name)
+
+
+@pytest.mark.parametrize("cfg", [3, 4])
+def test_fused_decode_is_bit_identical_to_write_then_attend(pa, cfg):
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload
+
+    outs, caches = [], []
+    for fused in (False, True):
+        dw = DeviceWorkload(workloads.build(cfg, "small"))
+        dw.run_setup()
+        st = dw.prepare_step()
+        outs.append(dw.run_step(st, fused=fused).clone())
+        caches.append((dw.k_cache.clone(), dw.v_cache.clone()))
+    torch.cuda.synchronize()
+    assert pa.read_device_errors(clear=True) == 0
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(caches[0][0], caches[1][0]) and torch.equal(caches[0][1], caches[1][1])
+
+
+FUSED_EDGE = [
+    ("single_token", workloads.Spec("bf16", 32, 8, 128, 16, 0.088), [0, 0, 5], [1, 1, 1]),
+    ("block_boundaries", workloads.Spec("bf16", 32, 8, 128, 16, 0.088), [15, 31, 47, 16, 32], [1] * 5),
+    ("fp32_b1_g1", workloads.Spec("f32", 2, 2, 64, 1, 0.125), [9, 17], [1, 1]),
+    ("bf16_b8_mqa", workloads.Spec("bf16", 4, 1, 128, 8, 0.088), [23, 8, 70], [1, 1, 1]),
+    ("bf16_d64_g8_b32", workloads.Spec("bf16", 16, 2, 64, 32, 0.125), [100, 5, 64], [1, 1, 1]),
+    ("mha_head_groups", workloads.Spec("bf16", 32, 32, 128, 16, 0.088), [40, 300, 1], [1, 1, 1]),
+    ("many_short", workloads.Spec("bf16", 32, 8, 128, 16, 0.088), list(range(0, 300)), [1] * 300),
+    ("mixed_prefill", workloads.Spec("bf16", 32, 8, 128, 16, 0.088), [0, 100, 300, 7], [200, 77, 1, 1]),
+    ("mixed_fp32", workloads.Spec("f32", 8, 4, 128, 16, 0.1), [33, 70, 1], [1, 1, 3]),
+]
+
+
+@pytest.mark.parametrize("name,spec,ctx,q_lens", FUSED_EDGE, ids=[e[0] for e in FUSED_EDGE])
+def test_fused_edge_cases(pa, name, spec, ctx, q_lens):
+    wl = workloads.custom(spec, ctx, q_lens, name=name)
+    dw, st, out, ref, t2s = _fused_step(pa, wl)
+    assert np.array_equal(t2s(dw.k_cache), ref.k_cache)
+    assert np.array_equal(t2s(dw.v_cache), ref.v_cache)
+    _close(out, ref.out, spec.dtype, name)
+
+
+def _hand_batch(dev, dtype=torch.bfloat16):
+    """Three decode requests of lengths 5, 20, 33 (new token included) in a 16-block pool of
+    16-token blocks, GQA 32 / 8 heads, head_dim 128; returns the pieces and each request's
+    slot of its last position."""
+    NB, B, Hkv, Hq, D = 16, 16, 8, 32, 128
+    g = torch.Generator().manual_seed(11)
+    kc = torch.randn((NB, B, Hkv, D), generator=g).to(dtype).to(dev)
+    vc = torch.randn((NB, B, Hkv, D), generator=g).to(dtype).to(dev)
+    lens = [5, 20, 33]
+    table = torch.tensor([[3, 0, 0], [7, 1, 0], [9, 12, 4]], dtype=torch.int32)
+    last = [int(table[s, (L - 1) // B]) * B + (L - 1) % B for s, L in enumerate(lens)]
+    q = torch.randn((3, Hq, D), generator=g).to(dtype).to(dev)
+    k_new = torch.randn((3, Hkv, D), generator=g).to(dtype).to(dev)
+    v_new = torch.randn((3, Hkv, D), generator=g).to(dtype).to(dev)
+    return dict(kc=kc, vc=vc, q=q, k_new=k_new, v_new=v_new, table=table.to(dev),
+                lens=torch.tensor(lens, dtype=torch.int32, device=dev),
+                qsl=torch.tensor([0, 1, 2, 3], dtype=torch.int32, device=dev), last=last, B=B)
+
+
+def _call(pa, h, slots, fused):
+    out = torch.empty_like(h["q"])
+    kc, vc = h["kc"].clone(), h["vc"].clone()
+    sm = torch.tensor(slots, dtype=torch.int64, device=kc.device)
+    kw = dict(max_query_len=1, max_seq_len=33, scale=0.088)
+    if fused:
+        pa.write_attention(out, h["q"], h["k_new"], h["v_new"], sm, kc, vc, h["table"], h["lens"], h["qsl"], **kw)
+    else:
+        pa.kv_write(h["k_new"], h["v_new"], kc, vc, sm)
+        pa.attention(out, h["q"], kc, vc, h["table"], h["lens"], h["qsl"], **kw)
+    torch.cuda.synchronize()
+    return out, kc, vc, pa.read_device_errors(clear=True)
+
+
+def test_fused_padding_token_writes_nothing(pa):
+    h = _hand_batch("cuda")
+    slots = [h["last"][0], -1, h["last"][2]]
+    a = _call(pa, h, slots, fused=False)
+    b = _call(pa, h, slots, fused=True)
+    assert a[3] == 0 and b[3] == 0
+    for x, y in zip(a[:3], b[:3]):
+        assert torch.equal(x, y)
+    B = h["B"]
+    s1 = h["last"][1]
+    assert torch.equal(b[1][s1 // B, s1 % B], h["kc"][s1 // B, s1 % B])  # stale row kept
+    # and the outputs are the oracle's over the cache as it stands
+    ref = paged_attention_ref(_st(h["q"]), _st(b[1]), _st(b[2]), h["table"].cpu().numpy(),
+                              h["lens"].cpu().numpy(), h["qsl"].cpu().numpy(), 0.088, B)
+    _close(_st(b[0]), ref, "bf16", "padding")
+
+
+def test_fused_slot_out_of_range_is_flagged_and_skipped(pa):
+    h = _hand_batch("cuda")
+    NB, B = h["kc"].shape[0], h["B"]
+    slots = [h["last"][0], NB * B + 3, h["last"][2]]
+    out, kc, vc, flags = _call(pa, h, slots, fused=True)
+    assert flags & pa.PA_DEVERR["slot_range"]
+    for s in (0, 2):
+        sl = h["last"][s]
+        assert torch.equal(kc[sl // B, sl % B], h["k_new"][s]) and torch.equal(vc[sl // B, sl % B], h["v_new"][s])
+    kref, vref = h["kc"].clone(), h["vc"].clone()
+    for s in (0, 2):
+        sl = h["last"][s]
+        kref[sl // B, sl % B], vref[sl // B, sl % B] = h["k_new"][s], h["v_new"][s]
+    assert torch.equal(kc, kref) and torch.equal(vc, vref)  # nothing else touched
+
+
+def test_fused_slot_mismatch_is_flagged(pa):
+    """A decode token whose slot is not its last position's slot: flagged, its row still
+    written where slot_mapping says, the other requests unaffected."""
+    h = _hand_batch("cuda")
+    B = h["B"]
+    wrong = 15 * B + 2  # block 15 belongs to no request
+    slots = [h["last"][0], wrong, h["last"][2]]
+    a = _call(pa, h, slots, fused=False)
+    b = _call(pa, h, slots, fused=True)
+    assert a[3] == 0
+    assert b[3] == pa.PA_DEVERR["slot_mismatch"]
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])  # cache as pa_kv_write leaves it
+    assert torch.equal(a[0][0], b[0][0]) and torch.equal(a[0][2], b[0][2])
+
+
+def test_fused_rejects_bad_arguments_before_enqueuing(pa):
+    h = _hand_batch("cuda")
+    out = torch.empty_like(h["q"])
+    sm = torch.tensor(h["last"], dtype=torch.int64, device="cuda")
+    with pytest.raises(ValueError):
+        pa.write_attention(out, h["q"], h["k_new"][:2], h["v_new"], sm, h["kc"], h["vc"], h["table"], h["lens"],
+                           h["qsl"], max_query_len=1, max_seq_len=33, scale=0.088)
+    kc = h["kc"].clone()
+    with pytest.raises(pa.PAError):  # table too narrow for max_seq_len: nothing may run
+        pa.write_attention(out, h["q"], h["k_new"], h["v_new"], sm, kc, h["vc"], h["table"], h["lens"],
+                           h["qsl"], max_query_len=1, max_seq_len=49, scale=0.088)
+    torch.cuda.synchronize()
+    assert torch.equal(kc, h["kc"])
+
+
+def _st(t):
+    from paged_kv_cache_161_gb300.device_workload import torch_to_storage
+
+    return torch_to_storage(t)

@@ -59,6 +59,13 @@ def test_bad_arguments_are_rejected_before_any_launch():
     a = list(args)
     a[5] = 1  # table too narrow for max_seq_len 64 at block size 16
     assert L.pa_attention(*a) == 1
+    # the fused write + attention: same checks, plus its write inputs
+    wargs = args[:2] + [16, 16, 16] + args[2:]  # k_new, v_new, slot_mapping after q
+    for i, val, want in [(17, 96, 2), (16, 3, 1), (18, 24, 2), (20, -1.0, 1), (8, 1, 1),
+                         (2, None, 1), (3, 8, 1), (4, 12, 1)]:
+        a = list(wargs)
+        a[i] = val
+        assert L.pa_write_attention(*a) == want, (i, val)
 
 
 def test_block_manager_rejects_bad_free_order():
