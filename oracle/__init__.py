@@ -8,6 +8,8 @@ separate ``workloads`` package, which holds none of the method's arithmetic.
 
 Contents, each citing the page passage it follows:
 - block_manager.BlockAllocator: blocks, tables, ref counts, fork, copy-on-write.
+- prefix_cache.PrefixCachingAllocator: the same plus reuse of cached full blocks
+  found by their token prefix, with LRU eviction through the free queue.
 - attention.kv_write_ref / copy_blocks_ref / paged_attention_ref /
   dense_causal_ref: the byte moves and the float64 attention.
 - runner.run_workload: a seeded workload, phase by phase.
@@ -26,4 +28,5 @@ from .attention import (  # noqa: F401
     to_f64,
 )
 from .block_manager import BlockAllocator, NoFreeBlocks, TooLarge  # noqa: F401
+from .prefix_cache import PrefixCachingAllocator  # noqa: F401
 from .runner import OracleResult, batch_metadata, run_allocator, run_workload  # noqa: F401
