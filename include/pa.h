@@ -227,7 +227,8 @@ int pa_attention_fixed_scratch(void* out, const void* q, const void* k_cache, co
  * (reference counting); [read] 5.1.1 and 5.2.1; [flow] 3.3 (pool of blocks, slots).
  *
  * Free blocks are handed out first-in first-out, starting from `free_order` (a
- * permutation of [0, num_blocks)); a released block rejoins the tail. Appending a
+ * permutation of [0, num_blocks)); a released block rejoins the tail (the free list is
+ * doubly linked so that prefix caching, below, can take a released block back out). Appending a
  * token takes a new block only when the sequence's last block is full (or it has none),
  * so a sequence of n tokens holds ceil(n / block_size) blocks. Writing into a last
  * block whose reference count is > 1 first moves the writer to a fresh block and
@@ -271,6 +272,39 @@ int64_t pa_bm_num_pending_copies(const pa_bm* bm);
 /* Moves up to `capacity` pending (src, dst) pairs, oldest first, into pairs_out
  * [capacity, 2]; returns how many were moved (or -1 on a bad argument). */
 int64_t pa_bm_take_copies(pa_bm* bm, int64_t* pairs_out, int64_t capacity);
+
+/* ------------------------------------------------------------------------------
+ * Prefix caching -- [docs] Copy-on-Write › shared-prefix detection (hash a prompt's
+ * prefix; if its KV is cached, reuse it and raise the blocks' reference counts) and
+ * Prefix Caching › mechanism (look up on arrival; a hit reuses the KV and skips that
+ * prefill, a miss computes and caches it); [flow] 3.3 (blocks on a doubly linked list,
+ * evicted least recently used first).
+ *
+ * Once enabled, a full block is keyed by its whole token prefix (all token ids of its
+ * sequence up to its last slot; a 128-bit hash chain encodes it). A block is registered
+ * when its last slot is written, unless its key is registered already (the first block
+ * stays registered). A released block keeps its registration at the tail of the free
+ * list; the free list hands blocks out from its head, and a registered block handed out
+ * loses its registration (eviction, least recently released first). Cached blocks are
+ * full, so nothing ever writes into them while they are shared.
+ * --------------------------------------------------------------------------- */
+/* Turns prefix caching on; only on a fresh manager (no sequence yet). From then on appends
+ * need token ids: pa_bm_append / pa_bm_append_batch return PA_ERR_INVALID_ARG. */
+int pa_bm_enable_prefix_caching(pa_bm* bm);
+/* Starts sequence `seq` from the longest cached prefix of prompt[0, n): whole blocks, walked
+ * from the start until the first miss, covering at most max_hit tokens (pass n - 1 so the
+ * last prompt token is always computed). The reused blocks' counts go up (a released one
+ * leaves the free list). *hit_out = tokens reused (a multiple of block_size); the caller
+ * appends prompt[*hit_out, n) next and computes only those rows. */
+int pa_bm_add_seq_cached(pa_bm* bm, int64_t seq, const int32_t* prompt, int64_t n, int64_t max_hit,
+                         int64_t* hit_out);
+/* pa_bm_append with the appended tokens' ids (token_ids[n]; ignored without caching). */
+int pa_bm_append_tokens(pa_bm* bm, int64_t seq, const int32_t* token_ids, int64_t n, int64_t* slots_out);
+/* pa_bm_append_batch with token ids, concatenated like the slots. */
+int pa_bm_append_tokens_batch(pa_bm* bm, const int64_t* seqs, const int64_t* counts, int64_t n,
+                              const int32_t* token_ids, int64_t* slots_out, int64_t* done_out);
+/* Registered blocks now, blocks reused by lookups so far, registrations evicted so far. */
+int pa_bm_prefix_stats(const pa_bm* bm, int64_t* cached_blocks, int64_t* hit_blocks, int64_t* evictions);
 
 #ifdef __cplusplus
 }

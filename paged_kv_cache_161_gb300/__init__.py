@@ -67,6 +67,11 @@ _sig = {
     "pa_bm_batch_tables": (_i, [_p, _p, _i64, _p, _i64, _p]),
     "pa_bm_num_pending_copies": (_i64, [_p]),
     "pa_bm_take_copies": (_i64, [_p, _p, _i64]),
+    "pa_bm_enable_prefix_caching": (_i, [_p]),
+    "pa_bm_add_seq_cached": (_i, [_p, _i64, _p, _i64, _i64, ctypes.POINTER(_i64)]),
+    "pa_bm_append_tokens": (_i, [_p, _i64, _p, _i64, _p]),
+    "pa_bm_append_tokens_batch": (_i, [_p, _p, _p, _i64, _p, _p, _p]),
+    "pa_bm_prefix_stats": (_i, [_p, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
 }
 for _name, (_res, _args) in _sig.items():
     _fn = getattr(lib, _name)
@@ -276,6 +281,60 @@ class BlockManager:
                                     len(s), out.ctypes.data if total else None, ctypes.byref(done))
         _check(st, f"pa_bm_append_batch (stopped after {done.value} entries)")
         return out[:total]
+
+    # -- prefix caching ----------------------------------------------------------
+    def enable_prefix_caching(self):
+        _check(lib.pa_bm_enable_prefix_caching(self._h), "pa_bm_enable_prefix_caching")
+
+    def add_seq_cached(self, seq: int, prompt, max_hit: int) -> int:
+        """Start ``seq`` from the longest cached prefix of ``prompt`` (token ids); returns
+        the number of tokens reused."""
+        import numpy as np
+
+        t = np.ascontiguousarray(np.asarray(prompt, np.int32))
+        hit = ctypes.c_int64(0)
+        _check(lib.pa_bm_add_seq_cached(self._h, seq, t.ctypes.data if t.size else None, t.size, max_hit,
+                                        ctypes.byref(hit)), "pa_bm_add_seq_cached")
+        return int(hit.value)
+
+    def append_tokens(self, seq: int, tokens):
+        """Append the tokens ``tokens`` (ids) to ``seq``; returns their slots (numpy int64)."""
+        import numpy as np
+
+        t = np.ascontiguousarray(np.asarray(tokens, np.int32))
+        out = np.empty(t.size, np.int64)
+        _check(lib.pa_bm_append_tokens(self._h, seq, t.ctypes.data if t.size else None, t.size,
+                                       out.ctypes.data if t.size else None), "pa_bm_append_tokens")
+        return out
+
+    def append_tokens_batch(self, seqs, counts, tokens, out=None):
+        """append_batch with token ids (``tokens`` concatenated in entry order)."""
+        import numpy as np
+
+        s = np.ascontiguousarray(np.asarray(seqs, np.int64))
+        c = np.ascontiguousarray(np.asarray(counts, np.int64))
+        t = np.ascontiguousarray(np.asarray(tokens, np.int32))
+        total = int(c.sum())
+        if t.size < total:
+            raise ValueError("tokens must hold sum(counts) ids")
+        if out is None:
+            out = np.empty(total, np.int64)
+        elif out.dtype != np.int64 or not out.flags.c_contiguous or out.size < total:
+            raise ValueError("out must be a contiguous int64 array of at least sum(counts) entries")
+        done = ctypes.c_int64(0)
+        st = lib.pa_bm_append_tokens_batch(self._h, s.ctypes.data if len(s) else None,
+                                           c.ctypes.data if len(c) else None, len(s),
+                                           t.ctypes.data if total else None, out.ctypes.data if total else None,
+                                           ctypes.byref(done))
+        _check(st, f"pa_bm_append_tokens_batch (stopped after {done.value} entries)")
+        return out[:total]
+
+    def prefix_stats(self):
+        """(registered blocks, blocks reused by lookups, registrations evicted)."""
+        a, b, c = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+        _check(lib.pa_bm_prefix_stats(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+               "pa_bm_prefix_stats")
+        return int(a.value), int(b.value), int(c.value)
 
     def fork(self, parent: int, child: int):
         _check(lib.pa_bm_fork(self._h, parent, child), "pa_bm_fork")

@@ -9,8 +9,23 @@
 // fresh block). Code-reading page 5.1.1 / 5.2.1 (the worked examples). vLLM 0.10.0 flow
 // page 3.3 (pool of free blocks; slot = block * B + offset).
 //
-// Free blocks leave a FIFO queue whose initial order is given by the caller; released
-// blocks join its tail. An append that cannot complete changes nothing.
+// Prefix caching (optional, pa_bm_enable_prefix_caching): "vLLM" docs page, Copy-on-Write ›
+// shared-prefix detection (hash the prompt prefix; reuse cached prefix KV, counts + 1) and
+// Prefix Caching › mechanism (look up on arrival, reuse on a hit, cache on a miss); vLLM
+// 0.10.0 flow page 3.3 (the pool's blocks on a doubly linked list, LRU eviction).
+//
+// Free blocks sit on a doubly linked list whose initial order is given by the caller: new
+// blocks come from the head, released blocks join the tail, and (with prefix caching) a
+// lookup that reuses a released block unlinks it from the middle. The list is the LRU
+// order. An append that cannot complete changes nothing.
+//
+// With prefix caching, a full block is keyed by its whole token prefix (every token of
+// the sequence up to the block's last slot), encoded as a 128-bit hash chain: the key of
+// block i is the key of block i - 1 folded with block i's token ids. It is registered
+// when its last slot is written unless the key is already registered (the first block
+// stays); it keeps its registration while released and loses it when the free list hands
+// it out again (eviction). Two different prefixes share a key only through a 128-bit hash
+// collision.
 #include <cstdint>
 #include <cstring>
 #include <deque>
@@ -20,65 +35,109 @@
 
 #include "pa.h"
 
-struct pa_bm {
-  struct Seq {
-    std::vector<int32_t> table;
-    int64_t len = 0;
-  };
-  int64_t num_blocks = 0;
-  int block_size = 0;
-  std::deque<int32_t> free_q;
-  std::vector<int32_t> ref;
-  std::unordered_map<int64_t, Seq> seqs;
-  std::deque<int64_t> copies;  // src, dst, src, dst, ...
+namespace {
 
-  int32_t take_block() {
-    const int32_t b = free_q.front();
-    free_q.pop_front();
-    ref[b] = 1;
-    return b;
-  }
+struct Key {
+  uint64_t a, b;
+  bool operator==(const Key& o) const { return a == o.a && b == o.b; }
 };
 
-namespace {
+struct KeyHash {
+  size_t operator()(const Key& k) const { return size_t(k.a ^ (k.b * 0x9E3779B97F4A7C15ull)); }
+};
+
+// Finaliser of the SplitMix64 generator (Steele, Lea and Flood, OOPSLA 2014): a
+// bijective 64-bit mixer.
+uint64_t mix64(uint64_t z) {
+  z ^= z >> 30;
+  z *= 0xBF58476D1CE4E5B9ull;
+  z ^= z >> 27;
+  z *= 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  return z;
+}
+
+// One token into both 64-bit lanes of a chain key (different injections per lane).
+Key chain_step(Key h, int32_t token) {
+  const uint64_t t = uint64_t(uint32_t(token));
+  return Key{mix64(h.a + 0x9E3779B97F4A7C15ull * (t + 1)), mix64(h.b ^ (0xD1B54A32D192ED03ull * (t + 0x632BE59BD9B4E019ull)))};
+}
+
+constexpr Key kRootKey{0x243F6A8885A308D3ull, 0x13198A2E03707344ull};  // the empty prefix
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
-extern "C" {
+struct pa_bm {
+  struct Seq {
+    std::vector<int32_t> table;
+    int64_t len = 0;
+    Key chain = kRootKey;          // key of the prefix through the last full block
+    std::vector<int32_t> partial;  // token ids of the partially filled last block
+  };
+  int64_t num_blocks = 0;
+  int block_size = 0;
+  // free list (doubly linked over block ids; -1 ends it)
+  std::vector<int32_t> nxt, prv;
+  std::vector<char> in_free;
+  int32_t head = -1, tail = -1;
+  int64_t nfree = 0;
+  std::vector<int32_t> ref;
+  std::unordered_map<int64_t, Seq> seqs;
+  std::deque<int64_t> copies;  // src, dst, src, dst, ...
+  // prefix caching
+  bool caching = false;
+  std::unordered_map<Key, int32_t, KeyHash> cache;
+  std::vector<Key> block_key;
+  std::vector<char> registered;
+  int64_t hit_blocks = 0, evictions = 0;
 
-pa_bm* pa_bm_create(int64_t num_blocks, int block_size, const int32_t* free_order) {
-  if (num_blocks < 1 || num_blocks > 0x7fffffff || block_size < 1 || !free_order) return nullptr;
-  pa_bm* bm = new (std::nothrow) pa_bm();
-  if (!bm) return nullptr;
-  bm->num_blocks = num_blocks;
-  bm->block_size = block_size;
-  std::vector<char> seen(size_t(num_blocks), 0);
-  for (int64_t i = 0; i < num_blocks; ++i) {
-    const int32_t b = free_order[i];
-    if (b < 0 || b >= num_blocks || seen[size_t(b)]) {
-      delete bm;
-      return nullptr;
-    }
-    seen[size_t(b)] = 1;
-    bm->free_q.push_back(b);
+  void push_free(int32_t b) {
+    nxt[b] = -1;
+    prv[b] = tail;
+    if (tail >= 0) nxt[tail] = b; else head = b;
+    tail = b;
+    in_free[b] = 1;
+    ++nfree;
   }
-  bm->ref.assign(size_t(num_blocks), 0);
-  return bm;
-}
+  void unlink_free(int32_t b) {
+    if (prv[b] >= 0) nxt[prv[b]] = nxt[b]; else head = nxt[b];
+    if (nxt[b] >= 0) prv[nxt[b]] = prv[b]; else tail = prv[b];
+    in_free[b] = 0;
+    --nfree;
+  }
+  int32_t take_block() {
+    const int32_t b = head;
+    unlink_free(b);
+    if (caching && registered[b]) {  // evicted: its content is about to be overwritten
+      cache.erase(block_key[b]);
+      registered[b] = 0;
+      ++evictions;
+    }
+    ref[b] = 1;
+    return b;
+  }
+  // Token `tok` was just written at position len - 1 of `sq`; register a block it filled.
+  void note_token(Seq& sq, int32_t tok) {
+    sq.partial.push_back(tok);
+    if (sq.len % block_size != 0) return;
+    Key k = sq.chain;
+    for (int32_t t : sq.partial) k = chain_step(k, t);
+    sq.partial.clear();
+    sq.chain = k;
+    const int32_t b = sq.table.back();
+    if (cache.emplace(k, b).second) {
+      block_key[b] = k;
+      registered[b] = 1;
+    }
+  }
+};
 
-void pa_bm_destroy(pa_bm* bm) { delete bm; }
+namespace {
 
-int pa_bm_add_seq(pa_bm* bm, int64_t seq) {
-  if (!bm) return PA_ERR_INVALID_ARG;
-  if (bm->seqs.count(seq)) return PA_ERR_NOT_FOUND;
-  bm->seqs.emplace(seq, pa_bm::Seq());
-  return PA_OK;
-}
-
-int pa_bm_append(pa_bm* bm, int64_t seq, int64_t n, int64_t* slots_out) {
-  if (!bm || n < 0 || (n > 0 && !slots_out)) return PA_ERR_INVALID_ARG;
+// Shared by pa_bm_append and pa_bm_append_tokens: tokens == nullptr without caching.
+int append_impl(pa_bm* bm, int64_t seq, int64_t n, const int32_t* tokens, int64_t* slots_out) {
   auto it = bm->seqs.find(seq);
   if (it == bm->seqs.end()) return PA_ERR_NOT_FOUND;
   pa_bm::Seq& sq = it->second;
@@ -89,7 +148,7 @@ int pa_bm_append(pa_bm* bm, int64_t seq, int64_t n, int64_t* slots_out) {
   // the first token lands in a partially filled block that others still hold.
   const bool cow = (sq.len % B != 0) && bm->ref[size_t(sq.table.back())] > 1;
   const int64_t need = ceil_div(sq.len + n, B) - ceil_div(sq.len, B) + (cow ? 1 : 0);
-  if (need > int64_t(bm->free_q.size())) return PA_ERR_NO_BLOCKS;
+  if (need > bm->nfree) return PA_ERR_NO_BLOCKS;
   for (int64_t i = 0; i < n; ++i) {
     const int64_t pos = sq.len;
     if (pos % B == 0) {
@@ -104,7 +163,112 @@ int pa_bm_append(pa_bm* bm, int64_t seq, int64_t n, int64_t* slots_out) {
     }
     slots_out[i] = int64_t(sq.table[size_t(pos / B)]) * B + pos % B;
     sq.len = pos + 1;
+    if (tokens) bm->note_token(sq, tokens[i]);
   }
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_bm* pa_bm_create(int64_t num_blocks, int block_size, const int32_t* free_order) {
+  if (num_blocks < 1 || num_blocks > 0x7fffffff || block_size < 1 || !free_order) return nullptr;
+  pa_bm* bm = new (std::nothrow) pa_bm();
+  if (!bm) return nullptr;
+  bm->num_blocks = num_blocks;
+  bm->block_size = block_size;
+  const size_t nb = size_t(num_blocks);
+  bm->nxt.assign(nb, -1);
+  bm->prv.assign(nb, -1);
+  bm->in_free.assign(nb, 0);
+  for (int64_t i = 0; i < num_blocks; ++i) {
+    const int32_t b = free_order[i];
+    if (b < 0 || b >= num_blocks || bm->in_free[size_t(b)]) {
+      delete bm;
+      return nullptr;
+    }
+    bm->push_free(b);
+  }
+  bm->ref.assign(nb, 0);
+  return bm;
+}
+
+int pa_bm_enable_prefix_caching(pa_bm* bm) {
+  if (!bm || !bm->seqs.empty() || bm->nfree != bm->num_blocks) return PA_ERR_INVALID_ARG;
+  bm->caching = true;
+  bm->block_key.assign(size_t(bm->num_blocks), Key{0, 0});
+  bm->registered.assign(size_t(bm->num_blocks), 0);
+  return PA_OK;
+}
+
+void pa_bm_destroy(pa_bm* bm) { delete bm; }
+
+int pa_bm_add_seq(pa_bm* bm, int64_t seq) {
+  if (!bm) return PA_ERR_INVALID_ARG;
+  if (bm->seqs.count(seq)) return PA_ERR_NOT_FOUND;
+  bm->seqs.emplace(seq, pa_bm::Seq());
+  return PA_OK;
+}
+
+int pa_bm_append(pa_bm* bm, int64_t seq, int64_t n, int64_t* slots_out) {
+  if (!bm || n < 0 || (n > 0 && !slots_out)) return PA_ERR_INVALID_ARG;
+  if (bm->caching) return PA_ERR_INVALID_ARG;  // needs the token ids: pa_bm_append_tokens
+  return append_impl(bm, seq, n, nullptr, slots_out);
+}
+
+int pa_bm_append_tokens(pa_bm* bm, int64_t seq, const int32_t* token_ids, int64_t n, int64_t* slots_out) {
+  if (!bm || n < 0 || (n > 0 && (!slots_out || !token_ids))) return PA_ERR_INVALID_ARG;
+  return append_impl(bm, seq, n, bm->caching ? token_ids : nullptr, slots_out);
+}
+
+int pa_bm_append_tokens_batch(pa_bm* bm, const int64_t* seqs, const int64_t* counts, int64_t n,
+                              const int32_t* token_ids, int64_t* slots_out, int64_t* done_out) {
+  if (done_out) *done_out = 0;
+  if (!bm || n < 0 || (n > 0 && (!seqs || !counts))) return PA_ERR_INVALID_ARG;
+  int64_t off = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const int st = pa_bm_append_tokens(bm, seqs[i], counts[i] > 0 ? token_ids + off : nullptr, counts[i],
+                                       counts[i] > 0 ? slots_out + off : nullptr);
+    if (st != PA_OK) return st;
+    off += counts[i];
+    if (done_out) *done_out = i + 1;
+  }
+  return PA_OK;
+}
+
+int pa_bm_add_seq_cached(pa_bm* bm, int64_t seq, const int32_t* prompt, int64_t n, int64_t max_hit,
+                         int64_t* hit_out) {
+  if (!bm || !bm->caching || n < 0 || (n > 0 && !prompt) || !hit_out) return PA_ERR_INVALID_ARG;
+  if (bm->seqs.count(seq)) return PA_ERR_NOT_FOUND;
+  pa_bm::Seq sq;
+  const int64_t B = bm->block_size;
+  const int64_t lim = max_hit < n ? max_hit : n;
+  Key k = kRootKey;
+  while (sq.len + B <= lim) {
+    Key kk = k;
+    for (int64_t i = 0; i < B; ++i) kk = chain_step(kk, prompt[sq.len + i]);
+    auto it = bm->cache.find(kk);
+    if (it == bm->cache.end()) break;
+    const int32_t b = it->second;
+    if (bm->ref[size_t(b)] == 0) bm->unlink_free(b);
+    bm->ref[size_t(b)] += 1;
+    sq.table.push_back(b);
+    sq.len += B;
+    k = kk;
+  }
+  sq.chain = k;
+  bm->hit_blocks += int64_t(sq.table.size());
+  *hit_out = sq.len;
+  bm->seqs.emplace(seq, std::move(sq));
+  return PA_OK;
+}
+
+int pa_bm_prefix_stats(const pa_bm* bm, int64_t* cached_blocks, int64_t* hit_blocks, int64_t* evictions) {
+  if (!bm || !cached_blocks || !hit_blocks || !evictions) return PA_ERR_INVALID_ARG;
+  *cached_blocks = int64_t(bm->cache.size());
+  *hit_blocks = bm->hit_blocks;
+  *evictions = bm->evictions;
   return PA_OK;
 }
 
@@ -137,7 +301,7 @@ int pa_bm_free_seq(pa_bm* bm, int64_t seq) {
   auto it = bm->seqs.find(seq);
   if (it == bm->seqs.end()) return PA_ERR_NOT_FOUND;
   for (int32_t b : it->second.table) {
-    if (--bm->ref[size_t(b)] == 0) bm->free_q.push_back(b);
+    if (--bm->ref[size_t(b)] == 0) bm->push_free(b);
   }
   bm->seqs.erase(it);
   return PA_OK;
@@ -160,13 +324,13 @@ int pa_bm_ref_count(const pa_bm* bm, int64_t block) {
   return bm->ref[size_t(block)];
 }
 
-int64_t pa_bm_num_free(const pa_bm* bm) { return bm ? int64_t(bm->free_q.size()) : -1; }
+int64_t pa_bm_num_free(const pa_bm* bm) { return bm ? bm->nfree : -1; }
 
 int pa_bm_free_queue(const pa_bm* bm, int32_t* out, int64_t capacity) {
-  if (!bm || (!out && !bm->free_q.empty())) return PA_ERR_INVALID_ARG;
-  if (capacity < int64_t(bm->free_q.size())) return PA_ERR_INVALID_ARG;
+  if (!bm || (!out && bm->nfree > 0)) return PA_ERR_INVALID_ARG;
+  if (capacity < bm->nfree) return PA_ERR_INVALID_ARG;
   int64_t i = 0;
-  for (int32_t b : bm->free_q) out[i++] = b;
+  for (int32_t b = bm->head; b >= 0; b = bm->nxt[size_t(b)]) out[i++] = b;
   return PA_OK;
 }
 
