@@ -63,7 +63,7 @@ def _args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--workload", choices=["gqa_decode", "mixed", "mha_decode", "shared_prefix"],
+    ap.add_argument("--workload", choices=["gqa_decode", "mixed", "mha_decode", "shared_prefix", "system_prompt"],
                     default="gqa_decode",
                     help="gqa_decode: the headline line (default); mixed: the chunked-prefill + decode "
                          "batch, timed whole and as its prefill-only and decode-only sub-batches; "
@@ -671,6 +671,117 @@ def run_secondary(a):
     return 0
 
 
+def _host_admission_ms(wl, reps=5):
+    """Host block accounting of the step alone (C++ manager): the admissions (lookups with
+    prefix caching) and token appends of every request, median of ``reps`` fresh runs."""
+    import paged_kv_cache_161_gb300 as pa
+
+    times = []
+    for _ in range(reps):
+        bm = pa.BlockManager(wl.num_blocks, wl.spec.block_size, wl.free_order)
+        if wl.prefix_caching:
+            bm.enable_prefix_caching()
+
+        def run(ops):
+            for op in ops:
+                if op[0] == "prompt":
+                    s, n = op[1], op[2]
+                    toks = wl.tokens(s, 0, n)
+                    if wl.prefix_caching:
+                        hit = bm.add_seq_cached(s, toks, n - 1)
+                        bm.append_tokens(s, toks[hit:])
+                    else:
+                        bm.add_seq(s)
+                        bm.append(s, n)
+                elif op[0] == "free":
+                    bm.free_seq(op[1])
+
+        for ph in wl.setup:
+            run(ph.ops)
+        t0 = time.perf_counter()
+        run(wl.step.ops)
+        times.append((time.perf_counter() - t0) * 1e3)
+    return sorted(times)[len(times) // 2]
+
+
+def run_system_prompt(a):
+    """Many requests sharing one system prompt, admitted as one chunked-prefill batch, with
+    and without prefix caching: each step is one pa_write_attention call (the write of the
+    computed tokens, then prefill attention over the whole prompt through the block table)."""
+    import torch
+
+    import paged_kv_cache_161_gb300 as pa
+    import workloads
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    hbm, tflops_peak, src = _peaks()
+
+    def timed(fn, steps, warm):
+        for _ in range(warm):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    steps = max(10, a.steps // 20)
+    res = {}
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    for caching in (True, False):
+        wl = workloads.system_prompt("full", caching=caching)
+        sp = wl.spec
+        dw = DeviceWorkload(wl, device=dev)
+        dw.run_setup()
+        st = dw.prepare_step()
+        pa.read_device_errors(clear=True)
+        ms = timed(lambda: dw.run_step(st, stream=stream, fused=True), steps, a.warmup)
+        if pa.read_device_errors(clear=True):
+            raise RuntimeError("device error flags set")
+        lens = st.seq_lens.cpu().tolist()
+        qlens = torch.diff(st.query_start_loc.cpu()).tolist()
+        pairs = sum(q * (L - q) + q * (q + 1) // 2 for L, q in zip(lens, qlens))
+        flops = 4.0 * sp.head_dim * sp.num_heads * pairs
+        tf = flops / (ms * 1e-3) / 1e12
+        res[caching] = {"ms": ms, "computed_tokens": int(sum(qlens)), "prompt_tokens": int(sum(lens)),
+                        "gflop": flops / 1e9, "tflops": tf, "frac_of_bf16_peak": tf / tflops_peak,
+                        "host_admission_ms": _host_admission_ms(wl),
+                        "kv_write_bytes": 2 * int(sum(qlens)) * sp.kv_token_bytes}
+        if caching:
+            res[caching]["prefix_stats"] = dict(zip(("cached_blocks", "hit_blocks", "evictions"),
+                                                    dw.bm.prefix_stats()))
+        meta = wl.meta
+        del dw, st
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    c, u = res[True], res[False]
+    line = {
+        "metric": "system-prompt batch: prompt tokens/s with prefix caching (64 requests, 2040-token shared prompt)",
+        "value": c["prompt_tokens"] / (c["ms"] * 1e-3), "unit": "prompt tokens/s", "n_gpus": 1, "steps": steps,
+        "warmup": a.warmup, "ms_per_step": c["ms"], "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "system_prompt_bf16: 64 requests = one 2040-token system prompt (computed once by a "
+                               "warm request that then ended) + user text U[64, 512]; 32 q / 8 kv heads, head_dim "
+                               "128, block 16", "requests": meta["requests"], "system_len": meta["system_len"],
+                   "seed": wl.seed},
+        "cached": c, "uncached": u, "speedup": u["ms"] / c["ms"],
+        "uncached_prompt_tokens_per_s": u["prompt_tokens"] / (u["ms"] * 1e-3),
+        "roofline": {"bound": "tensor", "achieved": c["tflops"], "peak": tflops_peak, "unit": "TFLOP/s",
+                     "frac": c["frac_of_bf16_peak"], "peak_source": src,
+                     "kernel": "pa_write_attention: kv_write + prefill_tc_kernel (tcgen05)"},
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main(argv=None):
     a = _args(argv)
     if a.impl == "reference":
@@ -679,6 +790,8 @@ def main(argv=None):
         return run_mixed(a)
     if a.workload in ("mha_decode", "shared_prefix"):
         return run_secondary(a)
+    if a.workload == "system_prompt":
+        return run_system_prompt(a)
     return run_ours(a)
 
 

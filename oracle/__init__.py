@@ -29,4 +29,4 @@ from .attention import (  # noqa: F401
 )
 from .block_manager import BlockAllocator, NoFreeBlocks, TooLarge  # noqa: F401
 from .prefix_cache import PrefixCachingAllocator  # noqa: F401
-from .runner import OracleResult, batch_metadata, run_allocator, run_workload  # noqa: F401
+from .runner import OracleResult, batch_metadata, run_allocator, run_script, run_workload, step_ranges  # noqa: F401

@@ -12,6 +12,7 @@ import numpy as np
 
 from .attention import BlockStore, copy_blocks_ref, kv_write_ref, paged_attention_ref
 from .block_manager import BlockAllocator
+from .prefix_cache import PrefixCachingAllocator
 
 
 @dataclass
@@ -29,26 +30,66 @@ class OracleResult:
     out: np.ndarray = None  # float64 [T, Hq, D] (NaN rows for sequences not evaluated)
 
 
-def run_allocator(wl):
-    """Block-manager side only: slots and copy pairs of every phase, final tables."""
-    alloc = BlockAllocator(wl.num_blocks, wl.spec.block_size, wl.free_order)
-    slots_per_phase, copies_per_phase = [], []
+def run_script(wl):
+    """Block-manager side only, every phase: (allocator, slots per phase, copy pairs per
+    phase, appended ranges (seq, start, n) per phase in operation order)."""
+    if wl.prefix_caching:
+        alloc = PrefixCachingAllocator(wl.num_blocks, wl.spec.block_size, wl.free_order)
+    else:
+        alloc = BlockAllocator(wl.num_blocks, wl.spec.block_size, wl.free_order)
+
+    def append(s, n):
+        L = alloc.seq_len(s)
+        if wl.prefix_caching:
+            return alloc.append(s, n, tokens=wl.tokens(s, L, n).tolist())
+        return alloc.append(s, n)
+
+    slots_per_phase, copies_per_phase, appends_per_phase = [], [], []
     for ph in wl.phases():
-        slots = []
+        slots, apps = [], []
         for op in ph.ops:
             if op[0] == "add":
                 alloc.add_seq(op[1])
             elif op[0] == "fork":
                 alloc.fork(op[1], op[2])
             elif op[0] == "append":
-                slots.extend(alloc.append(op[1], op[2]))
+                apps.append((op[1], alloc.seq_len(op[1]), op[2]))
+                slots.extend(append(op[1], op[2]))
+            elif op[0] == "prompt":
+                s, n = op[1], op[2]
+                if wl.prefix_caching:  # reuse what the cache holds, compute the rest
+                    hit = alloc.add_seq_cached(s, wl.tokens(s, 0, n).tolist(), max_hit=n - 1)
+                else:
+                    alloc.add_seq(s)
+                    hit = 0
+                apps.append((s, hit, n - hit))
+                slots.extend(append(s, n - hit))
+            elif op[0] == "free":
+                alloc.free_seq(op[1])
         slots_per_phase.append(np.asarray(slots, np.int64))
         copies_per_phase.append(alloc.take_copies())
-    return alloc, slots_per_phase, copies_per_phase
+        appends_per_phase.append(apps)
+    return alloc, slots_per_phase, copies_per_phase, appends_per_phase
 
 
-def batch_metadata(wl, alloc):
-    """block_table / seq_lens / query_start_loc of the step's batch (batch order)."""
+def run_allocator(wl):
+    """Block-manager side only: slots and copy pairs of every phase, final tables."""
+    alloc, slots, copies, _ = run_script(wl)
+    return alloc, slots, copies
+
+
+def step_ranges(wl, alloc, step_appends):
+    """(seq, start, q_len) of the step's query rows, from the allocator's final lengths."""
+    seqs = [s for s, _ in wl.step.batch or []]
+    appended = {}
+    for s, _, n in step_appends:
+        appended[s] = appended.get(s, 0) + n
+    return wl.step_queries({s: alloc.seq_len(s) for s in seqs}, appended)
+
+
+def batch_metadata(wl, alloc, ranges=None):
+    """block_table / seq_lens / query_start_loc of the step's batch (batch order);
+    ``ranges`` = step_ranges(...) where q_len depends on the block manager."""
     batch = wl.step.batch or []
     seqs = [s for s, _ in batch]
     tables = [alloc.block_table(s) for s in seqs]
@@ -58,7 +99,7 @@ def batch_metadata(wl, alloc):
         bt[i, : len(t)] = t
     seq_lens = np.asarray([alloc.seq_len(s) for s in seqs], np.int32)
     qsl = np.zeros(len(seqs) + 1, np.int32)
-    qsl[1:] = np.cumsum([q for _, q in batch])
+    qsl[1:] = np.cumsum([q for _, _, q in ranges] if ranges is not None else [q for _, q in batch])
     return bt, seq_lens, qsl, seqs
 
 
@@ -72,7 +113,7 @@ def run_workload(wl, eval_seqs=None) -> OracleResult:
     from workloads import relevant_seqs
 
     sp = wl.spec
-    alloc, slots_pp, copies_pp = run_allocator(wl)
+    alloc, slots_pp, copies_pp, apps_pp = run_script(wl)
     store_dtype = np.float32 if sp.dtype == "f32" else np.uint16
     batch = wl.step.batch or []
     if eval_seqs is None:
@@ -83,9 +124,7 @@ def run_workload(wl, eval_seqs=None) -> OracleResult:
         kc = BlockStore(sp.block_size, sp.num_kv_heads, sp.head_dim, store_dtype)
         vc = BlockStore(sp.block_size, sp.num_kv_heads, sp.head_dim, store_dtype)
         relevant = relevant_seqs(wl, [batch[i][0] for i in eval_seqs])
-    lens = {}
-    for ph, slots, copies in zip(wl.phases(), slots_pp, copies_pp):
-        apps = wl.appends(ph, lens)
+    for slots, copies, apps in zip(slots_pp, copies_pp, apps_pp):
         copy_blocks_ref(kc, vc, copies)
         reqs = [a for a in apps if relevant is None or a[0] in relevant]
         vals = dict(zip(reqs, wl.kv_many(reqs))) if reqs else {}
@@ -96,8 +135,9 @@ def run_workload(wl, eval_seqs=None) -> OracleResult:
                 k, v = vals[a]
                 kv_write_ref(kc, vc, k, v, slots[t0 : t0 + n], sp.block_size)
             t0 += n
-    bt, seq_lens, qsl, seqs = batch_metadata(wl, alloc)
-    q = np.concatenate([wl.q(s, start, n) for s, start, n in wl.step_queries()] or
+    ranges = step_ranges(wl, alloc, apps_pp[-1])
+    bt, seq_lens, qsl, seqs = batch_metadata(wl, alloc, ranges)
+    q = np.concatenate([wl.q(s, start, n) for s, start, n in ranges] or
                        [np.zeros((0, sp.num_heads, sp.head_dim), store_dtype)])
     out = paged_attention_ref(q, kc, vc, bt, seq_lens, qsl, sp.scale, sp.block_size, seqs=eval_seqs)
     return OracleResult(alloc, slots_pp, copies_pp, kc, vc, bt, seq_lens, qsl, seqs, q, out)

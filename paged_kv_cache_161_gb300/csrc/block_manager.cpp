@@ -21,7 +21,7 @@
 //
 // With prefix caching, a full block is keyed by its whole token prefix (every token of
 // the sequence up to the block's last slot), encoded as a 128-bit hash chain: the key of
-// block i is the key of block i - 1 folded with block i's token ids. It is registered
+// block i is the key of block i - 1 folded with block i's token ids (fold_block). It is registered
 // when its last slot is written unless the key is already registered (the first block
 // stays); it keeps its registration while released and loses it when the free list hands
 // it out again (eviction). Two different prefixes share a key only through a 128-bit hash
@@ -57,10 +57,25 @@ uint64_t mix64(uint64_t z) {
   return z;
 }
 
-// One token into both 64-bit lanes of a chain key (different injections per lane).
-Key chain_step(Key h, int32_t token) {
-  const uint64_t t = uint64_t(uint32_t(token));
-  return Key{mix64(h.a + 0x9E3779B97F4A7C15ull * (t + 1)), mix64(h.b ^ (0xD1B54A32D192ED03ull * (t + 0x632BE59BD9B4E019ull)))};
+// Key of a full block: its parent's key (the prefix before it) folded with its B token
+// ids. Each lane absorbs the ids two at a time as one 64-bit word with one multiply
+// (lane a: xor then multiply, as in FNV-1a over 64-bit words; lane b: add then multiply
+// by another odd constant), then goes through the bijective mixer, so the next block
+// starts from a well-mixed state.
+Key fold_block(Key parent, const int32_t* tokens, int64_t n) {
+  uint64_t a = parent.a, b = parent.b;
+  int64_t i = 0;
+  for (; i + 1 < n; i += 2) {
+    const uint64_t w = uint64_t(uint32_t(tokens[i])) | (uint64_t(uint32_t(tokens[i + 1])) << 32);
+    a = (a ^ w) * 0x00000100000001B3ull;
+    b = (b + w + 1) * 0xD1B54A32D192ED03ull;
+  }
+  if (i < n) {
+    const uint64_t w = uint64_t(uint32_t(tokens[i])) | (uint64_t(0xFFFFFFFFu) << 32);
+    a = (a ^ w) * 0x00000100000001B3ull;
+    b = (b + w + 1) * 0xD1B54A32D192ED03ull;
+  }
+  return Key{mix64(a ^ uint64_t(n)), mix64(b + 0x632BE59BD9B4E019ull)};
 }
 
 constexpr Key kRootKey{0x243F6A8885A308D3ull, 0x13198A2E03707344ull};  // the empty prefix
@@ -122,8 +137,7 @@ struct pa_bm {
   void note_token(Seq& sq, int32_t tok) {
     sq.partial.push_back(tok);
     if (sq.len % block_size != 0) return;
-    Key k = sq.chain;
-    for (int32_t t : sq.partial) k = chain_step(k, t);
+    const Key k = fold_block(sq.chain, sq.partial.data(), int64_t(sq.partial.size()));
     sq.partial.clear();
     sq.chain = k;
     const int32_t b = sq.table.back();
@@ -245,9 +259,9 @@ int pa_bm_add_seq_cached(pa_bm* bm, int64_t seq, const int32_t* prompt, int64_t 
   const int64_t B = bm->block_size;
   const int64_t lim = max_hit < n ? max_hit : n;
   Key k = kRootKey;
+  sq.table.reserve(size_t(n / B + 1));
   while (sq.len + B <= lim) {
-    Key kk = k;
-    for (int64_t i = 0; i < B; ++i) kk = chain_step(kk, prompt[sq.len + i]);
+    const Key kk = fold_block(k, prompt + sq.len, B);
     auto it = bm->cache.find(kk);
     if (it == bm->cache.end()) break;
     const int32_t b = it->second;

@@ -54,33 +54,52 @@ class DeviceWorkload:
         sp = wl.spec
         self.device = torch.device(device)
         self.bm = BlockManager(wl.num_blocks, sp.block_size, wl.free_order)
+        if wl.prefix_caching:
+            self.bm.enable_prefix_caching()
         self.dtype = torch.float32 if sp.dtype == "f32" else torch.bfloat16
         shape = (wl.num_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
         self.k_cache = torch.zeros(shape, dtype=self.dtype, device=self.device)
         self.v_cache = torch.zeros(shape, dtype=self.dtype, device=self.device)
-        self.lens: dict = {}
         self.table_width = table_width
         self.phase_slots: list = []
         self.phase_copies: list = []
 
     # -- block manager side ------------------------------------------------------
+    def _append(self, s, n):
+        if self.wl.prefix_caching:
+            return self.bm.append_tokens(s, self.wl.tokens(s, self.bm.seq_len(s), n))
+        return self.bm.append(s, n)
+
     def _ops(self, phase):
-        slots = []
+        """Run a phase's operations on the C++ block manager: (slots, copy pairs, appended
+        ranges (seq, start, n) in operation order)."""
+        slots, apps = [], []
         for op in phase.ops:
             if op[0] == "add":
                 self.bm.add_seq(op[1])
             elif op[0] == "fork":
                 self.bm.fork(op[1], op[2])
             elif op[0] == "append":
-                slots.append(self.bm.append(op[1], op[2]))
+                apps.append((op[1], self.bm.seq_len(op[1]), op[2]))
+                slots.append(self._append(op[1], op[2]))
+            elif op[0] == "prompt":
+                s, n = op[1], op[2]
+                if self.wl.prefix_caching:
+                    hit = self.bm.add_seq_cached(s, self.wl.tokens(s, 0, n), n - 1)
+                else:
+                    self.bm.add_seq(s)
+                    hit = 0
+                apps.append((s, hit, n - hit))
+                slots.append(self._append(s, n - hit))
+            elif op[0] == "free":
+                self.bm.free_seq(op[1])
         slots = np.concatenate(slots) if slots else np.zeros(0, np.int64)
         copies = self.bm.take_copies()
         self.phase_slots.append(slots)
         self.phase_copies.append(copies)
-        return slots, copies
+        return slots, copies, apps
 
-    def _values(self, phase):
-        apps = self.wl.appends(phase, self.lens)
+    def _values(self, apps):
         if not apps:
             sp = self.wl.spec
             z = torch.zeros((0, sp.num_kv_heads, sp.head_dim), dtype=self.dtype)
@@ -94,8 +113,8 @@ class DeviceWorkload:
     def run_setup(self):
         """All untimed phases: operations, copies, writes."""
         for ph in self.wl.setup:
-            slots, copies = self._ops(ph)
-            k, v = self._values(ph)
+            slots, copies, apps = self._ops(ph)
+            k, v = self._values(apps)
             if len(copies):
                 copy_blocks(self.k_cache, self.v_cache, torch.from_numpy(copies).to(self.device))
             if len(slots):
@@ -106,18 +125,22 @@ class DeviceWorkload:
         """Run the step's block-manager operations and stage its inputs on the device."""
         wl = self.wl
         sp = wl.spec
-        slots, copies = self._ops(wl.step)
-        k, v = self._values(wl.step)
+        slots, copies, apps = self._ops(wl.step)
+        self.step_appends = apps
+        k, v = self._values(apps)
         batch = wl.step.batch or []
         seqs = [s for s, _ in batch]
         nblk = [int(np.ceil(self.bm.seq_len(s) / sp.block_size)) for s in seqs]
         width = self.table_width or max(nblk + [1])
         table, lens = self.bm.batch_tables(seqs, width)
-        qranges = wl.step_queries()
+        appended = {}
+        for s, _, n in apps:
+            appended[s] = appended.get(s, 0) + n
+        qranges = wl.step_queries({s: self.bm.seq_len(s) for s in seqs}, appended)
         q = np.concatenate([wl.q(s, a, n) for s, a, n in qranges]) if qranges else \
             np.zeros((0, sp.num_heads, sp.head_dim), np.float32 if sp.dtype == "f32" else np.uint16)
         qsl = np.zeros(len(batch) + 1, np.int32)
-        qsl[1:] = np.cumsum([n for _, n in batch])
+        qsl[1:] = np.cumsum([n for _, _, n in qranges])
         dev = self.device
         qt = storage_to_torch(q).to(dev)
         ws = torch.empty(attention_workspace_size(len(batch), sp.num_heads, sp.num_kv_heads, sp.head_dim),
@@ -130,7 +153,7 @@ class DeviceWorkload:
             block_table=torch.from_numpy(table).to(dev),
             seq_lens=torch.from_numpy(lens).to(dev),
             query_start_loc=torch.from_numpy(qsl).to(dev),
-            max_query_len=int(max([n for _, n in batch] + [0])),
+            max_query_len=int(max([n for _, _, n in qranges] + [0])),
             max_seq_len=int(lens.max()) if len(lens) else 0,
             workspace=ws,
         )

@@ -121,3 +121,28 @@ def test_full_size_shapes():
     L = np.array(wl3.meta["final_lens"]) - 1
     assert L.min() >= 16 and L.max() <= 8192
     assert 700 < np.median(L) < 1400
+
+
+def test_system_prompt_cached_rows_equal_uncached_rows():
+    """With prefix caching a request computes only the rows after the reused prefix; those
+    rows see the same keys and values and must equal the uncached run's rows exactly, and
+    both must equal brute-force attention over the contiguous stream."""
+    c = run_workload(workloads.system_prompt("small", caching=True))
+    u = run_workload(workloads.system_prompt("small", caching=False))
+    wl = workloads.system_prompt("small", caching=True)
+    B, P = wl.spec.block_size, wl.meta["system_len"]
+    hit = (P // B) * B
+    for i, s in enumerate(c.batch_seqs):
+        L = int(c.seq_lens[i])
+        assert L == int(u.seq_lens[i]) == P + wl.meta["user_lens"][i]
+        ca, cb = c.query_start_loc[i], c.query_start_loc[i + 1]
+        ua, ub = u.query_start_loc[i], u.query_start_loc[i + 1]
+        assert cb - ca == L - hit and ub - ua == L
+        assert np.array_equal(c.out[ca:cb], u.out[ua + hit:ub])
+        # the cached request's K/V stream: the warm request's prompt, then its own tokens
+        ks, vs = wl.kv(s, 0, L)
+        table = c.block_table[i]
+        got_k = np.stack([c.k_cache[table[p // B]][p % B] for p in range(L)])
+        assert np.array_equal(got_k, ks)
+        want = dense_causal_ref(u.q[ua:ub], ks, vs, wl.spec.scale)
+        assert np.max(np.abs(u.out[ua:ub] - want)) < 1e-12

@@ -121,3 +121,39 @@ def test_prefix_caching_argument_rules():
     assert m2.append_tokens(0, [7, 8, 9]).tolist() == [0, 1, 2]
     with pytest.raises(pa.PAError):
         m2.add_seq_cached(0, [1, 2], 1)  # id in use
+
+
+@pytest.mark.parametrize("size", ["small", "full"])
+@pytest.mark.parametrize("caching", [True, False])
+def test_system_prompt_script_matches_oracle(size, caching):
+    """The system-prompt workload's script on the C++ manager: same reused counts, slots,
+    copy pairs and tables as the oracle; with caching every request reuses all of the
+    system prompt's full blocks."""
+    import workloads
+    from oracle import run_script
+
+    wl = workloads.system_prompt(size, caching=caching)
+    alloc, slots_pp, copies_pp, apps_pp = run_script(wl)
+    bm = pa.BlockManager(wl.num_blocks, wl.spec.block_size, wl.free_order)
+    if caching:
+        bm.enable_prefix_caching()
+    for ph, want_slots, want_copies, want_apps in zip(wl.phases(), slots_pp, copies_pp, apps_pp):
+        got, apps = [], []
+        for op in ph.ops:
+            if op[0] == "prompt":
+                s, n = op[1], op[2]
+                hit = bm.add_seq_cached(s, wl.tokens(s, 0, n), n - 1) if caching else (bm.add_seq(s) or 0)
+                apps.append((s, hit, n - hit))
+                got.append(bm.append_tokens(s, wl.tokens(s, hit, n - hit)) if caching else bm.append(s, n))
+            elif op[0] == "free":
+                bm.free_seq(op[1])
+        assert apps == want_apps
+        assert np.array_equal(np.concatenate(got) if got else np.zeros(0, np.int64), want_slots)
+        assert bm.take_copies().tolist() == [list(p) for p in want_copies]
+    B, P = wl.spec.block_size, wl.meta["system_len"]
+    for s, hit, _ in apps_pp[-1]:
+        assert hit == ((P // B) * B if caching else 0)
+        assert bm.block_table(s).tolist() == alloc.block_table(s)
+    if caching:
+        cached, hits, evictions = bm.prefix_stats()
+        assert hits == wl.meta["requests"] * (P // B) and evictions == 0

@@ -3,8 +3,8 @@
 This module is shared by the float64 oracle and by the CUDA path. It holds none
 of the method's arithmetic: it only fixes shapes, lengths, pool sizes, the
 permutation in which physical block ids are handed out, a script of block-manager
-operations (add a sequence, append tokens, fork) and the random values of
-q / K / V. Everything the method computes from these (slot mappings, block
+operations (add a sequence, append tokens, fork, admit a prompt, end a request),
+token ids where prefix caching needs them, and the random values of q / K / V. Everything the method computes from these (slot mappings, block
 tables, CoW pairs, cache contents, attention outputs) is computed separately
 by each side.
 
@@ -20,4 +20,5 @@ from .configs import (  # noqa: F401
     build,
     custom,
     relevant_seqs,
+    system_prompt,
 )

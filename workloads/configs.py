@@ -7,6 +7,17 @@ operations followed, optionally, by one attention batch:
     ('add', s)            start an empty sequence s
     ('append', s, n)      append n new tokens to s (their K/V are then written)
     ('fork', p, c)        c starts as a copy of p's block table (shared blocks)
+    ('prompt', s, n)      admit s with the first n tokens of its token stream: with
+                          prefix caching, start from whatever prefix the block manager
+                          can reuse, then append the rest; without, append all n
+    ('free', s)           the request s ends
+
+A batch entry (s, None) means "the tokens appended to s in this phase" (the count a
+'prompt' op leaves depends on what the block manager reused). Workloads with
+``token_ids`` give every sequence a stream of token ids; ``shared_kv`` maps a sequence
+to (owner, n): its first n positions hold the owner's K/V (the same tokens at the same
+positions give the same K/V), and ``q_whole`` makes a sequence's queries slices of one
+draw over its whole length, so rows at the same position agree however they are batched.
 
 Both the oracle and the CUDA path execute a phase the same way: run the
 operations on their own block manager, apply the copy-on-write pairs it emitted
@@ -65,6 +76,10 @@ class Workload:
     step: Phase
     num_seqs: int
     meta: dict = field(default_factory=dict)
+    prefix_caching: bool = False
+    token_ids: dict = field(default_factory=dict)  # seq -> int32 array (its token stream)
+    shared_kv: dict = field(default_factory=dict)  # seq -> (owner, n)
+    q_whole: dict = field(default_factory=dict)  # seq -> length of its one query draw
 
     # ---- random values -------------------------------------------------
     def _normal(self, kind: int, seq: int, start: int, shape) -> np.ndarray:
@@ -72,14 +87,38 @@ class Workload:
         x = np.random.Generator(np.random.PCG64(ss)).standard_normal(shape, dtype=np.float32)
         return _to_storage(x, self.spec.dtype)
 
+    def _whole(self, kind: int, seq: int, n: int, width: int) -> np.ndarray:
+        cache = self.__dict__.setdefault("_whole_cache", {})
+        key = (kind, seq, n)
+        if key not in cache:
+            cache[key] = self._normal(kind, seq, 0, (n, width, self.spec.head_dim))
+        return cache[key]
+
     def kv(self, seq: int, start: int, n: int):
         """K and V of tokens [start, start+n) of ``seq``: storage arrays [n, Hkv, D]."""
-        shp = (n, self.spec.num_kv_heads, self.spec.head_dim)
-        return self._normal(_KIND_K, seq, start, shp), self._normal(_KIND_V, seq, start, shp)
+        Hkv = self.spec.num_kv_heads
+        shp = (n, Hkv, self.spec.head_dim)
+        own = self.shared_kv.get(seq)
+        if own is None or start >= own[1]:
+            return self._normal(_KIND_K, seq, start, shp), self._normal(_KIND_V, seq, start, shp)
+        owner, ns = own
+        n1 = min(n, ns - start)
+        k = self._whole(_KIND_K, owner, ns, Hkv)[start:start + n1]
+        v = self._whole(_KIND_V, owner, ns, Hkv)[start:start + n1]
+        if n1 < n:
+            k2, v2 = self.kv(seq, ns, n - n1)
+            k, v = np.concatenate([k, k2]), np.concatenate([v, v2])
+        return k, v
 
     def q(self, seq: int, start: int, n: int) -> np.ndarray:
         """Queries of tokens [start, start+n) of ``seq``: storage array [n, Hq, D]."""
+        if seq in self.q_whole:
+            return self._whole(_KIND_Q, seq, self.q_whole[seq], self.spec.num_heads)[start:start + n]
         return self._normal(_KIND_Q, seq, start, (n, self.spec.num_heads, self.spec.head_dim))
+
+    def tokens(self, seq: int, start: int, n: int) -> np.ndarray:
+        """Token ids of positions [start, start+n) of ``seq``."""
+        return np.asarray(self.token_ids[seq][start:start + n], np.int32)
 
     def kv_many(self, reqs, threads: int | None = None):
         """``kv`` for a list of (seq, start, n), drawn on a thread pool."""
@@ -93,18 +132,28 @@ class Workload:
     def phases(self):
         return list(self.setup) + [self.step]
 
-    def step_queries(self):
-        """(seq, start, q_len) of every query range of the step's batch, in batch order."""
-        lens = {}
-        for ph in self.phases():
-            for op in ph.ops:
-                if op[0] == "add":
-                    lens[op[1]] = 0
-                elif op[0] == "append":
-                    lens[op[1]] += op[2]
-                elif op[0] == "fork":
-                    lens[op[2]] = lens[op[1]]
-        return [(s, lens[s] - ql, ql) for s, ql in (self.step.batch or [])]
+    def step_queries(self, lens: dict | None = None, appended: dict | None = None):
+        """(seq, start, q_len) of every query range of the step's batch, in batch order.
+
+        ``lens`` (final lengths) and ``appended`` (tokens appended to each sequence in the
+        step) come from a block manager when the script has 'prompt' operations."""
+        if lens is None:
+            lens = {}
+            for ph in self.phases():
+                for op in ph.ops:
+                    if op[0] == "add":
+                        lens[op[1]] = 0
+                    elif op[0] == "append":
+                        lens[op[1]] += op[2]
+                    elif op[0] == "fork":
+                        lens[op[2]] = lens[op[1]]
+                    elif op[0] == "prompt":
+                        raise ValueError("'prompt' lengths depend on the block manager: pass lens")
+        out = []
+        for s, ql in self.step.batch or []:
+            q = appended.get(s, 0) if ql is None else ql
+            out.append((s, lens[s] - q, q))
+        return out
 
     def appends(self, phase: Phase, lens: dict):
         """(seq, start, n) of each append of ``phase``; ``lens`` is advanced in place."""
@@ -130,17 +179,22 @@ def _to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def relevant_seqs(wl: Workload, seqs) -> set:
-    """``seqs`` together with every sequence they were forked from."""
+    """``seqs`` together with every sequence they were forked from or share K/V with."""
     parent = {}
     for ph in wl.phases():
         for op in ph.ops:
             if op[0] == "fork":
                 parent[op[2]] = op[1]
     out = set()
-    for s in seqs:
-        while s is not None and s not in out:
-            out.add(s)
-            s = parent.get(s)
+    todo = list(seqs)
+    while todo:
+        s = todo.pop()
+        if s is None or s in out:
+            continue
+        out.add(s)
+        todo.append(parent.get(s))
+        if s in wl.shared_kv:
+            todo.append(wl.shared_kv[s][0])
     return out
 
 
@@ -254,6 +308,41 @@ def _cfg5(size):
     return Workload("mixed_prefill_decode_bf16" + ("_small" if size == "small" else ""), spec, seed, pool,
                     rng.permutation(pool).astype(np.int32), [setup], step, S,
                     dict(chunks=n_chunk, chunk_len=chunk, prior=prior, decode_ctx=dec, final_lens=final))
+
+
+def system_prompt(size: str = "full", caching: bool = True) -> Workload:
+    """Many requests sharing one system prompt (the prefix-caching case of the docs page).
+
+    A warm request computes the system prompt and ends (its blocks are released, still
+    cached when ``caching``). The step admits R requests, each the system prompt plus its
+    own user text, as one chunked-prefill batch: with caching each request reuses the
+    prompt's full blocks and computes only the rest; without, it computes everything.
+    Full: R = 64, a 2040-token system prompt (127 full blocks + 8 tokens), user text
+    U[64, 512] tokens. Small: R = 6, 100-token prompt, user text U[5, 40].
+    """
+    seed = SEED_BASE + 6 + (100 if size == "small" else 0)
+    spec = Spec("bf16", **GQA)
+    rng = _rng(seed)
+    if size == "small":
+        R, P, ulo, uhi = 6, 100, 5, 40
+    else:
+        R, P, ulo, uhi = 64, 2040, 64, 512
+    vocab = 32000
+    sys_tokens = rng.integers(0, vocab, size=P)
+    user_lens = [int(u) for u in rng.integers(ulo, uhi, size=R, endpoint=True)]
+    W = R  # the warm request
+    token_ids = {W: sys_tokens.astype(np.int32)}
+    for r in range(R):
+        token_ids[r] = np.concatenate([sys_tokens, rng.integers(0, vocab, size=user_lens[r])]).astype(np.int32)
+    B = spec.block_size
+    pool = _pool(sum(-(-(P + u) // B) for u in user_lens))
+    setup = [Phase(ops=[("prompt", W, P), ("free", W)])]
+    step = Phase(ops=[("prompt", r, P + user_lens[r]) for r in range(R)], batch=[(r, None) for r in range(R)])
+    name = "system_prompt_bf16_" + ("cached" if caching else "uncached") + ("_small" if size == "small" else "")
+    return Workload(name, spec, seed, pool, rng.permutation(pool).astype(np.int32), setup, step, R,
+                    dict(requests=R, system_len=P, user_lens=user_lens, final_lens=[P + u for u in user_lens]),
+                    prefix_caching=caching, token_ids=token_ids, shared_kv={s: (W, P) for s in range(R + 1)},
+                    q_whole={r: P + user_lens[r] for r in range(R)})
 
 
 CONFIGS = {1: _cfg1, 2: _cfg2, 3: _cfg3, 4: _cfg4, 5: _cfg5}
