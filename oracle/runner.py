@@ -10,8 +10,9 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from .attention import BlockStore, copy_blocks_ref, kv_write_ref, paged_attention_ref
+from .attention import BlockStore, copy_blocks_ref, kv_write_ref, paged_attention_ref, to_f64
 from .block_manager import BlockAllocator
+from .fp8 import dequantize, kv_write_fp8_ref
 from .prefix_cache import PrefixCachingAllocator
 
 
@@ -103,6 +104,16 @@ def batch_metadata(wl, alloc, ranges=None):
     return bt, seq_lens, qsl, seqs
 
 
+def _dequantized(cache, scale):
+    """An E4M3 cache (codes) as float64 values: code value * scale, block by block."""
+    if isinstance(cache, BlockStore):
+        out = BlockStore(*cache.shape, np.float64)
+        for b, blk in cache.items():
+            out[b] = dequantize(blk, scale)
+        return out
+    return dequantize(cache, scale)
+
+
 def run_workload(wl, eval_seqs=None) -> OracleResult:
     """Execute ``wl`` in the oracle.
 
@@ -115,14 +126,16 @@ def run_workload(wl, eval_seqs=None) -> OracleResult:
     sp = wl.spec
     alloc, slots_pp, copies_pp, apps_pp = run_script(wl)
     store_dtype = np.float32 if sp.dtype == "f32" else np.uint16
+    fp8 = wl.kv_cache == "fp8_e4m3"
+    cache_dtype = np.uint8 if fp8 else store_dtype  # E4M3 codes, or the inputs' storage type
     batch = wl.step.batch or []
     if eval_seqs is None:
         shape = (wl.num_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
-        kc, vc = np.zeros(shape, store_dtype), np.zeros(shape, store_dtype)
+        kc, vc = np.zeros(shape, cache_dtype), np.zeros(shape, cache_dtype)
         relevant = None
     else:
-        kc = BlockStore(sp.block_size, sp.num_kv_heads, sp.head_dim, store_dtype)
-        vc = BlockStore(sp.block_size, sp.num_kv_heads, sp.head_dim, store_dtype)
+        kc = BlockStore(sp.block_size, sp.num_kv_heads, sp.head_dim, cache_dtype)
+        vc = BlockStore(sp.block_size, sp.num_kv_heads, sp.head_dim, cache_dtype)
         relevant = relevant_seqs(wl, [batch[i][0] for i in eval_seqs])
     for slots, copies, apps in zip(slots_pp, copies_pp, apps_pp):
         copy_blocks_ref(kc, vc, copies)
@@ -133,11 +146,16 @@ def run_workload(wl, eval_seqs=None) -> OracleResult:
             n = a[2]
             if a in vals:
                 k, v = vals[a]
-                kv_write_ref(kc, vc, k, v, slots[t0 : t0 + n], sp.block_size)
+                if fp8:
+                    kv_write_fp8_ref(kc, vc, to_f64(k).astype(np.float32), to_f64(v).astype(np.float32),
+                                     slots[t0 : t0 + n], sp.block_size, wl.k_scale, wl.v_scale)
+                else:
+                    kv_write_ref(kc, vc, k, v, slots[t0 : t0 + n], sp.block_size)
             t0 += n
     ranges = step_ranges(wl, alloc, apps_pp[-1])
     bt, seq_lens, qsl, seqs = batch_metadata(wl, alloc, ranges)
     q = np.concatenate([wl.q(s, start, n) for s, start, n in ranges] or
                        [np.zeros((0, sp.num_heads, sp.head_dim), store_dtype)])
-    out = paged_attention_ref(q, kc, vc, bt, seq_lens, qsl, sp.scale, sp.block_size, seqs=eval_seqs)
+    ka, va = (_dequantized(kc, wl.k_scale), _dequantized(vc, wl.v_scale)) if fp8 else (kc, vc)
+    out = paged_attention_ref(q, ka, va, bt, seq_lens, qsl, sp.scale, sp.block_size, seqs=eval_seqs)
     return OracleResult(alloc, slots_pp, copies_pp, kc, vc, bt, seq_lens, qsl, seqs, q, out)

@@ -146,3 +146,27 @@ def test_system_prompt_cached_rows_equal_uncached_rows():
         assert np.array_equal(got_k, ks)
         want = dense_causal_ref(u.q[ua:ub], ks, vs, wl.spec.scale)
         assert np.max(np.abs(u.out[ua:ub] - want)) < 1e-12
+
+
+@pytest.mark.parametrize("cfg", [3, 4, 5])
+def test_fp8_workloads_read_back_and_match_dense(cfg):
+    """Over an E4M3 cache every request reads back E4M3(x / scale) of its own K/V stream,
+    and attention equals brute force over the dequantised stream."""
+    from oracle import dequantize, quantize
+
+    wl = workloads.with_fp8_cache(workloads.build(cfg, "small"), k_scale=2.0 ** -6, v_scale=0.0123)
+    res = run_workload(wl)
+    B = wl.spec.block_size
+    for i, s in enumerate(res.batch_seqs):
+        L = int(res.seq_lens[i])
+        ks, vs = _streams(wl, s)
+        table = res.block_table[i]
+        got_k = np.stack([res.k_cache[table[p // B]][p % B] for p in range(L)])
+        got_v = np.stack([res.v_cache[table[p // B]][p % B] for p in range(L)])
+        assert np.array_equal(got_k, quantize(to_f64(ks).astype(np.float32), wl.k_scale))
+        assert np.array_equal(got_v, quantize(to_f64(vs).astype(np.float32), wl.v_scale))
+        a, b = res.query_start_loc[i], res.query_start_loc[i + 1]
+        if b > a:
+            want = dense_causal_ref(res.q[a:b], dequantize(got_k, wl.k_scale), dequantize(got_v, wl.v_scale),
+                                    wl.spec.scale)
+            assert np.max(np.abs(res.out[a:b] - want)) < 1e-12

@@ -21,4 +21,5 @@ from .configs import (  # noqa: F401
     custom,
     relevant_seqs,
     system_prompt,
+    with_fp8_cache,
 )

@@ -80,6 +80,9 @@ class Workload:
     token_ids: dict = field(default_factory=dict)  # seq -> int32 array (its token stream)
     shared_kv: dict = field(default_factory=dict)  # seq -> (owner, n)
     q_whole: dict = field(default_factory=dict)  # seq -> length of its one query draw
+    kv_cache: str = ""  # cache element type: "" (the spec's dtype) or "fp8_e4m3"
+    k_scale: float = 1.0  # fp8_e4m3: a K code c stands for value(c) * k_scale
+    v_scale: float = 1.0
 
     # ---- random values -------------------------------------------------
     def _normal(self, kind: int, seq: int, start: int, shape) -> np.ndarray:
@@ -308,6 +311,16 @@ def _cfg5(size):
     return Workload("mixed_prefill_decode_bf16" + ("_small" if size == "small" else ""), spec, seed, pool,
                     rng.permutation(pool).astype(np.int32), [setup], step, S,
                     dict(chunks=n_chunk, chunk_len=chunk, prior=prior, decode_ctx=dec, final_lens=final))
+
+
+def with_fp8_cache(wl: Workload, k_scale: float = 2.0 ** -6, v_scale: float = 2.0 ** -6) -> Workload:
+    """The same workload over an FP8 (E4M3) cache: inputs unchanged, the cache stores
+    E4M3(x / scale). The default scales (2^-6) put N(0, 1) values well inside E4M3's range
+    (|x| < 7 for every draw here -> codes below 448)."""
+    import dataclasses
+
+    return dataclasses.replace(wl, name=wl.name + "_fp8", kv_cache="fp8_e4m3", k_scale=float(k_scale),
+                               v_scale=float(v_scale))
 
 
 def system_prompt(size: str = "full", caching: bool = True) -> Workload:
