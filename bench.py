@@ -63,7 +63,8 @@ def _args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--workload", choices=["gqa_decode", "mixed", "mha_decode", "shared_prefix", "system_prompt"],
+    ap.add_argument("--workload", choices=["gqa_decode", "mixed", "mha_decode", "shared_prefix", "system_prompt",
+                                           "gqa_decode_fp8"],
                     default="gqa_decode",
                     help="gqa_decode: the headline line (default); mixed: the chunked-prefill + decode "
                          "batch, timed whole and as its prefill-only and decode-only sub-batches; "
@@ -782,6 +783,79 @@ def run_system_prompt(a):
     return 0
 
 
+def run_fp8_decode(a):
+    """The GQA batch-256 decode step over an FP8 (E4M3) cache: pa_kv_write_fp8 of the 256 new
+    tokens, then pa_attention_fp8 (split-K + merge over 1-byte K/V). Reports the K/V bytes
+    the attention reads per second (half of bf16's for the same tokens) and tokens/s; the
+    bf16 step of the same batch is timed in the same run for comparison."""
+    import torch
+
+    import paged_kv_cache_161_gb300 as pa
+    import workloads
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    hbm, _, src = _peaks()
+
+    def timed(fn, steps, warm):
+        for _ in range(warm):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    steps = max(50, a.steps // 2)
+    res = {}
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    for name, wl in (("fp8", workloads.with_fp8_cache(workloads.build(CONFIG_ID))), ("bf16", workloads.build(CONFIG_ID))):
+        sp = wl.spec
+        dw = DeviceWorkload(wl, device=dev, table_width=(8192 + 1 + 72 + 15) // 16)
+        dw.run_setup()
+        st = dw.prepare_step()
+        pa.read_device_errors(clear=True)
+        step_ms = timed(lambda: dw.run_step(st, stream=stream), steps, a.warmup)
+        attn_ms = timed(lambda: dw._attend(st, stream=stream), steps, a.warmup)
+        if pa.read_device_errors(clear=True):
+            raise RuntimeError("device error flags set")
+        tokens = int(st.seq_lens.sum().item())
+        el = 1 if name == "fp8" else 2
+        kv_bytes = tokens * 2 * sp.num_kv_heads * sp.head_dim * el
+        res[name] = {"step_ms": step_ms, "attention_ms": attn_ms, "kv_bytes": kv_bytes,
+                     "attention_gbs": kv_bytes / (attn_ms * 1e-3) / 1e9,
+                     "frac_of_hbm": kv_bytes / (attn_ms * 1e-3) / 1e9 / hbm,
+                     "tokens_per_s": int(st.seq_lens.shape[0]) / (step_ms * 1e-3)}
+        meta_seed = wl.seed
+        del dw, st
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    f, b = res["fp8"], res["bf16"]
+    line = {
+        "metric": "paged decode attention over an FP8 (E4M3) KV cache: K/V GB/s and tokens/s, batch 256",
+        "value": f["kv_bytes"] / (f["step_ms"] * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1, "steps": steps,
+        "warmup": a.warmup, "ms_per_step": f["step_ms"], "higher_is_better": True, "dtype": "fp8_e4m3 cache, bf16 q/out",
+        "data": "synthetic",
+        "config": {"workload": "gqa_bf16_decode_b256 over an E4M3 cache (k_scale = v_scale = 2^-6): 256 requests, "
+                               "32 q / 8 kv heads, head_dim 128, block 16, lognormal context", "seed": meta_seed},
+        "fp8": f, "bf16": b, "speedup_step": b["step_ms"] / f["step_ms"],
+        "speedup_attention": b["attention_ms"] / f["attention_ms"],
+        "roofline": {"bound": "hbm", "achieved": f["attention_gbs"], "peak": hbm, "unit": "GB/s",
+                     "frac": f["frac_of_hbm"], "peak_source": src,
+                     "kernel": "pa_attention_fp8 decode (split-K + merge, 1-byte K/V)"},
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main(argv=None):
     a = _args(argv)
     if a.impl == "reference":
@@ -792,6 +866,8 @@ def main(argv=None):
         return run_secondary(a)
     if a.workload == "system_prompt":
         return run_system_prompt(a)
+    if a.workload == "gqa_decode_fp8":
+        return run_fp8_decode(a)
     return run_ours(a)
 
 

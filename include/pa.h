@@ -5,6 +5,7 @@
  *   pa_kv_write     scatter new tokens' K/V into physical cache blocks through slot_mapping
  *   pa_attention    paged decode and chunked-prefill attention through block_table
  *   pa_write_attention  the two above in one call (the write fused into decode)
+ *   pa_kv_write_fp8 / pa_attention_fp8  the same over FP8 (E4M3) caches
  *   pa_copy_blocks  copy whole physical blocks (the copy step of copy-on-write)
  *   pa_bm_*         host-side block accounting: free queue, block tables, ref counts, CoW
  *
@@ -53,7 +54,7 @@ extern "C" {
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st* pa_stream_t;
 
-typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 /* caches only: see pa_kv_write_fp8 */ } pa_dtype;
 
 typedef enum {
   PA_OK = 0,
@@ -192,6 +193,39 @@ int pa_write_attention(void* out, const void* q, const void* k_new, const void* 
                        int max_query_len, int max_seq_len, int num_heads, int num_kv_heads,
                        int head_dim, int block_size, int64_t num_blocks, float scale,
                        pa_dtype dtype, void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------
+ * FP8 KV cache -- [docs] quantisation support (FP8: 8-bit, 2x smaller than 16-bit storage).
+ *
+ * k_cache / v_cache hold one E4M3 code per element (PA_FP8_E4M3: 1 sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits, no infinities, largest finite 448), same layout as
+ * above with 1-byte elements. A code c of the K (V) cache stands for value(c) * k_scale
+ * (v_scale): one positive scale per cache, chosen by the caller (e.g. max |K| / 448).
+ *
+ * pa_kv_write_fp8: for every t with s = slot_mapping[t] >= 0,
+ *     k_cache[s / B, s % B, :, :] = E4M3(k[t, :, :] / k_scale)      (same for v)
+ * where x is widened to binary32, divided once (binary32, round to nearest even), then
+ * rounded to E4M3 (nearest, ties to even; magnitudes beyond 448 saturate to 448).
+ * k, v are [num_tokens, num_kv_heads, head_dim] in `in_dtype` (PA_BF16 or PA_F32).
+ * num_kv_heads * head_dim must be a multiple of 16. Other rules as pa_kv_write.
+ *
+ * pa_attention_fp8: pa_attention over E4M3 caches with bf16 q and out: K and V are
+ * read as value(code) * scale (exact in fp32 up to the scale product), the rest is
+ * pa_attention's arithmetic. The split-K decode kernel reads the 1-byte cache directly
+ * (half the bytes of bf16); requests with q_len >= 2 run the CUDA-core prefill kernel.
+ * Workspace from pa_attention_workspace_size. pa_copy_blocks takes PA_FP8_E4M3 caches
+ * (byte copy), and pa_kv_write with dtype PA_FP8_E4M3 copies already-encoded rows.
+ * --------------------------------------------------------------------------- */
+int pa_kv_write_fp8(const void* k, const void* v, pa_dtype in_dtype, void* k_cache, void* v_cache,
+                    const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks, int block_size,
+                    int num_kv_heads, int head_dim, float k_scale, float v_scale, pa_stream_t stream);
+
+int pa_attention_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                     const int32_t* query_start_loc, int num_seqs, int num_tokens, int max_query_len,
+                     int max_seq_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                     int64_t num_blocks, float scale, float k_scale, float v_scale, void* workspace,
+                     size_t workspace_bytes, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------------
  * pa_attention_fixed_scratch -- no counterpart in the pages: an addition for callers that

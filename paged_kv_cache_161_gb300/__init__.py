@@ -23,13 +23,15 @@ __all__ = [
     "copy_blocks",
     "attention",
     "write_attention",
+    "kv_write_fp8",
+    "attention_fp8",
     "attention_workspace_size",
     "read_device_errors",
     "lib",
     "LIB_PATH",
 ]
 
-PA_F32, PA_BF16 = 0, 1
+PA_F32, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
 PA_DEVERR = {"slot_range": 0x1, "block_range": 0x2, "seq_range": 0x4, "timeout": 0x8, "slot_mismatch": 0x10}
 
 if not os.path.exists(LIB_PATH):
@@ -51,6 +53,9 @@ _sig = {
                           _sz, _p]),
     "pa_write_attention": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i,
                                 _i64, _f, _i, _p, _sz, _p]),
+    "pa_kv_write_fp8": (_i, [_p, _p, _i, _p, _p, _p, _i64, _i64, _i, _i, _i, _f, _f, _p]),
+    "pa_attention_fp8": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i64, _f, _f, _f,
+                              _p, _sz, _p]),
     "pa_bm_create": (_p, [_i64, _i, _p]),
     "pa_bm_destroy": (None, [_p]),
     "pa_bm_add_seq": (_i, [_p, _i64]),
@@ -98,7 +103,9 @@ def _dtype_code(t: torch.Tensor) -> int:
         return PA_F32
     if t.dtype == torch.bfloat16:
         return PA_BF16
-    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+    if t.dtype == torch.float8_e4m3fn:
+        return PA_FP8_E4M3
+    raise TypeError(f"unsupported dtype {t.dtype} (float32, bfloat16 or float8_e4m3fn)")
 
 
 def _dev(t: torch.Tensor, name: str, dtype=None, ndim=None):
@@ -223,6 +230,51 @@ def write_attention(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_
                                 int(max_seq_len), Hq, Hkv, D, B, NB, float(scale), _dtype_code(q), ws_ptr,
                                 workspace.numel(), _stream(stream, q.device))
     _check(st, "pa_write_attention")
+    return out
+
+
+def kv_write_fp8(k, v, k_cache, v_cache, slot_mapping, k_scale: float, v_scale: float, stream=None):
+    """pa_kv_write_fp8: cache[slot] = E4M3(x / scale) for every slot >= 0; k, v bf16 or
+    float32 [num_tokens, num_kv_heads, head_dim]; caches torch.float8_e4m3fn."""
+    NB, B, Hkv, D = _cache_geometry(k_cache, v_cache)
+    if k_cache.dtype != torch.float8_e4m3fn:
+        raise TypeError("the caches must be torch.float8_e4m3fn")
+    T = int(k.shape[0])
+    if tuple(k.shape) != (T, Hkv, D) or tuple(v.shape) != (T, Hkv, D) or k.dtype != v.dtype:
+        raise ValueError("k, v must be [num_tokens, num_kv_heads, head_dim] of one dtype")
+    if tuple(slot_mapping.shape) != (T,):
+        raise ValueError("slot_mapping must be [num_tokens]")
+    st = lib.pa_kv_write_fp8(_dev(k, "k"), _dev(v, "v"), _dtype_code(k), _dev(k_cache, "k_cache"),
+                             _dev(v_cache, "v_cache"), _dev(slot_mapping, "slot_mapping", torch.int64), T, NB, B,
+                             Hkv, D, float(k_scale), float(v_scale), _stream(stream, k_cache.device))
+    _check(st, "pa_kv_write_fp8")
+
+
+def attention_fp8(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, *, max_query_len: int,
+                  max_seq_len: int, scale: float, k_scale: float, v_scale: float, workspace=None, stream=None):
+    """pa_attention_fp8: attention() over float8_e4m3fn caches (values = code * scale);
+    q and out bfloat16."""
+    NB, B, Hkv, D = _cache_geometry(k_cache, v_cache)
+    if k_cache.dtype != torch.float8_e4m3fn:
+        raise TypeError("the caches must be torch.float8_e4m3fn")
+    T, Hq = int(q.shape[0]), int(q.shape[1])
+    if q.dim() != 3 or tuple(out.shape) != tuple(q.shape) or int(q.shape[2]) != D:
+        raise ValueError("q and out must be [num_tokens, num_heads, head_dim]")
+    if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise TypeError("q and out must be bfloat16")
+    S = int(seq_lens.shape[0])
+    if block_table.dim() != 2 or int(block_table.shape[0]) != S or tuple(query_start_loc.shape) != (S + 1,):
+        raise ValueError("block_table [S, W], seq_lens [S], query_start_loc [S + 1]")
+    if workspace is None:
+        workspace = torch.empty(attention_workspace_size(S, Hq, Hkv, D), dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace.numel() > 0 else 0
+    st = lib.pa_attention_fp8(_dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                              _dev(block_table, "block_table", torch.int32, 2), int(block_table.shape[1]),
+                              _dev(seq_lens, "seq_lens", torch.int32, 1),
+                              _dev(query_start_loc, "query_start_loc", torch.int32, 1), S, T, int(max_query_len),
+                              int(max_seq_len), Hq, Hkv, D, B, NB, float(scale), float(k_scale), float(v_scale),
+                              ws_ptr, workspace.numel(), _stream(stream, q.device))
+    _check(st, "pa_attention_fp8")
     return out
 
 

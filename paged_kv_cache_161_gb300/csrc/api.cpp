@@ -2,6 +2,7 @@
 // Nothing here allocates device memory or synchronises (except pa_read_device_errors).
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 
 #include "launch.h"
@@ -22,6 +23,7 @@ int elem_bytes(pa_dtype dt) {
   switch (dt) {
     case PA_F32: return 4;
     case PA_BF16: return 2;
+    case PA_FP8_E4M3: return 1;
   }
   return 0;
 }
@@ -123,10 +125,13 @@ int pa_attention_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
   if (e != cudaSuccess) return cuda_fail(e);
   const int ctas = pa::decode_num_ctas(dev, &e);
   if (e != cudaSuccess) return cuda_fail(e);
-  // The larger of the two element types' layouts, so one size serves both.
-  const size_t a = pa::decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, ctas, PA_BF16);
-  const size_t b = pa::decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, ctas, PA_F32);
-  *bytes_out = a > b ? a : b;
+  // The largest of the element types' layouts, so one size serves them all.
+  size_t need = 0;
+  for (pa_dtype dt : {PA_BF16, PA_F32, PA_FP8_E4M3}) {
+    const size_t n = pa::decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, ctas, dt);
+    need = n > need ? n : need;
+  }
+  *bytes_out = need;
   return PA_OK;
 }
 
@@ -141,9 +146,10 @@ int prepare_attention(void* out, const void* q, const void* k_cache, const void*
                       const int32_t* query_start_loc, int num_seqs, int num_tokens, int max_query_len,
                       int max_seq_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
                       int64_t num_blocks, float scale, pa_dtype dtype, void* workspace,
-                      size_t workspace_bytes, pa::AttnArgs& a, int& ctas, bool& nothing) {
+                      size_t workspace_bytes, pa::AttnArgs& a, int& ctas, bool& nothing,
+                      pa_dtype cache_dtype) {
   nothing = false;
-  int st = check_cache(k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim, dtype);
+  int st = check_cache(k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim, cache_dtype);
   if (st != PA_OK) return st;
   if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || max_seq_len < 0) return PA_ERR_INVALID_ARG;
   if (num_heads < 1 || num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
@@ -171,7 +177,7 @@ int prepare_attention(void* out, const void* q, const void* k_cache, const void*
   if (e != cudaSuccess) return cuda_fail(e);
   ctas = pa::decode_num_ctas(dev, &e);
   if (e != cudaSuccess) return cuda_fail(e);
-  const size_t need = pa::decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, ctas, dtype);
+  const size_t need = pa::decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, ctas, cache_dtype);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PA_ERR_WORKSPACE;
   unsigned int* err = pa::device_error_word(&e);
   if (!err) return cuda_fail(e);
@@ -194,6 +200,7 @@ int prepare_attention(void* out, const void* q, const void* k_cache, const void*
   a.num_blocks = num_blocks;
   a.scale = scale;
   a.dtype = dtype;
+  a.cache_dtype = cache_dtype;
   a.workspace = workspace;
   a.err = err;
   return PA_OK;
@@ -225,7 +232,7 @@ int pa_attention(void* out, const void* q, const void* k_cache, const void* v_ca
   const int st = prepare_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
                                    query_start_loc, num_seqs, num_tokens, max_query_len, max_seq_len, num_heads,
                                    num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace,
-                                   workspace_bytes, a, ctas, nothing);
+                                   workspace_bytes, a, ctas, nothing, dtype);
   if (st != PA_OK || nothing) return st;
   return run_attention(a, ctas, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -247,7 +254,7 @@ int pa_write_attention(void* out, const void* q, const void* k_new, const void* 
   const int st = prepare_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
                                    query_start_loc, num_seqs, num_tokens, max_query_len, max_seq_len, num_heads,
                                    num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace,
-                                   workspace_bytes, a, ctas, nothing);
+                                   workspace_bytes, a, ctas, nothing, dtype);
   if (st != PA_OK || nothing) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (max_query_len >= 2) {
@@ -263,6 +270,47 @@ int pa_write_attention(void* out, const void* q, const void* k_new, const void* 
   a.v_new = v_new;
   a.slot_mapping = slot_mapping;
   return run_attention(a, ctas, s);
+}
+
+int pa_kv_write_fp8(const void* k, const void* v, pa_dtype in_dtype, void* k_cache, void* v_cache,
+                    const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks, int block_size,
+                    int num_kv_heads, int head_dim, float k_scale, float v_scale, pa_stream_t stream) {
+  int st = check_cache(k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim, PA_FP8_E4M3);
+  if (st != PA_OK) return st;
+  if (in_dtype != PA_BF16 && in_dtype != PA_F32) return PA_ERR_INVALID_ARG;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale == INFINITY || v_scale == INFINITY) return PA_ERR_INVALID_ARG;
+  if ((int64_t(num_kv_heads) * head_dim) % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !aligned16(k) || !aligned16(v)) return PA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(slot_mapping) % 8 != 0) return PA_ERR_INVALID_ARG;
+  cudaError_t e;
+  unsigned int* err = pa::device_error_word(&e);
+  if (!err) return cuda_fail(e);
+  e = pa::launch_kv_write_fp8(k, v, in_dtype, k_cache, v_cache, slot_mapping, num_tokens, num_blocks * block_size,
+                              int64_t(num_kv_heads) * head_dim, k_scale, v_scale, err,
+                              reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int pa_attention_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                     const int32_t* query_start_loc, int num_seqs, int num_tokens, int max_query_len,
+                     int max_seq_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                     int64_t num_blocks, float scale, float k_scale, float v_scale, void* workspace,
+                     size_t workspace_bytes, pa_stream_t stream) {
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale == INFINITY || v_scale == INFINITY) return PA_ERR_INVALID_ARG;
+  pa::AttnArgs a;
+  int ctas = 0;
+  bool nothing = false;
+  const int st = prepare_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
+                                   query_start_loc, num_seqs, num_tokens, max_query_len, max_seq_len, num_heads,
+                                   num_kv_heads, head_dim, block_size, num_blocks, scale, PA_BF16, workspace,
+                                   workspace_bytes, a, ctas, nothing, PA_FP8_E4M3);
+  if (st != PA_OK || nothing) return st;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  return run_attention(a, ctas, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -53,6 +54,46 @@ struct Elem<__nv_bfloat16> {
       w[i] = *reinterpret_cast<uint32_t*>(&h);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// FP8 E4M3 cache element (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+// infinities, largest finite 448). Stored values stand for E4M3 value * scale.
+struct Fp8E4M3 {
+  uint8_t bits;
+};
+
+// Two E4M3 codes (low byte first) -> two floats, exactly (through the f16x2 hardware
+// conversion, which is exact: every E4M3 value is an f16 value).
+__device__ __forceinline__ float2 fp8x2_to_float2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h2) : "r"(two_codes));
+  const __half2 h = *reinterpret_cast<const __half2*>(&h2);
+  return __half22float2(h);
+}
+
+// Two floats -> two E4M3 codes (lo -> low byte): round to nearest even, magnitudes beyond
+// 448 saturate to 448.
+__device__ __forceinline__ uint32_t float2_to_fp8x2(float lo, float hi) {
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(hi), "f"(lo));
+  return c;
+}
+
+template <>
+struct Elem<Fp8E4M3> {
+  static constexpr int kBytes = 1;
+  // Sixteen E4M3 codes of a 16-byte vector -> fp32 (exact).
+  static __device__ __forceinline__ void unpack(const uint4& u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = fp8x2_to_float2(w[i] & 0xffffu), b = fp8x2_to_float2(w[i] >> 16);
+      f[4 * i] = a.x;
+      f[4 * i + 1] = a.y;
+      f[4 * i + 2] = b.x;
+      f[4 * i + 3] = b.y;
+    }
   }
 };
 

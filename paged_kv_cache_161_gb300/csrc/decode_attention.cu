@@ -43,7 +43,6 @@ namespace pa {
 namespace {
 
 constexpr int kTPS = 16;    // tokens per stage
-constexpr int kStages = 3;  // ring depth
 constexpr int kSmemLimit = 227 * 1024;
 
 enum : int { kFirst = 1, kLast = 2, kSeqStart = 4, kSeqEnd = 8, kBad = 16 };
@@ -82,7 +81,8 @@ struct DecodeParams {
   int group;    // query heads per KV head
   int qg;       // consumer warps per KV head = group / (query heads per warp)
   int num_ctas; // grid of the split-K kernel
-  float scale_log2;
+  float scale_log2;  // softmax scale * log2(e) (* k_scale for E4M3 caches)
+  float v_scale;     // 1, or the E4M3 V scale
 };
 
 // Keys of request s if it is a decode request (q_len == 1), else 0.
@@ -186,6 +186,18 @@ struct RowVec<__nv_bfloat16, VEC> {
   }
 };
 
+// FP8 E4M3 rows: 8 codes (8 bytes) per lane -> fp32, exact.
+template <int VEC>
+struct RowVec<Fp8E4M3, VEC> {
+  static_assert(VEC == 8, "E4M3 rows move 8 bytes per lane");
+  static __device__ __forceinline__ void load(const Fp8E4M3* p, float* f) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 a = fp8x2_to_float2(u.x & 0xffffu), b = fp8x2_to_float2(u.x >> 16);
+    const float2 c = fp8x2_to_float2(u.y & 0xffffu), d = fp8x2_to_float2(u.y >> 16);
+    f[0] = a.x, f[1] = a.y, f[2] = b.x, f[3] = b.y, f[4] = c.x, f[5] = c.y, f[6] = d.x, f[7] = d.y;
+  }
+};
+
 template <int VEC>
 struct RowVec<float, VEC> {
   static_assert(VEC == 4, "fp32 rows move 16 bytes per lane");
@@ -210,12 +222,17 @@ __device__ __forceinline__ float pick(const float (&a)[G], int g) {
 }
 
 // ---------------------------------------------------------------- compile-time layout
-// G here is the number of query heads one warp serves (at most 4; a KV head with 8 query
-// heads is served by two warps). One warp covers all 16 tokens of a stage for its heads.
-template <typename T, int D, int G>
+// KV is the cache element type. G here is the number of query heads one warp serves (at
+// most 4; a KV head with 8 query heads is served by two warps). One warp covers all 16
+// tokens of a stage for its heads.
+template <typename KV, int D, int G>
 struct Cfg {
-  static constexpr int EL = sizeof(T);
-  static constexpr int VEC = 16 / EL;  // dims per lane: one 16-byte vector of a row
+  static constexpr int EL = sizeof(KV);
+  // dims per lane: one 16-byte vector of a 16- or 32-bit row; 8 bytes of an E4M3 row (so
+  // the lane layout, and the query / output vectors, match the bf16 case)
+  static constexpr int VEC = EL == 1 ? 8 : 16 / EL;
+  // stages in the ring: the same bytes in flight for every element size
+  static constexpr int STAGES = EL == 1 ? 6 : 3;
   static constexpr int LPR = D / VEC;  // lanes per token row
   static_assert(LPR >= 1 && LPR <= 32 && (32 % LPR) == 0, "row must map onto a warp");
   static constexpr int RPI = 32 / LPR;  // token rows per warp instruction
@@ -235,9 +252,10 @@ struct Cfg {
   }
 };
 
-template <typename T, int D, int G>
+template <typename KV, int D, int G>
 struct Smem {
-  using C = Cfg<T, D, G>;
+  using C = Cfg<KV, D, G>;
+  static constexpr int kStages = C::STAGES;
   // Byte offsets inside the dynamic shared memory of one CTA with HG KV heads served by
   // `warps` consumer warps.
   static __host__ __device__ size_t stage_bytes(int hg) { return size_t(kTPS) * hg * D * C::EL; }
@@ -255,10 +273,11 @@ struct Smem {
 };
 
 // ---------------------------------------------------------------- the split-K kernel
-template <typename T, int D, int G>
+template <typename T, int D, int G, typename KV>
 __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_constant__ DecodeParams p) {
-  using C = Cfg<T, D, G>;
-  using SM = Smem<T, D, G>;
+  using C = Cfg<KV, D, G>;
+  using SM = Smem<KV, D, G>;
+  constexpr int kStages = C::STAGES;
   constexpr int VEC = C::VEC, LPR = C::LPR, RPI = C::RPI, TPL = C::TPL, NV = C::NV, NVF = C::NVF;
   constexpr int SH = C::SH, LOG_G = C::LOG_G;
   const int HG = p.hg_size, QG = p.qg, GF = p.group;
@@ -501,8 +520,8 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
   const int lir = lane & (LPR - 1), r = lane / LPR;
   const int Hq = p.num_heads;
   float* pbuf = reinterpret_cast<float*>(smem + SM::pbuf_off(HG)) + warp * SM::pbuf_floats_per_warp();
-  const T* kbase = reinterpret_cast<const T*>(smem + SM::k_off(HG));
-  const T* vbase = reinterpret_cast<const T*>(smem + SM::v_off(HG));
+  const KV* kbase = reinterpret_cast<const KV*>(smem + SM::k_off(HG));
+  const KV* vbase = reinterpret_cast<const KV*>(smem + SM::v_off(HG));
   const size_t stage_elems = sbytes / C::EL;
 
   // Butterfly without selects: slot s of this lane holds the partial dot of value
@@ -528,8 +547,8 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
   float2 acc[G][VEC / 2];  // unnormalised O of head g, this lane's dims, this row group
   float mrun[G];
   float lpart[NVF];
-  const T* kw = kbase + hk * D + lir * VEC;  // this lane's column in every K / V row
-  const T* vw = vbase + hk * D + lir * VEC;
+  const KV* kw = kbase + hk * D + lir * VEC;  // this lane's column in every K / V row
+  const KV* vw = vbase + hk * D + lir * VEC;
   const int row_stride = HG * D;
 
   int stage = 0;
@@ -559,14 +578,16 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
       for (int i = 0; i < NVF; ++i) lpart[i] = 0.f;
     }
     const int valid = (d.flags & kBad) ? 0 : d.valid;
-    const T* ks = kw + stage * stage_elems;
-    if (d.wslot >= 0 && qg == 0 && r == (d.valid - 1) % RPI) {
-      // fused KV write: this warp's KV head of the new token's row, shared -> cache
-      const int64_t off = d.wslot * kv_row_bytes + (int64_t(d.hg * HG + hk) * D + lir * VEC) * C::EL;
-      const int t = d.valid - 1;
-      *reinterpret_cast<uint4*>(p.k_cache_w + off) = *reinterpret_cast<const uint4*>(ks + t * row_stride);
-      *reinterpret_cast<uint4*>(p.v_cache_w + off) =
-          *reinterpret_cast<const uint4*>(vw + stage * stage_elems + t * row_stride);
+    const KV* ks = kw + stage * stage_elems;
+    if constexpr (sizeof(KV) == sizeof(T)) {  // the fused write exists for 16/32-bit caches only
+      if (d.wslot >= 0 && qg == 0 && r == (d.valid - 1) % RPI) {
+        // fused KV write: this warp's KV head of the new token's row, shared -> cache
+        const int64_t off = d.wslot * kv_row_bytes + (int64_t(d.hg * HG + hk) * D + lir * VEC) * C::EL;
+        const int t = d.valid - 1;
+        *reinterpret_cast<uint4*>(p.k_cache_w + off) = *reinterpret_cast<const uint4*>(ks + t * row_stride);
+        *reinterpret_cast<uint4*>(p.v_cache_w + off) =
+            *reinterpret_cast<const uint4*>(vw + stage * stage_elems + t * row_stride);
+      }
     }
 
     // ---- S = q . K: slot (tj, gj) holds token r + RPI * (tj ^ Pt), head gj ^ Pg
@@ -575,7 +596,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
     for (int tj = 0; tj < TPL; ++tj) {
       const int t = r + RPI * (tj ^ Pt);
       float kf[VEC];
-      RowVec<T, VEC>::load(ks + t * row_stride, kf);
+      RowVec<KV, VEC>::load(ks + t * row_stride, kf);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float2 a = make_float2(0.f, 0.f);
@@ -643,13 +664,13 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
     __syncwarp();
 
     // ---- O += P . V over this lane's tokens r + RPI * ti
-    const T* vs = vw + stage * stage_elems;
+    const KV* vs = vw + stage * stage_elems;
     if (valid == kTPS) {
 #pragma unroll
       for (int ti = 0; ti < TPL; ++ti) {
         const int t = r + RPI * ti;
         float vf[VEC];
-        RowVec<T, VEC>::load(vs + t * row_stride, vf);
+        RowVec<KV, VEC>::load(vs + t * row_stride, vf);
         float pw[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) pw[g] = pbuf[r * NV + ti * G + g];
@@ -665,7 +686,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
         const int t = r + RPI * ti;
         if (t < valid) {  // rows past the request's end hold stale data: skip, never multiply
           float vf[VEC];
-          RowVec<T, VEC>::load(vs + t * row_stride, vf);
+          RowVec<KV, VEC>::load(vs + t * row_stride, vf);
           float pw[G];
 #pragma unroll
           for (int g = 0; g < G; ++g) pw[g] = pbuf[r * NV + ti * G + g];
@@ -715,7 +736,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_splitk_kernel(const __grid_c
     if (r == 0) {
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float inv = lh[g] > 0.f ? 1.f / lh[g] : 0.f;
+        const float inv = lh[g] > 0.f ? p.v_scale / lh[g] : 0.f;  // V codes -> values: * v_scale
         float o[VEC];
 #pragma unroll
         for (int e = 0; e < VEC / 2; ++e) {
@@ -809,10 +830,10 @@ __global__ void __launch_bounds__(1024) decode_merge_kernel(const __grid_constan
 // GW = query heads per warp (<= 4), QG = G / GW consumer warps per KV head, HG = KV heads
 // per CTA: the largest power of two dividing num_kv_heads with HG * QG <= 8 consumer warps
 // whose stages fit in shared memory.
-template <typename T, int D, int GW>
+template <typename KV, int D, int GW>
 int pick_hg(int num_kv_heads, int qg) {
   for (int hg = 8; hg >= 1; hg >>= 1)
-    if (num_kv_heads % hg == 0 && hg * qg <= 8 && Smem<T, D, GW>::total(hg, hg * qg) <= size_t(kSmemLimit))
+    if (num_kv_heads % hg == 0 && hg * qg <= 8 && Smem<KV, D, GW>::total(hg, hg * qg) <= size_t(kSmemLimit))
       return hg;
   return 0;
 }
@@ -823,7 +844,10 @@ int hg_for(pa_dtype dt, int D, int G, int num_kv_heads) {
   const int GW = gw_of(G), QG = G / GW;
 #define PA_HG_CASE(TT, DD, WW) \
   if (D == DD && GW == WW) return pick_hg<TT, DD, WW>(num_kv_heads, QG);
-  if (dt == PA_BF16) {
+  if (dt == PA_FP8_E4M3) {
+    PA_HG_CASE(Fp8E4M3, 64, 1) PA_HG_CASE(Fp8E4M3, 64, 2) PA_HG_CASE(Fp8E4M3, 64, 4)
+    PA_HG_CASE(Fp8E4M3, 128, 1) PA_HG_CASE(Fp8E4M3, 128, 2) PA_HG_CASE(Fp8E4M3, 128, 4)
+  } else if (dt == PA_BF16) {
     PA_HG_CASE(__nv_bfloat16, 64, 1) PA_HG_CASE(__nv_bfloat16, 64, 2) PA_HG_CASE(__nv_bfloat16, 64, 4)
     PA_HG_CASE(__nv_bfloat16, 128, 1) PA_HG_CASE(__nv_bfloat16, 128, 2) PA_HG_CASE(__nv_bfloat16, 128, 4)
   } else {
@@ -834,12 +858,12 @@ int hg_for(pa_dtype dt, int D, int G, int num_kv_heads) {
   return 0;
 }
 
-template <typename T, int D, int GW>
+template <typename T, int D, int GW, typename KV>
 cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
-  using SM = Smem<T, D, GW>;
+  using SM = Smem<KV, D, GW>;
   const int G = a.num_heads / a.num_kv_heads;
   const int QG = G / GW;
-  const int hg = pick_hg<T, D, GW>(a.num_kv_heads, QG);
+  const int hg = pick_hg<KV, D, GW>(a.num_kv_heads, QG);
   if (hg == 0) return cudaErrorInvalidValue;
   DecodeParams p;
   p.out = a.out;
@@ -848,9 +872,10 @@ cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   p.v_cache = static_cast<const char*>(a.v_cache);
   p.k_cache_w = static_cast<char*>(const_cast<void*>(a.k_cache));
   p.v_cache_w = static_cast<char*>(const_cast<void*>(a.v_cache));
-  p.k_new = static_cast<const char*>(a.k_new);
-  p.v_new = static_cast<const char*>(a.v_new);
-  p.slot_mapping = a.slot_mapping;
+  const bool fused = sizeof(KV) == sizeof(T) && a.k_new != nullptr;
+  p.k_new = fused ? static_cast<const char*>(a.k_new) : nullptr;
+  p.v_new = fused ? static_cast<const char*>(a.v_new) : nullptr;
+  p.slot_mapping = fused ? a.slot_mapping : nullptr;
   p.block_table = a.block_table;
   p.seq_lens = a.seq_lens;
   p.qsl = a.query_start_loc;
@@ -874,9 +899,11 @@ cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   p.qg = QG;
   p.num_ctas = num_ctas;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  if (sizeof(KV) == 1) p.scale_log2 *= a.k_scale;  // K codes -> values: fold k_scale into q
+  p.v_scale = sizeof(KV) == 1 ? a.v_scale : 1.f;
   const int warps = hg * QG;
   const size_t smem = SM::total(hg, warps);
-  auto kern = decode_splitk_kernel<T, D, GW>;
+  auto kern = decode_splitk_kernel<T, D, GW, KV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_ctas), dim3((warps + 1) * 32), smem, stream, p);
@@ -886,12 +913,12 @@ cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
                     stream, p, G);
 }
 
-template <typename T, int D>
+template <typename T, int D, typename KV = T>
 cudaError_t run_g(const AttnArgs& a, int G, int num_ctas, cudaStream_t stream) {
   switch (gw_of(G)) {
-    case 1: return run<T, D, 1>(a, num_ctas, stream);
-    case 2: return run<T, D, 2>(a, num_ctas, stream);
-    case 4: return run<T, D, 4>(a, num_ctas, stream);
+    case 1: return run<T, D, 1, KV>(a, num_ctas, stream);
+    case 2: return run<T, D, 2, KV>(a, num_ctas, stream);
+    case 4: return run<T, D, 4, KV>(a, num_ctas, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -927,6 +954,11 @@ size_t decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int
 cudaError_t launch_decode(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   const int G = a.num_heads / a.num_kv_heads;
   if (a.num_seqs == 0) return cudaSuccess;
+  if (a.cache_dtype == PA_FP8_E4M3) {  // E4M3 caches: bf16 q and out only
+    if (a.dtype != PA_BF16) return cudaErrorInvalidValue;
+    if (a.head_dim == 64) return run_g<__nv_bfloat16, 64, Fp8E4M3>(a, G, num_ctas, stream);
+    return run_g<__nv_bfloat16, 128, Fp8E4M3>(a, G, num_ctas, stream);
+  }
   if (a.dtype == PA_BF16) {
     if (a.head_dim == 64) return run_g<__nv_bfloat16, 64>(a, G, num_ctas, stream);
     return run_g<__nv_bfloat16, 128>(a, G, num_ctas, stream);

@@ -17,6 +17,12 @@ cudaError_t launch_kv_write(const void* k, const void* v, void* k_cache, void* v
                             const int64_t* slot_mapping, int64_t num_tokens, int64_t num_slots,
                             int64_t row_bytes, unsigned int* err, cudaStream_t stream);
 
+// E4M3 cache write: row_elems = num_kv_heads * head_dim (a multiple of 16).
+cudaError_t launch_kv_write_fp8(const void* k, const void* v, pa_dtype in_dtype, void* k_cache, void* v_cache,
+                                const int64_t* slot_mapping, int64_t num_tokens, int64_t num_slots,
+                                int64_t row_elems, float k_scale, float v_scale, unsigned int* err,
+                                cudaStream_t stream);
+
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
                                int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
                                unsigned int* err, cudaStream_t stream);
@@ -39,7 +45,7 @@ struct AttnArgs {
   int block_size;
   int64_t num_blocks;
   float scale;
-  pa_dtype dtype;
+  pa_dtype dtype;  // of q and out (and of the caches unless cache_dtype says otherwise)
   void* workspace;
   unsigned int* err;
   // Fused KV write (decode requests only; all three null otherwise): row t of k_new / v_new
@@ -47,6 +53,10 @@ struct AttnArgs {
   const void* k_new = nullptr;
   const void* v_new = nullptr;
   const int64_t* slot_mapping = nullptr;
+  // FP8 E4M3 caches: cache_dtype = PA_FP8_E4M3, values = code * k_scale (v_scale).
+  pa_dtype cache_dtype = PA_BF16;
+  float k_scale = 1.f;
+  float v_scale = 1.f;
 };
 
 // Decode (q_len == 1 requests): workspace bytes needed, and the launch (split-K + merge).

@@ -26,7 +26,8 @@ constexpr size_t simple_smem_bytes() {
   return size_t(kRows) * D * 4 + size_t(kKT) * (D + 1) * 4 + size_t(kKT) * D * 4 + size_t(kRows) * kKT * 4;
 }
 
-template <typename T, int D, int G>
+// T: q / out element type; KV: cache element type (T, or Fp8E4M3 with bf16 T).
+template <typename T, int D, int G, typename KV>
 __global__ void __launch_bounds__(kThreads) prefill_simple_kernel(const __grid_constant__ AttnArgs a) {
   constexpr int kQT = kRows / G;       // queries per tile
   constexpr int R = kRows;             // rows of the tile
@@ -36,6 +37,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simple_kernel(const __grid_c
   constexpr int DPT = D / TPR;          // output dims per thread
   constexpr int EL = sizeof(T);
   constexpr int VEC = 16 / EL;
+  constexpr int KVEC = 16 / int(sizeof(KV));  // cache elements per 16-byte load
 
   const int s = blockIdx.x, hk = blockIdx.y;
   const int q0 = blockIdx.z * kQT;
@@ -86,14 +88,14 @@ __global__ void __launch_bounds__(kThreads) prefill_simple_kernel(const __grid_c
 
   const int last_key = pos0 + nq - 1;  // highest position any row of the tile sees
   const int32_t* bt = a.block_table + int64_t(s) * a.max_blocks_per_seq;
-  const T* kc = static_cast<const T*>(a.k_cache);
-  const T* vc = static_cast<const T*>(a.v_cache);
+  const KV* kc = static_cast<const KV*>(a.k_cache);
+  const KV* vc = static_cast<const KV*>(a.v_cache);
   for (int k0 = 0; k0 <= last_key; k0 += kKT) {
     __syncthreads();  // previous tile fully used
-    for (int i = threadIdx.x; i < kKT * (D / VEC); i += kThreads) {
-      const int t = i / (D / VEC), d0 = (i % (D / VEC)) * VEC;
+    for (int i = threadIdx.x; i < kKT * (D / KVEC); i += kThreads) {
+      const int t = i / (D / KVEC), d0 = (i % (D / KVEC)) * KVEC;
       const int kp = k0 + t;
-      float kf[VEC], vf[VEC];
+      float kf[KVEC], vf[KVEC];
       bool ok = kp <= last_key;
       int64_t blk = 0;
       if (ok) {
@@ -105,14 +107,21 @@ __global__ void __launch_bounds__(kThreads) prefill_simple_kernel(const __grid_c
       }
       if (ok) {
         const int64_t off = ((blk * B + kp % B) * Hkv + hk) * D + d0;
-        Elem<T>::unpack(*reinterpret_cast<const uint4*>(kc + off), kf);
-        Elem<T>::unpack(*reinterpret_cast<const uint4*>(vc + off), vf);
+        Elem<KV>::unpack(*reinterpret_cast<const uint4*>(kc + off), kf);
+        Elem<KV>::unpack(*reinterpret_cast<const uint4*>(vc + off), vf);
+        if constexpr (sizeof(KV) == 1) {  // E4M3 codes -> values
+#pragma unroll
+          for (int e = 0; e < KVEC; ++e) {
+            kf[e] *= a.k_scale;
+            vf[e] *= a.v_scale;
+          }
+        }
       } else {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) kf[e] = vf[e] = 0.f;
+        for (int e = 0; e < KVEC; ++e) kf[e] = vf[e] = 0.f;
       }
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
+      for (int e = 0; e < KVEC; ++e) {
         Ks[t][d0 + e] = kf[e];
         Vs[t][d0 + e] = vf[e];
       }
@@ -169,11 +178,11 @@ __global__ void __launch_bounds__(kThreads) prefill_simple_kernel(const __grid_c
   }
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, typename KV>
 cudaError_t run(const AttnArgs& a, cudaStream_t stream) {
   constexpr int kQT = kRows / G;
   const size_t smem = simple_smem_bytes<D>();
-  auto kern = prefill_simple_kernel<T, D, G>;
+  auto kern = prefill_simple_kernel<T, D, G, KV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(a.num_seqs, a.num_kv_heads, (a.max_query_len + kQT - 1) / kQT);
@@ -181,13 +190,13 @@ cudaError_t run(const AttnArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <typename T, int D>
+template <typename T, int D, typename KV = T>
 cudaError_t run_g(const AttnArgs& a, int G, cudaStream_t stream) {
   switch (G) {
-    case 1: return run<T, D, 1>(a, stream);
-    case 2: return run<T, D, 2>(a, stream);
-    case 4: return run<T, D, 4>(a, stream);
-    case 8: return run<T, D, 8>(a, stream);
+    case 1: return run<T, D, 1, KV>(a, stream);
+    case 2: return run<T, D, 2, KV>(a, stream);
+    case 4: return run<T, D, 4, KV>(a, stream);
+    case 8: return run<T, D, 8, KV>(a, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -203,6 +212,11 @@ bool prefill_supported(pa_dtype dtype, int head_dim, int group) {
 cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream) {
   if (a.max_query_len < 2 || a.num_seqs == 0) return cudaSuccess;
   const int G = a.num_heads / a.num_kv_heads;
+  if (a.cache_dtype == PA_FP8_E4M3) {  // E4M3 caches: bf16 q and out only
+    if (a.dtype != PA_BF16) return cudaErrorInvalidValue;
+    if (a.head_dim == 64) return run_g<__nv_bfloat16, 64, Fp8E4M3>(a, G, stream);
+    return run_g<__nv_bfloat16, 128, Fp8E4M3>(a, G, stream);
+  }
   if (a.dtype == PA_BF16) {
     if (a.head_dim == 64) return run_g<__nv_bfloat16, 64>(a, G, stream);
     return run_g<__nv_bfloat16, 128>(a, G, stream);

@@ -560,7 +560,7 @@ cudaError_t run_g(const AttnArgs& a, int G, int num_ctas, cudaStream_t stream) {
 
 bool prefill_tc_supported(const AttnArgs& a) {
   const int B = a.block_size;
-  return a.dtype == PA_BF16 && (a.head_dim == 64 || a.head_dim == 128) && B >= 8 && B <= kBN && kBN % B == 0 &&
+  return a.dtype == PA_BF16 && a.cache_dtype == PA_BF16 && (a.head_dim == 64 || a.head_dim == 128) && B >= 8 && B <= kBN && kBN % B == 0 &&
          a.num_seqs <= kMaxSeqs && encode_fn() != nullptr;
 }
 

@@ -14,7 +14,8 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from . import BlockManager, attention, attention_workspace_size, copy_blocks, kv_write, write_attention
+from . import (BlockManager, attention, attention_fp8, attention_workspace_size, copy_blocks, kv_write,
+               kv_write_fp8, write_attention)
 
 
 def storage_to_torch(a: np.ndarray) -> torch.Tensor:
@@ -25,9 +26,12 @@ def storage_to_torch(a: np.ndarray) -> torch.Tensor:
 
 
 def torch_to_storage(t: torch.Tensor) -> np.ndarray:
+    """float32 -> float32; bfloat16 -> uint16 bit patterns; float8_e4m3fn -> uint8 codes."""
     t = t.detach().cpu().contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).numpy()
     return t.numpy()
 
 
@@ -58,8 +62,10 @@ class DeviceWorkload:
             self.bm.enable_prefix_caching()
         self.dtype = torch.float32 if sp.dtype == "f32" else torch.bfloat16
         shape = (wl.num_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
-        self.k_cache = torch.zeros(shape, dtype=self.dtype, device=self.device)
-        self.v_cache = torch.zeros(shape, dtype=self.dtype, device=self.device)
+        self.fp8 = wl.kv_cache == "fp8_e4m3"
+        cache_dtype = torch.float8_e4m3fn if self.fp8 else self.dtype
+        self.k_cache = torch.zeros(shape, dtype=cache_dtype, device=self.device)
+        self.v_cache = torch.zeros(shape, dtype=cache_dtype, device=self.device)
         self.table_width = table_width
         self.phase_slots: list = []
         self.phase_copies: list = []
@@ -118,8 +124,7 @@ class DeviceWorkload:
             if len(copies):
                 copy_blocks(self.k_cache, self.v_cache, torch.from_numpy(copies).to(self.device))
             if len(slots):
-                kv_write(k.to(self.device), v.to(self.device), self.k_cache, self.v_cache,
-                         torch.from_numpy(slots).to(self.device))
+                self._write(k.to(self.device), v.to(self.device), torch.from_numpy(slots).to(self.device))
 
     def prepare_step(self) -> StepInputs:
         """Run the step's block-manager operations and stage its inputs on the device."""
@@ -158,6 +163,22 @@ class DeviceWorkload:
             workspace=ws,
         )
 
+    def _write(self, k, v, slots, stream=None):
+        if self.fp8:
+            kv_write_fp8(k, v, self.k_cache, self.v_cache, slots, self.wl.k_scale, self.wl.v_scale, stream=stream)
+        else:
+            kv_write(k, v, self.k_cache, self.v_cache, slots, stream=stream)
+
+    def _attend(self, st: StepInputs, stream=None):
+        kw = dict(max_query_len=st.max_query_len, max_seq_len=st.max_seq_len, scale=self.wl.spec.scale,
+                  workspace=st.workspace, stream=stream)
+        if self.fp8:
+            attention_fp8(st.out, st.q, self.k_cache, self.v_cache, st.block_table, st.seq_lens, st.query_start_loc,
+                          k_scale=self.wl.k_scale, v_scale=self.wl.v_scale, **kw)
+        else:
+            attention(st.out, st.q, self.k_cache, self.v_cache, st.block_table, st.seq_lens, st.query_start_loc,
+                      **kw)
+
     def fusable(self, st: StepInputs) -> bool:
         """The step appends exactly its query tokens (row t of k_new belongs to query row t)."""
         return st.q.shape[0] > 0 and st.slot_mapping.shape[0] == st.q.shape[0]
@@ -166,11 +187,11 @@ class DeviceWorkload:
         """The hot path of one step: copies, write, attention (all on the device).
 
         ``fused``: the write and the attention as one pa_write_attention call (the step
-        must be fusable)."""
+        must be fusable; an FP8 cache has no fused call and runs the two)."""
         sp = self.wl.spec
         if st.block_mapping.shape[0]:
             copy_blocks(self.k_cache, self.v_cache, st.block_mapping, stream=stream)
-        if fused:
+        if fused and not self.fp8:
             if not self.fusable(st):
                 raise ValueError("this step's appended tokens are not its query tokens")
             write_attention(st.out, st.q, st.k_new, st.v_new, st.slot_mapping, self.k_cache, self.v_cache,
@@ -178,9 +199,7 @@ class DeviceWorkload:
                             max_seq_len=st.max_seq_len, scale=sp.scale, workspace=st.workspace, stream=stream)
             return st.out
         if st.slot_mapping.shape[0]:
-            kv_write(st.k_new, st.v_new, self.k_cache, self.v_cache, st.slot_mapping, stream=stream)
+            self._write(st.k_new, st.v_new, st.slot_mapping, stream=stream)
         if st.q.shape[0]:
-            attention(st.out, st.q, self.k_cache, self.v_cache, st.block_table, st.seq_lens,
-                      st.query_start_loc, max_query_len=st.max_query_len, max_seq_len=st.max_seq_len,
-                      scale=sp.scale, workspace=st.workspace, stream=stream)
+            self._attend(st, stream=stream)
         return st.out
