@@ -11,6 +11,8 @@ Contents, each citing the page passage it follows:
 - prefix_cache.PrefixCachingAllocator: the same plus reuse of cached full blocks
   found by their token prefix, with LRU eviction through the free queue.
 - fp8: the E4M3 cache format, quantised writes (kv_write_fp8_ref) and dequantisation.
+- swap.SwappingAllocator / SwappingPrefixAllocator: a CPU block pool and the swap out /
+  swap in of preempted sequence groups.
 - attention.kv_write_ref / copy_blocks_ref / paged_attention_ref /
   dense_causal_ref: the byte moves and the float64 attention.
 - runner.run_workload: a seeded workload, phase by phase.
@@ -31,4 +33,5 @@ from .attention import (  # noqa: F401
 from .block_manager import BlockAllocator, NoFreeBlocks, TooLarge  # noqa: F401
 from .prefix_cache import PrefixCachingAllocator  # noqa: F401
 from .fp8 import dequantize, kv_write_fp8_ref, quantize  # noqa: F401
+from .swap import SwappingAllocator, SwappingPrefixAllocator  # noqa: F401
 from .runner import OracleResult, batch_metadata, run_allocator, run_script, run_workload, step_ranges  # noqa: F401
