@@ -7,6 +7,7 @@
  *   pa_write_attention  the two above in one call (the write fused into decode)
  *   pa_kv_write_fp8 / pa_attention_fp8  the same over FP8 (E4M3) caches
  *   pa_copy_blocks  copy whole physical blocks (the copy step of copy-on-write)
+ *   pa_swap_blocks  move whole blocks between the GPU pool and a CPU pool (preemption)
  *   pa_bm_*         host-side block accounting: free queue, block tables, ref counts, CoW
  *
  * Conventions shared by every entry point:
@@ -39,7 +40,8 @@
  *  [read]  vLLM code reading, sourceaix.com/community/post/7301643446391930880 --
  *          5.1.1 single request (logical vs physical blocks, '# filled'),
  *          5.2.1 parallel sampling (shared blocks, ref count, copy-on-write).
- *  [intro] VLLM overview, dn008.com.cn/news/553482 -- 2.1 KV cache (causal mask).
+ *  [intro] VLLM overview, dn008.com.cn/news/553482 -- 2.1 KV cache (causal mask); 4
+ *          scheduler (waiting / running / swapped queues, swap phase).
  */
 #ifndef PA_H_
 #define PA_H_
@@ -228,6 +230,26 @@ int pa_attention_fp8(void* out, const void* q, const void* k_cache, const void* 
                      size_t workspace_bytes, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------------
+ * pa_swap_blocks -- [read] 6.2.1 (a preempted sequence group's KV blocks are swapped out
+ * to the CPU, and swapped back in when GPU resources return); [intro] 4, scheduling flow,
+ * swap phase (the swapped queue lives in CPU memory).
+ *
+ * For each i in [0, num_pairs): s = block_mapping[2i], d = block_mapping[2i+1]:
+ *     dst_k[d] = src_k[s]; dst_v[d] = src_v[s]     (whole blocks, byte copy)
+ * src_* pools have src_num_blocks blocks, dst_* pools dst_num_blocks, all with the block
+ * geometry [block_size, num_kv_heads, head_dim] of `dtype` (PA_F32 / PA_BF16 /
+ * PA_FP8_E4M3). Each pool may be device memory or pinned host memory (cudaHostAlloc or
+ * cudaHostRegister'ed, used through its unified address): the kernel moves the blocks
+ * over the CPU-GPU link itself, one launch per call. block_mapping: int64 [num_pairs, 2],
+ * device or pinned host memory. No dst may repeat. Out-of-range ids are skipped and set
+ * PA_DEVERR_BLOCK_RANGE. The pairs come from pa_bm_swap_out / pa_bm_swap_in.
+ * --------------------------------------------------------------------------- */
+int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                   const int64_t* block_mapping, int64_t num_pairs, int64_t src_num_blocks,
+                   int64_t dst_num_blocks, int block_size, int num_kv_heads, int head_dim,
+                   pa_dtype dtype, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------
  * pa_attention_fixed_scratch -- no counterpart in the pages: an addition for callers that
  * cannot allocate device memory, so cannot provide pa_attention's workspace. Examples: a
  * serving loop that reserved the GPU's free memory for its KV pool at start-up and must not
@@ -339,6 +361,34 @@ int pa_bm_append_tokens_batch(pa_bm* bm, const int64_t* seqs, const int64_t* cou
                               const int32_t* token_ids, int64_t* slots_out, int64_t* done_out);
 /* Registered blocks now, blocks reused by lookups so far, registrations evicted so far. */
 int pa_bm_prefix_stats(const pa_bm* bm, int64_t* cached_blocks, int64_t* hit_blocks, int64_t* evictions);
+
+/* ------------------------------------------------------------------------------
+ * Swapping -- [read] 6.2.1 SequenceGroup (preempted groups are swapped out to the CPU and
+ * swapped back in later); [intro] 4, scheduling flow, swap phase (swapped queue in CPU
+ * memory).
+ *
+ * A CPU pool of num_cpu_blocks blocks with its own FIFO free queue (initial order
+ * cpu_free_order) and reference counts. pa_bm_swap_out moves a group of sequences to the
+ * CPU: each distinct block of their tables (first met walking seqs in order, each table
+ * from its first block) gets one CPU block whose count is the number of group members
+ * holding it; the GPU block's count drops by that number and it is released at 0 (a block
+ * still held outside the group stays). The (gpu, cpu) pairs to copy go to pairs_out
+ * [capacity, 2] and their number to *num_pairs_out; run pa_swap_blocks with them before
+ * the released GPU blocks are written again. pa_bm_swap_in is the reverse (new GPU
+ * blocks from the free list, (cpu, gpu) pairs; copy them before reading the sequences).
+ * Either returns PA_ERR_NO_BLOCKS (changing nothing) when the other pool is short,
+ * PA_ERR_INVALID_ARG when capacity is below the number of pairs, a sequence repeats or is
+ * already on the other side. A swapped sequence takes no append or fork and cannot be in
+ * pa_bm_batch_tables; pa_bm_free_seq releases its CPU blocks.
+ * --------------------------------------------------------------------------- */
+int pa_bm_enable_swap(pa_bm* bm, int64_t num_cpu_blocks, const int32_t* cpu_free_order);
+int pa_bm_swap_out(pa_bm* bm, const int64_t* seqs, int64_t n, int64_t* pairs_out, int64_t capacity,
+                   int64_t* num_pairs_out);
+int pa_bm_swap_in(pa_bm* bm, const int64_t* seqs, int64_t n, int64_t* pairs_out, int64_t capacity,
+                  int64_t* num_pairs_out);
+int pa_bm_is_swapped(const pa_bm* bm, int64_t seq);        /* 1, 0, or -1 if unknown */
+int64_t pa_bm_num_free_cpu(const pa_bm* bm);               /* -1 without swapping */
+int pa_bm_cpu_ref_count(const pa_bm* bm, int64_t block);  /* -1 if out of range */
 
 #ifdef __cplusplus
 }

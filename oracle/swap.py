@@ -8,8 +8,9 @@ Sources:
   blocks are swapped out to the CPU (status swapped), with one sequence they are freed and
   the request is recomputed later; when resources return the CPU blocks are swapped back
   in and the group runs again.
-- VLLM scheduling page (dn008.com.cn), §3 Swap phase: under resource pressure lower
-  priority work moves to CPU memory (the swapped queue), like page swapping in an OS.
+- VLLM overview page (dn008.com.cn), §4 scheduler structure › scheduling flow › swap
+  phase: under resource pressure lower-priority work moves to CPU memory (the swapped
+  queue), like page swapping in an OS.
 - vLLM docs page (docs.acceleratez.fun, "vLLM"), Copy-on-Write › reference counts
   (a block is held by several sequences; it is released when its count reaches 0).
 

@@ -21,6 +21,7 @@ __all__ = [
     "BlockManager",
     "kv_write",
     "copy_blocks",
+    "swap_blocks",
     "attention",
     "write_attention",
     "kv_write_fp8",
@@ -56,6 +57,13 @@ _sig = {
     "pa_kv_write_fp8": (_i, [_p, _p, _i, _p, _p, _p, _i64, _i64, _i, _i, _i, _f, _f, _p]),
     "pa_attention_fp8": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i64, _f, _f, _f,
                               _p, _sz, _p]),
+    "pa_swap_blocks": (_i, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i, _i, _i, _i, _p]),
+    "pa_bm_enable_swap": (_i, [_p, _i64, _p]),
+    "pa_bm_swap_out": (_i, [_p, _p, _i64, _p, _i64, ctypes.POINTER(_i64)]),
+    "pa_bm_swap_in": (_i, [_p, _p, _i64, _p, _i64, ctypes.POINTER(_i64)]),
+    "pa_bm_is_swapped": (_i, [_p, _i64]),
+    "pa_bm_num_free_cpu": (_i64, [_p]),
+    "pa_bm_cpu_ref_count": (_i, [_p, _i64]),
     "pa_bm_create": (_p, [_i64, _i, _p]),
     "pa_bm_destroy": (None, [_p]),
     "pa_bm_add_seq": (_i, [_p, _i64]),
@@ -156,6 +164,33 @@ def copy_blocks(k_cache, v_cache, block_mapping, stream=None):
     st = lib.pa_copy_blocks(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ptr, n, NB, B, Hkv, D,
                             _dtype_code(k_cache), _stream(stream, k_cache.device))
     _check(st, "pa_copy_blocks")
+
+
+def _pool_ptr(t: torch.Tensor, name: str) -> int:
+    """A CUDA tensor, or a pinned host tensor (used through its unified address)."""
+    if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous tensor")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    return t.data_ptr()
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping, stream=None):
+    """pa_swap_blocks: dst[d] = src[s] for each (s, d) row of block_mapping [n, 2], whole blocks,
+    between two pools of one block geometry; either pool may be pinned host memory."""
+    if src_k.shape[1:] != dst_k.shape[1:] or src_k.dtype != dst_k.dtype or src_k.shape != src_v.shape or \
+            dst_k.shape != dst_v.shape or src_k.dim() != 4:
+        raise ValueError("pools must be [num_blocks, block_size, num_kv_heads, head_dim] of one geometry and dtype")
+    if block_mapping.dim() != 2 or block_mapping.shape[1] != 2 or block_mapping.dtype != torch.int64:
+        raise ValueError("block_mapping must be int64 [num_pairs, 2]")
+    n = int(block_mapping.shape[0])
+    _, B, Hkv, D = (int(x) for x in src_k.shape)
+    dev = src_k.device if src_k.is_cuda else dst_k.device
+    st = lib.pa_swap_blocks(_pool_ptr(src_k, "src_k"), _pool_ptr(src_v, "src_v"), _pool_ptr(dst_k, "dst_k"),
+                            _pool_ptr(dst_v, "dst_v"), _pool_ptr(block_mapping, "block_mapping") if n else None, n,
+                            int(src_k.shape[0]), int(dst_k.shape[0]), B, Hkv, D, _dtype_code(src_k),
+                            _stream(stream, dev))
+    _check(st, "pa_swap_blocks")
 
 
 def attention_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int) -> int:
@@ -387,6 +422,45 @@ class BlockManager:
         _check(lib.pa_bm_prefix_stats(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
                "pa_bm_prefix_stats")
         return int(a.value), int(b.value), int(c.value)
+
+    # -- swapping ----------------------------------------------------------------
+    def enable_swap(self, num_cpu_blocks: int, cpu_free_order):
+        import numpy as np
+
+        order = np.ascontiguousarray(np.asarray(cpu_free_order, dtype=np.int32))
+        if order.shape != (num_cpu_blocks,):
+            raise ValueError("cpu_free_order must have num_cpu_blocks entries")
+        _check(lib.pa_bm_enable_swap(self._h, num_cpu_blocks, order.ctypes.data), "pa_bm_enable_swap")
+
+    def _swap(self, fn, what, seqs):
+        import numpy as np
+
+        s = np.ascontiguousarray(np.asarray(seqs, np.int64))
+        cap = sum(int(lib.pa_bm_num_seq_blocks(self._h, int(x))) for x in s)
+        out = np.empty((max(cap, 1), 2), np.int64)
+        n = ctypes.c_int64(0)
+        _check(fn(self._h, s.ctypes.data if len(s) else None, len(s), out.ctypes.data, cap, ctypes.byref(n)), what)
+        return out[: n.value]
+
+    def swap_out(self, seqs):
+        """Move the group to the CPU pool; returns the (gpu, cpu) pairs to copy, int64 [n, 2]."""
+        return self._swap(lib.pa_bm_swap_out, "pa_bm_swap_out", seqs)
+
+    def swap_in(self, seqs):
+        """Move the group back to the GPU; returns the (cpu, gpu) pairs to copy, int64 [n, 2]."""
+        return self._swap(lib.pa_bm_swap_in, "pa_bm_swap_in", seqs)
+
+    def is_swapped(self, seq: int) -> bool:
+        r = int(lib.pa_bm_is_swapped(self._h, seq))
+        if r < 0:
+            raise PAError(7, "pa_bm_is_swapped")
+        return bool(r)
+
+    def num_free_cpu(self) -> int:
+        return int(lib.pa_bm_num_free_cpu(self._h))
+
+    def cpu_ref_count(self, block: int) -> int:
+        return int(lib.pa_bm_cpu_ref_count(self._h, block))
 
     def fork(self, parent: int, child: int):
         _check(lib.pa_bm_fork(self._h, parent, child), "pa_bm_fork")

@@ -313,4 +313,26 @@ int pa_attention_fp8(void* out, const void* q, const void* k_cache, const void* 
   return run_attention(a, ctas, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v, const int64_t* block_mapping,
+                   int64_t num_pairs, int64_t src_num_blocks, int64_t dst_num_blocks, int block_size,
+                   int num_kv_heads, int head_dim, pa_dtype dtype, pa_stream_t stream) {
+  if (!src_k || !src_v || !dst_k || !dst_v) return PA_ERR_INVALID_ARG;
+  if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v)) return PA_ERR_INVALID_ARG;
+  if (src_num_blocks < 1 || dst_num_blocks < 1 || block_size < 1 || num_kv_heads < 1 || head_dim < 1)
+    return PA_ERR_INVALID_ARG;
+  if (elem_bytes(dtype) == 0) return PA_ERR_INVALID_ARG;
+  const int64_t block_bytes = int64_t(block_size) * num_kv_heads * head_dim * elem_bytes(dtype);
+  if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if (block_bytes / 16 > 0x7fffffff) return PA_ERR_UNSUPPORTED;
+  if (num_pairs < 0 || num_pairs > 0x7fffffff) return PA_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (!block_mapping || reinterpret_cast<uintptr_t>(block_mapping) % 8 != 0) return PA_ERR_INVALID_ARG;
+  cudaError_t e;
+  unsigned int* err = pa::device_error_word(&e);
+  if (!err) return cuda_fail(e);
+  e = pa::launch_swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping, num_pairs, src_num_blocks, dst_num_blocks,
+                             block_bytes, err, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 }  // extern "C"

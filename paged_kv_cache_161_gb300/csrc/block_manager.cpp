@@ -9,6 +9,11 @@
 // fresh block). Code-reading page 5.1.1 / 5.2.1 (the worked examples). vLLM 0.10.0 flow
 // page 3.3 (pool of free blocks; slot = block * B + offset).
 //
+// Swapping (optional, pa_bm_enable_swap): code-reading page 6.2.1 (a preempted sequence
+// group's KV blocks are swapped out to the CPU and back in when resources return); a CPU
+// pool with its own FIFO free queue and reference counts; each distinct block of a group
+// moves once, and a block still held outside the group stays on the GPU.
+//
 // Prefix caching (optional, pa_bm_enable_prefix_caching): "vLLM" docs page, Copy-on-Write ›
 // shared-prefix detection (hash the prompt prefix; reuse cached prefix KV, counts + 1) and
 // Prefix Caching › mechanism (look up on arrival, reuse on a hit, cache on a miss); vLLM
@@ -90,6 +95,7 @@ struct pa_bm {
     int64_t len = 0;
     Key chain = kRootKey;          // key of the prefix through the last full block
     std::vector<int32_t> partial;  // token ids of the partially filled last block
+    bool swapped = false;          // its table holds CPU block ids
   };
   int64_t num_blocks = 0;
   int block_size = 0;
@@ -107,6 +113,11 @@ struct pa_bm {
   std::vector<Key> block_key;
   std::vector<char> registered;
   int64_t hit_blocks = 0, evictions = 0;
+  // CPU block pool for swapping (FIFO free queue, reference counts)
+  bool swap = false;
+  int64_t num_cpu_blocks = 0;
+  std::deque<int32_t> cpu_free;
+  std::vector<int32_t> cpu_ref;
 
   void push_free(int32_t b) {
     nxt[b] = -1;
@@ -155,6 +166,7 @@ int append_impl(pa_bm* bm, int64_t seq, int64_t n, const int32_t* tokens, int64_
   auto it = bm->seqs.find(seq);
   if (it == bm->seqs.end()) return PA_ERR_NOT_FOUND;
   pa_bm::Seq& sq = it->second;
+  if (sq.swapped) return PA_ERR_INVALID_ARG;
   const int64_t B = bm->block_size;
   if (n == 0) return PA_OK;
   if (ceil_div(sq.len + n, B) > bm->num_blocks) return PA_ERR_TOO_LARGE;
@@ -304,6 +316,7 @@ int pa_bm_fork(pa_bm* bm, int64_t parent, int64_t child) {
   if (!bm) return PA_ERR_INVALID_ARG;
   auto it = bm->seqs.find(parent);
   if (it == bm->seqs.end() || bm->seqs.count(child)) return PA_ERR_NOT_FOUND;
+  if (it->second.swapped) return PA_ERR_INVALID_ARG;
   pa_bm::Seq c = it->second;
   for (int32_t b : c.table) bm->ref[size_t(b)] += 1;
   bm->seqs.emplace(child, std::move(c));
@@ -314,8 +327,13 @@ int pa_bm_free_seq(pa_bm* bm, int64_t seq) {
   if (!bm) return PA_ERR_INVALID_ARG;
   auto it = bm->seqs.find(seq);
   if (it == bm->seqs.end()) return PA_ERR_NOT_FOUND;
-  for (int32_t b : it->second.table) {
-    if (--bm->ref[size_t(b)] == 0) bm->push_free(b);
+  if (it->second.swapped) {
+    for (int32_t c : it->second.table)
+      if (--bm->cpu_ref[size_t(c)] == 0) bm->cpu_free.push_back(c);
+  } else {
+    for (int32_t b : it->second.table) {
+      if (--bm->ref[size_t(b)] == 0) bm->push_free(b);
+    }
   }
   bm->seqs.erase(it);
   return PA_OK;
@@ -366,6 +384,7 @@ int pa_bm_batch_tables(const pa_bm* bm, const int64_t* seqs, int64_t n, int32_t*
     auto it = bm->seqs.find(seqs[i]);
     if (it == bm->seqs.end()) return PA_ERR_NOT_FOUND;
     const auto& t = it->second.table;
+    if (it->second.swapped) return PA_ERR_INVALID_ARG;  // its blocks are not on the GPU
     if (int64_t(t.size()) > width || it->second.len > 0x7fffffff) return PA_ERR_INVALID_ARG;
     int32_t* row = table_out + i * width;
     if (!t.empty()) std::memcpy(row, t.data(), t.size() * sizeof(int32_t));
@@ -388,6 +407,127 @@ int64_t pa_bm_take_copies(pa_bm* bm, int64_t* pairs_out, int64_t capacity) {
     ++k;
   }
   return k;
+}
+
+// ---------------------------------------------------------------- swapping
+int pa_bm_enable_swap(pa_bm* bm, int64_t num_cpu_blocks, const int32_t* cpu_free_order) {
+  if (!bm || bm->swap || num_cpu_blocks < 1 || num_cpu_blocks > 0x7fffffff || !cpu_free_order)
+    return PA_ERR_INVALID_ARG;
+  std::vector<char> seen(size_t(num_cpu_blocks), 0);
+  for (int64_t i = 0; i < num_cpu_blocks; ++i) {
+    const int32_t c = cpu_free_order[i];
+    if (c < 0 || c >= num_cpu_blocks || seen[size_t(c)]) return PA_ERR_INVALID_ARG;
+    seen[size_t(c)] = 1;
+  }
+  bm->swap = true;
+  bm->num_cpu_blocks = num_cpu_blocks;
+  bm->cpu_free.assign(cpu_free_order, cpu_free_order + num_cpu_blocks);
+  bm->cpu_ref.assign(size_t(num_cpu_blocks), 0);
+  return PA_OK;
+}
+
+namespace {
+
+// Distinct blocks of the group's tables, first met walking the sequences in order and each
+// table from its first block, with how many of the sequences hold each.
+void group_blocks(pa_bm* bm, const int64_t* seqs, int64_t n, std::vector<int32_t>& order,
+                  std::unordered_map<int32_t, int32_t>& holders) {
+  for (int64_t i = 0; i < n; ++i)
+    for (int32_t b : bm->seqs.find(seqs[i])->second.table)
+      if (holders[b]++ == 0) order.push_back(b);
+}
+
+// Checks shared by both directions: swap on, distinct known sequences, all on the side the
+// move starts from.
+int check_group(pa_bm* bm, const int64_t* seqs, int64_t n, bool want_swapped) {
+  if (!bm || !bm->swap || n < 0 || (n > 0 && !seqs)) return PA_ERR_INVALID_ARG;
+  std::unordered_map<int64_t, char> seen;
+  for (int64_t i = 0; i < n; ++i) {
+    auto it = bm->seqs.find(seqs[i]);
+    if (it == bm->seqs.end()) return PA_ERR_NOT_FOUND;
+    if (it->second.swapped != want_swapped || seen[seqs[i]]++) return PA_ERR_INVALID_ARG;
+  }
+  return PA_OK;
+}
+
+}  // namespace
+
+int pa_bm_swap_out(pa_bm* bm, const int64_t* seqs, int64_t n, int64_t* pairs_out, int64_t capacity,
+                   int64_t* num_pairs_out) {
+  int st = check_group(bm, seqs, n, false);
+  if (st != PA_OK) return st;
+  if (!num_pairs_out) return PA_ERR_INVALID_ARG;
+  std::vector<int32_t> order;
+  std::unordered_map<int32_t, int32_t> holders;
+  group_blocks(bm, seqs, n, order, holders);
+  if (int64_t(order.size()) > capacity || (!order.empty() && !pairs_out)) return PA_ERR_INVALID_ARG;
+  if (int64_t(order.size()) > int64_t(bm->cpu_free.size())) return PA_ERR_NO_BLOCKS;
+  std::unordered_map<int32_t, int32_t> where;
+  int64_t k = 0;
+  for (int32_t g : order) {
+    const int32_t c = bm->cpu_free.front();
+    bm->cpu_free.pop_front();
+    const int32_t h = holders[g];
+    bm->cpu_ref[size_t(c)] = h;
+    bm->ref[size_t(g)] -= h;
+    if (bm->ref[size_t(g)] == 0) bm->push_free(g);
+    where[g] = c;
+    pairs_out[2 * k] = g;
+    pairs_out[2 * k + 1] = c;
+    ++k;
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    pa_bm::Seq& sq = bm->seqs.find(seqs[i])->second;
+    for (int32_t& b : sq.table) b = where[b];
+    sq.swapped = true;
+  }
+  *num_pairs_out = k;
+  return PA_OK;
+}
+
+int pa_bm_swap_in(pa_bm* bm, const int64_t* seqs, int64_t n, int64_t* pairs_out, int64_t capacity,
+                  int64_t* num_pairs_out) {
+  int st = check_group(bm, seqs, n, true);
+  if (st != PA_OK) return st;
+  if (!num_pairs_out) return PA_ERR_INVALID_ARG;
+  std::vector<int32_t> order;
+  std::unordered_map<int32_t, int32_t> holders;
+  group_blocks(bm, seqs, n, order, holders);
+  if (int64_t(order.size()) > capacity || (!order.empty() && !pairs_out)) return PA_ERR_INVALID_ARG;
+  if (int64_t(order.size()) > bm->nfree) return PA_ERR_NO_BLOCKS;
+  std::unordered_map<int32_t, int32_t> where;
+  int64_t k = 0;
+  for (int32_t c : order) {
+    const int32_t g = bm->take_block();
+    const int32_t h = holders[c];
+    bm->ref[size_t(g)] = h;
+    bm->cpu_ref[size_t(c)] -= h;
+    if (bm->cpu_ref[size_t(c)] == 0) bm->cpu_free.push_back(c);
+    where[c] = g;
+    pairs_out[2 * k] = c;
+    pairs_out[2 * k + 1] = g;
+    ++k;
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    pa_bm::Seq& sq = bm->seqs.find(seqs[i])->second;
+    for (int32_t& b : sq.table) b = where[b];
+    sq.swapped = false;
+  }
+  *num_pairs_out = k;
+  return PA_OK;
+}
+
+int pa_bm_is_swapped(const pa_bm* bm, int64_t seq) {
+  if (!bm) return -1;
+  auto it = bm->seqs.find(seq);
+  return it == bm->seqs.end() ? -1 : (it->second.swapped ? 1 : 0);
+}
+
+int64_t pa_bm_num_free_cpu(const pa_bm* bm) { return bm && bm->swap ? int64_t(bm->cpu_free.size()) : -1; }
+
+int pa_bm_cpu_ref_count(const pa_bm* bm, int64_t block) {
+  if (!bm || !bm->swap || block < 0 || block >= bm->num_cpu_blocks) return -1;
+  return bm->cpu_ref[size_t(block)];
 }
 
 }  // extern "C"

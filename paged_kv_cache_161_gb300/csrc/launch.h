@@ -27,6 +27,10 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* bloc
                                int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
                                unsigned int* err, cudaStream_t stream);
 
+cudaError_t launch_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                               const int64_t* block_mapping, int64_t num_pairs, int64_t src_blocks,
+                               int64_t dst_blocks, int64_t block_bytes, unsigned int* err, cudaStream_t stream);
+
 struct AttnArgs {
   void* out;
   const void* q;
