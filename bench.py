@@ -64,7 +64,7 @@ def _args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", choices=["gqa_decode", "mixed", "mha_decode", "shared_prefix", "system_prompt",
-                                           "gqa_decode_fp8"],
+                                           "gqa_decode_fp8", "swap"],
                     default="gqa_decode",
                     help="gqa_decode: the headline line (default); mixed: the chunked-prefill + decode "
                          "batch, timed whole and as its prefill-only and decode-only sub-batches; "
@@ -856,6 +856,75 @@ def run_fp8_decode(a):
     return 0
 
 
+def run_swap(a):
+    """Swap bandwidth: 8192 scattered blocks (16 tokens x 8 KV heads x 128 dims bf16, K and V:
+    512 MiB) moved GPU -> pinned CPU pool and back by pa_swap_blocks (one launch each way),
+    against a contiguous copy of the same bytes over the same link (cudaMemcpyAsync through
+    torch) timed in the same run."""
+    import torch
+
+    import paged_kv_cache_161_gb300 as pa
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    NB, NC, B, H, D, N = 40000, 16384, 16, 8, 128, 8192
+    g = torch.Generator().manual_seed(161008)
+    gk = torch.empty((NB, B, H, D), dtype=torch.bfloat16, device=dev).normal_()
+    gv = torch.empty_like(gk).normal_()
+    ck = torch.empty((NC, B, H, D), dtype=torch.bfloat16).pin_memory()
+    cv = torch.empty_like(ck).pin_memory()
+    src = torch.randperm(NB, generator=g)[:N]
+    dst = torch.randperm(NC, generator=g)[:N]
+    out_map = torch.stack([src, dst], 1).to(dev)
+    in_map = torch.stack([dst, torch.randperm(NB, generator=g)[:N]], 1).to(dev)
+    nbytes = 2 * N * B * H * D * 2
+
+    def timed(fn, steps, warm):
+        for _ in range(warm):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    steps = max(5, a.steps // 60)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    pa.read_device_errors(clear=True)
+    out_ms = timed(lambda: pa.swap_blocks(gk, gv, ck, cv, out_map, stream=stream), steps, a.warmup)
+    in_ms = timed(lambda: pa.swap_blocks(ck, cv, gk, gv, in_map, stream=stream), steps, a.warmup)
+    if pa.read_device_errors(clear=True):
+        raise RuntimeError("device error flags set")
+    flat_d = gk.view(-1)[: nbytes // 2]
+    flat_h = torch.empty(nbytes // 2, dtype=torch.bfloat16).pin_memory()
+    d2h_ms = timed(lambda: flat_h.copy_(flat_d, non_blocking=True), steps, a.warmup)
+    h2d_ms = timed(lambda: flat_d.copy_(flat_h, non_blocking=True), steps, a.warmup)
+    clk = clocks.stop()
+    gbs = lambda ms: nbytes / (ms * 1e-3) / 1e9  # noqa: E731
+    line = {
+        "metric": "swap_blocks: scattered KV blocks between the GPU pool and a pinned CPU pool, GB/s",
+        "value": gbs(out_ms), "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": a.warmup,
+        "ms_per_step": out_ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{N} random blocks of 16 x 8 x 128 bf16 (K and V, {nbytes / 2**20:.0f} MiB) from a "
+                               f"{NB}-block GPU pool to a {NC}-block pinned pool and back"},
+        "swap_out": {"ms": out_ms, "gbs": gbs(out_ms), "frac_of_contiguous_copy": d2h_ms / out_ms},
+        "swap_in": {"ms": in_ms, "gbs": gbs(in_ms), "frac_of_contiguous_copy": h2d_ms / in_ms},
+        "contiguous_copy": {"d2h_ms": d2h_ms, "d2h_gbs": gbs(d2h_ms), "h2d_ms": h2d_ms, "h2d_gbs": gbs(h2d_ms)},
+        "roofline": {"bound": "link", "achieved": gbs(out_ms), "peak": gbs(d2h_ms), "unit": "GB/s",
+                     "frac": d2h_ms / out_ms,
+                     "peak_source": "a contiguous device-to-host copy of the same bytes, same run"},
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main(argv=None):
     a = _args(argv)
     if a.impl == "reference":
@@ -868,6 +937,8 @@ def main(argv=None):
         return run_system_prompt(a)
     if a.workload == "gqa_decode_fp8":
         return run_fp8_decode(a)
+    if a.workload == "swap":
+        return run_swap(a)
     return run_ours(a)
 
 

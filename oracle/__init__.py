@@ -34,4 +34,5 @@ from .block_manager import BlockAllocator, NoFreeBlocks, TooLarge  # noqa: F401
 from .prefix_cache import PrefixCachingAllocator  # noqa: F401
 from .fp8 import dequantize, kv_write_fp8_ref, quantize  # noqa: F401
 from .swap import SwappingAllocator, SwappingPrefixAllocator  # noqa: F401
-from .runner import OracleResult, batch_metadata, run_allocator, run_script, run_workload, step_ranges  # noqa: F401
+from .runner import (OracleResult, batch_metadata, run_allocator, run_script, run_script_swaps,  # noqa: F401
+                     run_workload, step_ranges)

@@ -14,6 +14,7 @@ from .attention import BlockStore, copy_blocks_ref, kv_write_ref, paged_attentio
 from .block_manager import BlockAllocator
 from .fp8 import dequantize, kv_write_fp8_ref
 from .prefix_cache import PrefixCachingAllocator
+from .swap import SwappingAllocator, SwappingPrefixAllocator
 
 
 @dataclass
@@ -34,7 +35,16 @@ class OracleResult:
 def run_script(wl):
     """Block-manager side only, every phase: (allocator, slots per phase, copy pairs per
     phase, appended ranges (seq, start, n) per phase in operation order)."""
-    if wl.prefix_caching:
+    return run_script_swaps(wl)[:4]
+
+
+def run_script_swaps(wl):
+    """``run_script`` plus, per phase, the swaps in operation order: ("out" | "in", pairs)."""
+    if wl.cpu_blocks:
+        cls = SwappingPrefixAllocator if wl.prefix_caching else SwappingAllocator
+        alloc = cls(wl.num_blocks, wl.spec.block_size, wl.free_order)
+        alloc.enable_swap(wl.cpu_blocks, wl.cpu_free_order)
+    elif wl.prefix_caching:
         alloc = PrefixCachingAllocator(wl.num_blocks, wl.spec.block_size, wl.free_order)
     else:
         alloc = BlockAllocator(wl.num_blocks, wl.spec.block_size, wl.free_order)
@@ -45,9 +55,9 @@ def run_script(wl):
             return alloc.append(s, n, tokens=wl.tokens(s, L, n).tolist())
         return alloc.append(s, n)
 
-    slots_per_phase, copies_per_phase, appends_per_phase = [], [], []
+    slots_per_phase, copies_per_phase, appends_per_phase, swaps_per_phase = [], [], [], []
     for ph in wl.phases():
-        slots, apps = [], []
+        slots, apps, swaps = [], [], []
         for op in ph.ops:
             if op[0] == "add":
                 alloc.add_seq(op[1])
@@ -65,12 +75,21 @@ def run_script(wl):
                     hit = 0
                 apps.append((s, hit, n - hit))
                 slots.extend(append(s, n - hit))
+            elif op[0] == "fill":
+                n = alloc.num_free() * wl.spec.block_size
+                apps.append((op[1], 0, n))
+                slots.extend(append(op[1], n))
             elif op[0] == "free":
                 alloc.free_seq(op[1])
+            elif op[0] == "swap_out":
+                swaps.append(("out", alloc.swap_out(list(op[1]))))
+            elif op[0] == "swap_in":
+                swaps.append(("in", alloc.swap_in(list(op[1]))))
         slots_per_phase.append(np.asarray(slots, np.int64))
         copies_per_phase.append(alloc.take_copies())
         appends_per_phase.append(apps)
-    return alloc, slots_per_phase, copies_per_phase, appends_per_phase
+        swaps_per_phase.append(swaps)
+    return alloc, slots_per_phase, copies_per_phase, appends_per_phase, swaps_per_phase
 
 
 def run_allocator(wl):
@@ -124,7 +143,7 @@ def run_workload(wl, eval_seqs=None) -> OracleResult:
     from workloads import relevant_seqs
 
     sp = wl.spec
-    alloc, slots_pp, copies_pp, apps_pp = run_script(wl)
+    alloc, slots_pp, copies_pp, apps_pp, swaps_pp = run_script_swaps(wl)
     store_dtype = np.float32 if sp.dtype == "f32" else np.uint16
     fp8 = wl.kv_cache == "fp8_e4m3"
     cache_dtype = np.uint8 if fp8 else store_dtype  # E4M3 codes, or the inputs' storage type
@@ -137,8 +156,23 @@ def run_workload(wl, eval_seqs=None) -> OracleResult:
         kc = BlockStore(sp.block_size, sp.num_kv_heads, sp.head_dim, cache_dtype)
         vc = BlockStore(sp.block_size, sp.num_kv_heads, sp.head_dim, cache_dtype)
         relevant = relevant_seqs(wl, [batch[i][0] for i in eval_seqs])
-    for slots, copies, apps in zip(slots_pp, copies_pp, apps_pp):
+    ck = cv = None
+    if wl.cpu_blocks:  # the CPU pool (always dense: it is small)
+        cshape = (wl.cpu_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
+        ck, cv = np.zeros(cshape, cache_dtype), np.zeros(cshape, cache_dtype)
+    for slots, copies, apps, swaps in zip(slots_pp, copies_pp, apps_pp, swaps_pp):
         copy_blocks_ref(kc, vc, copies)
+        for direction, pairs in swaps:  # block copies between the pools, in operation order
+            src, dst = ((kc, vc), (ck, cv)) if direction == "out" else ((ck, cv), (kc, vc))
+            for s_blk, d_blk in pairs:
+                for a_src, a_dst in zip(src, dst):
+                    blk = a_src.get(s_blk) if isinstance(a_src, BlockStore) else a_src[s_blk]
+                    if blk is None:
+                        continue
+                    if isinstance(a_dst, BlockStore):
+                        a_dst[d_blk] = np.array(blk)
+                    else:
+                        a_dst[d_blk] = blk
         reqs = [a for a in apps if relevant is None or a[0] in relevant]
         vals = dict(zip(reqs, wl.kv_many(reqs))) if reqs else {}
         t0 = 0

@@ -15,7 +15,7 @@ import numpy as np
 import torch
 
 from . import (BlockManager, attention, attention_fp8, attention_workspace_size, copy_blocks, kv_write,
-               kv_write_fp8, write_attention)
+               kv_write_fp8, swap_blocks, write_attention)
 
 
 def storage_to_torch(a: np.ndarray) -> torch.Tensor:
@@ -60,12 +60,19 @@ class DeviceWorkload:
         self.bm = BlockManager(wl.num_blocks, sp.block_size, wl.free_order)
         if wl.prefix_caching:
             self.bm.enable_prefix_caching()
+        if wl.cpu_blocks:
+            self.bm.enable_swap(wl.cpu_blocks, wl.cpu_free_order)
         self.dtype = torch.float32 if sp.dtype == "f32" else torch.bfloat16
         shape = (wl.num_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
         self.fp8 = wl.kv_cache == "fp8_e4m3"
         cache_dtype = torch.float8_e4m3fn if self.fp8 else self.dtype
         self.k_cache = torch.zeros(shape, dtype=cache_dtype, device=self.device)
         self.v_cache = torch.zeros(shape, dtype=cache_dtype, device=self.device)
+        if wl.cpu_blocks:  # the CPU pool: pinned host memory, read and written by the swap kernel
+            cshape = (wl.cpu_blocks,) + shape[1:]
+            self.k_cpu = torch.zeros(cshape, dtype=cache_dtype).pin_memory()
+            self.v_cpu = torch.zeros(cshape, dtype=cache_dtype).pin_memory()
+        self.phase_swaps: list = []
         self.table_width = table_width
         self.phase_slots: list = []
         self.phase_copies: list = []
@@ -79,7 +86,7 @@ class DeviceWorkload:
     def _ops(self, phase):
         """Run a phase's operations on the C++ block manager: (slots, copy pairs, appended
         ranges (seq, start, n) in operation order)."""
-        slots, apps = [], []
+        slots, apps, swaps = [], [], []
         for op in phase.ops:
             if op[0] == "add":
                 self.bm.add_seq(op[1])
@@ -97,13 +104,33 @@ class DeviceWorkload:
                     hit = 0
                 apps.append((s, hit, n - hit))
                 slots.append(self._append(s, n - hit))
+            elif op[0] == "fill":
+                n = self.bm.num_free() * self.wl.spec.block_size
+                apps.append((op[1], 0, n))
+                slots.append(self._append(op[1], n))
             elif op[0] == "free":
                 self.bm.free_seq(op[1])
+            elif op[0] == "swap_out":
+                swaps.append(("out", self.bm.swap_out(list(op[1]))))
+            elif op[0] == "swap_in":
+                swaps.append(("in", self.bm.swap_in(list(op[1]))))
         slots = np.concatenate(slots) if slots else np.zeros(0, np.int64)
         copies = self.bm.take_copies()
         self.phase_slots.append(slots)
         self.phase_copies.append(copies)
+        self.phase_swaps.append(swaps)
+        self._pending_swaps = swaps
         return slots, copies, apps
+
+    def _apply_swaps(self, swaps, stream=None):
+        for direction, pairs in swaps:
+            if not len(pairs):
+                continue
+            m = torch.from_numpy(np.ascontiguousarray(pairs)).to(self.device)
+            if direction == "out":
+                swap_blocks(self.k_cache, self.v_cache, self.k_cpu, self.v_cpu, m, stream=stream)
+            else:
+                swap_blocks(self.k_cpu, self.v_cpu, self.k_cache, self.v_cache, m, stream=stream)
 
     def _values(self, apps):
         if not apps:
@@ -123,6 +150,7 @@ class DeviceWorkload:
             k, v = self._values(apps)
             if len(copies):
                 copy_blocks(self.k_cache, self.v_cache, torch.from_numpy(copies).to(self.device))
+            self._apply_swaps(self._pending_swaps)
             if len(slots):
                 self._write(k.to(self.device), v.to(self.device), torch.from_numpy(slots).to(self.device))
 
@@ -131,6 +159,7 @@ class DeviceWorkload:
         wl = self.wl
         sp = wl.spec
         slots, copies, apps = self._ops(wl.step)
+        self._apply_swaps(self._pending_swaps)  # (a step script normally has none)
         self.step_appends = apps
         k, v = self._values(apps)
         batch = wl.step.batch or []

@@ -170,3 +170,29 @@ def test_fp8_workloads_read_back_and_match_dense(cfg):
             want = dense_causal_ref(res.q[a:b], dequantize(got_k, wl.k_scale), dequantize(got_v, wl.v_scale),
                                     wl.spec.scale)
             assert np.max(np.abs(res.out[a:b] - want)) < 1e-12
+
+
+def test_preemption_workload_reads_back_after_swapping():
+    """The swapped-out group comes back (in other GPU blocks, after a long request
+    overwrote its old ones) reading exactly its own streams; attention matches brute force."""
+    from oracle import run_script_swaps
+
+    wl = workloads.preemption("small")
+    alloc, _, _, _, swaps = run_script_swaps(wl)
+    out_pairs = [p for ph in swaps for d, pairs in ph if d == "out" for p in pairs]
+    in_pairs = [p for ph in swaps for d, pairs in ph if d == "in" for p in pairs]
+    assert len(out_pairs) == len(in_pairs) > 0
+    res = run_workload(wl)
+    B = wl.spec.block_size
+    old_gpu = {g for g, _ in out_pairs}
+    new_gpu = {g for _, g in in_pairs}
+    assert old_gpu != new_gpu  # the group came back into other blocks
+    for i, s in enumerate(res.batch_seqs):
+        L = int(res.seq_lens[i])
+        ks, vs = _streams(wl, s)
+        table = res.block_table[i]
+        got_k = np.stack([res.k_cache[table[p // B]][p % B] for p in range(L)])
+        assert np.array_equal(got_k, ks)
+        a, b = res.query_start_loc[i], res.query_start_loc[i + 1]
+        want = dense_causal_ref(res.q[a:b], ks, vs, wl.spec.scale)
+        assert np.max(np.abs(res.out[a:b] - want)) < 1e-12

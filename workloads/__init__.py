@@ -20,6 +20,7 @@ from .configs import (  # noqa: F401
     build,
     custom,
     relevant_seqs,
+    preemption,
     system_prompt,
     with_fp8_cache,
 )

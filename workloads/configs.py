@@ -11,6 +11,13 @@ operations followed, optionally, by one attention batch:
                           prefix caching, start from whatever prefix the block manager
                           can reuse, then append the rest; without, append all n
     ('free', s)           the request s ends
+    ('fill', s)           append to the empty sequence s as many tokens as the free
+                          blocks hold (num_free * block_size, from the block manager)
+    ('swap_out', seqs)    preempt the group ``seqs`` (a tuple): its blocks go to the CPU
+    ('swap_in', seqs)     bring the group back to the GPU
+
+Swap operations sit in phases without appends; their block copies run after the
+phase's copy-on-write copies, in operation order.
 
 A batch entry (s, None) means "the tokens appended to s in this phase" (the count a
 'prompt' op leaves depends on what the block manager reused). Workloads with
@@ -80,6 +87,8 @@ class Workload:
     token_ids: dict = field(default_factory=dict)  # seq -> int32 array (its token stream)
     shared_kv: dict = field(default_factory=dict)  # seq -> (owner, n)
     q_whole: dict = field(default_factory=dict)  # seq -> length of its one query draw
+    cpu_blocks: int = 0  # CPU block pool for swapping (0: none)
+    cpu_free_order: np.ndarray | None = None
     kv_cache: str = ""  # cache element type: "" (the spec's dtype) or "fp8_e4m3"
     k_scale: float = 1.0  # fp8_e4m3: a K code c stands for value(c) * k_scale
     v_scale: float = 1.0
@@ -321,6 +330,49 @@ def with_fp8_cache(wl: Workload, k_scale: float = 2.0 ** -6, v_scale: float = 2.
 
     return dataclasses.replace(wl, name=wl.name + "_fp8", kv_cache="fp8_e4m3", k_scale=float(k_scale),
                                v_scale=float(v_scale))
+
+
+def preemption(size: str = "full") -> Workload:
+    """Preemption by swapping (the code-reading page's SequenceGroup lifecycle): groups of 4
+    samples forked from one prompt (tails written with copy-on-write); group 0 is swapped
+    out to the CPU; a long request then takes every free GPU block (overwriting group 0's
+    old blocks) and ends; group 0 is swapped back in; the step decodes every sample (one
+    new token each). Full: 16 groups, 1000-token prompts, tails U[0, 256]. Small: 3 groups,
+    40-token prompts, tails U[0, 20]."""
+    seed = SEED_BASE + 7 + (100 if size == "small" else 0)
+    spec = Spec("bf16", **GQA)
+    rng = _rng(seed)
+    if size == "small":
+        P, prompt_len, n_samp, tail_hi = 3, 40, 4, 20
+    else:
+        P, prompt_len, n_samp, tail_hi = 16, 1000, 4, 256
+    B = spec.block_size
+    tails = rng.integers(0, tail_hi, size=(P, n_samp), endpoint=True)
+    seq = lambda p, i: p * n_samp + i  # noqa: E731
+    S = P * n_samp
+    hog = S
+    prompt = Phase(ops=[op for p in range(P) for op in (("add", seq(p, 0)), ("append", seq(p, 0), prompt_len))])
+    fork = Phase(ops=[("fork", seq(p, 0), seq(p, i)) for p in range(P) for i in range(1, n_samp)])
+    tail = Phase(ops=[("append", seq(p, i), int(tails[p, i])) for p in range(P) for i in range(n_samp)
+                      if tails[p, i] > 0])
+    group0 = tuple(seq(0, i) for i in range(n_samp))
+    shared_full = prompt_len // B
+    # pool: 1.25x an upper bound of the blocks all samples hold after the step
+    per_group = [shared_full + sum(-(-(prompt_len + int(t) + 1) // B) - shared_full + 1 for t in tails[p])
+                 for p in range(P)]
+    pool = _pool(sum(per_group))
+    swap_out = Phase(ops=[("swap_out", group0)])
+    hog_phase = Phase(ops=[("add", hog), ("fill", hog)])  # overwrites group 0's old blocks
+    back = Phase(ops=[("free", hog)])
+    swap_in = Phase(ops=[("swap_in", group0)])
+    step = Phase(ops=[("append", s, 1) for s in range(S)], batch=[(s, 1) for s in range(S)])
+    cpu_blocks = int(math.ceil(1.5 * per_group[0]))
+    final = [prompt_len + int(tails[p, i]) + 1 for p in range(P) for i in range(n_samp)]
+    return Workload("preemption_swap_bf16" + ("_small" if size == "small" else ""), spec, seed, pool,
+                    rng.permutation(pool).astype(np.int32), [prompt, fork, tail, swap_out, hog_phase, back, swap_in],
+                    step, S, dict(groups=P, prompt_len=prompt_len, samples=n_samp, tails=tails, final_lens=final,
+                                  swapped_group=list(group0)),
+                    cpu_blocks=cpu_blocks, cpu_free_order=rng.permutation(cpu_blocks).astype(np.int32))
 
 
 def system_prompt(size: str = "full", caching: bool = True) -> Workload:
