@@ -242,7 +242,10 @@ int pa_attention_fp8(void* out, const void* q, const void* k_cache, const void* 
  * cudaHostRegister'ed, used through its unified address): the kernel moves the blocks
  * over the CPU-GPU link itself, one launch per call. block_mapping: int64 [num_pairs, 2],
  * device or pinned host memory. No dst may repeat. Out-of-range ids are skipped and set
- * PA_DEVERR_BLOCK_RANGE. The pairs come from pa_bm_swap_out / pa_bm_swap_in.
+ * PA_DEVERR_BLOCK_RANGE. The pairs come from pa_bm_swap_out / pa_bm_swap_in. Every
+ * pointer is checked with cudaPointerGetAttributes before the launch: another device's
+ * memory, pageable host memory or host memory not mapped at its own address gives
+ * PA_ERR_INVALID_ARG.
  * --------------------------------------------------------------------------- */
 int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
                    const int64_t* block_mapping, int64_t num_pairs, int64_t src_num_blocks,

@@ -313,6 +313,31 @@ int pa_attention_fp8(void* out, const void* q, const void* k_cache, const void* 
   return run_attention(a, ctas, reinterpret_cast<cudaStream_t>(stream));
 }
 
+}  // extern "C"
+
+namespace {
+
+// A pool pointer the kernels may dereference: device memory of the current device, managed
+// memory, or pinned host memory mapped at the same address (unified addressing).
+int check_kernel_visible(const void* p, int dev) {
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // reset the error state the failed query set
+    return PA_ERR_INVALID_ARG;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice: return at.device == dev ? PA_OK : PA_ERR_INVALID_ARG;
+    case cudaMemoryTypeManaged: return PA_OK;
+    case cudaMemoryTypeHost: return at.devicePointer == p ? PA_OK : PA_ERR_INVALID_ARG;
+    default: return PA_ERR_INVALID_ARG;  // pageable host memory
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
 int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v, const int64_t* block_mapping,
                    int64_t num_pairs, int64_t src_num_blocks, int64_t dst_num_blocks, int block_size,
                    int num_kv_heads, int head_dim, pa_dtype dtype, pa_stream_t stream) {
@@ -327,7 +352,14 @@ int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_
   if (num_pairs < 0 || num_pairs > 0x7fffffff) return PA_ERR_INVALID_ARG;
   if (num_pairs == 0) return PA_OK;
   if (!block_mapping || reinterpret_cast<uintptr_t>(block_mapping) % 8 != 0) return PA_ERR_INVALID_ARG;
-  cudaError_t e;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  for (const void* p : {src_k, src_v, static_cast<const void*>(dst_k), static_cast<const void*>(dst_v),
+                        static_cast<const void*>(block_mapping)}) {
+    const int st = check_kernel_visible(p, dev);
+    if (st != PA_OK) return st;
+  }
   unsigned int* err = pa::device_error_word(&e);
   if (!err) return cuda_fail(e);
   e = pa::launch_swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping, num_pairs, src_num_blocks, dst_num_blocks,

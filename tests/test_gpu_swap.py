@@ -101,3 +101,19 @@ def test_preemption_full_swapped_group_sampled(pa):
         table = ref.block_table[i]
         for pos in range(0, int(ref.seq_lens[i]), 5):
             assert np.array_equal(kc[table[pos // B], pos % B], ref.k_cache[table[pos // B]][pos % B])
+
+
+def test_swap_rejects_pageable_host_memory_before_launch(pa):
+    """A pool in ordinary (pageable) host memory is refused by the library's pointer check,
+    so no kernel ever dereferences it."""
+    NB, B, H, D = 4, 16, 8, 128
+    gk = torch.zeros((NB, B, H, D), dtype=torch.bfloat16, device="cuda")
+    gv = torch.zeros_like(gk)
+    host = np.zeros((NB, B, H, D), np.uint16)  # pageable
+    pairs = torch.tensor([[0, 1]], dtype=torch.int64, device="cuda")
+    st = pa.lib.pa_swap_blocks(gk.data_ptr(), gv.data_ptr(), host.ctypes.data, host.ctypes.data,
+                               pairs.data_ptr(), 1, NB, NB, B, H, D, pa.PA_BF16, None)
+    assert st == 1
+    with pytest.raises(ValueError):
+        pa.swap_blocks(gk, gv, torch.zeros((NB, B, H, D), dtype=torch.bfloat16),
+                       torch.zeros((NB, B, H, D), dtype=torch.bfloat16), pairs)
