@@ -25,7 +25,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libpa_gb300.so")
 
-CU_SOURCES = ["errors.cu", "kv_write.cu", "copy_blocks.cu", "decode_attention.cu", "prefill_attention.cu",
+CU_SOURCES = ["errors.cu", "kv_write.cu", "copy_blocks.cu", "decode_attention.cu", "decode_mma.cu", "prefill_attention.cu",
               "attention_fixed_scratch.cu", "prefill_tcgen05.cu"]
 CPP_SOURCES = ["api.cpp", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,0 +1,620 @@
+// Paged decode attention (requests with q_len == 1) with the dot products on the tensor
+// cores: split-K over the balanced partition of all K/V pages (decode_common.cuh), then
+// the log-sum-exp merge of the pieces.
+//
+// What it computes: the same as decode_attention.cu (vLLM 0.10.0 flow page, 3.5 Attention;
+// "vLLM" docs page, PagedAttention; code-reading page 5.1.1), for bf16 queries over bf16
+// or FP8 (E4M3) caches ("vLLM" docs page, quantisation support).
+//
+// Why: a decode step is a stream of K/V bytes, but with 16 tokens x 8 KV heads per stage
+// the CUDA-core consumers need as long per stage as the stage takes to arrive, and an
+// E4M3 cache halves the bytes without halving that work. Here each consumer warp does a
+// stage as 16-row matrix products on mma.sync (m16n8k16, fp32 accumulate): rows are the
+// G query heads of its KV head, so S = Q K^T (16 tokens) is 16 MMAs for D = 128 and
+// O += P V another 16, against ~500 FMA-pipe instructions on CUDA cores. (tcgen05 needs
+// M >= 64 rows and a TMEM round trip per stage; with at most 8 query heads per KV head
+// the register-file MMA has the shorter dependency chain.)
+//
+// Layout: the producer warp loads each stage with 3-D TMA tensor copies over the cache
+// viewed as (dim, token, KV head): a box of {128 bytes of dims, BT tokens, HG heads} lands
+// as [head][token][128 B] with the 128-byte swizzle, so the rows a warp reads for one
+// head at one 16-byte column sit in 8 different bank groups (conflict-free ldmatrix /
+// loads). The cache is read exactly once per stage.
+//
+// Precision: bf16 caches multiply in bf16 (Q and K exact), P rounded to bf16 for P V;
+// E4M3 caches multiply in f16 (E4M3 codes and bf16 queries of normal range are exact in
+// f16; P rounded to f16). Accumulation and softmax in fp32 (exp2 domain).
+#include <cudaTypedefs.h>
+
+#include "decode_common.cuh"
+#include "tcgen05.cuh"
+
+namespace pa {
+namespace {
+
+// ---------------------------------------------------------------- tensor-core wrappers
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1,
+                                          bool f16) {
+  // rows 8..15 of A are zero (at most 8 query heads per KV head): a1 = a3 = 0
+  if (f16)
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+  else
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 16-bit matrices, transposed: thread l gets (row 2(l%4), col l/4) and
+// (row 2(l%4)+1, col l/4) of each; lanes 8m..8m+7 give matrix m's row addresses.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
+// two fp32 -> packed bf16x2 / f16x2 (lo in the low half), round to nearest even
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// two E4M3 codes (low 16 bits, low byte first) -> f16x2, exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h2) : "r"(codes));
+  return h2;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// ---------------------------------------------------------------- layout
+// KV: __nv_bfloat16 or Fp8E4M3; BT: tokens per TMA box (8 or 16; 16 / BT boxes a stage).
+template <typename KV, int D, int BT>
+struct MmaCfg {
+  static constexpr int EL = sizeof(KV);
+  static constexpr bool kF16 = EL == 1;           // E4M3 caches multiply in f16
+  static constexpr int INNER = 128 / EL;          // elements of one swizzled 128-byte row
+  static constexpr int HALVES = D / INNER;        // boxes along the head dimension
+  static_assert(HALVES >= 1 && D % INNER == 0, "head_dim must fill 128-byte rows");
+  static constexpr int NBOX = kTPS / BT;          // boxes along the tokens of a stage
+  static constexpr int STAGES = EL == 1 ? 6 : 3;  // 192 KiB in flight at HG = 8, D = 128
+  static constexpr int KC = D / 16;               // 16-dim chunks (MMA k steps of S)
+  static constexpr int NT = D / 8;                // 8-dim tiles of O (MMA n tiles of P V)
+  // bytes
+  static __host__ __device__ uint32_t box_bytes(int hg) { return uint32_t(hg) * BT * 128; }
+  static __host__ __device__ uint32_t half_bytes(int hg) { return NBOX * box_bytes(hg); }
+  static __host__ __device__ uint32_t stage_bytes(int hg) { return HALVES * half_bytes(hg); }  // K (or V)
+  static __host__ __device__ uint32_t k_off(int hg, int st) { return uint32_t(st) * 2 * stage_bytes(hg); }
+  static __host__ __device__ uint32_t v_off(int hg, int st) { return k_off(hg, st) + stage_bytes(hg); }
+  static __host__ __device__ uint32_t desc_off(int hg) { return STAGES * 2 * stage_bytes(hg); }
+  static __host__ __device__ uint32_t bar_off(int hg) { return desc_off(hg) + STAGES * sizeof(StageDesc); }
+  static __host__ __device__ uint32_t red_off(int hg) { return bar_off(hg) + 2 * STAGES * 8; }
+  static __host__ __device__ uint32_t total(int hg) { return red_off(hg) + 40 * 4 + 1024; }  // + alignment
+  // Byte offset, inside a stage's K (or V), of 16-byte column `chunk` (of the 128-byte
+  // row of dims [half * INNER, half * INNER + INNER)) of token `tok` of head `h`.
+  static __device__ __forceinline__ uint32_t at(int hg, int half, int tok, int h, int chunk) {
+    const int row = h * BT + (tok % BT);  // row inside its box; box bases are 1024-aligned
+    return uint32_t(half) * half_bytes(hg) + uint32_t(tok / BT) * box_bytes(hg) + uint32_t(row) * 128 +
+           uint32_t((chunk ^ (row & 7)) * 16);
+  }
+};
+
+// ---------------------------------------------------------------- the kernel
+template <typename T, int D, typename KV, int BT>
+__global__ void __launch_bounds__(9 * 32, 1)
+    decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap) {
+  using C = MmaCfg<KV, D, BT>;
+  constexpr int STAGES = C::STAGES;
+  const int HG = p.hg_size, G = p.group;
+  const int S = p.num_seqs;
+
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1024-byte alignment
+  unsigned char* smem = smem_raw + (base - raw);
+  StageDesc* desc = reinterpret_cast<StageDesc*>(smem + C::desc_off(HG));
+  int* red = reinterpret_cast<int*>(smem + C::red_off(HG));
+  const uint32_t full0 = base + C::bar_off(HG), empty0 = full0 + 8 * STAGES;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_consumers = HG;  // one warp per KV head of the group
+
+  griddep_wait();
+  griddep_launch_dependents();
+
+  Plan pl;
+  if (!plan_range<T, D>(p, red, pl)) return;
+  const int64_t u_begin = pl.u_begin, u_end = pl.u_end, c = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, num_consumers);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int B = p.block_size;
+
+  if (warp == num_consumers) {
+    // =========================== producer warp ===========================
+    if (lane == 0) {
+      tc::prefetch_tensormap(&kmap);
+      tc::prefetch_tensormap(&vmap);
+    }
+    int s = pl.start_s, j = pl.start_j, hg = pl.start_hg;
+    int L = decode_len(p, s);
+    int units_s = units_of(L);
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int64_t u = u_begin; u < u_end; ++u) {
+      const int64_t u0 = u - j, u1 = u0 + units_s;
+      int flags = 0;
+      if (u == u_begin || j == 0) flags |= kFirst;
+      if (u == u_end - 1 || j == units_s - 1) flags |= kLast;
+      if (u0 >= u_begin) flags |= kSeqStart;
+      if (u1 <= u_end) flags |= kSeqEnd;
+      const int valid = min(kTPS, L - j * kTPS);
+      const int pos0 = j * kTPS;
+      const int32_t* bt = p.block_table + int64_t(s) * p.max_blocks_per_seq;
+      // Fused KV write (decode-only batches, 16-bit caches): at a request's last unit the
+      // consumers patch the new token's row (position L - 1) into the stage and store it to
+      // its slot; a slot that is not that position's is written here and flagged.
+      int64_t wslot = -1;
+      if (p.k_new && j == units_s - 1) {
+        const int qrow = __ldg(p.qsl + s);
+        const int64_t slot = __ldg(p.slot_mapping + qrow);
+        const int64_t at = int64_t(__ldg(bt + (L - 1) / B)) * B + (L - 1) % B;
+        const int64_t row_bytes = int64_t(p.num_kv_heads) * D * C::EL;
+        if (slot >= 0 && slot == at && slot < p.num_blocks * B) {
+          wslot = slot;
+        } else if (slot >= 0) {
+          if (lane == 0 && slot != at) raise_error(p.err, PA_DEVERR_SLOT_MISMATCH);
+          if (slot < p.num_blocks * B) {
+            const int64_t slice = int64_t(HG) * D * C::EL;
+            const int64_t src_off = int64_t(qrow) * row_bytes + hg * slice;
+            const int64_t dst_off = slot * row_bytes + hg * slice;
+            for (int64_t o = int64_t(lane) * 16; o < slice; o += 32 * 16) {
+              const uint4 kx = __ldg(reinterpret_cast<const uint4*>(p.k_new + src_off + o));
+              const uint4 vx = __ldg(reinterpret_cast<const uint4*>(p.v_new + src_off + o));
+              *reinterpret_cast<uint4*>(p.k_cache_w + dst_off + o) = kx;
+              *reinterpret_cast<uint4*>(p.v_cache_w + dst_off + o) = vx;
+            }
+          } else if (lane == 0) {
+            raise_error(p.err, PA_DEVERR_SLOT_RANGE);
+          }
+        }
+      }
+      // lane b < NBOX: the box of tokens [pos0 + b * BT, pos0 + b * BT + BT) (one block)
+      bool have = false, bad = false;
+      int y = 0;
+      if (lane < C::NBOX && lane * BT < valid) {
+        const int pos = pos0 + lane * BT;
+        const int64_t blk = __ldg(bt + pos / B);
+        bad = blk < 0 || blk >= p.num_blocks;
+        have = !bad;
+        y = int(blk * B + pos % B);
+      }
+      const int nhave = __popc(__ballot_sync(0xffffffffu, have));
+      const bool any_bad = __any_sync(0xffffffffu, bad);
+      if (any_bad) flags |= kBad;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(empty0 + 8 * stage, phase ^ 1) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        raise_error(p.err, PA_DEVERR_TIMEOUT);
+        break;
+      }
+      if (lane == 0) {
+        if (any_bad) raise_error(p.err, PA_DEVERR_BLOCK_RANGE);
+        StageDesc d;
+        d.s = s;
+        d.hg = hg;
+        d.j = j;
+        d.valid = valid;
+        d.flags = flags;
+        d.pad = 0;
+        d.wslot = wslot;
+        desc[stage] = d;
+        mbar_arrive_expect_tx(full0 + 8 * stage, uint32_t(nhave) * C::HALVES * 2 * C::box_bytes(HG));
+      }
+      __syncwarp();
+      if (have) {
+        const uint32_t kd = base + C::k_off(HG, stage) + uint32_t(lane) * C::box_bytes(HG);
+        const uint32_t vd = base + C::v_off(HG, stage) + uint32_t(lane) * C::box_bytes(HG);
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h) {
+          tc::tma_load_3d(kd + h * C::half_bytes(HG), &kmap, h * C::INNER, y, hg * HG, full0 + 8 * stage);
+          tc::tma_load_3d(vd + h * C::half_bytes(HG), &vmap, h * C::INNER, y, hg * HG, full0 + 8 * stage);
+        }
+      }
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1;
+      }
+      if (++j == units_s && u + 1 < u_end) {
+        j = 0;
+        if (++hg == p.num_hg) {
+          hg = 0;
+          do {
+            if (++s >= S) break;  // cannot happen: the plan counted these units
+            L = decode_len(p, s);
+            units_s = units_of(L);
+          } while (units_s == 0);
+          if (s >= S) {
+            raise_error(p.err, PA_DEVERR_TIMEOUT);
+            break;
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // =========================== consumer warps ===========================
+  // warp hk = KV head within the group; MMA rows = its G query heads. Lane (g, t):
+  // g = lane / 4 is an MMA row / token / dim index, t = lane % 4 a column pair.
+  const int hk = warp;
+  const int g = lane >> 2, t = lane & 3;
+  const int Hq = p.num_heads;
+  // Dims are permuted inside each 16-dim chunk so a lane reads 4 consecutive elements:
+  // MMA k = 2t + e <-> dim 4t + e, k = 2t + 8 + e <-> dim 4t + 2 + e (Q uses the same map).
+  uint32_t qa0[C::KC], qa2[C::KC];
+  uint4 knew = make_uint4(0u, 0u, 0u, 0u), vnew = knew;  // fused write: this lane's 16 bytes of the new row
+  constexpr int kRowChunks = D * C::EL / 16;               // 16-byte pieces of one head's row
+  float o[C::NT][4];
+  float mrun = -INFINITY, lpart = 0.f;
+  const float cscale = p.scale_log2;
+  const float v_scale = p.v_scale;
+
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int64_t u = u_begin; u < u_end; ++u) {
+    if (!mbar_wait(full0 + 8 * stage, phase)) {
+      raise_error(p.err, PA_DEVERR_TIMEOUT);
+      return;
+    }
+    const StageDesc d = desc[stage];
+    const int qrow = __ldg(p.qsl + d.s);
+    if (d.flags & kFirst) {
+      const int qh = (d.hg * HG + hk) * G + g;  // this lane's query head (row g)
+#pragma unroll
+      for (int kc = 0; kc < C::KC; ++kc) {
+        uint2 w = make_uint2(0u, 0u);
+        if (g < G) w = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const T*>(p.q) +
+                                                             (int64_t(qrow) * Hq + qh) * D + 16 * kc + 4 * t));
+        if constexpr (C::kF16) {  // bf16 -> f16 (exact in f16's normal range)
+          qa0[kc] = pack_f16(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+          qa2[kc] = pack_f16(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+        } else {
+          qa0[kc] = w.x;
+          qa2[kc] = w.y;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < C::NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      mrun = -INFINITY;
+      lpart = 0.f;
+      if constexpr (!C::kF16) {
+        if (p.k_new && (d.flags & kSeqEnd) && lane < kRowChunks) {  // this CTA ends the request
+          const int64_t off = (int64_t(qrow) * p.num_kv_heads + d.hg * HG + hk) * D * C::EL + lane * 16;
+          knew = __ldg(reinterpret_cast<const uint4*>(p.k_new + off));
+          vnew = __ldg(reinterpret_cast<const uint4*>(p.v_new + off));
+        }
+      }
+    }
+    const int valid = (d.flags & kBad) ? 0 : d.valid;
+    const uint32_t kb = base + C::k_off(HG, stage), vb = base + C::v_off(HG, stage);
+    if constexpr (!C::kF16) {
+      if (d.wslot >= 0) {  // fused write: the new row into the stage (row valid - 1) and its slot
+        if (lane < kRowChunks) {
+          const int half = (lane * 16) / 128, ch = ((lane * 16) % 128) / 16;
+          const uint32_t so = C::at(HG, half, d.valid - 1, hk, ch);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(kb + so), "r"(knew.x), "r"(knew.y),
+                       "r"(knew.z), "r"(knew.w)
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(vb + so), "r"(vnew.x), "r"(vnew.y),
+                       "r"(vnew.z), "r"(vnew.w)
+                       : "memory");
+          const int64_t go = d.wslot * (int64_t(p.num_kv_heads) * D * C::EL) + int64_t(d.hg * HG + hk) * D * C::EL +
+                             lane * 16;
+          *reinterpret_cast<uint4*>(p.k_cache_w + go) = knew;
+          *reinterpret_cast<uint4*>(p.v_cache_w + go) = vnew;
+        }
+        __syncwarp();
+      }
+    }
+
+    // ---- S = Q K^T: n tile j = tokens 8j .. 8j + 7, this lane's B column = token 8j + g
+    float sacc[2][4];
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) sacc[jj][0] = sacc[jj][1] = sacc[jj][2] = sacc[jj][3] = 0.f;
+#pragma unroll
+    for (int kc = 0; kc < C::KC; ++kc) {
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int tok = 8 * jj + g;
+        uint32_t b0, b1;
+        if constexpr (C::kF16) {  // 4 codes: dims 16kc + 4t .. + 3 (one 128-byte row per head)
+          const uint32_t w = lds32(kb + C::at(HG, 0, tok, hk, kc) + 4 * t);
+          b0 = e4m3x2_to_f16x2(w & 0xffffu);
+          b1 = e4m3x2_to_f16x2(w >> 16);
+        } else {  // 4 bf16: dims 16kc + 4t .. + 3 (64 dims per 128-byte row)
+          const int dim = 16 * kc + 4 * t;
+          const uint2 w =
+              lds64(kb + C::at(HG, dim / C::INNER, tok, hk, (dim % C::INNER) * 2 / 16) + ((dim % C::INNER) * 2) % 16);
+          b0 = w.x;
+          b1 = w.y;
+        }
+        mma_16816(sacc[jj], qa0[kc], qa2[kc], b0, b1, C::kF16);
+      }
+    }
+
+    // ---- online softmax over the stage's 16 tokens, row g (lanes of a quad share it)
+    float x[2][2];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tok = 8 * jj + 2 * t + e;
+        x[jj][e] = (tok < valid) ? sacc[jj][e] * cscale : -INFINITY;
+        mx = fmaxf(mx, x[jj][e]);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mnew = fmaxf(mrun, mx);
+    const float ms = (mnew == -INFINITY) ? 0.f : mnew;
+    const float alpha = exp2f(mrun - ms);
+    float pv[2][2];
+    float psum = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        pv[jj][e] = exp2f(x[jj][e] - ms);
+        psum += pv[jj][e];
+      }
+    lpart = lpart * alpha + psum;
+    mrun = mnew;
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+      for (int i = 0; i < C::NT; ++i) {
+        o[i][0] *= alpha;
+        o[i][1] *= alpha;
+      }
+    }
+    // P as the A operand of P V: row g, k = tokens 2t, 2t+1 (a0) and 8 + 2t, 9 + 2t (a2)
+    uint32_t pa0, pa2;
+    if constexpr (C::kF16) {
+      pa0 = pack_f16(pv[0][0], pv[0][1]);
+      pa2 = pack_f16(pv[1][0], pv[1][1]);
+    } else {
+      pa0 = pack_bf16(pv[0][0], pv[0][1]);
+      pa2 = pack_bf16(pv[1][0], pv[1][1]);
+    }
+
+    // ---- O += P V. Rows of V past `valid` hold stale or unwritten data: zero them in
+    // the B fragments (P is 0 there, but 0 * NaN would not be).
+    const bool partial = valid < kTPS;
+    if constexpr (C::kF16) {
+      // 4 tiles per 32 dims: tile i, column g <-> dim 32m + 4g + i; this lane reads 4 codes
+      // (dims 32m + 4g .. + 3) of tokens 2t, 2t+1, 8+2t, 9+2t and pairs them across tokens.
+#pragma unroll
+      for (int m = 0; m < D / 32; ++m) {
+        const int chunk = 2 * m + (g >> 2), off = 4 * (g & 3);
+        uint32_t w0 = lds32(vb + C::at(HG, 0, 2 * t, hk, chunk) + off);
+        uint32_t w1 = lds32(vb + C::at(HG, 0, 2 * t + 1, hk, chunk) + off);
+        uint32_t w2 = lds32(vb + C::at(HG, 0, 8 + 2 * t, hk, chunk) + off);
+        uint32_t w3 = lds32(vb + C::at(HG, 0, 9 + 2 * t, hk, chunk) + off);
+        if (partial) {
+          if (2 * t >= valid) w0 = 0u;
+          if (2 * t + 1 >= valid) w1 = 0u;
+          if (8 + 2 * t >= valid) w2 = 0u;
+          if (9 + 2 * t >= valid) w3 = 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t sel = uint32_t(i) | (uint32_t(4 + i) << 4);  // byte i of a, byte i of b
+          const uint32_t b0 = e4m3x2_to_f16x2(prmt(w0, w1, sel));
+          const uint32_t b1 = e4m3x2_to_f16x2(prmt(w2, w3, sel));
+          mma_16816(o[4 * m + i], pa0, pa2, b0, b1, true);
+        }
+      }
+    } else {
+      // ldmatrix.trans: matrices (tokens 0-7 | 8-15) x (dims 8i | 8i + 8) -> b0, b1 of
+      // tiles i and i + 1; lane l addresses row l % 8 of matrix l / 8
+      const int mi = lane >> 3, rr = lane & 7;
+      const int tok = (mi & 1) * 8 + rr;
+      uint32_t lo_mask = 0xffffffffu, hi_mask = 0xffffffffu;  // tokens 2t, 2t+1 | 8+2t, 9+2t
+      if (partial) {
+        lo_mask = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
+        hi_mask = (8 + 2 * t < valid ? 0x0000ffffu : 0u) | (9 + 2 * t < valid ? 0xffff0000u : 0u);
+      }
+#pragma unroll
+      for (int i2 = 0; i2 < C::NT / 2; ++i2) {
+        const int dim = 16 * i2 + (mi >> 1) * 8;
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_trans(vb + C::at(HG, dim / C::INNER, tok, hk, (dim % C::INNER) / 8), r0, r1, r2, r3);
+        mma_16816(o[2 * i2], pa0, pa2, r0 & lo_mask, r1 & hi_mask, false);
+        mma_16816(o[2 * i2 + 1], pa0, pa2, r2 & lo_mask, r3 & hi_mask, false);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+    if (++stage == STAGES) {
+      stage = 0;
+      phase ^= 1;
+    }
+
+    if (!(d.flags & kLast)) continue;
+
+    // ================= finalize this request's piece =================
+    float l = lpart;
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (g < G) {  // rows past the group's query heads are padding
+    const bool whole = (d.flags & kSeqStart) && (d.flags & kSeqEnd);
+    const int head_in_group = hk * G + g;
+    const int hq = d.hg * HG * G + head_in_group;
+    const float inv = l > 0.f ? v_scale / l : 0.f;
+    const int64_t slot = c + int64_t(d.s) * p.num_hg + d.hg;
+    const int64_t hrow = slot * (int64_t(HG) * G) + head_in_group;
+    if constexpr (C::kF16) {  // lane holds dims 32m + 8t .. + 7 (c0 of tiles 4m..4m+3, then c1)
+#pragma unroll
+      for (int m = 0; m < D / 32; ++m) {
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          f[i] = o[4 * m + i][0] * inv;
+          f[4 + i] = o[4 * m + i][1] * inv;
+        }
+        const int dim = 32 * m + 8 * t;
+        if (whole) {
+          *reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + dim) =
+              make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                         pack_bf16(f[6], f[7]));
+        } else {
+          float* dst = p.ws_o + hrow * D + dim;
+          *reinterpret_cast<float4*>(dst) = make_float4(f[0], f[1], f[2], f[3]);
+          *reinterpret_cast<float4*>(dst + 4) = make_float4(f[4], f[5], f[6], f[7]);
+        }
+      }
+    } else {  // lane holds dims 8i + 2t, 8i + 2t + 1 of every tile i
+#pragma unroll
+      for (int i = 0; i < C::NT; ++i) {
+        const int dim = 8 * i + 2 * t;
+        const float f0 = o[i][0] * inv, f1 = o[i][1] * inv;
+        if (whole) {
+          *reinterpret_cast<uint32_t*>(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + dim) =
+              pack_bf16(f0, f1);
+        } else {
+          *reinterpret_cast<float2*>(p.ws_o + hrow * D + dim) = make_float2(f0, f1);
+        }
+      }
+    }
+    if (!whole && t == 0) p.ws_lse[hrow] = (l > 0.f) ? mrun + __log2f(l) : -INFINITY;
+    }
+    __syncwarp();
+    if (warp == 0 && lane == 0) {
+      const int64_t v = int64_t(d.s) * p.num_hg + d.hg;
+      if (d.flags & kSeqStart) {
+        p.ws_meta[v].x = int(c);
+        p.ws_meta[v].z = pl.units_per_hg;
+        p.ws_meta[v].w = qrow;
+      }
+      if (d.flags & kSeqEnd) p.ws_meta[v].y = int(c);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// The cache as (dim, token, KV head) -- strides decrease, so a box of {128 bytes of dims,
+// bt tokens, hg heads} lands as [head][token][128 B].
+bool make_cache_map(CUtensorMap* m, const void* cache, int el, int D, int64_t slots, int hkv, int bt, int hg) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(slots), cuuint64_t(hkv)};
+  const cuuint64_t strides[2] = {cuuint64_t(hkv) * D * el, cuuint64_t(D) * el};
+  const cuuint32_t box[3] = {cuuint32_t(128 / el), cuuint32_t(bt), cuuint32_t(hg)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, el == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+            const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename KV, int D, int BT>
+cudaError_t run(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream) {
+  using C = MmaCfg<KV, D, BT>;
+  CUtensorMap km, vm;
+  const int64_t slots = a.num_blocks * a.block_size;
+  if (!make_cache_map(&km, a.k_cache, C::EL, D, slots, a.num_kv_heads, BT, hg) ||
+      !make_cache_map(&vm, a.v_cache, C::EL, D, slots, a.num_kv_heads, BT, hg))
+    return cudaErrorInvalidValue;
+  DecodeParams p = fill_decode_params(a, hg, 1, num_ctas, D);
+  if (C::EL == 2 && a.k_new != nullptr) {
+    p.k_new = static_cast<const char*>(a.k_new);
+    p.v_new = static_cast<const char*>(a.v_new);
+    p.slot_mapping = a.slot_mapping;
+  }
+  if (C::EL == 1) {
+    p.scale_log2 *= a.k_scale;
+    p.v_scale = a.v_scale;
+  }
+  const size_t smem = C::total(hg);
+  auto kern = decode_mma_kernel<__nv_bfloat16, D, KV, BT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(kern, dim3(num_ctas), dim3((hg + 1) * 32), smem, stream, p, km, vm);
+  if (e != cudaSuccess) return e;
+  return launch_merge<__nv_bfloat16, D>(p, stream);
+}
+
+}  // namespace
+
+bool decode_mma_supported(const AttnArgs& a, int hg) {
+  const int B = a.block_size, D = a.head_dim;
+  const int G = a.num_heads / a.num_kv_heads;
+  if (a.dtype != PA_BF16 || hg < 1 || G > 8) return false;
+  if (a.k_new != nullptr && a.cache_dtype != PA_BF16) return false;  // no fused write into E4M3
+  if (!(B == 8 || (B % 16 == 0 && B <= 1024))) return false;
+  if (a.num_blocks * B > 0x7fffffff) return false;  // TMA token coordinates are int32
+  if (a.cache_dtype == PA_BF16) {
+    if (D != 64 && D != 128) return false;
+  } else if (a.cache_dtype == PA_FP8_E4M3) {
+    if (D != 128) return false;
+  } else {
+    return false;
+  }
+  return encode_fn() != nullptr;
+}
+
+cudaError_t launch_decode_mma(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream) {
+  const bool bt8 = a.block_size == 8;
+  if (a.cache_dtype == PA_FP8_E4M3)
+    return bt8 ? run<Fp8E4M3, 128, 8>(a, hg, num_ctas, stream) : run<Fp8E4M3, 128, 16>(a, hg, num_ctas, stream);
+  if (a.head_dim == 64)
+    return bt8 ? run<__nv_bfloat16, 64, 8>(a, hg, num_ctas, stream) : run<__nv_bfloat16, 64, 16>(a, hg, num_ctas, stream);
+  return bt8 ? run<__nv_bfloat16, 128, 8>(a, hg, num_ctas, stream) : run<__nv_bfloat16, 128, 16>(a, hg, num_ctas, stream);
+}
+
+}  // namespace pa

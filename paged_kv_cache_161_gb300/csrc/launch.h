@@ -69,6 +69,12 @@ size_t decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int
 int decode_num_ctas(int device, cudaError_t* err);
 bool decode_supported(pa_dtype dtype, int head_dim, int group);
 cudaError_t launch_decode(const AttnArgs& a, int num_ctas, cudaStream_t stream);
+// The tensor-core decode kernel (bf16 queries; bf16 caches with head_dim 64 / 128, with or
+// without the fused write, or E4M3 caches with head_dim 128; block size 8 or a multiple of
+// 16), with the
+// CUDA-core kernel's head grouping `hg` so the workspace layout is the same.
+bool decode_mma_supported(const AttnArgs& a, int hg);
+cudaError_t launch_decode_mma(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream);
 
 // Prefill (q_len >= 2 requests): the tcgen05 tensor-core kernel where it applies (bf16,
 // block size 8..128 dividing 128, <= 4096 requests), else the CUDA-core tile kernel.
