@@ -32,14 +32,14 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode attention: K/V GB/s (% of GB300 HBM peak) and tokens/s, batch 256"
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one pa_write_attention decode
-# call on this workload -- split-K kernel (KV write fused in) plus merge kernel -- from one
-# ncu capture (the first timed step's two launches) of
+# call on this workload -- tensor-core split-K kernel (KV write fused in) plus merge kernel --
+# from one ncu capture (the first timed step's two launches) of
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum \
 #       --clock-control none --csv --log-file launches.csv \
 #       python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-e2e
 # It holds only for the kernel sources it was measured on (their SHA-256 below); any
 # change to them makes the reported traffic null until it is measured again.
-DECODE_TRAFFIC = {"sources_sha256": "26c642349bb987f141491e3d9c786561bc684e21c921e75a482fb41b04234d3e", "bytes": 1644220416}
+DECODE_TRAFFIC = {"sources_sha256": "3ff1c96a19e0a8197052a3b82f41b63b8ab3dd0f8e6f8daf4c824da186acc42a", "bytes": 1653146880}
 DECODE_SOURCES = ["paged_kv_cache_161_gb300/csrc/decode_attention.cu", "paged_kv_cache_161_gb300/csrc/decode_mma.cu",
                   "paged_kv_cache_161_gb300/csrc/decode_common.cuh", "paged_kv_cache_161_gb300/csrc/common.cuh"]
 
