@@ -58,6 +58,14 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
                : "memory");
 }
 
+// Four 8x8 16-bit matrices: thread l gets (row l/4, cols 2(l%4), 2(l%4)+1) of each.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
@@ -306,15 +314,15 @@ __global__ void __launch_bounds__(9 * 32, 1)
       const int qh = (d.hg * HG + hk) * G + g;  // this lane's query head (row g)
 #pragma unroll
       for (int kc = 0; kc < C::KC; ++kc) {
-        uint2 w = make_uint2(0u, 0u);
-        if (g < G) w = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const T*>(p.q) +
-                                                             (int64_t(qrow) * Hq + qh) * D + 16 * kc + 4 * t));
-        if constexpr (C::kF16) {  // bf16 -> f16 (exact in f16's normal range)
+        const T* qp = reinterpret_cast<const T*>(p.q) + (int64_t(qrow) * Hq + qh) * D + 16 * kc;
+        if constexpr (C::kF16) {  // dims 4t .. 4t+3 (see the K fragments); bf16 -> f16, exact in range
+          uint2 w = make_uint2(0u, 0u);
+          if (g < G) w = __ldg(reinterpret_cast<const uint2*>(qp + 4 * t));
           qa0[kc] = pack_f16(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
           qa2[kc] = pack_f16(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
-        } else {
-          qa0[kc] = w.x;
-          qa2[kc] = w.y;
+        } else {  // dims 2t, 2t+1 and 8 + 2t, 9 + 2t (the standard fragment)
+          qa0[kc] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 2 * t)) : 0u;
+          qa2[kc] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 8 + 2 * t)) : 0u;
         }
       }
 #pragma unroll
@@ -352,29 +360,44 @@ __global__ void __launch_bounds__(9 * 32, 1)
     }
 
     // ---- S = Q K^T: n tile j = tokens 8j .. 8j + 7, this lane's B column = token 8j + g
-    float sacc[2][4];
+    // two accumulators per tile (even / odd k chunks) halve the MMA dependency chain
+    float sacc[2][4], sacc2[2][4];
 #pragma unroll
-    for (int jj = 0; jj < 2; ++jj) sacc[jj][0] = sacc[jj][1] = sacc[jj][2] = sacc[jj][3] = 0.f;
+    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[jj][e] = sacc2[jj][e] = 0.f;
+    // ldmatrix: lane l addresses row l % 8 (a token) of matrix l / 8; matrices are
+    // (tokens 0-7 | 8-15) x (two 16-byte columns), so one x4 load gives B fragments for
+    // both token tiles. bf16: a column holds 8 dims, fragments are standard (b0 = dims
+    // 2t, 2t+1 of chunk kc, b1 = dims 8 + 2t, 9 + 2t). E4M3: a column holds 16 dims = one
+    // chunk; a lane's 4 codes are dims 4t .. 4t+3, so k = 2t + e <-> dim 4t + e and
+    // k = 2t + 8 + e <-> dim 4t + 2 + e (Q uses the same map).
+    const int lm = lane >> 3, lr = lane & 7;
 #pragma unroll
     for (int kc = 0; kc < C::KC; ++kc) {
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const int tok = 8 * jj + g;
-        uint32_t b0, b1;
-        if constexpr (C::kF16) {  // 4 codes: dims 16kc + 4t .. + 3 (one 128-byte row per head)
-          const uint32_t w = lds32(kb + C::at(HG, 0, tok, hk, kc) + 4 * t);
-          b0 = e4m3x2_to_f16x2(w & 0xffffu);
-          b1 = e4m3x2_to_f16x2(w >> 16);
-        } else {  // 4 bf16: dims 16kc + 4t .. + 3 (64 dims per 128-byte row)
-          const int dim = 16 * kc + 4 * t;
-          const uint2 w =
-              lds64(kb + C::at(HG, dim / C::INNER, tok, hk, (dim % C::INNER) * 2 / 16) + ((dim % C::INNER) * 2) % 16);
-          b0 = w.x;
-          b1 = w.y;
+      if constexpr (C::kF16) {
+        if ((kc & 1) == 0) {  // chunks kc, kc + 1 of tokens 0-7 and 8-15
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(kb + C::at(HG, 0, (lm & 1) * 8 + lr, hk, kc + (lm >> 1)), r0, r1, r2, r3);
+          mma_16816(sacc[0], qa0[kc], qa2[kc], e4m3x2_to_f16x2(r0 & 0xffffu), e4m3x2_to_f16x2(r0 >> 16), true);
+          mma_16816(sacc[1], qa0[kc], qa2[kc], e4m3x2_to_f16x2(r1 & 0xffffu), e4m3x2_to_f16x2(r1 >> 16), true);
+          mma_16816(sacc2[0], qa0[kc + 1], qa2[kc + 1], e4m3x2_to_f16x2(r2 & 0xffffu), e4m3x2_to_f16x2(r2 >> 16),
+                    true);
+          mma_16816(sacc2[1], qa0[kc + 1], qa2[kc + 1], e4m3x2_to_f16x2(r3 & 0xffffu), e4m3x2_to_f16x2(r3 >> 16),
+                    true);
         }
-        mma_16816(sacc[jj], qa0[kc], qa2[kc], b0, b1, C::kF16);
+      } else {  // chunk kc: dims 16kc .. 16kc + 15 = 16-byte columns 2kc % 8, +1 of half 16kc / 64
+        const int dim = 16 * kc + (lm >> 1) * 8;
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(kb + C::at(HG, dim / C::INNER, (lm & 1) * 8 + lr, hk, (dim % C::INNER) / 8), r0, r1, r2, r3);
+        mma_16816((kc & 1) ? sacc2[0] : sacc[0], qa0[kc], qa2[kc], r0, r2, false);
+        mma_16816((kc & 1) ? sacc2[1] : sacc[1], qa0[kc], qa2[kc], r1, r3, false);
       }
     }
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[jj][e] += sacc2[jj][e];
 
     // ---- online softmax over the stage's 16 tokens, row g (lanes of a quad share it)
     float x[2][2];
@@ -391,14 +414,14 @@ __global__ void __launch_bounds__(9 * 32, 1)
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     const float mnew = fmaxf(mrun, mx);
     const float ms = (mnew == -INFINITY) ? 0.f : mnew;
-    const float alpha = exp2f(mrun - ms);
+    const float alpha = ex2_ftz(mrun - ms);
     float pv[2][2];
     float psum = 0.f;
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        pv[jj][e] = exp2f(x[jj][e] - ms);
+        pv[jj][e] = ex2_ftz(x[jj][e] - ms);
         psum += pv[jj][e];
       }
     lpart = lpart * alpha + psum;
@@ -423,45 +446,46 @@ __global__ void __launch_bounds__(9 * 32, 1)
     // ---- O += P V. Rows of V past `valid` hold stale or unwritten data: zero them in
     // the B fragments (P is 0 there, but 0 * NaN would not be).
     const bool partial = valid < kTPS;
+    // ldmatrix.trans: lane l addresses row l % 8 (a token) of matrix l / 8; matrices are
+    // (tokens 0-7 | 8-15) x (two 16-byte columns); a lane gets rows 2t, 2t+1 (tokens) of
+    // column g of each.
+    const int mi = lane >> 3, rr = lane & 7;
+    const int vtok = (mi & 1) * 8 + rr;
+    uint32_t lo_mask = 0xffffffffu, hi_mask = 0xffffffffu;  // tokens 2t, 2t+1 | 8+2t, 9+2t
+    if (partial) {
+      lo_mask = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
+      hi_mask = (8 + 2 * t < valid ? 0x0000ffffu : 0u) | (9 + 2 * t < valid ? 0xffff0000u : 0u);
+    }
     if constexpr (C::kF16) {
-      // 4 tiles per 32 dims: tile i, column g <-> dim 32m + 4g + i; this lane reads 4 codes
-      // (dims 32m + 4g .. + 3) of tokens 2t, 2t+1, 8+2t, 9+2t and pairs them across tokens.
+      // A column is 16 dims; a lane's register holds dims 2g, 2g+1 of tokens 2t, 2t+1.
+      // Pairing across tokens gives two tiles per column: E (col g <-> dim 16c + 2g) and
+      // O (col g <-> dim 16c + 2g + 1), so the lane's outputs c0, c1 of E and O are dims
+      // 16c + 4t + {0, 2} and {1, 3}.
 #pragma unroll
-      for (int m = 0; m < D / 32; ++m) {
-        const int chunk = 2 * m + (g >> 2), off = 4 * (g & 3);
-        uint32_t w0 = lds32(vb + C::at(HG, 0, 2 * t, hk, chunk) + off);
-        uint32_t w1 = lds32(vb + C::at(HG, 0, 2 * t + 1, hk, chunk) + off);
-        uint32_t w2 = lds32(vb + C::at(HG, 0, 8 + 2 * t, hk, chunk) + off);
-        uint32_t w3 = lds32(vb + C::at(HG, 0, 9 + 2 * t, hk, chunk) + off);
-        if (partial) {
-          if (2 * t >= valid) w0 = 0u;
-          if (2 * t + 1 >= valid) w1 = 0u;
-          if (8 + 2 * t >= valid) w2 = 0u;
-          if (9 + 2 * t >= valid) w3 = 0u;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t sel = uint32_t(i) | (uint32_t(4 + i) << 4);  // byte i of a, byte i of b
-          const uint32_t b0 = e4m3x2_to_f16x2(prmt(w0, w1, sel));
-          const uint32_t b1 = e4m3x2_to_f16x2(prmt(w2, w3, sel));
-          mma_16816(o[4 * m + i], pa0, pa2, b0, b1, true);
-        }
+      for (int c2 = 0; c2 < C::KC / 2; ++c2) {
+        uint32_t r0, r1, r2, r3;  // (tok 0-7, col 2c2), (8-15, 2c2), (0-7, 2c2+1), (8-15, 2c2+1)
+        ldsm_x4_trans(vb + C::at(HG, 0, vtok, hk, 2 * c2 + (mi >> 1)), r0, r1, r2, r3);
+        r0 &= lo_mask;
+        r1 &= hi_mask;
+        r2 &= lo_mask;
+        r3 &= hi_mask;
+        mma_16816(o[4 * c2 + 0], pa0, pa2, e4m3x2_to_f16x2(prmt(r0, 0u, 0x20u)), e4m3x2_to_f16x2(prmt(r1, 0u, 0x20u)),
+                  true);
+        mma_16816(o[4 * c2 + 1], pa0, pa2, e4m3x2_to_f16x2(prmt(r0, 0u, 0x31u)), e4m3x2_to_f16x2(prmt(r1, 0u, 0x31u)),
+                  true);
+        mma_16816(o[4 * c2 + 2], pa0, pa2, e4m3x2_to_f16x2(prmt(r2, 0u, 0x20u)), e4m3x2_to_f16x2(prmt(r3, 0u, 0x20u)),
+                  true);
+        mma_16816(o[4 * c2 + 3], pa0, pa2, e4m3x2_to_f16x2(prmt(r2, 0u, 0x31u)), e4m3x2_to_f16x2(prmt(r3, 0u, 0x31u)),
+                  true);
       }
     } else {
-      // ldmatrix.trans: matrices (tokens 0-7 | 8-15) x (dims 8i | 8i + 8) -> b0, b1 of
-      // tiles i and i + 1; lane l addresses row l % 8 of matrix l / 8
-      const int mi = lane >> 3, rr = lane & 7;
-      const int tok = (mi & 1) * 8 + rr;
-      uint32_t lo_mask = 0xffffffffu, hi_mask = 0xffffffffu;  // tokens 2t, 2t+1 | 8+2t, 9+2t
-      if (partial) {
-        lo_mask = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
-        hi_mask = (8 + 2 * t < valid ? 0x0000ffffu : 0u) | (9 + 2 * t < valid ? 0xffff0000u : 0u);
-      }
+      // bf16: a column is 8 dims; matrices (dims 8i | 8i + 8) give b0, b1 of tiles i, i + 1
+      // with the standard fragment (col g <-> dim 8i + g)
 #pragma unroll
       for (int i2 = 0; i2 < C::NT / 2; ++i2) {
         const int dim = 16 * i2 + (mi >> 1) * 8;
         uint32_t r0, r1, r2, r3;
-        ldsm_x4_trans(vb + C::at(HG, dim / C::INNER, tok, hk, (dim % C::INNER) / 8), r0, r1, r2, r3);
+        ldsm_x4_trans(vb + C::at(HG, dim / C::INNER, vtok, hk, (dim % C::INNER) / 8), r0, r1, r2, r3);
         mma_16816(o[2 * i2], pa0, pa2, r0 & lo_mask, r1 & hi_mask, false);
         mma_16816(o[2 * i2 + 1], pa0, pa2, r2 & lo_mask, r3 & hi_mask, false);
       }
@@ -486,24 +510,17 @@ __global__ void __launch_bounds__(9 * 32, 1)
     const float inv = l > 0.f ? v_scale / l : 0.f;
     const int64_t slot = c + int64_t(d.s) * p.num_hg + d.hg;
     const int64_t hrow = slot * (int64_t(HG) * G) + head_in_group;
-    if constexpr (C::kF16) {  // lane holds dims 32m + 8t .. + 7 (c0 of tiles 4m..4m+3, then c1)
+    if constexpr (C::kF16) {  // lane holds dims 16c + 4t .. + 3: E.c0, O.c0, E.c1, O.c1 of chunk c
 #pragma unroll
-      for (int m = 0; m < D / 32; ++m) {
-        float f[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          f[i] = o[4 * m + i][0] * inv;
-          f[4 + i] = o[4 * m + i][1] * inv;
-        }
-        const int dim = 32 * m + 8 * t;
+      for (int cc = 0; cc < C::KC; ++cc) {
+        const float f0 = o[2 * cc][0] * inv, f1 = o[2 * cc + 1][0] * inv;
+        const float f2 = o[2 * cc][1] * inv, f3 = o[2 * cc + 1][1] * inv;
+        const int dim = 16 * cc + 4 * t;
         if (whole) {
-          *reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + dim) =
-              make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
-                         pack_bf16(f[6], f[7]));
+          *reinterpret_cast<uint2*>(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + dim) =
+              make_uint2(pack_bf16(f0, f1), pack_bf16(f2, f3));
         } else {
-          float* dst = p.ws_o + hrow * D + dim;
-          *reinterpret_cast<float4*>(dst) = make_float4(f[0], f[1], f[2], f[3]);
-          *reinterpret_cast<float4*>(dst + 4) = make_float4(f[4], f[5], f[6], f[7]);
+          *reinterpret_cast<float4*>(p.ws_o + hrow * D + dim) = make_float4(f0, f1, f2, f3);
         }
       }
     } else {  // lane holds dims 8i + 2t, 8i + 2t + 1 of every tile i
