@@ -309,8 +309,8 @@ __global__ void __launch_bounds__(9 * 32, 1)
       return;
     }
     const StageDesc d = desc[stage];
-    const int qrow = __ldg(p.qsl + d.s);
     if (d.flags & kFirst) {
+      const int qrow = __ldg(p.qsl + d.s);
       const int qh = (d.hg * HG + hk) * G + g;  // this lane's query head (row g)
 #pragma unroll
       for (int kc = 0; kc < C::KC; ++kc) {
@@ -503,6 +503,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
     float l = lpart;
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
+    const int qrow = __ldg(p.qsl + d.s);
     if (g < G) {  // rows past the group's query heads are padding
     const bool whole = (d.flags & kSeqStart) && (d.flags & kSeqEnd);
     const int head_in_group = hk * G + g;
