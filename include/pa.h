@@ -6,6 +6,7 @@
  *   pa_attention    paged decode and chunked-prefill attention through block_table
  *   pa_write_attention  the two above in one call (the write fused into decode)
  *   pa_kv_write_fp8 / pa_attention_fp8  the same over FP8 (E4M3) caches
+ *   pa_attention_grouped  decode attention reading a shared prefix once per group
  *   pa_copy_blocks  copy whole physical blocks (the copy step of copy-on-write)
  *   pa_swap_blocks  move whole blocks between the GPU pool and a CPU pool (preemption)
  *   pa_bm_*         host-side block accounting: free queue, block tables, ref counts, CoW
@@ -197,6 +198,39 @@ int pa_write_attention(void* out, const void* q, const void* k_new, const void* 
                        pa_dtype dtype, void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------------
+ * pa_attention_grouped -- pa_attention for a decode batch (one query per request) whose
+ * requests come in groups sharing a prefix of physical blocks: [read] 5.2.1 (samples of one
+ * prompt share its blocks), [docs] Copy-on-Write (shared blocks, reference counts).
+ *
+ * Same result as pa_attention. The grouping only changes how the work is done: for group
+ * g the first shared_len[g] positions are read once and multiplied against the queries of
+ * all its members together (the members' query heads become one set of matrix rows), and
+ * each member's remaining positions run on their own; the pieces are merged per request.
+ *  seq_group     device int32 [num_seqs]: the request's group, or -1
+ *  group_range   device int32 [num_groups, 2]: group g's members are the consecutive
+ *                requests [group_range[2g], group_range[2g+1])
+ *  shared_len    device int32 [num_groups]: positions [0, shared_len[g]) of every member
+ *                are the same physical slots (same block ids in their tables); the library
+ *                reads them through the first member's table
+ * The kernel uses whole 16-token chunks below shared_len and every member's length, and
+ * runs a group ungrouped when members x (num_heads / num_kv_heads) > 16 or it has fewer
+ * than 2 members; a request whose seq_group does not match group_range runs ungrouped.
+ * bf16 only (q, out, caches); head_dim 64 / 128; block size 8 or a multiple of 16;
+ * num_heads / num_kv_heads <= 8. Workspace from pa_attention_grouped_workspace_size.
+ * pa_bm_batch_groups builds the three arrays from the block manager's tables.
+ * --------------------------------------------------------------------------- */
+int pa_attention_grouped_workspace_size(int num_seqs, int num_groups, int num_heads, int num_kv_heads,
+                                        int head_dim, size_t* bytes_out);
+
+int pa_attention_grouped(void* out, const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                         const int32_t* query_start_loc, int num_seqs, int num_tokens, int max_seq_len,
+                         int num_heads, int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                         float scale, pa_dtype dtype, const int32_t* seq_group, const int32_t* group_range,
+                         const int32_t* shared_len, int num_groups, void* workspace, size_t workspace_bytes,
+                         pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------
  * FP8 KV cache -- [docs] quantisation support (FP8: 8-bit, 2x smaller than 16-bit storage).
  *
  * k_cache / v_cache hold one E4M3 code per element (PA_FP8_E4M3: 1 sign bit, 4 exponent
@@ -364,6 +398,16 @@ int pa_bm_append_tokens_batch(pa_bm* bm, const int64_t* seqs, const int64_t* cou
                               const int32_t* token_ids, int64_t* slots_out, int64_t* done_out);
 /* Registered blocks now, blocks reused by lookups so far, registrations evicted so far. */
 int pa_bm_prefix_stats(const pa_bm* bm, int64_t* cached_blocks, int64_t* hit_blocks, int64_t* evictions);
+
+/* Groups for pa_attention_grouped over the batch seqs[0, n) (in batch order): runs of
+ * consecutive sequences whose block tables start with the same block id, at most
+ * max_members each, become groups; shared_len = the number of leading table entries all
+ * members have in common x block_size, capped by the shortest member. Writes
+ * seq_group_out[n] (-1 outside groups), group_range_out[2 * groups] and
+ * shared_len_out[groups] (capacity >= n / 2 groups is always enough) and *num_groups_out. */
+int pa_bm_batch_groups(const pa_bm* bm, const int64_t* seqs, int64_t n, int max_members, int32_t* seq_group_out,
+                       int32_t* group_range_out, int32_t* shared_len_out, int64_t capacity,
+                       int64_t* num_groups_out);
 
 /* ------------------------------------------------------------------------------
  * Swapping -- [read] 6.2.1 SequenceGroup (preempted groups are swapped out to the CPU and

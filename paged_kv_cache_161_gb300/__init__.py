@@ -24,6 +24,8 @@ __all__ = [
     "swap_blocks",
     "attention",
     "write_attention",
+    "attention_grouped",
+    "attention_grouped_workspace_size",
     "kv_write_fp8",
     "attention_fp8",
     "attention_workspace_size",
@@ -58,6 +60,10 @@ _sig = {
     "pa_attention_fp8": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i64, _f, _f, _f,
                               _p, _sz, _p]),
     "pa_swap_blocks": (_i, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i, _i, _i, _i, _p]),
+    "pa_attention_grouped_workspace_size": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
+    "pa_attention_grouped": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i64, _f, _i, _p, _p,
+                                  _p, _i, _p, _sz, _p]),
+    "pa_bm_batch_groups": (_i, [_p, _p, _i64, _i, _p, _p, _p, _i64, ctypes.POINTER(_i64)]),
     "pa_bm_enable_swap": (_i, [_p, _i64, _p]),
     "pa_bm_swap_out": (_i, [_p, _p, _i64, _p, _i64, ctypes.POINTER(_i64)]),
     "pa_bm_swap_in": (_i, [_p, _p, _i64, _p, _i64, ctypes.POINTER(_i64)]),
@@ -313,6 +319,45 @@ def attention_fp8(out, q, k_cache, v_cache, block_table, seq_lens, query_start_l
     return out
 
 
+def attention_grouped_workspace_size(num_seqs: int, num_groups: int, num_heads: int, num_kv_heads: int,
+                                     head_dim: int) -> int:
+    """pa_attention_grouped_workspace_size for the current device."""
+    out = ctypes.c_size_t(0)
+    _check(lib.pa_attention_grouped_workspace_size(num_seqs, num_groups, num_heads, num_kv_heads, head_dim,
+                                                   ctypes.byref(out)), "pa_attention_grouped_workspace_size")
+    return int(out.value)
+
+
+def attention_grouped(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, seq_group, group_range,
+                      shared_len, *, max_seq_len: int, scale: float, workspace=None, stream=None):
+    """pa_attention_grouped: decode attention where each group's shared prefix is read once.
+
+    seq_group int32 [S], group_range int32 [num_groups, 2], shared_len int32 [num_groups]
+    (from BlockManager.batch_groups); the result equals attention() on the same batch."""
+    NB, B, Hkv, D = _cache_geometry(k_cache, v_cache)
+    T, Hq = int(q.shape[0]), int(q.shape[1])
+    if q.dim() != 3 or tuple(out.shape) != tuple(q.shape) or int(q.shape[2]) != D:
+        raise ValueError("q and out must be [num_tokens, num_heads, head_dim]")
+    S = int(seq_lens.shape[0])
+    G = int(shared_len.shape[0])
+    if tuple(seq_group.shape) != (S,) or tuple(group_range.shape) != (G, 2):
+        raise ValueError("seq_group [S], group_range [num_groups, 2], shared_len [num_groups]")
+    if workspace is None:
+        workspace = torch.empty(attention_grouped_workspace_size(S, G, Hq, Hkv, D), dtype=torch.uint8,
+                                device=q.device)
+    grp = lambda t, n: _dev(t, n, torch.int32) if G > 0 else 0  # noqa: E731
+    st = lib.pa_attention_grouped(_dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                                  _dev(block_table, "block_table", torch.int32, 2), int(block_table.shape[1]),
+                                  _dev(seq_lens, "seq_lens", torch.int32, 1),
+                                  _dev(query_start_loc, "query_start_loc", torch.int32, 1), S, T, int(max_seq_len),
+                                  Hq, Hkv, D, B, NB, float(scale), _dtype_code(q), grp(seq_group, "seq_group"),
+                                  grp(group_range, "group_range"), grp(shared_len, "shared_len"), G,
+                                  workspace.data_ptr() if workspace.numel() else 0, workspace.numel(),
+                                  _stream(stream, q.device))
+    _check(st, "pa_attention_grouped")
+    return out
+
+
 def read_device_errors(clear: bool = True) -> int:
     """The current device's error word (PA_DEVERR bits); synchronises the device."""
     flags = ctypes.c_uint(0)
@@ -422,6 +467,23 @@ class BlockManager:
         _check(lib.pa_bm_prefix_stats(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
                "pa_bm_prefix_stats")
         return int(a.value), int(b.value), int(c.value)
+
+    def batch_groups(self, seqs, max_members: int):
+        """(seq_group int32 [n], group_range int32 [groups, 2], shared_len int32 [groups]) for
+        pa_attention_grouped over the batch ``seqs`` (batch order)."""
+        import numpy as np
+
+        s = np.ascontiguousarray(np.asarray(seqs, np.int64))
+        n = len(s)
+        cap = max(n // 2, 1)
+        sg = np.empty(n, np.int32)
+        gr = np.empty((cap, 2), np.int32)
+        sl = np.empty(cap, np.int32)
+        ng = ctypes.c_int64(0)
+        _check(lib.pa_bm_batch_groups(self._h, s.ctypes.data if n else None, n, max_members,
+                                      sg.ctypes.data if n else None, gr.ctypes.data, sl.ctypes.data, cap,
+                                      ctypes.byref(ng)), "pa_bm_batch_groups")
+        return sg, gr[: ng.value].copy(), sl[: ng.value].copy()
 
     # -- swapping ----------------------------------------------------------------
     def enable_swap(self, num_cpu_blocks: int, cpu_free_order):

@@ -367,4 +367,56 @@ int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
+int pa_attention_grouped_workspace_size(int num_seqs, int num_groups, int num_heads, int num_kv_heads, int head_dim,
+                                        size_t* bytes_out) {
+  if (!bytes_out || num_seqs < 0 || num_groups < 0 || num_heads < 1 || num_kv_heads < 1) return PA_ERR_INVALID_ARG;
+  if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+  size_t plain = 0;
+  const int st = pa_attention_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, &plain);
+  if (st != PA_OK) return st;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int ctas = pa::decode_num_ctas(dev, &e);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int G = num_heads / num_kv_heads;
+  size_t need = plain;
+  for (pa_dtype dt : {PA_BF16, PA_FP8_E4M3}) {
+    const int hg = pa::decode_hg(dt, head_dim, G, num_kv_heads);
+    const size_t n = pa::decode_grouped_workspace_bytes(num_seqs, num_groups, num_kv_heads, head_dim, hg, ctas);
+    need = n > need ? n : need;
+  }
+  *bytes_out = need;
+  return PA_OK;
+}
+
+int pa_attention_grouped(void* out, const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                         const int32_t* query_start_loc, int num_seqs, int num_tokens, int max_seq_len,
+                         int num_heads, int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                         float scale, pa_dtype dtype, const int32_t* seq_group, const int32_t* group_range,
+                         const int32_t* shared_len, int num_groups, void* workspace, size_t workspace_bytes,
+                         pa_stream_t stream) {
+  if (num_groups < 0) return PA_ERR_INVALID_ARG;
+  if (num_groups > 0 && (!seq_group || !group_range || !shared_len)) return PA_ERR_INVALID_ARG;
+  pa::AttnArgs a;
+  int ctas = 0;
+  bool nothing = false;
+  int st = prepare_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, query_start_loc,
+                             num_seqs, num_tokens, 1, max_seq_len, num_heads, num_kv_heads, head_dim, block_size,
+                             num_blocks, scale, dtype, workspace, workspace_bytes, a, ctas, nothing, dtype);
+  if (st != PA_OK || nothing) return st;
+  if (num_tokens != num_seqs) return PA_ERR_INVALID_ARG;  // a decode batch: one query per request
+  const int hg = pa::decode_hg(dtype, head_dim, num_heads / num_kv_heads, num_kv_heads);
+  a.seq_group = seq_group;
+  a.group_start = group_range;
+  a.shared_len = shared_len;
+  a.num_groups = num_groups;
+  if (!pa::decode_mma_supported(a, hg)) return PA_ERR_UNSUPPORTED;
+  const size_t need = pa::decode_grouped_workspace_bytes(num_seqs, num_groups, num_kv_heads, head_dim, hg, ctas);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+  const cudaError_t e = pa::launch_decode_mma(a, hg, ctas, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 }  // extern "C"

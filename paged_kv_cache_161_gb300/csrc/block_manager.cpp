@@ -530,4 +530,49 @@ int pa_bm_cpu_ref_count(const pa_bm* bm, int64_t block) {
   return bm->cpu_ref[size_t(block)];
 }
 
+int pa_bm_batch_groups(const pa_bm* bm, const int64_t* seqs, int64_t n, int max_members, int32_t* seq_group_out,
+                       int32_t* group_range_out, int32_t* shared_len_out, int64_t capacity,
+                       int64_t* num_groups_out) {
+  if (!bm || n < 0 || max_members < 2 || !num_groups_out || (n > 0 && (!seqs || !seq_group_out)))
+    return PA_ERR_INVALID_ARG;
+  if (n > 0x7fffffff) return PA_ERR_INVALID_ARG;
+  std::vector<const pa_bm::Seq*> sq(static_cast<size_t>(n));
+  for (int64_t i = 0; i < n; ++i) {
+    auto it = bm->seqs.find(seqs[i]);
+    if (it == bm->seqs.end()) return PA_ERR_NOT_FOUND;
+    sq[size_t(i)] = &it->second;
+  }
+  int64_t ng = 0;
+  int64_t i = 0;
+  while (i < n) {
+    const auto& first = *sq[size_t(i)];
+    int64_t j = i + 1;
+    int64_t common = int64_t(first.table.size());  // leading entries shared with the first member
+    int64_t min_len = first.len;
+    while (j < n && j - i < max_members && !first.swapped && !sq[size_t(j)]->swapped) {
+      const auto& t = sq[size_t(j)]->table;
+      int64_t k = 0;
+      while (k < common && k < int64_t(t.size()) && t[size_t(k)] == first.table[size_t(k)]) ++k;
+      if (k == 0) break;
+      common = k;
+      min_len = sq[size_t(j)]->len < min_len ? sq[size_t(j)]->len : min_len;
+      ++j;
+    }
+    if (j - i >= 2) {
+      if (ng >= capacity || !group_range_out || !shared_len_out) return PA_ERR_INVALID_ARG;
+      group_range_out[2 * ng] = int32_t(i);
+      group_range_out[2 * ng + 1] = int32_t(j);
+      const int64_t shared = common * bm->block_size;
+      shared_len_out[ng] = int32_t(shared < min_len ? shared : min_len);
+      for (int64_t m = i; m < j; ++m) seq_group_out[m] = int32_t(ng);
+      ++ng;
+    } else {
+      seq_group_out[i] = -1;
+    }
+    i = j;
+  }
+  *num_groups_out = ng;
+  return PA_OK;
+}
+
 }  // extern "C"

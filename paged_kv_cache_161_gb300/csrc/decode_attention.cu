@@ -618,6 +618,10 @@ cudaError_t run_g(const AttnArgs& a, int G, int num_ctas, cudaStream_t stream) {
 
 }  // namespace
 
+int decode_hg(pa_dtype cache_dtype, int head_dim, int group, int num_kv_heads) {
+  return hg_for(cache_dtype, head_dim, group, num_kv_heads);
+}
+
 bool decode_supported(pa_dtype dtype, int head_dim, int group) {
   if (head_dim != 64 && head_dim != 128) return false;
   if (group != 1 && group != 2 && group != 4 && group != 8) return false;

@@ -52,6 +52,14 @@ struct DecodeParams {
   int num_ctas; // grid of the split-K kernel
   float scale_log2;  // softmax scale * log2(e) (* k_scale for E4M3 caches)
   float v_scale;     // 1, or the E4M3 V scale
+  // Shared-prefix groups (tensor-core kernel; num_groups = 0: none): request s belongs to
+  // group seq_group[s] (or -1); group g's members are requests [group_start[2g],
+  // group_start[2g+1]) and their first shared_len[g] positions are the same physical slots.
+  const int32_t* seq_group;
+  const int32_t* group_start;
+  const int32_t* shared_len;
+  int num_groups;
+  int rmax;  // workspace rows per KV head of a piece: G, or 16 with groups
 };
 
 // Keys of request s if it is a decode request (q_len == 1), else 0.
@@ -341,6 +349,11 @@ inline DecodeParams fill_decode_params(const AttnArgs& a, int hg, int qg, int nu
   p.num_ctas = num_ctas;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.v_scale = 1.f;
+  p.seq_group = nullptr;
+  p.group_start = nullptr;
+  p.shared_len = nullptr;
+  p.num_groups = 0;
+  p.rmax = G;
   return p;
 }
 

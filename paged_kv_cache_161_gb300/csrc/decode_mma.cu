@@ -33,19 +33,19 @@ namespace pa {
 namespace {
 
 // ---------------------------------------------------------------- tensor-core wrappers
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1,
-                                          bool f16) {
-  // rows 8..15 of A are zero (at most 8 query heads per KV head): a1 = a3 = 0
+// D (16 x 8, fp32) += A (16 x 16) B (16 x 8): a0 / a2 rows g, a1 / a3 rows g + 8.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1, bool f16) {
   if (f16)
     asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   else
     asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // Four 8x8 16-bit matrices, transposed: thread l gets (row 2(l%4), col l/4) and
@@ -120,7 +120,7 @@ struct MmaCfg {
   static __host__ __device__ uint32_t k_off(int hg, int st) { return uint32_t(st) * 2 * stage_bytes(hg); }
   static __host__ __device__ uint32_t v_off(int hg, int st) { return k_off(hg, st) + stage_bytes(hg); }
   static __host__ __device__ uint32_t desc_off(int hg) { return STAGES * 2 * stage_bytes(hg); }
-  static __host__ __device__ uint32_t bar_off(int hg) { return desc_off(hg) + STAGES * sizeof(StageDesc); }
+  static __host__ __device__ uint32_t bar_off(int hg) { return desc_off(hg) + STAGES * 48; }  // MmaDesc
   static __host__ __device__ uint32_t red_off(int hg) { return bar_off(hg) + 2 * STAGES * 8; }
   static __host__ __device__ uint32_t total(int hg) { return red_off(hg) + 40 * 4 + 1024; }  // + alignment
   // Byte offset, inside a stage's K (or V), of 16-byte column `chunk` (of the 128-byte
@@ -132,21 +132,122 @@ struct MmaCfg {
   }
 };
 
+// ---------------------------------------------------------------- segments
+// The unit numbering runs over segments. Without groups a segment is a request. With
+// shared-prefix groups, segments [0, num_groups) are the groups' shared prefixes (16-token
+// chunks every member holds in the same physical slots; the MMA rows are all members'
+// query heads, so those K/V bytes are read once for the whole group) and segment
+// num_groups + s is request s past its group's shared chunks.
+struct MmaDesc {
+  int s;      // the request (own segment) or the group's first member (shared segment)
+  int hg, j, valid, flags;
+  int seg;    // segment index
+  int nmem;   // requests whose query heads are the MMA rows (1 for an own segment)
+  int pos0;   // position of the stage's first token
+  int64_t wslot;
+  int64_t pad;  // the own segment's skipped (shared) chunks
+};
+static_assert(sizeof(MmaDesc) == 48, "the shared-memory layout reserves 48 bytes a descriptor");
+
+// Group g's members: requests [group_start[2g], group_start[2g + 1]) (clamped to the batch).
+__device__ __forceinline__ void group_span(const DecodeParams& p, int g, int& a, int& b) {
+  a = min(max(__ldg(p.group_start + 2 * g), 0), p.num_seqs);
+  b = min(max(__ldg(p.group_start + 2 * g + 1), a), p.num_seqs);
+}
+
+// Shared 16-token chunks of group g: whole chunks below shared_len and every member's
+// length; 0 for a group that is too small or too large for 16 MMA rows.
+__device__ int shared_chunks(const DecodeParams& p, int g) {
+  int a, b;
+  group_span(p, g, a, b);
+  if (b - a < 2 || (b - a) * p.group > 16) return 0;
+  int lim = __ldg(p.shared_len + g);
+  for (int s = a; s < b; ++s) lim = min(lim, decode_len(p, s));
+  return max(lim, 0) / kTPS;
+}
+
+// Leading chunks of request s that its group's shared segment covers.
+__device__ int own_skip(const DecodeParams& p, int s) {
+  if (p.num_groups == 0) return 0;
+  const int g = __ldg(p.seq_group + s);
+  if (g < 0 || g >= p.num_groups) return 0;
+  int a, b;
+  group_span(p, g, a, b);
+  if (s < a || s >= b) return 0;  // inconsistent membership: the request runs on its own
+  return shared_chunks(p, g);
+}
+
+__device__ int seg_units(const DecodeParams& p, int k) {
+  if (k < p.num_groups) return shared_chunks(p, k);
+  const int s = k - p.num_groups;
+  return max(units_of(decode_len(p, s)) - own_skip(p, s), 0);
+}
+
+// The CTA's range over the segment-major numbering (as plan_range over requests).
+template <typename T, int D>
+__device__ bool plan_segments(const DecodeParams& p, int* red, Plan& pl) {
+  const int S = p.num_seqs, NS = p.num_groups + S;
+  int my_units = 0;
+  for (int k = threadIdx.x; k < NS; k += blockDim.x) my_units += seg_units(p, k);
+  pl.units_per_hg = block_sum(my_units, red);
+  const int64_t U = int64_t(pl.units_per_hg) * p.num_hg;
+  const int64_t c = blockIdx.x, C_ = gridDim.x;
+  if (c == 0) {
+    for (int k = threadIdx.x; k < NS; k += blockDim.x) {
+      if (seg_units(p, k) > 0) continue;
+      for (int hg = 0; hg < p.num_hg; ++hg) p.ws_meta[int64_t(k) * p.num_hg + hg] = make_int4(-1, -1, 0, 0);
+      if (k < p.num_groups) continue;
+      const int s = k - p.num_groups;
+      const int q0 = __ldg(p.qsl + s);
+      if (__ldg(p.qsl + s + 1) - q0 == 1 && decode_len(p, s) == 0) {  // a decode query without keys
+        raise_error(p.err, PA_DEVERR_SEQ_RANGE);
+        T* o = reinterpret_cast<T*>(p.out) + int64_t(q0) * p.num_heads * D;
+        for (int i = 0; i < p.num_heads * D; ++i) o[i] = T(0.f);
+      }
+    }
+  }
+  pl.u_begin = c * U / C_;
+  pl.u_end = (c + 1) * U / C_;
+  if (pl.u_begin >= pl.u_end) return false;
+  const int64_t rem = pl.u_begin;
+  int64_t run = 0;
+  for (int base = 0; base < NS; base += blockDim.x) {
+    const int k = base + threadIdx.x;
+    const int us = k < NS ? seg_units(p, k) * p.num_hg : 0;
+    int total;
+    const int ex = block_exclusive_scan(us, red, &total);
+    if (us > 0 && run + ex <= rem && rem < run + ex + us) {
+      red[34] = k;
+      red[35] = int(rem - (run + ex));
+    }
+    __syncthreads();
+    run += total;
+    if (run > rem) break;
+  }
+  pl.start_s = red[34];  // a segment here
+  const int start_us = seg_units(p, pl.start_s);
+  pl.start_hg = red[35] / start_us;
+  pl.start_j = red[35] % start_us;
+  return true;
+}
+
 // ---------------------------------------------------------------- the kernel
-template <typename T, int D, typename KV, int BT>
+// GROUPED: shared-prefix segments may put up to 16 query heads (several requests) on the
+// MMA rows, so rows 8..15 carry data (A fragments a1 / a3, a second softmax row per lane).
+template <typename T, int D, typename KV, int BT, bool GROUPED>
 __global__ void __launch_bounds__(9 * 32, 1)
     decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap) {
   using C = MmaCfg<KV, D, BT>;
   constexpr int STAGES = C::STAGES;
   const int HG = p.hg_size, G = p.group;
-  const int S = p.num_seqs;
+  const int NG = p.num_groups, NS = NG + p.num_seqs;
 
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1024-byte alignment
   unsigned char* smem = smem_raw + (base - raw);
-  StageDesc* desc = reinterpret_cast<StageDesc*>(smem + C::desc_off(HG));
+  MmaDesc* desc = reinterpret_cast<MmaDesc*>(smem + C::desc_off(HG));
   int* red = reinterpret_cast<int*>(smem + C::red_off(HG));
   const uint32_t full0 = base + C::bar_off(HG), empty0 = full0 + 8 * STAGES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -156,7 +257,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
   griddep_launch_dependents();
 
   Plan pl;
-  if (!plan_range<T, D>(p, red, pl)) return;
+  if (!plan_segments<T, D>(p, red, pl)) return;
   const int64_t u_begin = pl.u_begin, u_end = pl.u_end, c = blockIdx.x;
 
   if (threadIdx.x == 0) {
@@ -176,9 +277,28 @@ __global__ void __launch_bounds__(9 * 32, 1)
       tc::prefetch_tensormap(&kmap);
       tc::prefetch_tensormap(&vmap);
     }
-    int s = pl.start_s, j = pl.start_j, hg = pl.start_hg;
-    int L = decode_len(p, s);
-    int units_s = units_of(L);
+    // the segment being walked: its request (or first member), members, first chunk,
+    // chunk count and key count
+    int k = pl.start_s, j = pl.start_j, hg = pl.start_hg;
+    int s, nmem, skip, units_s, L;
+    auto open_segment = [&](int kk) {
+      if (kk < NG) {
+        int a, b;
+        group_span(p, kk, a, b);
+        s = a;
+        nmem = b - a;
+        skip = 0;
+        units_s = shared_chunks(p, kk);
+        L = units_s * kTPS;
+      } else {
+        s = kk - NG;
+        nmem = 1;
+        skip = own_skip(p, s);
+        L = decode_len(p, s);
+        units_s = max(units_of(L) - skip, 0);
+      }
+    };
+    open_segment(k);
     int stage = 0;
     uint32_t phase = 0;
     for (int64_t u = u_begin; u < u_end; ++u) {
@@ -188,14 +308,14 @@ __global__ void __launch_bounds__(9 * 32, 1)
       if (u == u_end - 1 || j == units_s - 1) flags |= kLast;
       if (u0 >= u_begin) flags |= kSeqStart;
       if (u1 <= u_end) flags |= kSeqEnd;
-      const int valid = min(kTPS, L - j * kTPS);
-      const int pos0 = j * kTPS;
+      const int pos0 = (skip + j) * kTPS;
+      const int valid = min(kTPS, L - pos0);
       const int32_t* bt = p.block_table + int64_t(s) * p.max_blocks_per_seq;
-      // Fused KV write (decode-only batches, 16-bit caches): at a request's last unit the
-      // consumers patch the new token's row (position L - 1) into the stage and store it to
-      // its slot; a slot that is not that position's is written here and flagged.
+      // Fused KV write (decode-only batches without groups, 16-bit caches): at a request's
+      // last unit the consumers patch the new token's row (position L - 1) into the stage
+      // and store it to its slot; a slot that is not that position's is written here.
       int64_t wslot = -1;
-      if (p.k_new && j == units_s - 1) {
+      if (!GROUPED && p.k_new && j == units_s - 1) {
         const int qrow = __ldg(p.qsl + s);
         const int64_t slot = __ldg(p.slot_mapping + qrow);
         const int64_t at = int64_t(__ldg(bt + (L - 1) / B)) * B + (L - 1) % B;
@@ -241,14 +361,17 @@ __global__ void __launch_bounds__(9 * 32, 1)
       }
       if (lane == 0) {
         if (any_bad) raise_error(p.err, PA_DEVERR_BLOCK_RANGE);
-        StageDesc d;
+        MmaDesc d;
         d.s = s;
         d.hg = hg;
         d.j = j;
         d.valid = valid;
         d.flags = flags;
-        d.pad = 0;
+        d.seg = k;
+        d.nmem = nmem;
+        d.pos0 = pos0;
         d.wslot = wslot;
+        d.pad = skip;
         desc[stage] = d;
         mbar_arrive_expect_tx(full0 + 8 * stage, uint32_t(nhave) * C::HALVES * 2 * C::box_bytes(HG));
       }
@@ -271,11 +394,10 @@ __global__ void __launch_bounds__(9 * 32, 1)
         if (++hg == p.num_hg) {
           hg = 0;
           do {
-            if (++s >= S) break;  // cannot happen: the plan counted these units
-            L = decode_len(p, s);
-            units_s = units_of(L);
+            if (++k >= NS) break;  // cannot happen: the plan counted these units
+            open_segment(k);
           } while (units_s == 0);
-          if (s >= S) {
+          if (k >= NS) {
             raise_error(p.err, PA_DEVERR_TIMEOUT);
             break;
           }
@@ -286,20 +408,38 @@ __global__ void __launch_bounds__(9 * 32, 1)
   }
 
   // =========================== consumer warps ===========================
-  // warp hk = KV head within the group; MMA rows = its G query heads. Lane (g, t):
-  // g = lane / 4 is an MMA row / token / dim index, t = lane % 4 a column pair.
+  // warp hk = KV head within the group; MMA rows = the G query heads of its KV head for
+  // each of the stage's nmem requests (row r: request r / G, head r % G). Lane (g, t):
+  // g = lane / 4 is an MMA row (g and g + 8) / token / dim index, t = lane % 4 a column pair.
   const int hk = warp;
   const int g = lane >> 2, t = lane & 3;
   const int Hq = p.num_heads;
-  // Dims are permuted inside each 16-dim chunk so a lane reads 4 consecutive elements:
-  // MMA k = 2t + e <-> dim 4t + e, k = 2t + 8 + e <-> dim 4t + 2 + e (Q uses the same map).
-  uint32_t qa0[C::KC], qa2[C::KC];
+  uint32_t qa0[C::KC], qa2[C::KC];  // A fragments of rows g (and, GROUPED, g + 8: qa1, qa3)
+  uint32_t qa1[GROUPED ? C::KC : 1], qa3[GROUPED ? C::KC : 1];
   uint4 knew = make_uint4(0u, 0u, 0u, 0u), vnew = knew;  // fused write: this lane's 16 bytes of the new row
   constexpr int kRowChunks = D * C::EL / 16;               // 16-byte pieces of one head's row
   float o[C::NT][4];
-  float mrun = -INFINITY, lpart = 0.f;
+  float mrun0 = -INFINITY, lpart0 = 0.f, mrun1 = -INFINITY, lpart1 = 0.f;
   const float cscale = p.scale_log2;
   const float v_scale = p.v_scale;
+  const int rmax = p.rmax;
+
+  // one row's 16-dim chunk kc of q -> the A-fragment pair for that row (zero past nrows)
+  auto load_q = [&](int row, int nrows, int s0, int hgi, int kc, uint32_t& lo, uint32_t& hi) {
+    lo = hi = 0u;
+    if (row >= nrows) return;
+    const int qrow = __ldg(p.qsl + s0 + row / G);
+    const int qh = (hgi * HG + hk) * G + row % G;
+    const T* qp = reinterpret_cast<const T*>(p.q) + (int64_t(qrow) * Hq + qh) * D + 16 * kc;
+    if constexpr (C::kF16) {  // dims 4t .. 4t+3 (see the K fragments); bf16 -> f16, exact in range
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(qp + 4 * t));
+      lo = pack_f16(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+      hi = pack_f16(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+    } else {  // dims 2t, 2t+1 and 8 + 2t, 9 + 2t (the standard fragment)
+      lo = __ldg(reinterpret_cast<const uint32_t*>(qp + 2 * t));
+      hi = __ldg(reinterpret_cast<const uint32_t*>(qp + 8 + 2 * t));
+    }
+  };
 
   int stage = 0;
   uint32_t phase = 0;
@@ -308,29 +448,21 @@ __global__ void __launch_bounds__(9 * 32, 1)
       raise_error(p.err, PA_DEVERR_TIMEOUT);
       return;
     }
-    const StageDesc d = desc[stage];
+    const MmaDesc d = desc[stage];
+    const int nrows = d.nmem * G;
     if (d.flags & kFirst) {
-      const int qrow = __ldg(p.qsl + d.s);
-      const int qh = (d.hg * HG + hk) * G + g;  // this lane's query head (row g)
 #pragma unroll
       for (int kc = 0; kc < C::KC; ++kc) {
-        const T* qp = reinterpret_cast<const T*>(p.q) + (int64_t(qrow) * Hq + qh) * D + 16 * kc;
-        if constexpr (C::kF16) {  // dims 4t .. 4t+3 (see the K fragments); bf16 -> f16, exact in range
-          uint2 w = make_uint2(0u, 0u);
-          if (g < G) w = __ldg(reinterpret_cast<const uint2*>(qp + 4 * t));
-          qa0[kc] = pack_f16(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
-          qa2[kc] = pack_f16(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
-        } else {  // dims 2t, 2t+1 and 8 + 2t, 9 + 2t (the standard fragment)
-          qa0[kc] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 2 * t)) : 0u;
-          qa2[kc] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 8 + 2 * t)) : 0u;
-        }
+        load_q(g, nrows, d.s, d.hg, kc, qa0[kc], qa2[kc]);
+        if constexpr (GROUPED) load_q(g + 8, nrows, d.s, d.hg, kc, qa1[kc], qa3[kc]);
       }
 #pragma unroll
       for (int i = 0; i < C::NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-      mrun = -INFINITY;
-      lpart = 0.f;
-      if constexpr (!C::kF16) {
+      mrun0 = mrun1 = -INFINITY;
+      lpart0 = lpart1 = 0.f;
+      if constexpr (!C::kF16 && !GROUPED) {
         if (p.k_new && (d.flags & kSeqEnd) && lane < kRowChunks) {  // this CTA ends the request
+          const int qrow = __ldg(p.qsl + d.s);
           const int64_t off = (int64_t(qrow) * p.num_kv_heads + d.hg * HG + hk) * D * C::EL + lane * 16;
           knew = __ldg(reinterpret_cast<const uint4*>(p.k_new + off));
           vnew = __ldg(reinterpret_cast<const uint4*>(p.v_new + off));
@@ -339,7 +471,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
     }
     const int valid = (d.flags & kBad) ? 0 : d.valid;
     const uint32_t kb = base + C::k_off(HG, stage), vb = base + C::v_off(HG, stage);
-    if constexpr (!C::kF16) {
+    if constexpr (!C::kF16 && !GROUPED) {
       if (d.wslot >= 0) {  // fused write: the new row into the stage (row valid - 1) and its slot
         if (lane < kRowChunks) {
           const int half = (lane * 16) / 128, ch = ((lane * 16) % 128) / 16;
@@ -375,23 +507,28 @@ __global__ void __launch_bounds__(9 * 32, 1)
     const int lm = lane >> 3, lr = lane & 7;
 #pragma unroll
     for (int kc = 0; kc < C::KC; ++kc) {
+      const uint32_t a1 = GROUPED ? qa1[GROUPED ? kc : 0] : 0u, a3 = GROUPED ? qa3[GROUPED ? kc : 0] : 0u;
       if constexpr (C::kF16) {
         if ((kc & 1) == 0) {  // chunks kc, kc + 1 of tokens 0-7 and 8-15
+          const uint32_t a1n = GROUPED ? qa1[GROUPED ? kc + 1 : 0] : 0u;
+          const uint32_t a3n = GROUPED ? qa3[GROUPED ? kc + 1 : 0] : 0u;
           uint32_t r0, r1, r2, r3;
           ldsm_x4(kb + C::at(HG, 0, (lm & 1) * 8 + lr, hk, kc + (lm >> 1)), r0, r1, r2, r3);
-          mma_16816(sacc[0], qa0[kc], qa2[kc], e4m3x2_to_f16x2(r0 & 0xffffu), e4m3x2_to_f16x2(r0 >> 16), true);
-          mma_16816(sacc[1], qa0[kc], qa2[kc], e4m3x2_to_f16x2(r1 & 0xffffu), e4m3x2_to_f16x2(r1 >> 16), true);
-          mma_16816(sacc2[0], qa0[kc + 1], qa2[kc + 1], e4m3x2_to_f16x2(r2 & 0xffffu), e4m3x2_to_f16x2(r2 >> 16),
+          mma_16816(sacc[0], qa0[kc], a1, qa2[kc], a3, e4m3x2_to_f16x2(r0 & 0xffffu), e4m3x2_to_f16x2(r0 >> 16),
                     true);
-          mma_16816(sacc2[1], qa0[kc + 1], qa2[kc + 1], e4m3x2_to_f16x2(r3 & 0xffffu), e4m3x2_to_f16x2(r3 >> 16),
+          mma_16816(sacc[1], qa0[kc], a1, qa2[kc], a3, e4m3x2_to_f16x2(r1 & 0xffffu), e4m3x2_to_f16x2(r1 >> 16),
                     true);
+          mma_16816(sacc2[0], qa0[kc + 1], a1n, qa2[kc + 1], a3n, e4m3x2_to_f16x2(r2 & 0xffffu),
+                    e4m3x2_to_f16x2(r2 >> 16), true);
+          mma_16816(sacc2[1], qa0[kc + 1], a1n, qa2[kc + 1], a3n, e4m3x2_to_f16x2(r3 & 0xffffu),
+                    e4m3x2_to_f16x2(r3 >> 16), true);
         }
       } else {  // chunk kc: dims 16kc .. 16kc + 15 = 16-byte columns 2kc % 8, +1 of half 16kc / 64
         const int dim = 16 * kc + (lm >> 1) * 8;
         uint32_t r0, r1, r2, r3;
         ldsm_x4(kb + C::at(HG, dim / C::INNER, (lm & 1) * 8 + lr, hk, (dim % C::INNER) / 8), r0, r1, r2, r3);
-        mma_16816((kc & 1) ? sacc2[0] : sacc[0], qa0[kc], qa2[kc], r0, r2, false);
-        mma_16816((kc & 1) ? sacc2[1] : sacc[1], qa0[kc], qa2[kc], r1, r3, false);
+        mma_16816((kc & 1) ? sacc2[0] : sacc[0], qa0[kc], a1, qa2[kc], a3, r0, r2, false);
+        mma_16816((kc & 1) ? sacc2[1] : sacc[1], qa0[kc], a1, qa2[kc], a3, r1, r3, false);
       }
     }
 #pragma unroll
@@ -399,48 +536,78 @@ __global__ void __launch_bounds__(9 * 32, 1)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sacc[jj][e] += sacc2[jj][e];
 
-    // ---- online softmax over the stage's 16 tokens, row g (lanes of a quad share it)
-    float x[2][2];
-    float mx = -INFINITY;
+    // ---- online softmax over the stage's 16 tokens, rows g (c0, c1) and g + 8 (c2, c3);
+    // the lanes of a quad share a row
+    float x[2][4];
+    float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int tok = 8 * jj + 2 * t + e;
-        x[jj][e] = (tok < valid) ? sacc[jj][e] * cscale : -INFINITY;
-        mx = fmaxf(mx, x[jj][e]);
+        const bool in = 8 * jj + 2 * t + e < valid;
+        x[jj][e] = in ? sacc[jj][e] * cscale : -INFINITY;
+        x[jj][2 + e] = in ? sacc[jj][2 + e] * cscale : -INFINITY;
+        mx0 = fmaxf(mx0, x[jj][e]);
+        mx1 = fmaxf(mx1, x[jj][2 + e]);
       }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float mnew = fmaxf(mrun, mx);
-    const float ms = (mnew == -INFINITY) ? 0.f : mnew;
-    const float alpha = ex2_ftz(mrun - ms);
-    float pv[2][2];
-    float psum = 0.f;
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    const float mnew0 = fmaxf(mrun0, mx0);
+    const float ms0 = (mnew0 == -INFINITY) ? 0.f : mnew0;
+    const float alpha0 = ex2_ftz(mrun0 - ms0);
+    float alpha1 = 1.f, ms1 = 0.f;
+    if constexpr (GROUPED) {
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mnew1 = fmaxf(mrun1, mx1);
+      ms1 = (mnew1 == -INFINITY) ? 0.f : mnew1;
+      alpha1 = ex2_ftz(mrun1 - ms1);
+      mrun1 = mnew1;
+    }
+    float pv[2][4];
+    float psum0 = 0.f, psum1 = 0.f;
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        pv[jj][e] = ex2_ftz(x[jj][e] - ms);
-        psum += pv[jj][e];
+        pv[jj][e] = ex2_ftz(x[jj][e] - ms0);
+        psum0 += pv[jj][e];
+        if constexpr (GROUPED) {
+          pv[jj][2 + e] = ex2_ftz(x[jj][2 + e] - ms1);
+          psum1 += pv[jj][2 + e];
+        } else {
+          pv[jj][2 + e] = 0.f;
+        }
       }
-    lpart = lpart * alpha + psum;
-    mrun = mnew;
-    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+    lpart0 = lpart0 * alpha0 + psum0;
+    lpart1 = lpart1 * alpha1 + psum1;
+    mrun0 = mnew0;
+    if (__any_sync(0xffffffffu, alpha0 != 1.f || alpha1 != 1.f)) {
 #pragma unroll
       for (int i = 0; i < C::NT; ++i) {
-        o[i][0] *= alpha;
-        o[i][1] *= alpha;
+        o[i][0] *= alpha0;
+        o[i][1] *= alpha0;
+        o[i][2] *= alpha1;
+        o[i][3] *= alpha1;
       }
     }
-    // P as the A operand of P V: row g, k = tokens 2t, 2t+1 (a0) and 8 + 2t, 9 + 2t (a2)
-    uint32_t pa0, pa2;
+    // P as the A operand of P V: row g, k = tokens 2t, 2t+1 (a0) and 8 + 2t, 9 + 2t (a2);
+    // row g + 8 likewise (a1, a3)
+    uint32_t pa0, pa1 = 0u, pa2, pa3 = 0u;
     if constexpr (C::kF16) {
       pa0 = pack_f16(pv[0][0], pv[0][1]);
       pa2 = pack_f16(pv[1][0], pv[1][1]);
+      if constexpr (GROUPED) {
+        pa1 = pack_f16(pv[0][2], pv[0][3]);
+        pa3 = pack_f16(pv[1][2], pv[1][3]);
+      }
     } else {
       pa0 = pack_bf16(pv[0][0], pv[0][1]);
       pa2 = pack_bf16(pv[1][0], pv[1][1]);
+      if constexpr (GROUPED) {
+        pa1 = pack_bf16(pv[0][2], pv[0][3]);
+        pa3 = pack_bf16(pv[1][2], pv[1][3]);
+      }
     }
 
     // ---- O += P V. Rows of V past `valid` hold stale or unwritten data: zero them in
@@ -469,14 +636,14 @@ __global__ void __launch_bounds__(9 * 32, 1)
         r1 &= hi_mask;
         r2 &= lo_mask;
         r3 &= hi_mask;
-        mma_16816(o[4 * c2 + 0], pa0, pa2, e4m3x2_to_f16x2(prmt(r0, 0u, 0x20u)), e4m3x2_to_f16x2(prmt(r1, 0u, 0x20u)),
-                  true);
-        mma_16816(o[4 * c2 + 1], pa0, pa2, e4m3x2_to_f16x2(prmt(r0, 0u, 0x31u)), e4m3x2_to_f16x2(prmt(r1, 0u, 0x31u)),
-                  true);
-        mma_16816(o[4 * c2 + 2], pa0, pa2, e4m3x2_to_f16x2(prmt(r2, 0u, 0x20u)), e4m3x2_to_f16x2(prmt(r3, 0u, 0x20u)),
-                  true);
-        mma_16816(o[4 * c2 + 3], pa0, pa2, e4m3x2_to_f16x2(prmt(r2, 0u, 0x31u)), e4m3x2_to_f16x2(prmt(r3, 0u, 0x31u)),
-                  true);
+        mma_16816(o[4 * c2 + 0], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(prmt(r0, 0u, 0x20u)),
+                  e4m3x2_to_f16x2(prmt(r1, 0u, 0x20u)), true);
+        mma_16816(o[4 * c2 + 1], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(prmt(r0, 0u, 0x31u)),
+                  e4m3x2_to_f16x2(prmt(r1, 0u, 0x31u)), true);
+        mma_16816(o[4 * c2 + 2], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(prmt(r2, 0u, 0x20u)),
+                  e4m3x2_to_f16x2(prmt(r3, 0u, 0x20u)), true);
+        mma_16816(o[4 * c2 + 3], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(prmt(r2, 0u, 0x31u)),
+                  e4m3x2_to_f16x2(prmt(r3, 0u, 0x31u)), true);
       }
     } else {
       // bf16: a column is 8 dims; matrices (dims 8i | 8i + 8) give b0, b1 of tiles i, i + 1
@@ -486,8 +653,8 @@ __global__ void __launch_bounds__(9 * 32, 1)
         const int dim = 16 * i2 + (mi >> 1) * 8;
         uint32_t r0, r1, r2, r3;
         ldsm_x4_trans(vb + C::at(HG, dim / C::INNER, vtok, hk, (dim % C::INNER) / 8), r0, r1, r2, r3);
-        mma_16816(o[2 * i2], pa0, pa2, r0 & lo_mask, r1 & hi_mask, false);
-        mma_16816(o[2 * i2 + 1], pa0, pa2, r2 & lo_mask, r3 & hi_mask, false);
+        mma_16816(o[2 * i2], pa0, pa1, pa2, pa3, r0 & lo_mask, r1 & hi_mask, false);
+        mma_16816(o[2 * i2 + 1], pa0, pa1, pa2, pa3, r2 & lo_mask, r3 & hi_mask, false);
       }
     }
     __syncwarp();
@@ -499,55 +666,150 @@ __global__ void __launch_bounds__(9 * 32, 1)
 
     if (!(d.flags & kLast)) continue;
 
-    // ================= finalize this request's piece =================
-    float l = lpart;
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    const int qrow = __ldg(p.qsl + d.s);
-    if (g < G) {  // rows past the group's query heads are padding
-    const bool whole = (d.flags & kSeqStart) && (d.flags & kSeqEnd);
-    const int head_in_group = hk * G + g;
-    const int hq = d.hg * HG * G + head_in_group;
-    const float inv = l > 0.f ? v_scale / l : 0.f;
-    const int64_t slot = c + int64_t(d.s) * p.num_hg + d.hg;
-    const int64_t hrow = slot * (int64_t(HG) * G) + head_in_group;
-    if constexpr (C::kF16) {  // lane holds dims 16c + 4t .. + 3: E.c0, O.c0, E.c1, O.c1 of chunk c
-#pragma unroll
-      for (int cc = 0; cc < C::KC; ++cc) {
-        const float f0 = o[2 * cc][0] * inv, f1 = o[2 * cc + 1][0] * inv;
-        const float f2 = o[2 * cc][1] * inv, f3 = o[2 * cc + 1][1] * inv;
-        const int dim = 16 * cc + 4 * t;
-        if (whole) {
-          *reinterpret_cast<uint2*>(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + dim) =
-              make_uint2(pack_bf16(f0, f1), pack_bf16(f2, f3));
-        } else {
-          *reinterpret_cast<float4*>(p.ws_o + hrow * D + dim) = make_float4(f0, f1, f2, f3);
-        }
-      }
-    } else {  // lane holds dims 8i + 2t, 8i + 2t + 1 of every tile i
-#pragma unroll
-      for (int i = 0; i < C::NT; ++i) {
-        const int dim = 8 * i + 2 * t;
-        const float f0 = o[i][0] * inv, f1 = o[i][1] * inv;
-        if (whole) {
-          *reinterpret_cast<uint32_t*>(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + dim) =
-              pack_bf16(f0, f1);
-        } else {
-          *reinterpret_cast<float2*>(p.ws_o + hrow * D + dim) = make_float2(f0, f1);
-        }
-      }
+    // ================= finalize this segment's piece =================
+    float l0 = lpart0, l1 = lpart1;
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    if constexpr (GROUPED) {
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     }
-    if (!whole && t == 0) p.ws_lse[hrow] = (l > 0.f) ? mrun + __log2f(l) : -INFINITY;
+    // `out` directly only when this CTA holds the whole request (no shared part, no cut)
+    const bool whole = (d.flags & kSeqStart) && (d.flags & kSeqEnd) && d.seg >= NG && d.pad == 0;
+    const int64_t slot = c + int64_t(d.seg) * p.num_hg + d.hg;
+#pragma unroll
+    for (int half_row = 0; half_row < (GROUPED ? 2 : 1); ++half_row) {
+      const int row = g + 8 * half_row;
+      if (row < nrows) {
+        const float l = half_row ? l1 : l0;
+        const float mr = half_row ? mrun1 : mrun0;
+        const int qrow = __ldg(p.qsl + d.s + row / G);
+        const int hq = (d.hg * HG + hk) * G + row % G;
+        const float inv = l > 0.f ? v_scale / l : 0.f;
+        const int64_t hrow = (slot * HG + hk) * rmax + row;
+        const int e0 = 2 * half_row;  // o[i][e0], o[i][e0 + 1]: this row's two columns
+        if constexpr (C::kF16) {  // lane holds dims 16c + 4t .. + 3: E.c0, O.c0, E.c1, O.c1 of chunk c
+#pragma unroll
+          for (int cc = 0; cc < C::KC; ++cc) {
+            const float f0 = o[2 * cc][e0] * inv, f1 = o[2 * cc + 1][e0] * inv;
+            const float f2 = o[2 * cc][e0 + 1] * inv, f3 = o[2 * cc + 1][e0 + 1] * inv;
+            const int dim = 16 * cc + 4 * t;
+            if (whole) {
+              *reinterpret_cast<uint2*>(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + dim) =
+                  make_uint2(pack_bf16(f0, f1), pack_bf16(f2, f3));
+            } else {
+              *reinterpret_cast<float4*>(p.ws_o + hrow * D + dim) = make_float4(f0, f1, f2, f3);
+            }
+          }
+        } else {  // lane holds dims 8i + 2t, 8i + 2t + 1 of every tile i
+#pragma unroll
+          for (int i = 0; i < C::NT; ++i) {
+            const int dim = 8 * i + 2 * t;
+            const float f0 = o[i][e0] * inv, f1 = o[i][e0 + 1] * inv;
+            if (whole) {
+              *reinterpret_cast<uint32_t*>(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + dim) =
+                  pack_bf16(f0, f1);
+            } else {
+              *reinterpret_cast<float2*>(p.ws_o + hrow * D + dim) = make_float2(f0, f1);
+            }
+          }
+        }
+        if (!whole && t == 0) p.ws_lse[hrow] = (l > 0.f) ? mr + __log2f(l) : -INFINITY;
+      }
     }
     __syncwarp();
     if (warp == 0 && lane == 0) {
-      const int64_t v = int64_t(d.s) * p.num_hg + d.hg;
+      const int64_t v = int64_t(d.seg) * p.num_hg + d.hg;
       if (d.flags & kSeqStart) {
         p.ws_meta[v].x = int(c);
         p.ws_meta[v].z = pl.units_per_hg;
-        p.ws_meta[v].w = qrow;
+        p.ws_meta[v].w = __ldg(p.qsl + d.s);
       }
       if (d.flags & kSeqEnd) p.ws_meta[v].y = int(c);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- merge with groups
+// One CTA per (request, head group): the request's own pieces and, when its group's shared
+// prefix ran as a segment, that segment's pieces (rows of this member), combined by their
+// log-sum-exps. (Without groups the common merge kernel runs instead.)
+template <typename T, int D>
+__global__ void __launch_bounds__(1024) decode_merge_grouped_kernel(const __grid_constant__ DecodeParams p) {
+  griddep_wait();
+  const int s = blockIdx.x / p.num_hg, hg = blockIdx.x % p.num_hg;
+  const int NG = p.num_groups, G = p.group, HG = p.hg_size;
+  const int vo = (NG + s) * p.num_hg + hg;
+  int4 mo = p.ws_meta[vo];
+  int4 msh = make_int4(-1, -1, 0, 0);
+  int vs = -1, member = 0;
+  const int skip = own_skip(p, s);
+  if (skip > 0) {
+    const int gi = __ldg(p.seq_group + s);
+    int a, b;
+    group_span(p, gi, a, b);
+    member = s - a;
+    vs = gi * p.num_hg + hg;
+    msh = p.ws_meta[vs];
+  } else if (mo.x < 0 || mo.x == mo.y) {
+    return;  // nothing here / one CTA wrote `out` itself
+  }
+  const int q0 = __ldg(p.qsl + s);
+  if (__ldg(p.qsl + s + 1) - q0 != 1 || decode_len(p, s) == 0) return;
+  auto bad = [&](const int4& m) { return m.x >= 0 && (m.y >= p.num_ctas || m.x > m.y || m.z <= 0); };
+  if (bad(mo) || bad(msh) || (skip > 0 && msh.x < 0)) {
+    if (threadIdx.x == 0) raise_error(p.err, PA_DEVERR_TIMEOUT);
+    return;
+  }
+  const int64_t C = p.num_ctas;
+  const int units = mo.x >= 0 ? mo.z : msh.z;
+  const int64_t U = int64_t(units) * p.num_hg;
+  T* out = reinterpret_cast<T*>(p.out);
+  constexpr int D4 = D / 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int n_own = mo.x >= 0 ? mo.y - mo.x + 1 : 0;
+  const int n_sh = (skip > 0 && msh.x >= 0) ? msh.y - msh.x + 1 : 0;
+  const int npieces = n_own + n_sh;
+  // piece i -> (CTA, workspace row base)
+  auto piece = [&](int i, int64_t& cc, int64_t& rowbase) {
+    if (i < n_own) {
+      cc = mo.x + i;
+      rowbase = ((cc + vo) * HG) * p.rmax;
+    } else {
+      cc = msh.x + (i - n_own);
+      rowbase = ((cc + vs) * HG) * p.rmax + member * G;
+    }
+  };
+  for (int head = warp; head < HG * G; head += nwarps) {
+    const int hk = head / G, h = head % G;
+    float M = -INFINITY;
+    for (int i = lane; i < npieces; i += 32) {
+      int64_t cc, rb;
+      piece(i, cc, rb);
+      if (cc * U / C != (cc + 1) * U / C) M = fmaxf(M, p.ws_lse[rb + hk * p.rmax + h]);
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+    const float Ms = (M == -INFINITY) ? 0.f : M;
+    if (lane < D4) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
+      for (int i = 0; i < npieces; ++i) {
+        int64_t cc, rb;
+        piece(i, cc, rb);
+        if (cc * U / C == (cc + 1) * U / C) continue;
+        const int64_t hrow = rb + hk * p.rmax + h;
+        const float w = exp2f(p.ws_lse[hrow] - Ms);
+        const float4 ov = *reinterpret_cast<const float4*>(p.ws_o + hrow * D + lane * 4);
+        acc[0] += w * ov.x;
+        acc[1] += w * ov.y;
+        acc[2] += w * ov.z;
+        acc[3] += w * ov.w;
+        wsum += w;
+      }
+      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] *= inv;
+      RowVec<T, 4>::store(out + (int64_t(q0) * p.num_heads + (hg * HG + hk) * G + h) * D + lane * 4, acc);
     }
   }
 }
@@ -580,7 +842,7 @@ bool make_cache_map(CUtensorMap* m, const void* cache, int el, int D, int64_t sl
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename KV, int D, int BT>
+template <typename KV, int D, int BT, bool GROUPED>
 cudaError_t run(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream) {
   using C = MmaCfg<KV, D, BT>;
   CUtensorMap km, vm;
@@ -589,7 +851,7 @@ cudaError_t run(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream) {
       !make_cache_map(&vm, a.v_cache, C::EL, D, slots, a.num_kv_heads, BT, hg))
     return cudaErrorInvalidValue;
   DecodeParams p = fill_decode_params(a, hg, 1, num_ctas, D);
-  if (C::EL == 2 && a.k_new != nullptr) {
+  if (C::EL == 2 && a.k_new != nullptr && !GROUPED) {
     p.k_new = static_cast<const char*>(a.k_new);
     p.v_new = static_cast<const char*>(a.v_new);
     p.slot_mapping = a.slot_mapping;
@@ -598,13 +860,36 @@ cudaError_t run(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream) {
     p.scale_log2 *= a.k_scale;
     p.v_scale = a.v_scale;
   }
+  if (GROUPED) {  // pieces of every segment, 16 rows a KV head
+    p.seq_group = a.seq_group;
+    p.group_start = a.group_start;
+    p.shared_len = a.shared_len;
+    p.num_groups = a.num_groups;
+    p.rmax = 16;
+    const int64_t nseg = int64_t(a.num_groups) + a.num_seqs;
+    const int64_t pslots = int64_t(num_ctas) + nseg * p.num_hg;
+    const int64_t rows = pslots * hg * 16;
+    char* ws = static_cast<char*>(a.workspace);
+    p.ws_o = reinterpret_cast<float*>(ws);
+    p.ws_lse = reinterpret_cast<float*>(ws + rows * D * 4);
+    p.ws_meta = reinterpret_cast<int4*>(ws + rows * D * 4 + ((rows * 4 + 15) / 16) * 16);
+  }
   const size_t smem = C::total(hg);
-  auto kern = decode_mma_kernel<__nv_bfloat16, D, KV, BT>;
+  auto kern = decode_mma_kernel<__nv_bfloat16, D, KV, BT, GROUPED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_ctas), dim3((hg + 1) * 32), smem, stream, p, km, vm);
   if (e != cudaSuccess) return e;
-  return launch_merge<__nv_bfloat16, D>(p, stream);
+  if (!GROUPED) return launch_merge<__nv_bfloat16, D>(p, stream);
+  const int threads = 32 * (hg * p.group < 32 ? hg * p.group : 32);
+  return launch_pdl(decode_merge_grouped_kernel<__nv_bfloat16, D>, dim3(unsigned(int64_t(a.num_seqs) * p.num_hg)),
+                    dim3(threads), 0, stream, p);
+}
+
+template <typename KV, int D, int BT>
+cudaError_t run_g(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream) {
+  return a.num_groups > 0 ? run<KV, D, BT, true>(a, hg, num_ctas, stream)
+                          : run<KV, D, BT, false>(a, hg, num_ctas, stream);
 }
 
 }  // namespace
@@ -614,6 +899,7 @@ bool decode_mma_supported(const AttnArgs& a, int hg) {
   const int G = a.num_heads / a.num_kv_heads;
   if (a.dtype != PA_BF16 || hg < 1 || G > 8) return false;
   if (a.k_new != nullptr && a.cache_dtype != PA_BF16) return false;  // no fused write into E4M3
+  if (a.k_new != nullptr && a.num_groups > 0) return false;          // nor with groups
   if (!(B == 8 || (B % 16 == 0 && B <= 1024))) return false;
   if (a.num_blocks * B > 0x7fffffff) return false;  // TMA token coordinates are int32
   if (a.cache_dtype == PA_BF16) {
@@ -629,10 +915,21 @@ bool decode_mma_supported(const AttnArgs& a, int hg) {
 cudaError_t launch_decode_mma(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream) {
   const bool bt8 = a.block_size == 8;
   if (a.cache_dtype == PA_FP8_E4M3)
-    return bt8 ? run<Fp8E4M3, 128, 8>(a, hg, num_ctas, stream) : run<Fp8E4M3, 128, 16>(a, hg, num_ctas, stream);
+    return bt8 ? run_g<Fp8E4M3, 128, 8>(a, hg, num_ctas, stream) : run_g<Fp8E4M3, 128, 16>(a, hg, num_ctas, stream);
   if (a.head_dim == 64)
-    return bt8 ? run<__nv_bfloat16, 64, 8>(a, hg, num_ctas, stream) : run<__nv_bfloat16, 64, 16>(a, hg, num_ctas, stream);
-  return bt8 ? run<__nv_bfloat16, 128, 8>(a, hg, num_ctas, stream) : run<__nv_bfloat16, 128, 16>(a, hg, num_ctas, stream);
+    return bt8 ? run_g<__nv_bfloat16, 64, 8>(a, hg, num_ctas, stream)
+               : run_g<__nv_bfloat16, 64, 16>(a, hg, num_ctas, stream);
+  return bt8 ? run_g<__nv_bfloat16, 128, 8>(a, hg, num_ctas, stream)
+             : run_g<__nv_bfloat16, 128, 16>(a, hg, num_ctas, stream);
+}
+
+size_t decode_grouped_workspace_bytes(int num_seqs, int num_groups, int num_kv_heads, int head_dim, int hg,
+                                      int num_ctas) {
+  if (hg < 1) return 0;
+  const int64_t num_hg = num_kv_heads / hg;
+  const int64_t nseg = int64_t(num_groups) + num_seqs;
+  const int64_t rows = (int64_t(num_ctas) + nseg * num_hg) * hg * 16;
+  return size_t(rows * head_dim * 4 + ((rows * 4 + 15) / 16) * 16 + nseg * num_hg * 16);
 }
 
 }  // namespace pa

@@ -61,6 +61,11 @@ struct AttnArgs {
   pa_dtype cache_dtype = PA_BF16;
   float k_scale = 1.f;
   float v_scale = 1.f;
+  // Shared-prefix groups of a decode batch (tensor-core kernel only; see pa_attention_grouped)
+  const int32_t* seq_group = nullptr;
+  const int32_t* group_start = nullptr;
+  const int32_t* shared_len = nullptr;
+  int num_groups = 0;
 };
 
 // Decode (q_len == 1 requests): workspace bytes needed, and the launch (split-K + merge).
@@ -68,6 +73,8 @@ size_t decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int
                               int num_ctas, pa_dtype dtype);
 int decode_num_ctas(int device, cudaError_t* err);
 bool decode_supported(pa_dtype dtype, int head_dim, int group);
+// KV heads per CTA of the decode kernels for this cache type and shape (0: unsupported).
+int decode_hg(pa_dtype cache_dtype, int head_dim, int group, int num_kv_heads);
 cudaError_t launch_decode(const AttnArgs& a, int num_ctas, cudaStream_t stream);
 // The tensor-core decode kernel (bf16 queries; bf16 caches with head_dim 64 / 128, with or
 // without the fused write, or E4M3 caches with head_dim 128; block size 8 or a multiple of
@@ -75,6 +82,9 @@ cudaError_t launch_decode(const AttnArgs& a, int num_ctas, cudaStream_t stream);
 // CUDA-core kernel's head grouping `hg` so the workspace layout is the same.
 bool decode_mma_supported(const AttnArgs& a, int hg);
 cudaError_t launch_decode_mma(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream);
+// Workspace of a grouped decode call (the pieces carry 16 rows per KV head).
+size_t decode_grouped_workspace_bytes(int num_seqs, int num_groups, int num_kv_heads, int head_dim, int hg,
+                                      int num_ctas);
 
 // Prefill (q_len >= 2 requests): the tcgen05 tensor-core kernel where it applies (bf16,
 // block size 8..128 dividing 128, <= 4096 requests), else the CUDA-core tile kernel.

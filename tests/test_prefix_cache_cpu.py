@@ -157,3 +157,38 @@ def test_system_prompt_script_matches_oracle(size, caching):
     if caching:
         cached, hits, evictions = bm.prefix_stats()
         assert hits == wl.meta["requests"] * (P // B) and evictions == 0
+
+
+def test_batch_groups_from_shared_tables():
+    """pa_bm_batch_groups on the shared-prefix workload: each prompt's samples form a group
+    whose shared length is the longest run of identical leading blocks (brute force over
+    the oracle's tables), capped by the shortest member."""
+    import workloads
+    from oracle import run_allocator
+
+    wl = workloads.build(4, "small")
+    ref, _, _ = run_allocator(wl)
+    bm = pa.BlockManager(wl.num_blocks, wl.spec.block_size, wl.free_order)
+    for ph in wl.phases():
+        for op in ph.ops:
+            if op[0] == "add":
+                bm.add_seq(op[1])
+            elif op[0] == "fork":
+                bm.fork(op[1], op[2])
+            else:
+                bm.append(op[1], op[2])
+        bm.take_copies()
+    seqs = [s for s, _ in wl.step.batch]
+    sg, gr, sl = bm.batch_groups(seqs, max_members=4)
+    n_samp = wl.meta["samples"]
+    assert len(gr) == wl.meta["prompts"]
+    B = wl.spec.block_size
+    for g, (a, b) in enumerate(gr.tolist()):
+        assert b - a == n_samp and all(sg[a:b] == g)
+        tabs = [ref.block_table(seqs[i]) for i in range(a, b)]
+        k = 0
+        while all(len(t) > k for t in tabs) and len({t[k] for t in tabs}) == 1:
+            k += 1
+        assert sl[g] == min(k * B, min(ref.seq_len(seqs[i]) for i in range(a, b)))
+    sg2, gr2, _ = bm.batch_groups(seqs, max_members=2)
+    assert len(gr2) == 2 * wl.meta["prompts"] and (gr2[:, 1] - gr2[:, 0] == 2).all()
