@@ -39,7 +39,7 @@ METRIC = "paged decode attention: K/V GB/s (% of GB300 HBM peak) and tokens/s, b
 #       python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-e2e
 # It holds only for the kernel sources it was measured on (their SHA-256 below); any
 # change to them makes the reported traffic null until it is measured again.
-DECODE_TRAFFIC = {"sources_sha256": "b3351229f7da09b20cc21e262c1f8344da0a2c7c52c32eb5f78a2bcbea6c4d70", "bytes": 1653273856}
+DECODE_TRAFFIC = {"sources_sha256": "36af42b7c62a87bc4c671f78b17f4712fb5cfd78a03faf70446d755c18d78f69", "bytes": 1653317376}
 DECODE_SOURCES = ["paged_kv_cache_161_gb300/csrc/decode_attention.cu", "paged_kv_cache_161_gb300/csrc/decode_mma.cu",
                   "paged_kv_cache_161_gb300/csrc/decode_common.cuh", "paged_kv_cache_161_gb300/csrc/common.cuh"]
 
@@ -656,7 +656,26 @@ def run_secondary(a):
         wr_ms = timed(lambda: pa.kv_write(st.k_new, st.v_new, dw.k_cache, dw.v_cache, st.slot_mapping,
                                           stream=stream), steps, a.warmup)
         wr_bytes = 2 * int(st.slot_mapping.shape[0]) * sp.kv_token_bytes
+        # grouped decode: each group's shared prefix read once, members' own tails separately
+        seqs = [s for s, _ in wl.step.batch]
+        sg, gr, sl = dw.bm.batch_groups(seqs, 4)
+        sg_d, gr_d, sl_d = (torch.from_numpy(x).to(dev) for x in (sg, gr, sl))
+        gws = torch.zeros(pa.attention_grouped_workspace_size(len(seqs), len(sl), sp.num_heads, sp.num_kv_heads,
+                                                              sp.head_dim), dtype=torch.uint8, device=dev)
+        gout = torch.empty_like(st.out)
+        grp = lambda: pa.attention_grouped(gout, st.q, dw.k_cache, dw.v_cache, st.block_table, st.seq_lens,  # noqa: E731
+                                           st.query_start_loc, sg_d, gr_d, sl_d, max_seq_len=st.max_seq_len,
+                                           scale=sp.scale, workspace=gws, stream=stream)
+        grp_ms = timed(grp, steps, a.warmup)
+        shared_tok = sum(int(sl[g]) for g in range(len(sl)))
+        own_tok = sum(int(lens[i]) - (int(sl[sg[i]]) if sg[i] >= 0 else 0) for i in range(len(seqs)))
+        grp_read = (shared_tok + own_tok) * sp.kv_token_bytes
         line.update({
+            "grouped": {"groups": int(len(sl)), "members": int((sg >= 0).sum()), "ms": grp_ms,
+                        "speedup_vs_attention": attn_ms / grp_ms,
+                        "kv_bytes_read": grp_read, "gbs_read": grp_read / (grp_ms * 1e-3) / 1e9,
+                        "frac_read": grp_read / (grp_ms * 1e-3) / 1e9 / hbm,
+                        "gbs_unique": uniq / (grp_ms * 1e-3) / 1e9, "frac_unique": uniq / (grp_ms * 1e-3) / 1e9 / hbm},
             "attention_gbs_unique": uniq / (attn_ms * 1e-3) / 1e9, "frac_unique": uniq / (attn_ms * 1e-3) / 1e9 / hbm,
             "copy_blocks": {"pairs": int(pairs.shape[0]), "ms": cp_ms, "gbs": cp_bytes / (cp_ms * 1e-3) / 1e9,
                             "bytes": cp_bytes},

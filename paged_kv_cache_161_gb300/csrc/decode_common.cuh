@@ -255,10 +255,12 @@ __device__ __forceinline__ float pick(const float (&a)[G], int g) {
 // ---------------------------------------------------------------- merge of the pieces
 // One CTA per (head group, request). It reads the request's descriptor written by the
 // split-K kernel and leaves at once unless the request was cut into pieces; then warp w
-// merges heads w, w + nwarps, ...: lanes read the pieces' log-sum-exps in parallel for the
-// max, and each lane accumulates its 4 dims over the pieces with independent float4 loads.
+// merges heads w, w + nwarps, ...: lane i reads piece i's log-sum-exp (32 pieces at a
+// time) for the max and the weights, which reach the other lanes by shuffles, and each
+// lane accumulates its 4 dims over the pieces four at a time, their loads issued together.
 template <typename T, int D>
 __global__ void __launch_bounds__(1024) decode_merge_kernel(const __grid_constant__ DecodeParams p, int group) {
+  griddep_launch_dependents();  // the next kernel may be scheduled; it still waits for this grid
   griddep_wait();  // the split-K grid's pieces and descriptors must be complete and visible
   const int v = blockIdx.x;
   const int hg = v % p.num_hg;
@@ -273,34 +275,48 @@ __global__ void __launch_bounds__(1024) decode_merge_kernel(const __grid_constan
   const int qrow = meta.w;
   T* out = reinterpret_cast<T*>(p.out);
   constexpr int D4 = D / 4;
-  // CTAs whose range is empty (fewer units than CTAs) left no piece: skip them.
+  // CTAs whose range is empty (fewer units than CTAs) left no piece: weight 0, not read.
   const int64_t U = int64_t(meta.z) * p.num_hg, C = p.num_ctas;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int npieces = meta.y - meta.x + 1;
+  auto lse_of = [&](int i, int head) {  // piece i's log-sum-exp, -inf for an empty range
+    const int64_t cc = meta.x + i;
+    return (cc * U / C != (cc + 1) * U / C) ? p.ws_lse[(cc + v) * HGG + head] : -INFINITY;
+  };
   for (int head = warp; head < HGG; head += nwarps) {
-    float M = -INFINITY;
-    for (int i = lane; i < npieces; i += 32) {
-      const int64_t cc = meta.x + i;
-      if (cc * U / C != (cc + 1) * U / C) M = fmaxf(M, p.ws_lse[(cc + v) * HGG + head]);
-    }
+    float l0 = lane < npieces ? lse_of(lane, head) : -INFINITY;  // pieces 0..31, kept
+    float M = l0;
+    for (int i = 32 + lane; i < npieces; i += 32) M = fmaxf(M, lse_of(i, head));
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
     const float Ms = (M == -INFINITY) ? 0.f : M;
-    if (lane < D4) {
-      float a[4] = {0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
-#pragma unroll 4
-      for (int i = 0; i < npieces; ++i) {
-        const int64_t cc = meta.x + i;
-        if (cc * U / C == (cc + 1) * U / C) continue;
-        const int64_t hrow = (cc + v) * HGG + head;
-        const float w = exp2f(p.ws_lse[hrow] - Ms);
-        const float4 o = *reinterpret_cast<const float4*>(p.ws_o + hrow * D + lane * 4);
-        a[0] += w * o.x;
-        a[1] += w * o.y;
-        a[2] += w * o.z;
-        a[3] += w * o.w;
-        wsum += w;
+    float a[4] = {0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
+    for (int i0 = 0; i0 < npieces; i0 += 32) {
+      const float lw = (i0 == 0) ? l0 : (i0 + lane < npieces ? lse_of(i0 + lane, head) : -INFINITY);
+      const float wl = exp2f(lw - Ms);  // 0 for an empty range or an empty piece
+      const int n = min(32, npieces - i0);
+      for (int b = 0; b < n; b += 4) {
+        float w[4];
+        float4 o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          w[q] = __shfl_sync(0xffffffffu, wl, b + q);
+          if (b + q >= n) w[q] = 0.f;
+          o[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (lane < D4 && w[q] > 0.f)
+            o[q] = *reinterpret_cast<const float4*>(p.ws_o + ((meta.x + i0 + b + q + v) * HGG + head) * D + lane * 4);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          a[0] += w[q] * o[q].x;
+          a[1] += w[q] * o[q].y;
+          a[2] += w[q] * o[q].z;
+          a[3] += w[q] * o[q].w;
+          wsum += w[q];
+        }
       }
+    }
+    if (lane < D4) {
       const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) a[e] *= inv;

@@ -736,6 +736,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
 // log-sum-exps. (Without groups the common merge kernel runs instead.)
 template <typename T, int D>
 __global__ void __launch_bounds__(1024) decode_merge_grouped_kernel(const __grid_constant__ DecodeParams p) {
+  griddep_launch_dependents();  // the next kernel may be scheduled; it still waits for this grid
   griddep_wait();
   const int s = blockIdx.x / p.num_hg, hg = blockIdx.x % p.num_hg;
   const int NG = p.num_groups, G = p.group, HG = p.hg_size;
