@@ -424,20 +424,30 @@ __global__ void __launch_bounds__(9 * 32, 1)
   const float v_scale = p.v_scale;
   const int rmax = p.rmax;
 
-  // one row's 16-dim chunk kc of q -> the A-fragment pair for that row (zero past nrows)
-  auto load_q = [&](int row, int nrows, int s0, int hgi, int kc, uint32_t& lo, uint32_t& hi) {
-    lo = hi = 0u;
-    if (row >= nrows) return;
-    const int qrow = __ldg(p.qsl + s0 + row / G);
-    const int qh = (hgi * HG + hk) * G + row % G;
-    const T* qp = reinterpret_cast<const T*>(p.q) + (int64_t(qrow) * Hq + qh) * D + 16 * kc;
+  // All KC chunks of one MMA row of q -> its A fragments (zero past nrows): the row's
+  // token is looked up once, then every chunk's load is issued before any is used.
+  auto load_q = [&](int row, int nrows, int s0, int hgi, uint32_t (&lo)[C::KC], uint32_t (&hi)[C::KC]) {
+    const bool have = row < nrows;
+    const int r = have ? row : 0;
+    const int qrow = have ? __ldg(p.qsl + s0 + r / G) : 0;
+    const int qh = (hgi * HG + hk) * G + r % G;
+    const T* qp = reinterpret_cast<const T*>(p.q) + (int64_t(qrow) * Hq + qh) * D;
     if constexpr (C::kF16) {  // dims 4t .. 4t+3 (see the K fragments); bf16 -> f16, exact in range
-      const uint2 w = __ldg(reinterpret_cast<const uint2*>(qp + 4 * t));
-      lo = pack_f16(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
-      hi = pack_f16(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+      uint2 w[C::KC];
+#pragma unroll
+      for (int kc = 0; kc < C::KC; ++kc)
+        w[kc] = have ? __ldg(reinterpret_cast<const uint2*>(qp + 16 * kc + 4 * t)) : make_uint2(0u, 0u);
+#pragma unroll
+      for (int kc = 0; kc < C::KC; ++kc) {
+        lo[kc] = pack_f16(__uint_as_float(w[kc].x << 16), __uint_as_float(w[kc].x & 0xffff0000u));
+        hi[kc] = pack_f16(__uint_as_float(w[kc].y << 16), __uint_as_float(w[kc].y & 0xffff0000u));
+      }
     } else {  // dims 2t, 2t+1 and 8 + 2t, 9 + 2t (the standard fragment)
-      lo = __ldg(reinterpret_cast<const uint32_t*>(qp + 2 * t));
-      hi = __ldg(reinterpret_cast<const uint32_t*>(qp + 8 + 2 * t));
+#pragma unroll
+      for (int kc = 0; kc < C::KC; ++kc) {
+        lo[kc] = have ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * kc + 2 * t)) : 0u;
+        hi[kc] = have ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * kc + 8 + 2 * t)) : 0u;
+      }
     }
   };
 
@@ -451,11 +461,8 @@ __global__ void __launch_bounds__(9 * 32, 1)
     const MmaDesc d = desc[stage];
     const int nrows = d.nmem * G;
     if (d.flags & kFirst) {
-#pragma unroll
-      for (int kc = 0; kc < C::KC; ++kc) {
-        load_q(g, nrows, d.s, d.hg, kc, qa0[kc], qa2[kc]);
-        if constexpr (GROUPED) load_q(g + 8, nrows, d.s, d.hg, kc, qa1[kc], qa3[kc]);
-      }
+      load_q(g, nrows, d.s, d.hg, qa0, qa2);
+      if constexpr (GROUPED) load_q(g + 8, nrows, d.s, d.hg, qa1, qa3);
 #pragma unroll
       for (int i = 0; i < C::NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
       mrun0 = mrun1 = -INFINITY;
@@ -536,8 +543,9 @@ __global__ void __launch_bounds__(9 * 32, 1)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sacc[jj][e] += sacc2[jj][e];
 
-    // ---- online softmax over the stage's 16 tokens, rows g (c0, c1) and g + 8 (c2, c3);
-    // the lanes of a quad share a row
+    // ---- online softmax over the stage's 16 tokens, rows g (c0, c1) and, GROUPED, g + 8
+    // (c2, c3); the lanes of a quad share a row. Without groups nothing of row g + 8 is
+    // computed (its MMA rows are zero padding).
     float x[2][4];
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -546,9 +554,11 @@ __global__ void __launch_bounds__(9 * 32, 1)
       for (int e = 0; e < 2; ++e) {
         const bool in = 8 * jj + 2 * t + e < valid;
         x[jj][e] = in ? sacc[jj][e] * cscale : -INFINITY;
-        x[jj][2 + e] = in ? sacc[jj][2 + e] * cscale : -INFINITY;
         mx0 = fmaxf(mx0, x[jj][e]);
-        mx1 = fmaxf(mx1, x[jj][2 + e]);
+        if constexpr (GROUPED) {
+          x[jj][2 + e] = in ? sacc[jj][2 + e] * cscale : -INFINITY;
+          mx1 = fmaxf(mx1, x[jj][2 + e]);
+        }
       }
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
@@ -575,20 +585,28 @@ __global__ void __launch_bounds__(9 * 32, 1)
         if constexpr (GROUPED) {
           pv[jj][2 + e] = ex2_ftz(x[jj][2 + e] - ms1);
           psum1 += pv[jj][2 + e];
-        } else {
-          pv[jj][2 + e] = 0.f;
         }
       }
     lpart0 = lpart0 * alpha0 + psum0;
-    lpart1 = lpart1 * alpha1 + psum1;
     mrun0 = mnew0;
-    if (__any_sync(0xffffffffu, alpha0 != 1.f || alpha1 != 1.f)) {
+    if constexpr (GROUPED) {
+      lpart1 = lpart1 * alpha1 + psum1;
+      if (__any_sync(0xffffffffu, alpha0 != 1.f || alpha1 != 1.f)) {
 #pragma unroll
-      for (int i = 0; i < C::NT; ++i) {
-        o[i][0] *= alpha0;
-        o[i][1] *= alpha0;
-        o[i][2] *= alpha1;
-        o[i][3] *= alpha1;
+        for (int i = 0; i < C::NT; ++i) {
+          o[i][0] *= alpha0;
+          o[i][1] *= alpha0;
+          o[i][2] *= alpha1;
+          o[i][3] *= alpha1;
+        }
+      }
+    } else {
+      if (__any_sync(0xffffffffu, alpha0 != 1.f)) {
+#pragma unroll
+        for (int i = 0; i < C::NT; ++i) {
+          o[i][0] *= alpha0;
+          o[i][1] *= alpha0;
+        }
       }
     }
     // P as the A operand of P V: row g, k = tokens 2t, 2t+1 (a0) and 8 + 2t, 9 + 2t (a2);
