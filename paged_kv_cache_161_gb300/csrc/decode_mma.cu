@@ -299,6 +299,11 @@ __global__ void __launch_bounds__(9 * 32, 1)
       }
     };
     open_segment(k);
+    // block ids come from a window of 32 consecutive entries of the walked request's table
+    // row, one entry a lane, refilled when a stage's boxes leave it (once per 32 blocks or
+    // segment) instead of one dependent load per stage
+    int win_s = -1, win_base = 0;
+    int32_t win = -1;
     int stage = 0;
     uint32_t phase = 0;
     for (int64_t u = u_begin; u < u_end; ++u) {
@@ -340,11 +345,18 @@ __global__ void __launch_bounds__(9 * 32, 1)
         }
       }
       // lane b < NBOX: the box of tokens [pos0 + b * BT, pos0 + b * BT + BT) (one block)
+      const int bi0 = pos0 / B, bi_last = (pos0 + (C::NBOX - 1) * BT) / B;  // table indices of the boxes
+      if (s != win_s || bi0 < win_base || bi_last >= win_base + 32) {  // warp-uniform
+        win_s = s;
+        win_base = bi0;
+        win = win_base + lane < p.max_blocks_per_seq ? __ldg(bt + win_base + lane) : -1;
+      }
+      const int32_t blk_l = __shfl_sync(0xffffffffu, win, (pos0 + min(lane, C::NBOX - 1) * BT) / B - win_base);
       bool have = false, bad = false;
       int y = 0;
       if (lane < C::NBOX && lane * BT < valid) {
         const int pos = pos0 + lane * BT;
-        const int64_t blk = __ldg(bt + pos / B);
+        const int64_t blk = blk_l;
         bad = blk < 0 || blk >= p.num_blocks;
         have = !bad;
         y = int(blk * B + pos % B);
@@ -749,32 +761,54 @@ __global__ void __launch_bounds__(9 * 32, 1)
 }
 
 // ---------------------------------------------------------------- merge with groups
+// Keys of request s as decode_len counts them, without raising errors (the split-K kernel
+// has raised them already).
+__device__ __forceinline__ int decode_len_quiet(const DecodeParams& p, int s) {
+  if (__ldg(p.qsl + s + 1) - __ldg(p.qsl + s) != 1) return 0;
+  const int L = min(__ldg(p.seq_lens + s), p.max_blocks_per_seq * p.block_size);
+  return L > 0 ? L : 0;
+}
+
 // One CTA per (request, head group): the request's own pieces and, when its group's shared
 // prefix ran as a segment, that segment's pieces (rows of this member), combined by their
-// log-sum-exps. (Without groups the common merge kernel runs instead.)
+// log-sum-exps. (Without groups the common merge kernel runs instead.) Loads that do not
+// depend on one another are issued together -- the request's descriptor, group and length;
+// then the group's span, shared length and descriptor; then the members' lengths, one lane
+// each -- and the pieces are merged as in the common merge kernel.
 template <typename T, int D>
 __global__ void __launch_bounds__(1024) decode_merge_grouped_kernel(const __grid_constant__ DecodeParams p) {
   griddep_launch_dependents();  // the next kernel may be scheduled; it still waits for this grid
   griddep_wait();
   const int s = blockIdx.x / p.num_hg, hg = blockIdx.x % p.num_hg;
   const int NG = p.num_groups, G = p.group, HG = p.hg_size;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int vo = (NG + s) * p.num_hg + hg;
-  int4 mo = p.ws_meta[vo];
+  const int4 mo = p.ws_meta[vo];
+  const int gi = NG > 0 ? __ldg(p.seq_group + s) : -1;
+  const int Ls = decode_len_quiet(p, s);
+  const int q0 = __ldg(p.qsl + s);
+  // the shared segment this request's leading chunks ran in (own_skip of the split-K kernel)
+  int skip = 0, member = 0, vs = -1;
   int4 msh = make_int4(-1, -1, 0, 0);
-  int vs = -1, member = 0;
-  const int skip = own_skip(p, s);
-  if (skip > 0) {
-    const int gi = __ldg(p.seq_group + s);
+  if (gi >= 0 && gi < NG) {
     int a, b;
     group_span(p, gi, a, b);
-    member = s - a;
-    vs = gi * p.num_hg + hg;
-    msh = p.ws_meta[vs];
-  } else if (mo.x < 0 || mo.x == mo.y) {
-    return;  // nothing here / one CTA wrote `out` itself
+    const int shl = __ldg(p.shared_len + gi);
+    const int4 m = p.ws_meta[gi * p.num_hg + hg];
+    if (s >= a && s < b && b - a >= 2 && (b - a) * G <= 16) {  // at most 8 members
+      int lim = lane < b - a ? decode_len_quiet(p, a + lane) : INT_MAX;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) lim = min(lim, __shfl_xor_sync(0xffffffffu, lim, o));
+      skip = max(min(lim, shl), 0) / kTPS;
+      if (skip > 0) {
+        member = s - a;
+        vs = gi * p.num_hg + hg;
+        msh = m;
+      }
+    }
   }
-  const int q0 = __ldg(p.qsl + s);
-  if (__ldg(p.qsl + s + 1) - q0 != 1 || decode_len(p, s) == 0) return;
+  if (skip == 0 && (mo.x < 0 || mo.x == mo.y)) return;  // nothing here / one CTA wrote `out` itself
+  if (Ls == 0) return;
   auto bad = [&](const int4& m) { return m.x >= 0 && (m.y >= p.num_ctas || m.x > m.y || m.z <= 0); };
   if (bad(mo) || bad(msh) || (skip > 0 && msh.x < 0)) {
     if (threadIdx.x == 0) raise_error(p.err, PA_DEVERR_TIMEOUT);
@@ -785,46 +819,61 @@ __global__ void __launch_bounds__(1024) decode_merge_grouped_kernel(const __grid
   const int64_t U = int64_t(units) * p.num_hg;
   T* out = reinterpret_cast<T*>(p.out);
   constexpr int D4 = D / 4;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int n_own = mo.x >= 0 ? mo.y - mo.x + 1 : 0;
   const int n_sh = (skip > 0 && msh.x >= 0) ? msh.y - msh.x + 1 : 0;
   const int npieces = n_own + n_sh;
-  // piece i -> (CTA, workspace row base)
-  auto piece = [&](int i, int64_t& cc, int64_t& rowbase) {
-    if (i < n_own) {
-      cc = mo.x + i;
-      rowbase = ((cc + vo) * HG) * p.rmax;
-    } else {
-      cc = msh.x + (i - n_own);
-      rowbase = ((cc + vs) * HG) * p.rmax + member * G;
-    }
+  // piece i -> its workspace row base, or -1 for a CTA whose range is empty (no piece)
+  auto piece_row = [&](int i) -> int64_t {
+    const bool own = i < n_own;
+    const int64_t cc = own ? mo.x + i : msh.x + (i - n_own);
+    if (cc * U / C == (cc + 1) * U / C) return -1;
+    return own ? ((cc + vo) * HG) * p.rmax : ((cc + vs) * HG) * p.rmax + member * G;
   };
   for (int head = warp; head < HG * G; head += nwarps) {
-    const int hk = head / G, h = head % G;
-    float M = -INFINITY;
-    for (int i = lane; i < npieces; i += 32) {
-      int64_t cc, rb;
-      piece(i, cc, rb);
-      if (cc * U / C != (cc + 1) * U / C) M = fmaxf(M, p.ws_lse[rb + hk * p.rmax + h]);
+    const int hk = head / G, h = head % G, off = hk * p.rmax + h;
+    // lane i: piece i's row and log-sum-exp (32 pieces at a time)
+    int64_t r0 = lane < npieces ? piece_row(lane) : -1;
+    float l0 = r0 >= 0 ? p.ws_lse[r0 + off] : -INFINITY;
+    float M = l0;
+    for (int i = 32 + lane; i < npieces; i += 32) {
+      const int64_t r = piece_row(i);
+      if (r >= 0) M = fmaxf(M, p.ws_lse[r + off]);
     }
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
     const float Ms = (M == -INFINITY) ? 0.f : M;
-    if (lane < D4) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
-      for (int i = 0; i < npieces; ++i) {
-        int64_t cc, rb;
-        piece(i, cc, rb);
-        if (cc * U / C == (cc + 1) * U / C) continue;
-        const int64_t hrow = rb + hk * p.rmax + h;
-        const float w = exp2f(p.ws_lse[hrow] - Ms);
-        const float4 ov = *reinterpret_cast<const float4*>(p.ws_o + hrow * D + lane * 4);
-        acc[0] += w * ov.x;
-        acc[1] += w * ov.y;
-        acc[2] += w * ov.z;
-        acc[3] += w * ov.w;
-        wsum += w;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
+    for (int i0 = 0; i0 < npieces; i0 += 32) {
+      int64_t rl = r0;
+      float ll = l0;
+      if (i0 > 0) {
+        rl = i0 + lane < npieces ? piece_row(i0 + lane) : -1;
+        ll = rl >= 0 ? p.ws_lse[rl + off] : -INFINITY;
       }
+      const float wl = exp2f(ll - Ms);  // 0 for an empty range or an empty piece
+      const int n = min(32, npieces - i0);
+      for (int b = 0; b < n; b += 4) {
+        float w[4];
+        float4 ov[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          w[q] = __shfl_sync(0xffffffffu, wl, b + q);
+          const int64_t rq = __shfl_sync(0xffffffffu, rl, b + q);
+          if (b + q >= n) w[q] = 0.f;
+          ov[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (lane < D4 && w[q] > 0.f) ov[q] = *reinterpret_cast<const float4*>(p.ws_o + (rq + off) * D + lane * 4);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[0] += w[q] * ov[q].x;
+          acc[1] += w[q] * ov[q].y;
+          acc[2] += w[q] * ov[q].z;
+          acc[3] += w[q] * ov[q].w;
+          wsum += w[q];
+        }
+      }
+    }
+    if (lane < D4) {
       const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[e] *= inv;
