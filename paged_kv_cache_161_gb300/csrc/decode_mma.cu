@@ -89,10 +89,11 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return r;
 }
 // two E4M3 codes (low 16 bits, low byte first) -> f16x2, exact
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
-  uint32_t h2;
-  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h2) : "r"(codes));
-  return h2;
+// The four E4M3 codes of x -> f16x2 of codes (0, 1) and of codes (2, 3) (exact).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& c01, uint32_t& c23) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(c01), "=r"(c23)
+      : "r"(x));
 }
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
@@ -533,14 +534,15 @@ __global__ void __launch_bounds__(9 * 32, 1)
           const uint32_t a3n = GROUPED ? qa3[GROUPED ? kc + 1 : 0] : 0u;
           uint32_t r0, r1, r2, r3;
           ldsm_x4(kb + C::at(HG, 0, (lm & 1) * 8 + lr, hk, kc + (lm >> 1)), r0, r1, r2, r3);
-          mma_16816(sacc[0], qa0[kc], a1, qa2[kc], a3, e4m3x2_to_f16x2(r0 & 0xffffu), e4m3x2_to_f16x2(r0 >> 16),
-                    true);
-          mma_16816(sacc[1], qa0[kc], a1, qa2[kc], a3, e4m3x2_to_f16x2(r1 & 0xffffu), e4m3x2_to_f16x2(r1 >> 16),
-                    true);
-          mma_16816(sacc2[0], qa0[kc + 1], a1n, qa2[kc + 1], a3n, e4m3x2_to_f16x2(r2 & 0xffffu),
-                    e4m3x2_to_f16x2(r2 >> 16), true);
-          mma_16816(sacc2[1], qa0[kc + 1], a1n, qa2[kc + 1], a3n, e4m3x2_to_f16x2(r3 & 0xffffu),
-                    e4m3x2_to_f16x2(r3 >> 16), true);
+          uint32_t k0l, k0h, k1l, k1h, k2l, k2h, k3l, k3h;
+          e4m3x4_to_f16x2x2(r0, k0l, k0h);
+          e4m3x4_to_f16x2x2(r1, k1l, k1h);
+          e4m3x4_to_f16x2x2(r2, k2l, k2h);
+          e4m3x4_to_f16x2x2(r3, k3l, k3h);
+          mma_16816(sacc[0], qa0[kc], a1, qa2[kc], a3, k0l, k0h, true);
+          mma_16816(sacc[1], qa0[kc], a1, qa2[kc], a3, k1l, k1h, true);
+          mma_16816(sacc2[0], qa0[kc + 1], a1n, qa2[kc + 1], a3n, k2l, k2h, true);
+          mma_16816(sacc2[1], qa0[kc + 1], a1n, qa2[kc + 1], a3n, k3l, k3h, true);
         }
       } else {  // chunk kc: dims 16kc .. 16kc + 15 = 16-byte columns 2kc % 8, +1 of half 16kc / 64
         const int dim = 16 * kc + (lm >> 1) * 8;
@@ -666,14 +668,17 @@ __global__ void __launch_bounds__(9 * 32, 1)
         r1 &= hi_mask;
         r2 &= lo_mask;
         r3 &= hi_mask;
-        mma_16816(o[4 * c2 + 0], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(prmt(r0, 0u, 0x20u)),
-                  e4m3x2_to_f16x2(prmt(r1, 0u, 0x20u)), true);
-        mma_16816(o[4 * c2 + 1], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(prmt(r0, 0u, 0x31u)),
-                  e4m3x2_to_f16x2(prmt(r1, 0u, 0x31u)), true);
-        mma_16816(o[4 * c2 + 2], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(prmt(r2, 0u, 0x20u)),
-                  e4m3x2_to_f16x2(prmt(r3, 0u, 0x20u)), true);
-        mma_16816(o[4 * c2 + 3], pa0, pa1, pa2, pa3, e4m3x2_to_f16x2(prmt(r2, 0u, 0x31u)),
-                  e4m3x2_to_f16x2(prmt(r3, 0u, 0x31u)), true);
+        // codes (0, 1) and (2, 3) of each register to f16x2, then the E / O token pairs
+        // (codes 0, 2 and 1, 3) by permuting the f16 halves
+        uint32_t v0l, v0h, v1l, v1h, v2l, v2h, v3l, v3h;
+        e4m3x4_to_f16x2x2(r0, v0l, v0h);
+        e4m3x4_to_f16x2x2(r1, v1l, v1h);
+        e4m3x4_to_f16x2x2(r2, v2l, v2h);
+        e4m3x4_to_f16x2x2(r3, v3l, v3h);
+        mma_16816(o[4 * c2 + 0], pa0, pa1, pa2, pa3, prmt(v0l, v0h, 0x5410u), prmt(v1l, v1h, 0x5410u), true);
+        mma_16816(o[4 * c2 + 1], pa0, pa1, pa2, pa3, prmt(v0l, v0h, 0x7632u), prmt(v1l, v1h, 0x7632u), true);
+        mma_16816(o[4 * c2 + 2], pa0, pa1, pa2, pa3, prmt(v2l, v2h, 0x5410u), prmt(v3l, v3h, 0x5410u), true);
+        mma_16816(o[4 * c2 + 3], pa0, pa1, pa2, pa3, prmt(v2l, v2h, 0x7632u), prmt(v3l, v3h, 0x7632u), true);
       }
     } else {
       // bf16: a column is 8 dims; matrices (dims 8i | 8i + 8) give b0, b1 of tiles i, i + 1
