@@ -58,6 +58,17 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
                : "memory");
 }
 
+// Two 16x16 byte matrices, transposed: lanes 0-15 address rows 0-15 of the first, lanes
+// 16-31 those of the second; lane (g, t) = (l / 4, l % 4) gets rows 4t .. 4t+3 of column g
+// (r0) and of column g + 8 (r1) of the first, the same of the second in r2, r3.
+__device__ __forceinline__ void ldsm_b8_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                 uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
 // Four 8x8 16-bit matrices: thread l gets (row l/4, cols 2(l%4), 2(l%4)+1) of each.
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -66,16 +77,6 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                : "memory");
 }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
-  return v;
-}
 
 // two fp32 -> packed bf16x2 / f16x2 (lo in the low half), round to nearest even
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -94,11 +95,6 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& c01, uin
   asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
       : "=r"(c01), "=r"(c23)
       : "r"(x));
-}
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
 }
 
 // ---------------------------------------------------------------- layout
@@ -533,7 +529,9 @@ __global__ void __launch_bounds__(9 * 32, 1)
           const uint32_t a1n = GROUPED ? qa1[GROUPED ? kc + 1 : 0] : 0u;
           const uint32_t a3n = GROUPED ? qa3[GROUPED ? kc + 1 : 0] : 0u;
           uint32_t r0, r1, r2, r3;
-          ldsm_x4(kb + C::at(HG, 0, (lm & 1) * 8 + lr, hk, kc + (lm >> 1)), r0, r1, r2, r3);
+          // token rows: tile 0 = tokens 0, 1, 4, 5, .., tile 1 = 2, 3, 6, 7, ..: the lane's
+          // scores then cover tokens 4t .. 4t+3, the order in which P V reads V (below)
+          ldsm_x4(kb + C::at(HG, 0, 4 * (lr >> 1) + (lr & 1) + 2 * (lm & 1), hk, kc + (lm >> 1)), r0, r1, r2, r3);
           uint32_t k0l, k0h, k1l, k1h, k2l, k2h, k3l, k3h;
           e4m3x4_to_f16x2x2(r0, k0l, k0h);
           e4m3x4_to_f16x2x2(r1, k1l, k1h);
@@ -566,7 +564,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
     for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const bool in = 8 * jj + 2 * t + e < valid;
+        const bool in = (C::kF16 ? 4 * t + 2 * jj + e : 8 * jj + 2 * t + e) < valid;  // the token
         x[jj][e] = in ? sacc[jj][e] * cscale : -INFINITY;
         mx0 = fmaxf(mx0, x[jj][e]);
         if constexpr (GROUPED) {
@@ -645,44 +643,46 @@ __global__ void __launch_bounds__(9 * 32, 1)
     // ---- O += P V. Rows of V past `valid` hold stale or unwritten data: zero them in
     // the B fragments (P is 0 there, but 0 * NaN would not be).
     const bool partial = valid < kTPS;
-    // ldmatrix.trans: lane l addresses row l % 8 (a token) of matrix l / 8; matrices are
-    // (tokens 0-7 | 8-15) x (two 16-byte columns); a lane gets rows 2t, 2t+1 (tokens) of
-    // column g of each.
-    const int mi = lane >> 3, rr = lane & 7;
-    const int vtok = (mi & 1) * 8 + rr;
-    uint32_t lo_mask = 0xffffffffu, hi_mask = 0xffffffffu;  // tokens 2t, 2t+1 | 8+2t, 9+2t
-    if (partial) {
-      lo_mask = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
-      hi_mask = (8 + 2 * t < valid ? 0x0000ffffu : 0u) | (9 + 2 * t < valid ? 0xffff0000u : 0u);
-    }
     if constexpr (C::kF16) {
-      // A column is 16 dims; a lane's register holds dims 2g, 2g+1 of tokens 2t, 2t+1.
-      // Pairing across tokens gives two tiles per column: E (col g <-> dim 16c + 2g) and
-      // O (col g <-> dim 16c + 2g + 1), so the lane's outputs c0, c1 of E and O are dims
-      // 16c + 4t + {0, 2} and {1, 3}.
+      // A 16-byte column c of V is a 16-token x 16-dim byte matrix; transposed, lane (g, t)
+      // gets tokens 4t .. 4t+3 of dims 16c + g and 16c + 8 + g. P's k slots 2t, 2t+1 and
+      // 2t+8, 2t+9 hold tokens 4t, 4t+1 and 4t+2, 4t+3 (the S token order above), so each
+      // register's two halves, converted, are the B fragments of tiles 2c and 2c + 1.
+      uint32_t vmask = 0xffffffffu;  // bytes of tokens 4t .. 4t+3 that are valid
+      if (partial)
+        vmask = (4 * t < valid ? 0x000000ffu : 0u) | (4 * t + 1 < valid ? 0x0000ff00u : 0u) |
+                (4 * t + 2 < valid ? 0x00ff0000u : 0u) | (4 * t + 3 < valid ? 0xff000000u : 0u);
 #pragma unroll
       for (int c2 = 0; c2 < C::KC / 2; ++c2) {
-        uint32_t r0, r1, r2, r3;  // (tok 0-7, col 2c2), (8-15, 2c2), (0-7, 2c2+1), (8-15, 2c2+1)
-        ldsm_x4_trans(vb + C::at(HG, 0, vtok, hk, 2 * c2 + (mi >> 1)), r0, r1, r2, r3);
-        r0 &= lo_mask;
-        r1 &= hi_mask;
-        r2 &= lo_mask;
-        r3 &= hi_mask;
-        // codes (0, 1) and (2, 3) of each register to f16x2, then the E / O token pairs
-        // (codes 0, 2 and 1, 3) by permuting the f16 halves
-        uint32_t v0l, v0h, v1l, v1h, v2l, v2h, v3l, v3h;
-        e4m3x4_to_f16x2x2(r0, v0l, v0h);
-        e4m3x4_to_f16x2x2(r1, v1l, v1h);
-        e4m3x4_to_f16x2x2(r2, v2l, v2h);
-        e4m3x4_to_f16x2x2(r3, v3l, v3h);
-        mma_16816(o[4 * c2 + 0], pa0, pa1, pa2, pa3, prmt(v0l, v0h, 0x5410u), prmt(v1l, v1h, 0x5410u), true);
-        mma_16816(o[4 * c2 + 1], pa0, pa1, pa2, pa3, prmt(v0l, v0h, 0x7632u), prmt(v1l, v1h, 0x7632u), true);
-        mma_16816(o[4 * c2 + 2], pa0, pa1, pa2, pa3, prmt(v2l, v2h, 0x5410u), prmt(v3l, v3h, 0x5410u), true);
-        mma_16816(o[4 * c2 + 3], pa0, pa1, pa2, pa3, prmt(v2l, v2h, 0x7632u), prmt(v3l, v3h, 0x7632u), true);
+        uint32_t r0, r1, r2, r3;  // columns 2c2 (r0, r1) and 2c2 + 1 (r2, r3)
+        ldsm_b8_x2_trans(vb + C::at(HG, 0, lane & 15, hk, 2 * c2 + (lane >> 4)), r0, r1, r2, r3);
+        if (partial) {
+          r0 &= vmask;
+          r1 &= vmask;
+          r2 &= vmask;
+          r3 &= vmask;
+        }
+        uint32_t b00, b01, b10, b11, b20, b21, b30, b31;
+        e4m3x4_to_f16x2x2(r0, b00, b01);
+        e4m3x4_to_f16x2x2(r1, b10, b11);
+        e4m3x4_to_f16x2x2(r2, b20, b21);
+        e4m3x4_to_f16x2x2(r3, b30, b31);
+        mma_16816(o[4 * c2 + 0], pa0, pa1, pa2, pa3, b00, b01, true);
+        mma_16816(o[4 * c2 + 1], pa0, pa1, pa2, pa3, b10, b11, true);
+        mma_16816(o[4 * c2 + 2], pa0, pa1, pa2, pa3, b20, b21, true);
+        mma_16816(o[4 * c2 + 3], pa0, pa1, pa2, pa3, b30, b31, true);
       }
     } else {
-      // bf16: a column is 8 dims; matrices (dims 8i | 8i + 8) give b0, b1 of tiles i, i + 1
-      // with the standard fragment (col g <-> dim 8i + g)
+      // bf16: ldmatrix.trans, lane l addressing row l % 8 (a token) of matrix l / 8; the
+      // matrices are (tokens 0-7 | 8-15) x (dims 8i | 8i + 8) and give b0, b1 of tiles i,
+      // i + 1 with the standard fragment (col g <-> dim 8i + g; tokens 2t, 2t+1 | 8+2t, 9+2t)
+      const int mi = lane >> 3, rr = lane & 7;
+      const int vtok = (mi & 1) * 8 + rr;
+      uint32_t lo_mask = 0xffffffffu, hi_mask = 0xffffffffu;
+      if (partial) {
+        lo_mask = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
+        hi_mask = (8 + 2 * t < valid ? 0x0000ffffu : 0u) | (9 + 2 * t < valid ? 0xffff0000u : 0u);
+      }
 #pragma unroll
       for (int i2 = 0; i2 < C::NT / 2; ++i2) {
         const int dim = 16 * i2 + (mi >> 1) * 8;
@@ -723,30 +723,16 @@ __global__ void __launch_bounds__(9 * 32, 1)
         const float inv = l > 0.f ? v_scale / l : 0.f;
         const int64_t hrow = (slot * HG + hk) * rmax + row;
         const int e0 = 2 * half_row;  // o[i][e0], o[i][e0 + 1]: this row's two columns
-        if constexpr (C::kF16) {  // lane holds dims 16c + 4t .. + 3: E.c0, O.c0, E.c1, O.c1 of chunk c
+        // lane holds dims 8i + 2t, 8i + 2t + 1 of every tile i
 #pragma unroll
-          for (int cc = 0; cc < C::KC; ++cc) {
-            const float f0 = o[2 * cc][e0] * inv, f1 = o[2 * cc + 1][e0] * inv;
-            const float f2 = o[2 * cc][e0 + 1] * inv, f3 = o[2 * cc + 1][e0 + 1] * inv;
-            const int dim = 16 * cc + 4 * t;
-            if (whole) {
-              *reinterpret_cast<uint2*>(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + dim) =
-                  make_uint2(pack_bf16(f0, f1), pack_bf16(f2, f3));
-            } else {
-              *reinterpret_cast<float4*>(p.ws_o + hrow * D + dim) = make_float4(f0, f1, f2, f3);
-            }
-          }
-        } else {  // lane holds dims 8i + 2t, 8i + 2t + 1 of every tile i
-#pragma unroll
-          for (int i = 0; i < C::NT; ++i) {
-            const int dim = 8 * i + 2 * t;
-            const float f0 = o[i][e0] * inv, f1 = o[i][e0 + 1] * inv;
-            if (whole) {
-              *reinterpret_cast<uint32_t*>(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + dim) =
-                  pack_bf16(f0, f1);
-            } else {
-              *reinterpret_cast<float2*>(p.ws_o + hrow * D + dim) = make_float2(f0, f1);
-            }
+        for (int i = 0; i < C::NT; ++i) {
+          const int dim = 8 * i + 2 * t;
+          const float f0 = o[i][e0] * inv, f1 = o[i][e0 + 1] * inv;
+          if (whole) {
+            *reinterpret_cast<uint32_t*>(reinterpret_cast<T*>(p.out) + (int64_t(qrow) * Hq + hq) * D + dim) =
+                pack_bf16(f0, f1);
+          } else {
+            *reinterpret_cast<float2*>(p.ws_o + hrow * D + dim) = make_float2(f0, f1);
           }
         }
         if (!whole && t == 0) p.ws_lse[hrow] = (l > 0.f) ? mr + __log2f(l) : -INFINITY;
