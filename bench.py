@@ -11,7 +11,8 @@ of the new token of every request plus one paged decode attention over all of th
 Prints one JSON line. `value` is K/V bytes read by attention per second over the whole
 step (device-resident inputs); `e2e` is the same metric through the public API with host
 buffers (host block accounting, host->device copies of the step's inputs, the kernels,
-device->host copy of the output, all inside the timed region). With --gpus N > 1 (under
+device->host copy of the output waited for before the next step, all inside the timed
+region; the next step's accounting overlaps the GPU's work). With --gpus N > 1 (under
 torchrun) every rank runs its own batch of 256 requests (weak scaling, no collective on
 the data path); `value` is all ranks' bytes over the slowest rank's time.
 """
@@ -401,9 +402,12 @@ def run_ours(a):
 
 
 def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
-    """Decode steps as a user runs them: host block accounting (C++, one batched append and
-    one table fill per step) into a pinned staging buffer, one host->device copy of the
-    step's inputs, write + attention, output copied back; host wall time per step."""
+    """Decode steps as a serving loop runs them: host block accounting (C++, one batched
+    append and one table fill per step) into a pinned staging buffer, one host->device copy
+    of the step's inputs, write + attention, output copied back and waited for before the
+    next step is launched; host wall time per step. The accounting of step n + 1 does not
+    depend on step n's output (one token per request), so it runs while the GPU works on
+    step n, into the other of two staging buffers."""
     import numpy as np
     import torch
 
@@ -412,27 +416,27 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
     ones = np.ones(len(seqs), np.int64)
     S = len(seqs)
     width = int(st.block_table.shape[1])
-    # one pinned buffer holding every input of a step, and its device twin
+    # pinned buffers holding every input of a step (two, used in turn), and one device twin
     parts = [("q", st.q.numel() * 2), ("k", st.k_new.numel() * 2), ("v", st.v_new.numel() * 2),
              ("slots", S * 8), ("table", S * width * 4), ("lens", S * 4), ("qsl", (S + 1) * 4)]
     off, offs = 0, {}
     for name, nbytes in parts:
         offs[name] = (off, nbytes)
         off += (nbytes + 255) // 256 * 256
-    h_buf = torch.empty(off, dtype=torch.uint8).pin_memory()
+    h_bufs = [torch.empty(off, dtype=torch.uint8).pin_memory() for _ in range(2)]
     d_buf = torch.empty(off, dtype=torch.uint8, device=dev)
 
     def view(buf, name, dtype, shape):
         o, nb = offs[name]
         return buf[o:o + nb].view(dtype).view(shape)
 
-    view(h_buf, "q", torch.bfloat16, st.q.shape).copy_(st.q.cpu())
-    view(h_buf, "k", torch.bfloat16, st.k_new.shape).copy_(st.k_new.cpu())
-    view(h_buf, "v", torch.bfloat16, st.v_new.shape).copy_(st.v_new.cpu())
-    view(h_buf, "qsl", torch.int32, (S + 1,)).copy_(torch.arange(S + 1, dtype=torch.int32))
-    slots_h = view(h_buf, "slots", torch.int64, (S,)).numpy()
-    table_h = view(h_buf, "table", torch.int32, (S, width)).numpy()
-    lens_h = view(h_buf, "lens", torch.int32, (S,)).numpy()
+    for h_buf in h_bufs:
+        view(h_buf, "q", torch.bfloat16, st.q.shape).copy_(st.q.cpu())
+        view(h_buf, "k", torch.bfloat16, st.k_new.shape).copy_(st.k_new.cpu())
+        view(h_buf, "v", torch.bfloat16, st.v_new.shape).copy_(st.v_new.cpu())
+        view(h_buf, "qsl", torch.int32, (S + 1,)).copy_(torch.arange(S + 1, dtype=torch.int32))
+    host = [(view(h, "slots", torch.int64, (S,)).numpy(), view(h, "table", torch.int32, (S, width)).numpy(),
+             view(h, "lens", torch.int32, (S,)).numpy()) for h in h_bufs]
     q_d = view(d_buf, "q", torch.bfloat16, st.q.shape)
     k_d = view(d_buf, "k", torch.bfloat16, st.k_new.shape)
     v_d = view(d_buf, "v", torch.bfloat16, st.v_new.shape)
@@ -445,31 +449,67 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
     h2d = off
     d2h = out_h.numel() * out_h.element_size()
     bm = dw.bm
-    kv_bytes_steps = []
+    done = torch.cuda.Event()
 
-    def one_step():
-        dw.bm.append_batch(seqs, ones, out=slots_h)
+    def account(b):  # the next step's slots, tables and lengths into staging buffer b
+        slots_h, table_h, lens_h = host[b]
+        bm.append_batch(seqs, ones, out=slots_h)
         bm.batch_tables(seqs, width, table_out=table_h, lens_out=lens_h)
-        with torch.cuda.stream(stream):
-            d_buf.copy_(h_buf, non_blocking=True)
-            pa.write_attention(out_d, q_d, k_d, v_d, slots_d, dw.k_cache, dw.v_cache, table_d, lens_d, qsl_d,
-                               max_query_len=1, max_seq_len=int(lens_h.max()), scale=sp.scale,
-                               workspace=st.workspace, stream=stream)
-            out_h.copy_(out_d, non_blocking=True)
-        stream.synchronize()
-        return int(lens_h.astype(np.int64).sum()) * sp.kv_token_bytes
+        return int(lens_h.max()), int(lens_h.astype(np.int64).sum()) * sp.kv_token_bytes
+
+    def enqueue(b, max_len, s):  # the step's copies and call on stream s
+        d_buf.copy_(h_bufs[b], non_blocking=True)
+        pa.write_attention(out_d, q_d, k_d, v_d, slots_d, dw.k_cache, dw.v_cache, table_d, lens_d, qsl_d,
+                           max_query_len=1, max_seq_len=max_len, scale=sp.scale, workspace=st.workspace, stream=s)
+        out_h.copy_(out_d, non_blocking=True)
+
+    graphs = None  # after the warm-up: one CUDA graph per staging buffer (H2D, call, D2H)
+
+    def run(n):
+        """n steps; returns the K/V bytes of each. Staging buffer b is refilled only after
+        the step that copied from it has completed (its result was waited for)."""
+        kv = []
+        nxt = account(0)
+        for i in range(n):
+            b = i % 2
+            max_len, kv_bytes = nxt
+            with torch.cuda.stream(stream):
+                if graphs is not None:
+                    graphs[b].replay()
+                else:
+                    enqueue(b, max_len, stream)
+                done.record(stream)
+            if i + 1 < n:
+                nxt = account(1 - b)  # overlaps the GPU's step i
+            done.synchronize()  # step i's output is on the host
+            kv.append(kv_bytes)
+        return kv
 
     # each end-to-end step appends a real token to every request: cap the count so the
     # requests stay inside the workload's block pool (1.25x the blocks of the batch)
     steps, warm = min(a.steps, 64), min(a.warmup, 8)
-    for _ in range(warm):
-        one_step()
+    run(warm)
+    # Capture the launch side as a serving loop would (the table capacity as max_seq_len:
+    # it only bounds the lengths the kernels read from the device).
+    graph_note = "CUDA graph per staging buffer (H2D, pa_write_attention, D2H), replayed each step"
+    try:
+        torch.cuda.synchronize()
+        captured = []
+        for b in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                enqueue(b, width * sp.block_size, torch.cuda.current_stream())
+            captured.append(g)
+        graphs = captured
+        run(2)
+    except Exception as e:  # report and time the launches without a graph
+        graphs = None
+        graph_note = f"no CUDA graph ({type(e).__name__}: {e}); launches issued per step"
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        kv_bytes_steps.append(one_step())
+    kv_bytes_steps = run(steps)
     secs = (time.perf_counter() - t0) / steps
     secs = max_over_ranks([secs], dist, dev)[0]
     if pa.read_device_errors(clear=True):
@@ -478,7 +518,9 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
     return {"value": job_gbs(world, mean_bytes, secs * 1e3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": secs * 1e3, "steps": steps, "warmup": warm,
             "includes": "host block accounting (pa_bm_append_batch, pa_bm_batch_tables) into pinned memory, one "
-                        "H2D copy of q/k/v/slots/table/lens/query_start_loc, pa_write_attention, D2H of out"}
+                        "H2D copy of q/k/v/slots/table/lens/query_start_loc, pa_write_attention, D2H of out, "
+                        "waited for before the next step is launched; the next step's accounting runs while "
+                        "the GPU works (two staging buffers)", "launch": graph_note}
 
 
 def _peaks():
