@@ -60,6 +60,10 @@ struct DecodeParams {
   const int32_t* shared_len;
   int num_groups;
   int rmax;  // workspace rows per KV head of a piece: G, or 16 with groups
+  // tensor-core kernel without groups: bytes of a query slot in shared memory (the head
+  // group's query rows, and the new K / V rows of a fused write), filled by the producer's
+  // bulk copies; 0: consumers read the queries from global memory
+  int q_slot;
 };
 
 // Keys of request s if it is a decode request (q_len == 1), else 0.
@@ -370,6 +374,7 @@ inline DecodeParams fill_decode_params(const AttnArgs& a, int hg, int qg, int nu
   p.shared_len = nullptr;
   p.num_groups = 0;
   p.rmax = G;
+  p.q_slot = 0;
   return p;
 }
 

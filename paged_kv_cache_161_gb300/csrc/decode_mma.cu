@@ -58,6 +58,23 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
                : "memory");
 }
 
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // Two 16x16 byte matrices, transposed: lanes 0-15 address rows 0-15 of the first, lanes
 // 16-31 those of the second; lane (g, t) = (l / 4, l % 4) gets rows 4t .. 4t+3 of column g
 // (r0) and of column g + 8 (r1) of the first, the same of the second in r2, r3.
@@ -119,7 +136,12 @@ struct MmaCfg {
   static __host__ __device__ uint32_t desc_off(int hg) { return STAGES * 2 * stage_bytes(hg); }
   static __host__ __device__ uint32_t bar_off(int hg) { return desc_off(hg) + STAGES * 48; }  // MmaDesc
   static __host__ __device__ uint32_t red_off(int hg) { return bar_off(hg) + 2 * STAGES * 8; }
-  static __host__ __device__ uint32_t total(int hg) { return red_off(hg) + 40 * 4 + 1024; }  // + alignment
+  // query slots (no groups): 2 mbarriers, then 2 slots of q_slot bytes, 16-byte aligned
+  static __host__ __device__ uint32_t qbar_off(int hg) { return red_off(hg) + 40 * 4; }
+  static __host__ __device__ uint32_t qslot_off(int hg) { return (qbar_off(hg) + 16 + 15) / 16 * 16; }
+  static __host__ __device__ uint32_t total(int hg, uint32_t q_slot) {  // + alignment slack
+    return qslot_off(hg) + 2 * q_slot + 1024;
+  }
   // Byte offset, inside a stage's K (or V), of 16-byte column `chunk` (of the 128-byte
   // row of dims [half * INNER, half * INNER + INNER)) of token `tok` of head `h`.
   static __device__ __forceinline__ uint32_t at(int hg, int half, int tok, int h, int chunk) {
@@ -247,6 +269,11 @@ __global__ void __launch_bounds__(9 * 32, 1)
   MmaDesc* desc = reinterpret_cast<MmaDesc*>(smem + C::desc_off(HG));
   int* red = reinterpret_cast<int*>(smem + C::red_off(HG));
   const uint32_t full0 = base + C::bar_off(HG), empty0 = full0 + 8 * STAGES;
+  // query slots: filled with a segment's first stage in this CTA, released by the consumer
+  // warps after its last stage (no groups, when they fit in shared memory: p.q_slot > 0)
+  constexpr bool kQSlots = !GROUPED && C::EL == 2;  // compiled in for bf16 caches without groups
+  const bool qsm = kQSlots && p.q_slot > 0;
+  const uint32_t qbar0 = base + C::qbar_off(HG), qslot0 = base + C::qslot_off(HG);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_consumers = HG;  // one warp per KV head of the group
 
@@ -261,6 +288,10 @@ __global__ void __launch_bounds__(9 * 32, 1)
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(full0 + 8 * i, 1);
       mbar_init(empty0 + 8 * i, num_consumers);
+    }
+    if (kQSlots) {
+      mbar_init(qbar0, num_consumers);
+      mbar_init(qbar0 + 8, num_consumers);
     }
     fence_mbar_init();
   }
@@ -277,7 +308,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
     // the segment being walked: its request (or first member), members, first chunk,
     // chunk count and key count
     int k = pl.start_s, j = pl.start_j, hg = pl.start_hg;
-    int s, nmem, skip, units_s, L;
+    int s, nmem, skip, units_s, L, qrow = 0;
     auto open_segment = [&](int kk) {
       if (kk < NG) {
         int a, b;
@@ -292,6 +323,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
         nmem = 1;
         skip = own_skip(p, s);
         L = decode_len(p, s);
+        if (kQSlots) qrow = __ldg(p.qsl + s);
         units_s = max(units_of(L) - skip, 0);
       }
     };
@@ -301,7 +333,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
     // segment) instead of one dependent load per stage
     int win_s = -1, win_base = 0;
     int32_t win = -1;
-    int stage = 0;
+    int stage = 0, qord = 0;  // qord: segments started in this CTA (query slot qord % 2)
     uint32_t phase = 0;
     for (int64_t u = u_begin; u < u_end; ++u) {
       const int64_t u0 = u - j, u1 = u0 + units_s;
@@ -361,8 +393,13 @@ __global__ void __launch_bounds__(9 * 32, 1)
       const int nhave = __popc(__ballot_sync(0xffffffffu, have));
       const bool any_bad = __any_sync(0xffffffffu, bad);
       if (any_bad) flags |= kBad;
+      const int qslot = (qsm && (flags & kFirst)) ? (qord & 1) : -1;
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(empty0 + 8 * stage, phase ^ 1) ? 1 : 0;
+      if (lane == 0) {
+        ok = mbar_wait(empty0 + 8 * stage, phase ^ 1) ? 1 : 0;
+        if (ok && qslot >= 0) ok = mbar_wait(qbar0 + 8 * qslot, ((qord >> 1) & 1) ^ 1) ? 1 : 0;
+      }
+      if (qslot >= 0) ++qord;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         raise_error(p.err, PA_DEVERR_TIMEOUT);
@@ -382,7 +419,24 @@ __global__ void __launch_bounds__(9 * 32, 1)
         d.wslot = wslot;
         d.pad = skip;
         desc[stage] = d;
-        mbar_arrive_expect_tx(full0 + 8 * stage, uint32_t(nhave) * C::HALVES * 2 * C::box_bytes(HG));
+        uint32_t tx = uint32_t(nhave) * C::HALVES * 2 * C::box_bytes(HG);
+        // a segment's first stage here also brings its query rows (heads of this head group
+        // of one token: contiguous) and, when the segment ends here with a fused write, the
+        // new token's K and V rows of the head group
+        const uint32_t qb = uint32_t(HG * G * D) * 2u, nb = uint32_t(HG * D) * 2u;
+        const bool with_new = qslot >= 0 && p.k_new && (flags & kSeqEnd);
+        if (qslot >= 0) tx += qb + (with_new ? 2u * nb : 0u);
+        mbar_arrive_expect_tx(full0 + 8 * stage, tx);
+        if (qslot >= 0) {
+          const uint32_t dst = qslot0 + uint32_t(qslot) * uint32_t(p.q_slot);
+          bulk_g2s(dst, static_cast<const char*>(p.q) + (int64_t(qrow) * p.num_heads + int64_t(hg) * HG * G) * D * 2,
+                   qb, full0 + 8 * stage);
+          if (with_new) {
+            const int64_t off = (int64_t(qrow) * p.num_kv_heads + int64_t(hg) * HG) * D * 2;
+            bulk_g2s(dst + qb, p.k_new + off, nb, full0 + 8 * stage);
+            bulk_g2s(dst + qb + nb, p.v_new + off, nb, full0 + 8 * stage);
+          }
+        }
       }
       __syncwarp();
       if (have) {
@@ -460,6 +514,25 @@ __global__ void __launch_bounds__(9 * 32, 1)
     }
   };
 
+  // The same fragments from this segment's query slot (row g = query head hk * G + g of
+  // the head group; rows past G are zero).
+  int qord = 0, qcur = 0;  // segments started in this CTA; the current one's slot
+  auto load_q_slot = [&](uint32_t (&lo)[C::KC], uint32_t (&hi)[C::KC]) {
+    const bool have = g < G;
+    const uint32_t row = qslot0 + uint32_t(qcur) * uint32_t(p.q_slot) + uint32_t((hk * G + (have ? g : 0)) * D * 2);
+#pragma unroll
+    for (int kc = 0; kc < C::KC; ++kc) {
+      if constexpr (C::kF16) {
+        const uint2 w = have ? lds64(row + uint32_t(16 * kc + 4 * t) * 2u) : make_uint2(0u, 0u);
+        lo[kc] = pack_f16(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+        hi[kc] = pack_f16(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+      } else {
+        lo[kc] = have ? lds32(row + uint32_t(16 * kc + 2 * t) * 2u) : 0u;
+        hi[kc] = have ? lds32(row + uint32_t(16 * kc + 8 + 2 * t) * 2u) : 0u;
+      }
+    }
+  };
+
   int stage = 0;
   uint32_t phase = 0;
   for (int64_t u = u_begin; u < u_end; ++u) {
@@ -470,14 +543,24 @@ __global__ void __launch_bounds__(9 * 32, 1)
     const MmaDesc d = desc[stage];
     const int nrows = d.nmem * G;
     if (d.flags & kFirst) {
-      load_q(g, nrows, d.s, d.hg, qa0, qa2);
+      if (qsm) {
+        qcur = qord & 1;
+        ++qord;
+        load_q_slot(qa0, qa2);
+        if (!p.k_new) {  // nothing else is read from the slot: hand it back now
+          __syncwarp();
+          if (lane == 0) mbar_arrive(qbar0 + 8 * qcur);
+        }
+      } else {
+        load_q(g, nrows, d.s, d.hg, qa0, qa2);
+      }
       if constexpr (GROUPED) load_q(g + 8, nrows, d.s, d.hg, qa1, qa3);
 #pragma unroll
       for (int i = 0; i < C::NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
       mrun0 = mrun1 = -INFINITY;
       lpart0 = lpart1 = 0.f;
       if constexpr (!C::kF16 && !GROUPED) {
-        if (p.k_new && (d.flags & kSeqEnd) && lane < kRowChunks) {  // this CTA ends the request
+        if (!qsm && p.k_new && (d.flags & kSeqEnd) && lane < kRowChunks) {  // this CTA ends the request
           const int qrow = __ldg(p.qsl + d.s);
           const int64_t off = (int64_t(qrow) * p.num_kv_heads + d.hg * HG + hk) * D * C::EL + lane * 16;
           knew = __ldg(reinterpret_cast<const uint4*>(p.k_new + off));
@@ -490,6 +573,12 @@ __global__ void __launch_bounds__(9 * 32, 1)
     if constexpr (!C::kF16 && !GROUPED) {
       if (d.wslot >= 0) {  // fused write: the new row into the stage (row valid - 1) and its slot
         if (lane < kRowChunks) {
+          if (qsm) {  // the rows came with the segment's first stage, after its query rows
+            const uint32_t nrow = qslot0 + uint32_t(qcur) * uint32_t(p.q_slot) + uint32_t(HG * G * D * 2) +
+                                  uint32_t(hk * D * 2 + lane * 16);
+            knew = lds128(nrow);
+            vnew = lds128(nrow + uint32_t(HG * D * 2));
+          }
           const int half = (lane * 16) / 128, ch = ((lane * 16) % 128) / 16;
           const uint32_t so = C::at(HG, half, d.valid - 1, hk, ch);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(kb + so), "r"(knew.x), "r"(knew.y),
@@ -700,6 +789,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
     }
 
     if (!(d.flags & kLast)) continue;
+    if (qsm && p.k_new && lane == 0) mbar_arrive(qbar0 + 8 * qcur);  // the new rows are written
 
     // ================= finalize this segment's piece =================
     float l0 = lpart0, l1 = lpart1;
@@ -933,7 +1023,16 @@ cudaError_t run(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream) {
     p.ws_lse = reinterpret_cast<float*>(ws + rows * D * 4);
     p.ws_meta = reinterpret_cast<int4*>(ws + rows * D * 4 + ((rows * 4 + 15) / 16) * 16);
   }
-  const size_t smem = C::total(hg);
+  // query slots when they fit beside the stages (bf16 caches; with E4M3 caches the slots,
+  // which push shared memory to the next carveout, measured slower than global loads)
+  uint32_t q_slot = 0;
+  if (!GROUPED && C::EL == 2) {
+    q_slot = uint32_t(hg * p.group * D * 2) + (p.k_new ? uint32_t(2 * hg * D * 2) : 0u);
+    q_slot = (q_slot + 15) / 16 * 16;
+    if (C::total(hg, q_slot) > uint32_t(kSmemLimit)) q_slot = 0;
+  }
+  p.q_slot = int(q_slot);
+  const size_t smem = C::total(hg, q_slot);
   auto kern = decode_mma_kernel<__nv_bfloat16, D, KV, BT, GROUPED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
