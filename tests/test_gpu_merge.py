@@ -2,7 +2,8 @@
 
 - Outputs against the oracle for batches whose cuts fall everywhere: one short request
   (a few units spread over CTAs far apart, empty CTAs in between), one long request (tens
-  of pieces), a mix of lengths; GQA, MHA and head_dim 64, bf16; and an E4M3 cache.
+  of pieces), a mix of lengths; GQA, MHA, head_dim 64, 8 query heads per KV head and
+  block size 8, bf16, through pa_write_attention (the KV write fused in); and an E4M3 cache.
 - One workspace reused across batches of different shapes (never cleared, holding the
   previous call's pieces) gives the same bits as a fresh workspace per call.
 
@@ -20,6 +21,8 @@ pytestmark = pytest.mark.gpu
 GQA = workloads.Spec("bf16", 32, 8, 128, 16, 128 ** -0.5)
 MHA = workloads.Spec("bf16", 32, 32, 128, 16, 128 ** -0.5)
 D64 = workloads.Spec("bf16", 16, 4, 64, 16, 64 ** -0.5)
+G8 = workloads.Spec("bf16", 32, 4, 128, 16, 128 ** -0.5)   # query rows too large for shared-memory slots
+B8 = workloads.Spec("bf16", 32, 8, 128, 8, 128 ** -0.5)    # two 8-token boxes per stage
 CASES = {
     "one_short": [39],
     "one_long": [20000],
@@ -56,9 +59,9 @@ def _run(pa, wl, ws=None, fused=False):
 
 
 @pytest.mark.parametrize("case", list(CASES))
-@pytest.mark.parametrize("spec_name", ["gqa", "mha", "d64"])
+@pytest.mark.parametrize("spec_name", ["gqa", "mha", "d64", "g8", "b8"])
 def test_cut_requests_match_oracle(pa, case, spec_name):
-    spec = {"gqa": GQA, "mha": MHA, "d64": D64}[spec_name]
+    spec = {"gqa": GQA, "mha": MHA, "d64": D64, "g8": G8, "b8": B8}[spec_name]
     ctx = CASES[case]
     wl = workloads.custom(spec, ctx, [1] * len(ctx), name=f"{case}_{spec_name}")
     out, _ = _run(pa, wl, fused=True)
