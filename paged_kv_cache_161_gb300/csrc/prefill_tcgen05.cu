@@ -71,7 +71,8 @@ struct Layout {
   static constexpr uint32_t K = Q + 2 * NH * kHalf;     // 2 stages
   static constexpr uint32_t V = K + 2 * NH * kHalf;     // 2 stages
   static constexpr uint32_t PFX = V + 2 * NH * kHalf;   // int[kMaxSeqs + 8]
-  static constexpr uint32_t BAR = PFX + (kMaxSeqs + 8) * 4;
+  static constexpr uint32_t ORD = PFX + (kMaxSeqs + 8) * 4;  // int[kMaxSeqs + 8], right after PFX
+  static constexpr uint32_t BAR = ORD + (kMaxSeqs + 8) * 4;
   static constexpr int NBAR = 24;
   static constexpr uint32_t MISC = BAR + NBAR * 8;       // tmem base, abort flag
   static constexpr uint32_t BYTES = MISC + 16;
@@ -90,22 +91,26 @@ struct Pair {
   int q0[2], nq[2], pos0[2];
 };
 
+// Pair t of the enumeration: the prefill requests in the order ord[0..P) (longest first),
+// each request's pairs with the KV head fastest and the query tiles from the last one back
+// (the last tiles see the most keys).
 template <int G>
-__device__ __forceinline__ void pair_info(const PrefillParams& p, const int* pfx, int S, int t, Pair& pr) {
-  int lo = 0, hi = S;  // find s with pfx[s] <= t < pfx[s + 1]
+__device__ __forceinline__ void pair_info(const PrefillParams& p, const int* pfx, int P, int t, Pair& pr) {
+  const int* ord = pfx + (kMaxSeqs + 8);  // the order array follows the prefix (Layout::ORD)
+  int lo = 0, hi = P;  // find i with pfx[i] <= t < pfx[i + 1]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (pfx[mid] <= t) lo = mid; else hi = mid;
   }
   constexpr int TOK = kBM / G;
-  const int s = lo;
-  const int r = t - pfx[s];
+  const int s = ord[lo];
+  const int r = t - pfx[lo];
   const int Hkv = p.num_kv_heads;
   pr.s = s;
   pr.hk = r % Hkv;
-  const int qp = r / Hkv;
   pr.qs = __ldg(p.qsl + s);
   const int q_len = __ldg(p.qsl + s + 1) - pr.qs;
+  const int qp = (q_len + 2 * TOK - 1) / (2 * TOK) - 1 - r / Hkv;
   int L = __ldg(p.seq_lens + s);
   const int cap = p.max_blocks_per_seq * p.block_size;
   if (L > cap) L = cap;
@@ -145,35 +150,81 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const int S = p.num_seqs;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- per-request pair prefix (pairs = ceil(q_len / (2 TOK)) x num_kv_heads for q_len >= 2)
-  int run = 0;
-  for (int b0 = 0; b0 <= S; b0 += kThreads) {
-    const int s = b0 + threadIdx.x;
-    int cnt = 0;
-    if (s < S) {
-      const int q_len = __ldg(p.qsl + s + 1) - __ldg(p.qsl + s);
-      if (q_len >= 2) cnt = ((q_len + 2 * TOK - 1) / (2 * TOK)) * p.num_kv_heads;
-    }
-    int inc = cnt;
+  // ---- the prefill requests (q_len >= 2), their order and the pair prefix in that order
+  // (pairs = ceil(q_len / (2 TOK)) x num_kv_heads). Pairs are dealt to the CTAs in a snake
+  // (round r: CTA c takes pair r C + c, or r C + C - 1 - c when r is odd) over the requests
+  // longest first (keys, then batch order, when at most one per thread; else batch order):
+  // the costliest pairs spread first and the last round's cheap pairs even out the loads.
+  int* ord = reinterpret_cast<int*>(sm + LY::ORD);
+  __shared__ int wsum[kThreads / 32];
+  // Block-wide exclusive scan of x (thread order); returns it, the total in *tot.
+  auto block_scan = [&](int x, int* tot) {
+    int inc = x;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, inc, d);
       if (lane >= d) inc += y;
     }
-    __shared__ int wsum[kThreads / 32];
     if (lane == 31) wsum[warp] = inc;
     __syncthreads();
-    int off = 0, tot = 0;
+    int off = 0, t = 0;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) {
       if (w < warp) off += wsum[w];
-      tot += wsum[w];
+      t += wsum[w];
     }
-    if (s <= S) pfx[s] = run + off + inc - cnt;  // exclusive prefix; pfx[S] = total
-    run += tot;
+    __syncthreads();
+    *tot = t;
+    return off + inc - x;
+  };
+  const int cap = p.max_blocks_per_seq * p.block_size;
+  int P = 0;  // compact: ord[i] = the i-th prefill request, pfx[i] = its length (the key)
+  for (int b0 = 0; b0 < S; b0 += kThreads) {
+    const int s = b0 + threadIdx.x;
+    const int flag = (s < S && __ldg(p.qsl + s + 1) - __ldg(p.qsl + s) >= 2) ? 1 : 0;
+    int tot;
+    const int at = P + block_scan(flag, &tot);
+    if (flag) {
+      ord[at] = s;
+      pfx[at] = min(__ldg(p.seq_lens + s), cap);
+    }
+    P += tot;
+  }
+  __syncthreads();
+  if (P <= kThreads) {  // rank: longer first, then batch order
+    int my_s = 0, my_key = 0, rank = 0;
+    if (int(threadIdx.x) < P) {
+      my_s = ord[threadIdx.x];
+      my_key = pfx[threadIdx.x];
+      for (int i = 0; i < P; ++i) {
+        const int k = pfx[i];
+        rank += (k > my_key || (k == my_key && i < int(threadIdx.x))) ? 1 : 0;
+      }
+    }
+    __syncthreads();
+    if (int(threadIdx.x) < P) ord[rank] = my_s;
     __syncthreads();
   }
-  const int total = pfx[S];
+  int run = 0;  // pfx[i]: pairs of ord[0..i); pfx[P] = total
+  for (int b0 = 0; b0 <= P; b0 += kThreads) {
+    const int i = b0 + threadIdx.x;
+    int cnt = 0;
+    if (i < P) {
+      const int s = ord[i];
+      const int q_len = __ldg(p.qsl + s + 1) - __ldg(p.qsl + s);
+      cnt = ((q_len + 2 * TOK - 1) / (2 * TOK)) * p.num_kv_heads;
+    }
+    int tot;
+    const int ex = block_scan(cnt, &tot);
+    if (i <= P) pfx[i] = run + ex;
+    run += tot;
+  }
+  __syncthreads();
+  auto pair_at = [&](int it) {  // this CTA's it-th pair (snake over the rounds)
+    const int c = (it & 1) ? int(gridDim.x) - 1 - int(blockIdx.x) : int(blockIdx.x);
+    return it * int(gridDim.x) + c;
+  };
+  const int total = pfx[P];
   if (int(blockIdx.x) >= total) return;
 
   if (threadIdx.x == 0) {
@@ -209,9 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int nb = kBN / B;  // physical blocks per step (<= 16)
     int n = 0, tt = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int it = 0, t = pair_at(0); t < total && ok; t = pair_at(++it)) {
       Pair pr;
-      pair_info<G>(p, pfx, S, t, pr);
+      pair_info<G>(p, pfx, P, t, pr);
       if (pr.nt == 0) continue;
       if (is_k) {
         int qok = 1;
@@ -294,9 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       };
       int n = 0, tt = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int it = 0, t = pair_at(0); t < total && ok; t = pair_at(++it)) {
         Pair pr;
-        pair_info<G>(p, pfx, S, t, pr);
+        pair_info<G>(p, pfx, P, t, pr);
         if (pr.nt == 0) continue;
         const int n0 = n;
         if (!mbar_wait(bar(bQFull), tt & 1)) { ok = false; break; }
@@ -349,9 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const float sc = p.scale_log2;
     int n = 0, tt = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int it = 0, t = pair_at(0); t < total && ok; t = pair_at(++it)) {
       Pair pr;
-      pair_info<G>(p, pfx, S, t, pr);
+      pair_info<G>(p, pfx, P, t, pr);
       if (pr.nt == 0) continue;
       const int i = r / G, g = r % G;
       const int nq_x = x ? pr.nq[1] : pr.nq[0];  // selects, not a runtime index into the struct
