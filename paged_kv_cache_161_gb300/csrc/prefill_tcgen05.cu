@@ -20,7 +20,8 @@
 // The two tiles ping-pong: while tile A's softmax runs, the tensor core does tile B's
 // P.V and next Q.K, and the other way round.
 //
-// Roles (352 threads, one CTA per SM, persistent over a static round-robin of pairs):
+// Roles (352 threads, one CTA per SM, persistent over a static snake of pairs: requests
+// longest first, each request's last tiles first, alternate rounds dealt in reverse):
 //   warps 0-3 / 4-7  softmax + epilogue of tile A / tile B (thread = row = TMEM lane);
 //   warp 8           TMA: both Q tiles once per pair (3-D box {64 dims, G heads, 128 / G
 //                    tokens}, 128-byte swizzle) and K (2-deep ring, one 3-D box per
