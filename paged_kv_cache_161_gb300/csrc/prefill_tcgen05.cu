@@ -418,27 +418,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int key0 = kb * kBN;
         const bool diag = key0 + kBN - 1 > pos_lo;
         float s[64];
-        // pass 1: the row max over both 64-key halves
-        float mt = -INFINITY;
+        // pass 1: the row max over both 64-key halves; each 32-column part of the second
+        // half is loaded as soon as the part of the first half in its registers is reduced
+        auto mask = [&](int c0, int koff) {  // keys past this row's position, for 32 columns
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          tc::tmem_ld32(trow + scol + uint32_t(hf * 64), *reinterpret_cast<float(*)[32]>(s));
-          tc::tmem_ld32(trow + scol + uint32_t(hf * 64 + 32), *reinterpret_cast<float(*)[32]>(s + 32));
-          tc::tmem_wait_ld();
-          if (diag) {
+          for (int c = c0; c < c0 + 32; ++c) s[c] = (key0 + koff + c <= mypos) ? s[c] : -INFINITY;
+        };
+        auto max32 = [&](int c0) {
+          float m10[10];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) s[c] = (key0 + hf * 64 + c <= mypos) ? s[c] : -INFINITY;
-          }
-          float m22[22];
-#pragma unroll
-          for (int c = 0; c < 21; ++c) m22[c] = fmax3(s[3 * c], s[3 * c + 1], s[3 * c + 2]);
-          m22[21] = s[63];
-          float m8[8];
-#pragma unroll
-          for (int c = 0; c < 7; ++c) m8[c] = fmax3(m22[3 * c], m22[3 * c + 1], m22[3 * c + 2]);
-          m8[7] = m22[21];
-          mt = fmax3(mt, fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), m8[6]), m8[7]);
+          for (int c = 0; c < 10; ++c) m10[c] = fmax3(s[c0 + 3 * c], s[c0 + 3 * c + 1], s[c0 + 3 * c + 2]);
+          const float a = fmax3(m10[0], m10[1], m10[2]), b = fmax3(m10[3], m10[4], m10[5]);
+          const float d = fmax3(m10[6], m10[7], m10[8]);
+          return fmax3(fmax3(a, b, d), m10[9], fmaxf(s[c0 + 30], s[c0 + 31]));
+        };
+        tc::tmem_ld32(trow + scol, *reinterpret_cast<float(*)[32]>(s));
+        tc::tmem_ld32(trow + scol + 32u, *reinterpret_cast<float(*)[32]>(s + 32));
+        tc::tmem_wait_ld();
+        if (diag) {
+          mask(0, 0);
+          mask(32, 0);
         }
+        float mt = max32(0);
+        tc::tmem_ld32(trow + scol + 64u, *reinterpret_cast<float(*)[32]>(s));
+        mt = fmaxf(mt, max32(32));
+        tc::tmem_ld32(trow + scol + 96u, *reinterpret_cast<float(*)[32]>(s + 32));
+        tc::tmem_wait_ld();
+        if (diag) {
+          mask(0, 64);
+          mask(32, 64);
+        }
+        mt = fmax3(mt, max32(0), max32(32));
         const float m_new = fmaxf(m_used, mt);
         const bool grow = (m_new - m_used) * sc > 8.f;  // also true on the first step
         const float m_use = grow ? m_new : m_used;
@@ -458,29 +468,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             tc::tmem_st32(trow + ocol + uint32_t(c * 32), o);
           }
         }
-        // pass 2: p = 2^(s * scale_log2 - m * scale_log2); the half still in registers
-        // (keys 64..127) goes to columns 64..95, then keys 0..63 are reloaded and go to 0..31
-#pragma unroll
-        for (int hf = 1; hf >= 0; --hf) {
-          if (hf == 0) {
-            tc::tmem_ld32(trow + scol, *reinterpret_cast<float(*)[32]>(s));
-            tc::tmem_ld32(trow + scol + 32u, *reinterpret_cast<float(*)[32]>(s + 32));
-            tc::tmem_wait_ld();
-            if (diag) {
-#pragma unroll
-              for (int c = 0; c < 64; ++c) s[c] = (key0 + c <= mypos) ? s[c] : -INFINITY;
-            }
-          }
+        // pass 2: p = 2^(s * scale_log2 - m * scale_log2). Keys 64..127 (still in registers)
+        // go to columns 64..95; keys 0..63 are reloaded, the first 32 as soon as their
+        // registers are free (the load overlaps the remaining exponentials), and go to 0..31.
+        auto exps = [&](float* pk, int c) {
+          const float2 xv = ffma2v(make_float2(s[c], s[c + 1]), sc2, bias2);
+          const float2 pp = make_float2(ex2_ftz(xv.x), ex2_ftz(xv.y));
+          rs[(c >> 1) & 3] = fadd2(rs[(c >> 1) & 3], pp);
+          __nv_bfloat162 hh = __floats2bfloat162_rn(pp.x, pp.y);
+          pk[c / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&hh));
+        };
+        {
           float pk[32];
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
-            const float2 xv = ffma2v(make_float2(s[c], s[c + 1]), sc2, bias2);
-            const float2 pp = make_float2(ex2_ftz(xv.x), ex2_ftz(xv.y));
-            rs[(c >> 1) & 3] = fadd2(rs[(c >> 1) & 3], pp);
-            __nv_bfloat162 hh = __floats2bfloat162_rn(pp.x, pp.y);
-            pk[c / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&hh));
+            exps(pk, c);
+            if (c == 30) tc::tmem_ld32(trow + scol, *reinterpret_cast<float(*)[32]>(s));  // s[0..31] are free
           }
-          tc::tmem_st32(trow + scol + uint32_t(hf * 64), pk);
+          tc::tmem_st32(trow + scol + 64u, pk);
+        }
+        tc::tmem_ld32(trow + scol + 32u, *reinterpret_cast<float(*)[32]>(s + 32));
+        tc::tmem_wait_ld();
+        if (diag) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) s[c] = (key0 + c <= mypos) ? s[c] : -INFINITY;
+        }
+        {
+          float pk[32];
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) exps(pk, c);
+          tc::tmem_st32(trow + scol, pk);
         }
         const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
         l = l * alpha + ((r01.x + r01.y) + (r23.x + r23.y));
