@@ -528,17 +528,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
                            (int64_t(pr.qs + q0_x + i) * p.num_heads + pr.hk * G + g) * D;
+      // two 32-column loads per wait (the score registers are free here)
+      float o2[64];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        tc::tmem_ld32(trow + ocol + uint32_t(c * 32), o);
+      for (int c = 0; c < D / 32; c += 2) {
+        tc::tmem_ld32(trow + ocol + uint32_t(c * 32), *reinterpret_cast<float(*)[32]>(o2));
+        tc::tmem_ld32(trow + ocol + uint32_t(c * 32 + 32), *reinterpret_cast<float(*)[32]>(o2 + 32));
         tc::tmem_wait_ld();
         if (active) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
+          for (int e = 0; e < 64; e += 8) {
             float f[8];
 #pragma unroll
-            for (int xx = 0; xx < 8; ++xx) f[xx] = o[e + xx] * inv;
+            for (int xx = 0; xx < 8; ++xx) f[xx] = o2[e + xx] * inv;
             *reinterpret_cast<uint4*>(out + c * 32 + e) = Elem<__nv_bfloat16>::pack(f);
           }
         }
