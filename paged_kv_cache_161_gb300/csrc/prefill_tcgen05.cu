@@ -320,27 +320,33 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     if (lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kBM, kBN, 0);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kBM, D, 1);
+      // Descriptors are built once per operand and advanced by the byte offset / 16 (the
+      // start-address field counts 16-byte units; shared addresses stay below 256 KB, so
+      // the 14-bit field never carries), keeping the issuing thread's work per MMA small.
+      const uint64_t dq0 = tc::smem_desc_sw128(base + LY::Q, 16, 1024);
+      const uint64_t dk0 = tc::smem_desc_sw128(base + LY::K, 16, 1024);
+      const uint64_t dv0 = tc::smem_desc_sw128(base + LY::V, kHalf, 1024);
       auto qk = [&](int x, int nn) {  // S_x = Q_x . K(nn)^T
         const int stage = nn & 1;
+        const uint64_t a0 = dq0 + uint64_t((uint32_t(x * NH) * kHalf) >> 4);
+        const uint64_t b0 = dk0 + uint64_t((uint32_t(stage * NH) * kHalf) >> 4);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t koff = uint32_t(k / 4) * kHalf + uint32_t(k % 4) * 32;
-          const uint64_t a = tc::smem_desc_sw128(base + LY::Q + uint32_t(x * NH) * kHalf + koff, 16, 1024);
-          const uint64_t b = tc::smem_desc_sw128(base + LY::K + uint32_t(stage * NH) * kHalf + koff, 16, 1024);
-          tc::mma_f16(tmem + uint32_t(x * kBN), a, b, idesc_qk, k > 0 ? 1u : 0u);
+          tc::mma_f16(tmem + uint32_t(x * kBN), a0 + (koff >> 4), b0 + (koff >> 4), idesc_qk, k > 0 ? 1u : 0u);
         }
         tc::mma_commit(bar(bSFull0 + x));
       };
       auto pv = [&](int x, int nn, bool first) {  // O_x += P_x . V(nn)
         const int stage = nn & 1;
         const uint32_t pcol = tmem + uint32_t(x * kBN);
+        const uint64_t b0 = dv0 + uint64_t((uint32_t(stage * NH) * kHalf) >> 4);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {
           // P keys 0..63 packed in columns 0..31, keys 64..127 in columns 64..95
           const uint32_t acol = pcol + (k < 4 ? uint32_t(k * 8) : uint32_t(64 + (k - 4) * 8));
-          const uint64_t b = tc::smem_desc_sw128(base + LY::V + uint32_t(stage * NH) * kHalf + uint32_t(k) * 2048,
-                                                 kHalf, 1024);
-          tc::mma_f16_ts(tmem + 256u + uint32_t(x * kBN), acol, b, idesc_pv, (!first || k > 0) ? 1u : 0u);
+          tc::mma_f16_ts(tmem + 256u + uint32_t(x * kBN), acol, b0 + uint64_t((uint32_t(k) * 2048) >> 4), idesc_pv,
+                         (!first || k > 0) ? 1u : 0u);
         }
         tc::mma_commit(bar(bPVDone0 + x));
       };
