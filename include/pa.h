@@ -140,7 +140,10 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
  * The result does not depend on which physical blocks hold the tokens: the reduction
  * order is fixed by positions only, so relabelling block ids gives identical bits.
  *
- * out           device, [num_tokens, num_heads, head_dim], `dtype` (written)
+ * out           device, [num_tokens, num_heads, head_dim], `dtype` (written, never read);
+ *               may also be page-locked host memory mapped into the unified address
+ *               space: the kernels then store the rows over the CPU-GPU link and the host
+ *               sees them once the stream has been synchronised
  * q             device, [num_tokens, num_heads, head_dim], `dtype`
  * block_table   device, int32 [num_seqs, max_blocks_per_seq] (entries past a request's
  *               ceil(L / block_size) blocks are never read)

@@ -172,6 +172,16 @@ def copy_blocks(k_cache, v_cache, block_mapping, stream=None):
     _check(st, "pa_copy_blocks")
 
 
+def _out(t: torch.Tensor) -> int:
+    """An attention output: a CUDA tensor, or a pinned host tensor (the kernels store the
+    rows through its unified address; they are on the host once the stream has synchronised)."""
+    if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+        raise ValueError("out must be a contiguous tensor")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError("out must be a CUDA tensor or pinned host memory")
+    return t.data_ptr()
+
+
 def _pool_ptr(t: torch.Tensor, name: str) -> int:
     """A CUDA tensor, or a pinned host tensor (used through its unified address)."""
     if not isinstance(t, torch.Tensor) or not t.is_contiguous():
@@ -228,7 +238,7 @@ def attention(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, 
     if workspace is None:
         workspace = torch.empty(attention_workspace_size(S, Hq, Hkv, D), dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if workspace.numel() > 0 else 0
-    st = lib.pa_attention(_dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+    st = lib.pa_attention(_out(out), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
                           _dev(block_table, "block_table", torch.int32, 2), int(block_table.shape[1]),
                           _dev(seq_lens, "seq_lens", torch.int32, 1),
                           _dev(query_start_loc, "query_start_loc", torch.int32, 1), S, T, int(max_query_len),
@@ -263,7 +273,7 @@ def write_attention(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_
     if workspace is None:
         workspace = torch.empty(attention_workspace_size(S, Hq, Hkv, D), dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if workspace.numel() > 0 else 0
-    st = lib.pa_write_attention(_dev(out, "out"), _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+    st = lib.pa_write_attention(_out(out), _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
                                 _dev(slot_mapping, "slot_mapping", torch.int64), _dev(k_cache, "k_cache"),
                                 _dev(v_cache, "v_cache"), _dev(block_table, "block_table", torch.int32, 2),
                                 int(block_table.shape[1]), _dev(seq_lens, "seq_lens", torch.int32, 1),
@@ -309,7 +319,7 @@ def attention_fp8(out, q, k_cache, v_cache, block_table, seq_lens, query_start_l
     if workspace is None:
         workspace = torch.empty(attention_workspace_size(S, Hq, Hkv, D), dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if workspace.numel() > 0 else 0
-    st = lib.pa_attention_fp8(_dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+    st = lib.pa_attention_fp8(_out(out), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
                               _dev(block_table, "block_table", torch.int32, 2), int(block_table.shape[1]),
                               _dev(seq_lens, "seq_lens", torch.int32, 1),
                               _dev(query_start_loc, "query_start_loc", torch.int32, 1), S, T, int(max_query_len),
@@ -346,7 +356,7 @@ def attention_grouped(out, q, k_cache, v_cache, block_table, seq_lens, query_sta
         workspace = torch.empty(attention_grouped_workspace_size(S, G, Hq, Hkv, D), dtype=torch.uint8,
                                 device=q.device)
     grp = lambda t, n: _dev(t, n, torch.int32) if G > 0 else 0  # noqa: E731
-    st = lib.pa_attention_grouped(_dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+    st = lib.pa_attention_grouped(_out(out), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
                                   _dev(block_table, "block_table", torch.int32, 2), int(block_table.shape[1]),
                                   _dev(seq_lens, "seq_lens", torch.int32, 1),
                                   _dev(query_start_loc, "query_start_loc", torch.int32, 1), S, T, int(max_seq_len),

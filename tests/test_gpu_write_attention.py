@@ -216,3 +216,52 @@ def _st(t):
     from paged_kv_cache_161_gb300.device_workload import torch_to_storage
 
     return torch_to_storage(t)
+
+
+@pytest.mark.parametrize("cfg,fused,fp8", [(3, True, False), (5, True, False), (1, False, False), (5, False, False),
+                                           (3, False, True), (5, False, True)])
+def test_output_in_pinned_host_memory_is_bit_identical(pa, cfg, fused, fp8):
+    """`out` may be page-locked host memory: every attention kernel (split-K decode and its
+    merge, the tensor-core and CUDA-core prefill, E4M3 caches) then stores its rows over the
+    CPU-GPU link, with the same bits as into device memory."""
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload
+
+    wl = workloads.build(cfg, "small")
+    if fp8:
+        wl = workloads.with_fp8_cache(wl)
+    outs = []
+    for host in (False, True):
+        dw = DeviceWorkload(wl)
+        dw.run_setup()
+        st = dw.prepare_step()
+        if host:
+            st.out = torch.full(st.out.shape, float("nan"), dtype=st.out.dtype).pin_memory()
+        outs.append(dw.run_step(st, fused=fused))
+        torch.cuda.synchronize()
+        assert pa.read_device_errors(clear=True) == 0
+    assert not outs[1].is_cuda
+    assert torch.equal(outs[0].cpu(), outs[1])
+
+
+def test_grouped_output_in_pinned_host_memory(pa):
+    """The grouped decode (shared-prefix segments and their merge) into pinned host memory."""
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload
+
+    wl = workloads.build(4, "small")
+    dw = DeviceWorkload(wl)
+    dw.run_setup()
+    st = dw.prepare_step()
+    dw.run_step(st)
+    seq_group, group_range, shared_len = dw.bm.batch_groups([s for s, _ in wl.step.batch], 4)
+    dev = st.q.device
+    args = (st.q, dw.k_cache, dw.v_cache, st.block_table, st.seq_lens, st.query_start_loc,
+            torch.from_numpy(seq_group).to(dev), torch.from_numpy(group_range).to(dev),
+            torch.from_numpy(shared_len).to(dev))
+    out_d = torch.empty_like(st.q)
+    out_h = torch.full(st.q.shape, float("nan"), dtype=st.q.dtype).pin_memory()
+    for out in (out_d, out_h):
+        pa.attention_grouped(out, *args, max_seq_len=st.max_seq_len, scale=wl.spec.scale)
+    torch.cuda.synchronize()
+    assert pa.read_device_errors(clear=True) == 0
+    assert len(group_range) > 0
+    assert torch.equal(out_d.cpu(), out_h)
