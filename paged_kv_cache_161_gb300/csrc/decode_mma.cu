@@ -136,7 +136,7 @@ struct MmaCfg {
   static __host__ __device__ uint32_t desc_off(int hg) { return STAGES * 2 * stage_bytes(hg); }
   static __host__ __device__ uint32_t bar_off(int hg) { return desc_off(hg) + STAGES * 48; }  // MmaDesc
   static __host__ __device__ uint32_t red_off(int hg) { return bar_off(hg) + 2 * STAGES * 8; }
-  // query slots (no groups): 2 mbarriers, then 2 slots of q_slot bytes, 16-byte aligned
+  // query slots: 2 mbarriers, then 2 slots of q_slot bytes, 16-byte aligned
   static __host__ __device__ uint32_t qbar_off(int hg) { return red_off(hg) + 40 * 4; }
   static __host__ __device__ uint32_t qslot_off(int hg) { return (qbar_off(hg) + 16 + 15) / 16 * 16; }
   static __host__ __device__ uint32_t total(int hg, uint32_t q_slot) {  // + alignment slack
@@ -270,8 +270,9 @@ __global__ void __launch_bounds__(9 * 32, 1)
   int* red = reinterpret_cast<int*>(smem + C::red_off(HG));
   const uint32_t full0 = base + C::bar_off(HG), empty0 = full0 + 8 * STAGES;
   // query slots: filled with a segment's first stage in this CTA, released by the consumer
-  // warps after its last stage (no groups, when they fit in shared memory: p.q_slot > 0)
-  constexpr bool kQSlots = !GROUPED && C::EL == 2;  // compiled in for bf16 caches without groups
+  // warps after its last stage (bf16 caches, when they fit in shared memory: p.q_slot > 0;
+  // with groups, for the segments of one request, whose query rows are one token's)
+  constexpr bool kQSlots = C::EL == 2;  // compiled in for bf16 caches
   const bool qsm = kQSlots && p.q_slot > 0;
   const uint32_t qbar0 = base + C::qbar_off(HG), qslot0 = base + C::qslot_off(HG);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -393,7 +394,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
       const int nhave = __popc(__ballot_sync(0xffffffffu, have));
       const bool any_bad = __any_sync(0xffffffffu, bad);
       if (any_bad) flags |= kBad;
-      const int qslot = (qsm && (flags & kFirst)) ? (qord & 1) : -1;
+      const int qslot = (qsm && (flags & kFirst) && nmem == 1) ? (qord & 1) : -1;
       int ok = 1;
       if (lane == 0) {
         ok = mbar_wait(empty0 + 8 * stage, phase ^ 1) ? 1 : 0;
@@ -543,7 +544,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
     const MmaDesc d = desc[stage];
     const int nrows = d.nmem * G;
     if (d.flags & kFirst) {
-      if (qsm) {
+      if (qsm && d.nmem == 1) {
         qcur = qord & 1;
         ++qord;
         load_q_slot(qa0, qa2);
@@ -1026,7 +1027,7 @@ cudaError_t run(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream) {
   // query slots when they fit beside the stages (bf16 caches; with E4M3 caches the slots,
   // which push shared memory to the next carveout, measured slower than global loads)
   uint32_t q_slot = 0;
-  if (!GROUPED && C::EL == 2) {
+  if (C::EL == 2) {
     q_slot = uint32_t(hg * p.group * D * 2) + (p.k_new ? uint32_t(2 * hg * D * 2) : 0u);
     q_slot = (q_slot + 15) / 16 * 16;
     if (C::total(hg, q_slot) > uint32_t(kSmemLimit)) q_slot = 0;
