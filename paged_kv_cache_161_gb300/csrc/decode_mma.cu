@@ -835,7 +835,8 @@ __global__ void __launch_bounds__(9 * 32, 1)
       if (d.flags & kSeqStart) {
         p.ws_meta[v].x = int(c);
         p.ws_meta[v].z = pl.units_per_hg;
-        p.ws_meta[v].w = __ldg(p.qsl + d.s);
+        // grouped: the chunks the segment skips (its group's shared ones), for the merge
+        p.ws_meta[v].w = GROUPED ? d.pad : __ldg(p.qsl + d.s);
       }
       if (d.flags & kSeqEnd) p.ws_meta[v].y = int(c);
     }
@@ -855,8 +856,9 @@ __device__ __forceinline__ int decode_len_quiet(const DecodeParams& p, int s) {
 // prefix ran as a segment, that segment's pieces (rows of this member), combined by their
 // log-sum-exps. (Without groups the common merge kernel runs instead.) Loads that do not
 // depend on one another are issued together -- the request's descriptor, group and length;
-// then the group's span, shared length and descriptor; then the members' lengths, one lane
-// each -- and the pieces are merged as in the common merge kernel.
+// then the group's span and descriptor (the split-K kernel left the skipped chunk count in
+// the request's own descriptor; only a request without own chunks reads the members'
+// lengths) -- and the pieces are merged as in the common merge kernel.
 template <typename T, int D>
 __global__ void __launch_bounds__(1024) decode_merge_grouped_kernel(const __grid_constant__ DecodeParams p) {
   griddep_launch_dependents();  // the next kernel may be scheduled; it still waits for this grid
@@ -875,13 +877,17 @@ __global__ void __launch_bounds__(1024) decode_merge_grouped_kernel(const __grid
   if (gi >= 0 && gi < NG) {
     int a, b;
     group_span(p, gi, a, b);
-    const int shl = __ldg(p.shared_len + gi);
     const int4 m = p.ws_meta[gi * p.num_hg + hg];
     if (s >= a && s < b && b - a >= 2 && (b - a) * G <= 16) {  // at most 8 members
-      int lim = lane < b - a ? decode_len_quiet(p, a + lane) : INT_MAX;
+      if (mo.x >= 0) {  // the request's own segment ran: its descriptor holds the skip
+        skip = mo.w;
+      } else {  // no own chunks: the skip from the members' lengths, as the split-K kernel
+        const int shl = __ldg(p.shared_len + gi);
+        int lim = lane < b - a ? decode_len_quiet(p, a + lane) : INT_MAX;
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) lim = min(lim, __shfl_xor_sync(0xffffffffu, lim, o));
-      skip = max(min(lim, shl), 0) / kTPS;
+        for (int o = 16; o >= 1; o >>= 1) lim = min(lim, __shfl_xor_sync(0xffffffffu, lim, o));
+        skip = max(min(lim, shl), 0) / kTPS;
+      }
       if (skip > 0) {
         member = s - a;
         vs = gi * p.num_hg + hg;
