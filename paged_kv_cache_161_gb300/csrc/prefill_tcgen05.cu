@@ -83,7 +83,8 @@ struct Layout {
 // barrier indices (X = tile A or B: index + X)
 enum : int {
   bQFull = 0, bQEmpty, bKFull0, bKFull1, bKEmpty0, bKEmpty1, bVFull0, bVFull1, bVEmpty0, bVEmpty1,
-  bSFull0, bSFull1, bPFull0, bPFull1, bPVDone0, bPVDone1, bOEmpty0, bOEmpty1, bMmaDone
+  bSFull0, bSFull1, bPFull0, bPFull1, bPVDone0, bPVDone1, bOEmpty0, bOEmpty1, bMmaDone,
+  bPHalf0, bPHalf1  // P of keys 64..127 is in TMEM (the first half of P.V may start)
 };
 
 // A pair of consecutive query tiles of one (request, KV head); they share every K/V step.
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   if (threadIdx.x == 0) {
     for (int i = 0; i < LY::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i == bPFull0 || i == bPFull1 || i == bOEmpty0 || i == bOEmpty1) cnt = 4;
+      if (i == bPFull0 || i == bPFull1 || i == bOEmpty0 || i == bOEmpty1 || i == bPHalf0 || i == bPHalf1) cnt = 4;
       mbar_init(bar(i), cnt);
     }
     fence_mbar_init();
@@ -337,18 +338,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
         tc::mma_commit(bar(bSFull0 + x));
       };
-      auto pv = [&](int x, int nn, bool first) {  // O_x += P_x . V(nn)
+      // O_x += P_x . V(nn) over keys 64 h .. 64 h + 63 (h = 1 first: the softmax stores
+      // those first); `first`: the pair's first step, whose first MMA starts O afresh
+      auto pv_half = [&](int x, int nn, int h, bool first) {
         const int stage = nn & 1;
         const uint32_t pcol = tmem + uint32_t(x * kBN);
         const uint64_t b0 = dv0 + uint64_t((uint32_t(stage * NH) * kHalf) >> 4);
 #pragma unroll
-        for (int k = 0; k < kBN / 16; ++k) {
+        for (int kk = 0; kk < 4; ++kk) {
+          const int k = 4 * h + kk;
           // P keys 0..63 packed in columns 0..31, keys 64..127 in columns 64..95
-          const uint32_t acol = pcol + (k < 4 ? uint32_t(k * 8) : uint32_t(64 + (k - 4) * 8));
+          const uint32_t acol = pcol + uint32_t(64 * h + kk * 8);
           tc::mma_f16_ts(tmem + 256u + uint32_t(x * kBN), acol, b0 + uint64_t((uint32_t(k) * 2048) >> 4), idesc_pv,
-                         (!first || k > 0) ? 1u : 0u);
+                         (first && kk == 0) ? 0u : 1u);
         }
-        tc::mma_commit(bar(bPVDone0 + x));
       };
       int n = 0, tt = 0;
       bool ok = true;
@@ -372,11 +375,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           const bool more = kb + 1 < pr.nt;
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
-            if (!mbar_wait(bar(bPFull0 + x), n & 1)) { ok = false; break; }
+            if (!mbar_wait(bar(bPHalf0 + x), n & 1)) { ok = false; break; }
             if (kb == 0 && !mbar_wait(bar(bOEmpty0 + x), (tt & 1) ^ 1)) { ok = false; break; }
             if (x == 0 && !mbar_wait(bar(bVFull0 + (n & 1)), (n >> 1) & 1)) { ok = false; break; }
             tc::fence_after_sync();
-            pv(x, n, kb == 0);
+            pv_half(x, n, 1, kb == 0);
+            if (!mbar_wait(bar(bPFull0 + x), n & 1)) { ok = false; break; }
+            tc::fence_after_sync();
+            pv_half(x, n, 0, false);
+            tc::mma_commit(bar(bPVDone0 + x));
             if (x == 1) tc::mma_commit(bar(bVEmpty0 + (n & 1)));
             if (more) {
               if (!mbar_wait(bar(bPVDone0 + x), n & 1)) { ok = false; break; }
@@ -494,6 +501,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           tc::tmem_st32(trow + scol + 64u, pk);
         }
         tc::tmem_ld32(trow + scol + 32u, *reinterpret_cast<float(*)[32]>(s + 32));
+        // last step: V rows past the keys the pair needs may hold stale or invalid data;
+        // P is 0 there, but 0 * NaN is NaN in the MMA: tile A's threads zero them before
+        // any P.V of the step starts
+        if (x == 0 && kb == pr.nt - 1 && pr.leff - key0 < kBN) {
+          if (!mbar_wait(bar(bVFull0 + (n & 1)), (n >> 1) & 1)) { ok = false; break; }
+          if (r >= pr.leff - key0) {
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+#pragma unroll
+              for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4*>(sm + LY::V + uint32_t((n & 1) * NH + h) * kHalf + uint32_t(r) * 128 +
+                                          ch * 16) = make_uint4(0, 0, 0, 0);
+          }
+          tc::fence_proxy_async_smem();
+        }
+        // keys 64..127 of P are in place: the MMA thread may start on them
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bPHalf0 + x));
         tc::tmem_wait_ld();
         if (diag) {
 #pragma unroll
@@ -509,20 +536,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         l = l * alpha + ((r01.x + r01.y) + (r23.x + r23.y));
         m_used = m_use;
         tc::tmem_wait_st();
-        // last step: V rows past the keys the pair needs may hold stale or invalid data;
-        // P is 0 there, but 0 * NaN is NaN in the MMA: tile A's threads zero them
-        if (x == 0 && kb == pr.nt - 1 && pr.leff - key0 < kBN) {
-          if (!mbar_wait(bar(bVFull0 + (n & 1)), (n >> 1) & 1)) { ok = false; break; }
-          if (r >= pr.leff - key0) {
-#pragma unroll
-            for (int h = 0; h < NH; ++h)
-#pragma unroll
-              for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4*>(sm + LY::V + uint32_t((n & 1) * NH + h) * kHalf + uint32_t(r) * 128 +
-                                          ch * 16) = make_uint4(0, 0, 0, 0);
-          }
-          tc::fence_proxy_async_smem();
-        }
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(bPFull0 + x));
