@@ -152,9 +152,10 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
  *               num_tokens
  * max_query_len host: an upper bound of every q_len (sizes the prefill grid)
  * max_seq_len   host: an upper bound of every L (validated against the table width)
- * workspace     device scratch of at least pa_attention_workspace_size() bytes (may be
- *               NULL only when that size is 0); no initial contents needed; must not be
- *               used by another call that may run concurrently.
+ * workspace     device scratch of at least pa_attention_workspace_size() bytes (at least
+ *               16: its last part holds the prefill kernel's work counter, which the call
+ *               zeroes on its stream before that kernel); no initial contents needed; must
+ *               not be used by another call that may run concurrently.
  * Supported: dtype PA_F32 / PA_BF16; head_dim 64 / 128; num_heads / num_kv_heads in
  * {1, 2, 4, 8}; block_size a divisor of 16 (1, 2, 4, 8, 16) or a multiple of 16.
  * --------------------------------------------------------------------------- */

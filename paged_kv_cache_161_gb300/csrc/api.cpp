@@ -131,7 +131,7 @@ int pa_attention_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
     const size_t n = pa::decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, ctas, dt);
     need = n > need ? n : need;
   }
-  *bytes_out = need;
+  *bytes_out = need + pa::kPrefillSchedBytes;
   return PA_OK;
 }
 
@@ -177,8 +177,9 @@ int prepare_attention(void* out, const void* q, const void* k_cache, const void*
   if (e != cudaSuccess) return cuda_fail(e);
   ctas = pa::decode_num_ctas(dev, &e);
   if (e != cudaSuccess) return cuda_fail(e);
-  const size_t need = pa::decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, ctas, cache_dtype);
-  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PA_ERR_WORKSPACE;
+  const size_t dneed = pa::decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, ctas, cache_dtype);
+  const size_t need = dneed + pa::kPrefillSchedBytes;
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
   unsigned int* err = pa::device_error_word(&e);
   if (!err) return cuda_fail(e);
 
@@ -202,6 +203,7 @@ int prepare_attention(void* out, const void* q, const void* k_cache, const void*
   a.dtype = dtype;
   a.cache_dtype = cache_dtype;
   a.workspace = workspace;
+  a.prefill_sched = reinterpret_cast<int*>(static_cast<unsigned char*>(workspace) + dneed);
   a.err = err;
   return PA_OK;
 }

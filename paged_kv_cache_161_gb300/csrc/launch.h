@@ -10,6 +10,10 @@
 
 namespace pa {
 
+// Bytes of an attention workspace after the decode kernels' part: the tensor-core prefill
+// kernel's pair counter (16-byte aligned, like the parts before it).
+constexpr size_t kPrefillSchedBytes = 16;
+
 // Device address of the per-device error word (set up once per device).
 unsigned int* device_error_word(cudaError_t* err);
 
@@ -52,6 +56,9 @@ struct AttnArgs {
   pa_dtype dtype;  // of q and out (and of the caches unless cache_dtype says otherwise)
   void* workspace;
   unsigned int* err;
+  // The tensor-core prefill kernel's pair counter: kPrefillSchedBytes at the end of the
+  // caller's workspace (after the decode kernels' part); reset by the launch itself.
+  int* prefill_sched = nullptr;
   // Fused KV write (decode requests only; all three null otherwise): row t of k_new / v_new
   // [num_tokens, num_kv_heads, head_dim] goes to cache slot slot_mapping[t].
   const void* k_new = nullptr;

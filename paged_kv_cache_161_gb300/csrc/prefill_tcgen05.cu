@@ -56,6 +56,7 @@ struct PrefillParams {
   const int32_t* seq_lens;
   const int32_t* qsl;
   unsigned int* err;
+  int* sched;  // pair counter, zero at launch: CTA c's pairs after its first come from it
   int64_t num_blocks;
   int max_blocks_per_seq;
   int num_seqs;
@@ -74,9 +75,10 @@ struct Layout {
   static constexpr uint32_t PFX = V + 2 * NH * kHalf;   // int[kMaxSeqs + 8]
   static constexpr uint32_t ORD = PFX + (kMaxSeqs + 8) * 4;  // int[kMaxSeqs + 8], right after PFX
   static constexpr uint32_t BAR = ORD + (kMaxSeqs + 8) * 4;
-  static constexpr int NBAR = 24;
+  static constexpr int NBAR = 26;
   static constexpr uint32_t MISC = BAR + NBAR * 8;       // tmem base, abort flag
-  static constexpr uint32_t BYTES = MISC + 16;
+  static constexpr uint32_t RING = MISC + 16;            // int[2]: the next pairs, for every role
+  static constexpr uint32_t BYTES = RING + 16;
   static constexpr uint32_t SMEM = BYTES + 1024;         // + alignment slack
 };
 
@@ -84,8 +86,13 @@ struct Layout {
 enum : int {
   bQFull = 0, bQEmpty, bKFull0, bKFull1, bKEmpty0, bKEmpty1, bVFull0, bVFull1, bVEmpty0, bVEmpty1,
   bSFull0, bSFull1, bPFull0, bPFull1, bPVDone0, bPVDone1, bOEmpty0, bOEmpty1, bMmaDone,
-  bPHalf0, bPHalf1  // P of keys 64..127 is in TMEM (the first half of P.V may start)
+  bPHalf0, bPHalf1,  // P of keys 64..127 is in TMEM (the first half of P.V may start)
+  bRingFull0, bRingFull1, bRingEmpty0, bRingEmpty1
 };
+// roles that take each pair from the ring: the V producer, the MMA thread, 8 softmax warps
+constexpr uint32_t kRingTakers = 10;
+static_assert(bRingEmpty1 < Layout<128>::NBAR && bRingEmpty1 < Layout<64>::NBAR,
+              "every barrier index needs a slot in the shared-memory layout");
 
 // A pair of consecutive query tiles of one (request, KV head); they share every K/V step.
 struct Pair {
@@ -222,17 +229,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     run += tot;
   }
   __syncthreads();
-  auto pair_at = [&](int it) {  // this CTA's it-th pair (snake over the rounds)
-    const int c = (it & 1) ? int(gridDim.x) - 1 - int(blockIdx.x) : int(blockIdx.x);
-    return it * int(gridDim.x) + c;
-  };
   const int total = pfx[P];
   if (int(blockIdx.x) >= total) return;
+  // The i-th pair of this CTA: for i = 0 pair blockIdx.x, after that the next ticket of a
+  // counter shared by the grid (dealt in enumeration order as CTAs run out of work; -1 when
+  // none is left). The Q/K producer draws the tickets and passes each pair to the other
+  // roles through a two-slot ring in shared memory.
+  volatile int* ring = reinterpret_cast<volatile int*>(sm + LY::RING);
+  auto ring_take = [&](int i, int& t) -> bool {  // one thread; false on a timeout
+    if (!mbar_wait(bar(bRingFull0 + (i & 1)), uint32_t(i >> 1) & 1u)) return false;
+    t = ring[i & 1];
+    mbar_arrive(bar(bRingEmpty0 + (i & 1)));
+    return true;
+  };
+  auto ring_take_warp = [&](int i, int& t) -> bool {  // a whole warp: lane 0 takes, all get it
+    int v = -1, okv = 1;
+    if (lane == 0) okv = ring_take(i, v) ? 1 : 0;
+    okv = __shfl_sync(0xffffffffu, okv, 0);
+    t = __shfl_sync(0xffffffffu, v, 0);
+    return okv != 0;
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < LY::NBAR; ++i) {
       uint32_t cnt = 1;
       if (i == bPFull0 || i == bPFull1 || i == bOEmpty0 || i == bOEmpty1 || i == bPHalf0 || i == bPHalf1) cnt = 4;
+      if (i == bRingEmpty0 || i == bRingEmpty1) cnt = kRingTakers;
       mbar_init(bar(i), cnt);
     }
     fence_mbar_init();
@@ -262,7 +284,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int nb = kBN / B;  // physical blocks per step (<= 16)
     int n = 0, tt = 0;
     bool ok = true;
-    for (int it = 0, t = pair_at(0); t < total && ok; t = pair_at(++it)) {
+    for (int i = 0; ok; ++i) {
+      int t = -1;
+      if (is_k) {  // draw the CTA's i-th pair and publish it in ring slot i % 2
+        int rok = 1;
+        if (lane == 0) {
+          if (i == 0) {
+            t = int(blockIdx.x);
+          } else {
+            t = int(gridDim.x) + atomicAdd(p.sched, 1);
+            if (t >= total) t = -1;
+          }
+          rok = mbar_wait(bar(bRingEmpty0 + (i & 1)), (uint32_t(i >> 1) & 1u) ^ 1u) ? 1 : 0;
+          if (rok) {
+            ring[i & 1] = t;
+            mbar_arrive(bar(bRingFull0 + (i & 1)));
+          }
+        }
+        t = __shfl_sync(0xffffffffu, t, 0);
+        if (!__shfl_sync(0xffffffffu, rok, 0)) { ok = false; break; }
+      } else if (!ring_take_warp(i, t)) {
+        ok = false;
+        break;
+      }
+      if (t < 0) break;
       Pair pr;
       pair_info<G>(p, pfx, P, t, pr);
       if (pr.nt == 0) continue;
@@ -355,7 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       };
       int n = 0, tt = 0;
       bool ok = true;
-      for (int it = 0, t = pair_at(0); t < total && ok; t = pair_at(++it)) {
+      for (int i = 0; ok; ++i) {
+        int t = -1;
+        if (!ring_take(i, t)) { ok = false; break; }
+        if (t < 0) break;
         Pair pr;
         pair_info<G>(p, pfx, P, t, pr);
         if (pr.nt == 0) continue;
@@ -414,7 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const float sc = p.scale_log2;
     int n = 0, tt = 0;
     bool ok = true;
-    for (int it = 0, t = pair_at(0); t < total && ok; t = pair_at(++it)) {
+    for (int it = 0; ok; ++it) {
+      int t = -1;
+      if (!ring_take_warp(it, t)) { ok = false; break; }
+      if (t < 0) break;
       Pair pr;
       pair_info<G>(p, pfx, P, t, pr);
       if (pr.nt == 0) continue;
@@ -621,6 +672,7 @@ cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   p.seq_lens = a.seq_lens;
   p.qsl = a.query_start_loc;
   p.err = a.err;
+  p.sched = a.prefill_sched;
   p.num_blocks = a.num_blocks;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
   p.num_seqs = a.num_seqs;
@@ -631,6 +683,9 @@ cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   auto kern = prefill_tc_kernel<D, G>;
   const size_t smem = Layout<D>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  if (!p.sched) return cudaErrorInvalidValue;
+  e = cudaMemsetAsync(p.sched, 0, sizeof(int), stream);  // the pair counter starts at 0
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(num_ctas), dim3(kThreads), smem, stream, p, qm, km, vm);
 }
