@@ -20,10 +20,12 @@
 // The two tiles ping-pong: while tile A's softmax runs, the tensor core does tile B's
 // P.V and next Q.K, and the other way round.
 //
-// Roles (352 threads, one CTA per SM, persistent over a static snake of pairs: requests
-// longest first, each request's last tiles first, alternate rounds dealt in reverse):
+// Roles (352 threads, one CTA per SM, persistent: pairs enumerated with the requests
+// longest first and each request's last tiles first; CTA c starts with pair c and then
+// draws the next unclaimed pair from a grid-wide counter whenever it needs one):
 //   warps 0-3 / 4-7  softmax + epilogue of tile A / tile B (thread = row = TMEM lane);
-//   warp 8           TMA: both Q tiles once per pair (3-D box {64 dims, G heads, 128 / G
+//   warp 8           draws the pairs (ring of two slots in shared memory, read by every
+//                    other role); TMA: both Q tiles once per pair (3-D box {64 dims, G heads, 128 / G
 //                    tokens}, 128-byte swizzle) and K (2-deep ring, one 3-D box per
 //                    physical block and 64-dim half, block-table entries read by the
 //                    warp's lanes one step ahead);
@@ -160,10 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- the prefill requests (q_len >= 2), their order and the pair prefix in that order
-  // (pairs = ceil(q_len / (2 TOK)) x num_kv_heads). Pairs are dealt to the CTAs in a snake
-  // (round r: CTA c takes pair r C + c, or r C + C - 1 - c when r is odd) over the requests
-  // longest first (keys, then batch order, when at most one per thread; else batch order):
-  // the costliest pairs spread first and the last round's cheap pairs even out the loads.
+  // (pairs = ceil(q_len / (2 TOK)) x num_kv_heads). Pairs are claimed in this order by the
+  // CTAs as they run out of work, requests longest first (keys, then batch order, when at
+  // most one per thread; else batch order): the costliest pairs start first and the cheap
+  // ones at the end fill the CTAs that finish early.
   int* ord = reinterpret_cast<int*>(sm + LY::ORD);
   __shared__ int wsum[kThreads / 32];
   // Block-wide exclusive scan of x (thread order); returns it, the total in *tot.
