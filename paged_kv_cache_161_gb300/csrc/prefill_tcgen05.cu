@@ -16,7 +16,8 @@
 //                  ex2.approx.ftz), lazy rescaling of O only when the row max grows by
 //                  more than 2^8, P packed to bf16 and written back over S
 //   O_x += P_x.V   (8 x tcgen05.mma 128xDx16, A = P from TMEM, B = V as an MN-major
-//                  shared-memory operand), O in TMEM
+//                  shared-memory operand), O in TMEM; issued in two halves of 4, keys
+//                  64..127 as soon as the softmax has stored their P, then keys 0..63
 // The two tiles ping-pong: while tile A's softmax runs, the tensor core does tile B's
 // P.V and next Q.K, and the other way round.
 //
