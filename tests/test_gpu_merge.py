@@ -78,10 +78,13 @@ def test_cut_requests_fp8_cache(pa, case):
 
 
 def test_one_workspace_reused_across_shapes(pa):
+    """One workspace of arbitrary contents serves decode batches and a prefill batch whose
+    ~580 tensor-core pairs outnumber the CTAs (the prefill's pair counter lives in it)."""
     wls = [workloads.custom(GQA, CASES["mixed"], [1] * 8, name="a"),
            workloads.custom(MHA, [5000, 39, 1200], [1, 1, 1], name="b"),
            workloads.custom(D64, CASES["one_long"], [1], name="c"),
-           workloads.build(3, "small")]
+           workloads.build(3, "small"),
+           workloads.custom(GQA, [0, 2000, 700, 0, 3000, 100], [1500, 600, 900, 1200, 300, 1], name="p")]
     need = max(pa.attention_workspace_size(len(wl.step.batch), wl.spec.num_heads, wl.spec.num_kv_heads,
                                            wl.spec.head_dim) for wl in wls)
     ws = torch.full((need,), 0xA5, dtype=torch.uint8, device="cuda")  # arbitrary contents
