@@ -37,7 +37,7 @@ def _call(f, out, q, kc, vc, bt, lens, qsl, max_q, max_s, scale):
              int(q.shape[1]), Hkv, D, B, NB, float(scale), dt, torch.cuda.current_stream().cuda_stream)
 
 
-@pytest.mark.parametrize("cfg,size", [(3, "small"), (3, "full"), (5, "small"), (1, "full"), (2, "small")])
+@pytest.mark.parametrize("cfg,size", [(3, "small"), (3, "full"), (5, "small"), (5, "full"), (1, "full"), (2, "small")])
 def test_matches_workspace_entry_point_on_two_calls(cfg, size):
     import paged_kv_cache_161_gb300 as pa
     from paged_kv_cache_161_gb300.device_workload import DeviceWorkload, torch_to_storage
