@@ -224,7 +224,9 @@ def attention(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, 
     out, q: [num_tokens, num_heads, head_dim]; block_table int32 [num_seqs, max_blocks];
     seq_lens int32 [num_seqs]; query_start_loc int32 [num_seqs + 1]. ``max_query_len`` and
     ``max_seq_len`` are host-side upper bounds. ``workspace`` is a uint8 CUDA tensor of at
-    least attention_workspace_size(...) bytes; when None one is allocated with torch.
+    least attention_workspace_size(...) bytes (no initial contents needed); when None one is
+    allocated with torch. ``out`` may be a pinned host tensor: the kernels then store the
+    rows over the CPU-GPU link, and they are in place once the stream has synchronised.
     """
     NB, B, Hkv, D = _cache_geometry(k_cache, v_cache)
     T, Hq = int(q.shape[0]), int(q.shape[1])
