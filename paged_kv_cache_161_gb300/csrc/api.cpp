@@ -209,16 +209,64 @@ int prepare_attention(void* out, const void* q, const void* k_cache, const void*
 }
 
 int run_attention(const pa::AttnArgs& a, int ctas, cudaStream_t s) {
+  if (a.max_query_len >= 2 && a.concurrent && pa::prefill_tc_supported(a)) {
+    // A batch with prefill rows: the decode kernels (HBM-bound) run on 3/5 of the SMs, on a
+    // side stream of the highest priority, beside a first prefill launch (tensor-bound) of
+    // as many CTAs as the other SMs on the caller's stream, so neither can take the other's
+    // SMs whichever is dispatched first. A second prefill launch queued behind the decode
+    // merge on the side stream takes the SMs the decode kernel leaves; both launches draw
+    // the remaining pairs from one counter, zeroed before the fork. The caller's stream
+    // then waits for the side stream.
+    pa::SideStream side;
+    cudaError_t e;
+    if (!pa::side_stream(&side, &e)) return cuda_fail(e);
+    pa::AttnArgs ad = a;
+    ad.merge_pdl = false;  // the merge's CTAs must not hold SMs while the decode kernel runs
+    const int dctas = ctas > 1 ? ctas * 3 / 5 : 1;
+    const int pctas = ctas - dctas > 0 ? ctas - dctas : 1;
+    std::lock_guard<std::mutex> lock(*side.mu);
+    e = cudaMemsetAsync(a.prefill_sched, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaEventRecord(side.fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side.stream, side.fork, 0);
+    if (e == cudaSuccess) e = pa::launch_decode(ad, dctas, side.stream);
+    if (e == cudaSuccess) e = pa::launch_prefill_tc(a, pctas, s, pa::PrefillLaunch{true, pctas, false});
+    if (e == cudaSuccess) e = pa::launch_prefill_tc(a, ctas, side.stream, pa::PrefillLaunch{false, pctas, false});
+    if (e == cudaSuccess) e = cudaEventRecord(side.join, side.stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, side.join, 0);
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+  }
   cudaError_t e = pa::launch_decode(a, ctas, s);
   if (e != cudaSuccess) return cuda_fail(e);
   if (a.max_query_len >= 2) {
-    e = pa::prefill_tc_supported(a) ? pa::launch_prefill_tc(a, ctas, s) : pa::launch_prefill(a, s);
+    e = pa::prefill_tc_supported(a) ? pa::launch_prefill_tc(a, ctas, s, pa::PrefillLaunch{true, ctas, true})
+                                    : pa::launch_prefill(a, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return PA_OK;
 }
 
 }  // namespace
+
+namespace pa {
+
+int attention_entry(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                    int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* query_start_loc, int num_seqs,
+                    int num_tokens, int max_query_len, int max_seq_len, int num_heads, int num_kv_heads,
+                    int head_dim, int block_size, int64_t num_blocks, float scale, pa_dtype dtype, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream, bool concurrent) {
+  AttnArgs a;
+  int ctas = 0;
+  bool nothing = false;
+  const int st = prepare_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
+                                   query_start_loc, num_seqs, num_tokens, max_query_len, max_seq_len, num_heads,
+                                   num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace,
+                                   workspace_bytes, a, ctas, nothing, dtype);
+  if (st != PA_OK || nothing) return st;
+  a.concurrent = concurrent;
+  return run_attention(a, ctas, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace pa
 
 extern "C" {
 
@@ -228,15 +276,9 @@ int pa_attention(void* out, const void* q, const void* k_cache, const void* v_ca
                  int max_seq_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
                  int64_t num_blocks, float scale, pa_dtype dtype, void* workspace,
                  size_t workspace_bytes, pa_stream_t stream) {
-  pa::AttnArgs a;
-  int ctas = 0;
-  bool nothing = false;
-  const int st = prepare_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
-                                   query_start_loc, num_seqs, num_tokens, max_query_len, max_seq_len, num_heads,
-                                   num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace,
-                                   workspace_bytes, a, ctas, nothing, dtype);
-  if (st != PA_OK || nothing) return st;
-  return run_attention(a, ctas, reinterpret_cast<cudaStream_t>(stream));
+  return pa::attention_entry(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, query_start_loc,
+                             num_seqs, num_tokens, max_query_len, max_seq_len, num_heads, num_kv_heads, head_dim,
+                             block_size, num_blocks, scale, dtype, workspace, workspace_bytes, stream, true);
 }
 
 int pa_write_attention(void* out, const void* q, const void* k_new, const void* v_new,

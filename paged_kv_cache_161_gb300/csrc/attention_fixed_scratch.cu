@@ -15,6 +15,7 @@
 
 #include <mutex>
 
+#include "launch.h"
 #include "pa.h"
 
 namespace {
@@ -62,8 +63,8 @@ extern "C" int pa_attention_fixed_scratch(void* out, const void* q, const void* 
   cudaError_t e;
   void* scratch = fixed_scratch_address(&e);
   if (!scratch) return PA_ERR_CUDA;
-  return pa_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
-                      query_start_loc, num_seqs, num_tokens, max_query_len, max_seq_len, num_heads,
-                      num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, scratch,
-                      kFixedScratchBytes, stream);
+  return pa::attention_entry(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
+                             query_start_loc, num_seqs, num_tokens, max_query_len, max_seq_len, num_heads,
+                             num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, scratch,
+                             kFixedScratchBytes, stream, false);
 }

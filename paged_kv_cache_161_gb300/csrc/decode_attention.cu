@@ -603,7 +603,7 @@ cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_ctas), dim3((warps + 1) * 32), smem, stream, p);
   if (e != cudaSuccess) return e;
-  return launch_merge<T, D>(p, stream);
+  return launch_merge<T, D>(p, stream, a.merge_pdl);
 }
 
 template <typename T, int D, typename KV = T>

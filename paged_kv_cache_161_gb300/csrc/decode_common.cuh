@@ -378,13 +378,19 @@ inline DecodeParams fill_decode_params(const AttnArgs& a, int hg, int qg, int nu
   return p;
 }
 
-// The merge of the pieces, after the split-K grid (programmatic dependent launch).
+// The merge of the pieces, after the split-K grid: by programmatic dependent launch, or
+// (pdl false) in plain stream order, so that its CTAs take no SM while the split-K grid
+// runs (a prefill grid on another stream is then filling the SMs the split-K grid leaves).
 template <typename T, int D>
-cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream, bool pdl) {
   const int64_t HGG = int64_t(p.hg_size) * p.group;
   const int merge_threads = 32 * (HGG < 32 ? int(HGG) : 32);
-  return launch_pdl(decode_merge_kernel<T, D>, dim3(unsigned(int64_t(p.num_seqs) * p.num_hg)), dim3(merge_threads), 0,
-                    stream, p, p.group);
+  const dim3 grid(unsigned(int64_t(p.num_seqs) * p.num_hg));
+  if (!pdl) {
+    decode_merge_kernel<T, D><<<grid, dim3(merge_threads), 0, stream>>>(p, p.group);
+    return cudaGetLastError();
+  }
+  return launch_pdl(decode_merge_kernel<T, D>, grid, dim3(merge_threads), 0, stream, p, p.group);
 }
 
 }  // namespace

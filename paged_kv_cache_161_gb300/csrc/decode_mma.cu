@@ -1045,7 +1045,7 @@ cudaError_t run(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_ctas), dim3((hg + 1) * 32), smem, stream, p, km, vm);
   if (e != cudaSuccess) return e;
-  if (!GROUPED) return launch_merge<__nv_bfloat16, D>(p, stream);
+  if (!GROUPED) return launch_merge<__nv_bfloat16, D>(p, stream, a.merge_pdl);
   const int threads = 32 * (hg * p.group < 32 ? hg * p.group : 32);
   return launch_pdl(decode_merge_grouped_kernel<__nv_bfloat16, D>, dim3(unsigned(int64_t(a.num_seqs) * p.num_hg)),
                     dim3(threads), 0, stream, p);

@@ -10,6 +10,33 @@ namespace pa {
 
 static __device__ unsigned int g_error_word;
 
+bool side_stream(SideStream* out, cudaError_t* err) {
+  static std::mutex mu;
+  static std::mutex call_mu[64];
+  static SideStream cached[64] = {};
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return false;
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return false;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev].stream) {
+    int least = 0, greatest = 0;  // greatest priority = numerically lowest value
+    *err = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (*err != cudaSuccess) return false;
+    SideStream s = {nullptr, nullptr, nullptr, &call_mu[dev]};
+    *err = cudaStreamCreateWithPriority(&s.stream, cudaStreamNonBlocking, greatest);
+    if (*err == cudaSuccess) *err = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+    if (*err == cudaSuccess) *err = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+    if (*err != cudaSuccess) return false;
+    cached[dev] = s;
+  }
+  *out = cached[dev];
+  return true;
+}
+
 unsigned int* device_error_word(cudaError_t* err) {
   // One address per device; the lookup runs with that device current.
   static std::mutex mu;

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "pa.h"
 
 namespace pa {
@@ -13,6 +15,26 @@ namespace pa {
 // Bytes of an attention workspace after the decode kernels' part: the tensor-core prefill
 // kernel's pair counter (16-byte aligned, like the parts before it).
 constexpr size_t kPrefillSchedBytes = 16;
+
+// A second stream of the current device, of the highest priority, with a fork and a join
+// event, on which the decode kernels of a mixed batch run beside the prefill kernel (which
+// stays on the caller's stream); created on first use, kept until exit. `mu` serialises
+// the fork, the launches and the join of one call against other host threads (the events
+// are shared).
+struct SideStream {
+  cudaStream_t stream;
+  cudaEvent_t fork, join;
+  std::mutex* mu;
+};
+bool side_stream(SideStream* out, cudaError_t* err);
+
+// pa_attention's body; `concurrent` false keeps every kernel on the caller's stream
+// (no side stream: for callers that must not create CUDA resources).
+int attention_entry(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                    int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* query_start_loc, int num_seqs,
+                    int num_tokens, int max_query_len, int max_seq_len, int num_heads, int num_kv_heads,
+                    int head_dim, int block_size, int64_t num_blocks, float scale, pa_dtype dtype, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream, bool concurrent);
 
 // Device address of the per-device error word (set up once per device).
 unsigned int* device_error_word(cudaError_t* err);
@@ -59,6 +81,11 @@ struct AttnArgs {
   // The tensor-core prefill kernel's pair counter: kPrefillSchedBytes at the end of the
   // caller's workspace (after the decode kernels' part); reset by the launch itself.
   int* prefill_sched = nullptr;
+  // false: the decode merge kernel is launched in plain stream order (see launch_merge)
+  bool merge_pdl = true;
+  // false: never run the prefill kernel on the side stream (callers that must not create
+  // CUDA resources)
+  bool concurrent = true;
   // Fused KV write (decode requests only; all three null otherwise): row t of k_new / v_new
   // [num_tokens, num_kv_heads, head_dim] goes to cache slot slot_mapping[t].
   const void* k_new = nullptr;
@@ -98,6 +125,14 @@ size_t decode_grouped_workspace_bytes(int num_seqs, int num_groups, int num_kv_h
 bool prefill_supported(pa_dtype dtype, int head_dim, int group);
 cudaError_t launch_prefill(const AttnArgs& a, cudaStream_t stream);
 bool prefill_tc_supported(const AttnArgs& a);
-cudaError_t launch_prefill_tc(const AttnArgs& a, int num_ctas, cudaStream_t stream);
+// How one launch of the tensor-core prefill kernel takes its pairs: a call's first launch
+// starts CTA c on pair c (first_static) after zeroing the pair counter (zero_counter); a
+// second launch of the same call takes tickets only. ticket_base = the first launch's grid.
+struct PrefillLaunch {
+  bool first_static;
+  int ticket_base;
+  bool zero_counter;
+};
+cudaError_t launch_prefill_tc(const AttnArgs& a, int num_ctas, cudaStream_t stream, const PrefillLaunch& how);
 
 }  // namespace pa

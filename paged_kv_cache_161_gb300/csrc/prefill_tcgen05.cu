@@ -59,7 +59,12 @@ struct PrefillParams {
   const int32_t* seq_lens;
   const int32_t* qsl;
   unsigned int* err;
-  int* sched;  // pair counter, zero at launch: CTA c's pairs after its first come from it
+  int* sched;  // pair counter, zero before the first launch of the call
+  // first_static: CTA c takes pair c first, then tickets; else every pair is a ticket.
+  // A ticket is ticket_base + the counter's next value (ticket_base: the grid size of the
+  // call's first launch, whose CTAs took pairs 0 .. ticket_base - 1 statically).
+  int first_static;
+  int ticket_base;
   int64_t num_blocks;
   int max_blocks_per_seq;
   int num_seqs;
@@ -233,10 +238,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   }
   __syncthreads();
   const int total = pfx[P];
-  if (int(blockIdx.x) >= total) return;
-  // The i-th pair of this CTA: for i = 0 pair blockIdx.x, after that the next ticket of a
-  // counter shared by the grid (dealt in enumeration order as CTAs run out of work; -1 when
-  // none is left). The Q/K producer draws the tickets and passes each pair to the other
+  if (p.first_static ? int(blockIdx.x) >= total : p.ticket_base >= total) return;
+  // The i-th pair of this CTA: for i = 0 pair blockIdx.x (first_static), after that the
+  // next ticket of a counter shared by the grid and by a second launch of the same call
+  // (dealt in enumeration order as CTAs run out of work; -1 when none is left). The Q/K producer draws the tickets and passes each pair to the other
   // roles through a two-slot ring in shared memory.
   volatile int* ring = reinterpret_cast<volatile int*>(sm + LY::RING);
   auto ring_take = [&](int i, int& t) -> bool {  // one thread; false on a timeout
@@ -292,10 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (is_k) {  // draw the CTA's i-th pair and publish it in ring slot i % 2
         int rok = 1;
         if (lane == 0) {
-          if (i == 0) {
+          if (i == 0 && p.first_static) {
             t = int(blockIdx.x);
           } else {
-            t = int(gridDim.x) + atomicAdd(p.sched, 1);
+            t = p.ticket_base + atomicAdd(p.sched, 1);
             if (t >= total) t = -1;
           }
           rok = mbar_wait(bar(bRingEmpty0 + (i & 1)), (uint32_t(i >> 1) & 1u) ^ 1u) ? 1 : 0;
@@ -662,7 +667,7 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_
 }
 
 template <int D, int G>
-cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
+cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream, const PrefillLaunch& how) {
   CUtensorMap qm, km, vm;
   const int B = a.block_size;
   if (!make_map(&qm, a.q, D, uint64_t(a.num_heads), uint64_t(a.num_tokens), G, kBM / G) ||
@@ -676,6 +681,8 @@ cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   p.qsl = a.query_start_loc;
   p.err = a.err;
   p.sched = a.prefill_sched;
+  p.first_static = how.first_static ? 1 : 0;
+  p.ticket_base = how.ticket_base;
   p.num_blocks = a.num_blocks;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
   p.num_seqs = a.num_seqs;
@@ -687,19 +694,21 @@ cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   const size_t smem = Layout<D>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  if (!p.sched) return cudaErrorInvalidValue;
-  e = cudaMemsetAsync(p.sched, 0, sizeof(int), stream);  // the pair counter starts at 0
-  if (e != cudaSuccess) return e;
+  if (!p.sched || how.ticket_base < 0) return cudaErrorInvalidValue;
+  if (how.zero_counter) {
+    e = cudaMemsetAsync(p.sched, 0, sizeof(int), stream);  // the pair counter starts at 0
+    if (e != cudaSuccess) return e;
+  }
   return launch_pdl(kern, dim3(num_ctas), dim3(kThreads), smem, stream, p, qm, km, vm);
 }
 
 template <int D>
-cudaError_t run_g(const AttnArgs& a, int G, int num_ctas, cudaStream_t stream) {
+cudaError_t run_g(const AttnArgs& a, int G, int num_ctas, cudaStream_t stream, const PrefillLaunch& how) {
   switch (G) {
-    case 1: return run<D, 1>(a, num_ctas, stream);
-    case 2: return run<D, 2>(a, num_ctas, stream);
-    case 4: return run<D, 4>(a, num_ctas, stream);
-    case 8: return run<D, 8>(a, num_ctas, stream);
+    case 1: return run<D, 1>(a, num_ctas, stream, how);
+    case 2: return run<D, 2>(a, num_ctas, stream, how);
+    case 4: return run<D, 4>(a, num_ctas, stream, how);
+    case 8: return run<D, 8>(a, num_ctas, stream, how);
   }
   return cudaErrorInvalidValue;
 }
@@ -712,10 +721,10 @@ bool prefill_tc_supported(const AttnArgs& a) {
          a.num_seqs <= kMaxSeqs && encode_fn() != nullptr;
 }
 
-cudaError_t launch_prefill_tc(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
+cudaError_t launch_prefill_tc(const AttnArgs& a, int num_ctas, cudaStream_t stream, const PrefillLaunch& how) {
   const int G = a.num_heads / a.num_kv_heads;
-  if (a.head_dim == 64) return run_g<64>(a, G, num_ctas, stream);
-  return run_g<128>(a, G, num_ctas, stream);
+  if (a.head_dim == 64) return run_g<64>(a, G, num_ctas, stream, how);
+  return run_g<128>(a, G, num_ctas, stream, how);
 }
 
 }  // namespace pa
