@@ -620,6 +620,9 @@ def run_mixed(a):
                                "248 decodes, L ~ U[256, 4096]; 32 q / 8 kv heads, head_dim 128, block 16",
                    "prefill_gflop": pf_flops / 1e9, "decode_kv_bytes": dec_bytes, "seed": wl.seed},
         "attention_ms": attn_ms, "roofline_time_ms": t_star,
+        "execution": "one pa_attention call: the decode kernels on 3/5 of the SMs on a side stream beside the "
+                     "prefill kernel, whose CTAs also take the rest of the GPU once the decode CTAs are done; "
+                     "the two parts below are the same call on each sub-batch alone",
         "prefill": {"ms": pre_ms, "tflops": pre_tf, "peak_tflops": tflops_peak, "frac": pre_tf / tflops_peak,
                     "bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05)"},
         "decode": {"ms": dec_ms, "gbs": dec_gbs, "peak_gbs": hbm, "frac": dec_gbs / hbm, "bound": "hbm"},
