@@ -40,7 +40,7 @@ METRIC = "paged decode attention: K/V GB/s (% of GB300 HBM peak) and tokens/s, b
 #       python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-e2e
 # It holds only for the kernel sources it was measured on (their SHA-256 below); any
 # change to them makes the reported traffic null until it is measured again.
-DECODE_TRAFFIC = {"sources_sha256": "9ac4361de6896ab615c932566bc0a78e3b373ec5d79ce68fefca289270e4de2c", "bytes": 1653148928}
+DECODE_TRAFFIC = {"sources_sha256": "98e9193d9cd3500b321ca5ed99c1c9204cc5876661b230b28c1c993e369fee10", "bytes": 1653689600}
 DECODE_SOURCES = ["paged_kv_cache_161_gb300/csrc/decode_attention.cu", "paged_kv_cache_161_gb300/csrc/decode_mma.cu",
                   "paged_kv_cache_161_gb300/csrc/decode_common.cuh", "paged_kv_cache_161_gb300/csrc/common.cuh"]
 
