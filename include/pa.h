@@ -137,6 +137,13 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
  * Softmax and accumulation in fp32; out is written in `dtype` (bf16 rounded to nearest
  * even). Requests with q_len == 1 run the split-K decode kernel; q_len >= 2 the prefill
  * kernel; q_len == 0 produces no rows. Requires q_len <= L.
+ * With rows of both kinds (max_query_len >= 2, bf16) the two kernels run side by side: the
+ * call forks an internal stream of the highest priority off `stream` (event record and
+ * wait), runs the decode kernels there on 3/5 of the SMs and joins it back before
+ * returning, so later work on `stream` is ordered after the whole call, as for one stream.
+ * The first such call on a device creates that stream and two events (kept until exit);
+ * make it before any stream capture. The decode rows' bits then come from a split over
+ * fewer CTAs than in a decode-only call (same tolerance).
  * The result does not depend on which physical blocks hold the tokens: the reduction
  * order is fixed by positions only, so relabelling block ids gives identical bits.
  *
@@ -298,7 +305,8 @@ int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_
  * memory); a plugin inside a host framework whose allocator it cannot reach; a binding from
  * a language with no device allocator.
  *
- * Same arguments and result as pa_attention, minus workspace / workspace_bytes. The split-K
+ * Same arguments and result as pa_attention, minus workspace / workspace_bytes, and with
+ * every kernel on `stream` (no internal stream, so nothing is created). The split-K
  * scratch is instead a fixed 16 MiB array inside the library, which every GPU that loads
  * the library holds until the process exits. Allocates nothing (no cudaMalloc / cudaFree,
  * no allocating library call).
