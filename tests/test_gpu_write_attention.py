@@ -265,3 +265,43 @@ def test_grouped_output_in_pinned_host_memory(pa):
     assert pa.read_device_errors(clear=True) == 0
     assert len(group_range) > 0
     assert torch.equal(out_d.cpu(), out_h)
+
+
+def test_mixed_calls_from_two_host_threads(pa):
+    """Mixed decode + prefill calls fork the library's internal stream; calls issued at once
+    from two host threads, on two streams with two workspaces, give the single-call bits."""
+    import threading
+
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload
+
+    wl = workloads.build(5, "small")
+    dw = DeviceWorkload(wl)
+    dw.run_setup()
+    st = dw.prepare_step()
+    kw = dict(max_query_len=st.max_query_len, max_seq_len=st.max_seq_len, scale=wl.spec.scale)
+    args = (st.q, dw.k_cache, dw.v_cache, st.block_table, st.seq_lens, st.query_start_loc)
+    ref = torch.empty_like(st.q)
+    pa.attention(ref, *args, workspace=st.workspace, **kw)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.full_like(st.q, float("nan")) for _ in streams]
+    wss = [torch.empty_like(st.workspace) for _ in streams]
+    errors = []
+
+    def work(i):
+        try:
+            for _ in range(20):
+                pa.attention(outs[i], *args, workspace=wss[i], stream=streams[i], **kw)
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    assert pa.read_device_errors(clear=True) == 0
+    for out in outs:
+        assert torch.equal(out, ref)
