@@ -375,10 +375,14 @@ def run_ours(a):
     if rank == 0 and not a.no_cpu_baseline and world == 1:
         sample = list(range(n_req))
         ost = _oracle_state(wl, sample)
-        secs = _oracle_step(wl, ost, sample)
+        passes = []  # whole passes of the step (idempotent) until about 10 s of CPU work
+        while sum(passes) < 10.0 and len(passes) < 10:
+            passes.append(_oracle_step(wl, ost, sample))
+        secs = sum(passes) / len(passes)
         cpu = {"value": _cpu_sample_bytes(wl, ost, sample) / secs / 1e9, "unit": "GB/s", "cores": 1,
-               "kind": "oracle", "seconds": secs,
-               "sample": "the whole step (all 256 requests: their KV writes and attention), one pass"}
+               "kind": "oracle", "seconds": secs, "passes": len(passes), "total_seconds": sum(passes),
+               "sample": f"the whole step (all 256 requests: their KV writes and attention), {len(passes)} "
+                         "passes, mean per pass"}
 
     if rank == 0:
         line = {
