@@ -1,5 +1,6 @@
 // The per-device error word that kernels set when they skip an out-of-range index or
-// give up a wait (bits PA_DEVERR_* of pa.h).
+// give up a wait (bits PA_DEVERR_* of pa.h), and the per-device side stream on which the
+// decode kernels of a mixed batch run beside the prefill kernel.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -30,7 +31,11 @@ bool side_stream(SideStream* out, cudaError_t* err) {
     *err = cudaStreamCreateWithPriority(&s.stream, cudaStreamNonBlocking, greatest);
     if (*err == cudaSuccess) *err = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
     if (*err == cudaSuccess) *err = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
-    if (*err != cudaSuccess) return false;
+    if (*err != cudaSuccess) {  // release what was created; a later call tries again
+      if (s.fork) cudaEventDestroy(s.fork);
+      if (s.stream) cudaStreamDestroy(s.stream);
+      return false;
+    }
     cached[dev] = s;
   }
   *out = cached[dev];
