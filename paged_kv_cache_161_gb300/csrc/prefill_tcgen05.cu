@@ -241,8 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   if (p.first_static ? int(blockIdx.x) >= total : p.ticket_base >= total) return;
   // The i-th pair of this CTA: for i = 0 pair blockIdx.x (first_static), after that the
   // next ticket of a counter shared by the grid and by a second launch of the same call
-  // (dealt in enumeration order as CTAs run out of work; -1 when none is left). The Q/K producer draws the tickets and passes each pair to the other
-  // roles through a two-slot ring in shared memory.
+  // (dealt in enumeration order as CTAs run out of work; -1 when none is left). The Q/K
+  // producer draws the tickets and passes each pair to the other roles through a two-slot
+  // ring in shared memory.
   volatile int* ring = reinterpret_cast<volatile int*>(sm + LY::RING);
   auto ring_take = [&](int i, int& t) -> bool {  // one thread; false on a timeout
     if (!mbar_wait(bar(bRingFull0 + (i & 1)), uint32_t(i >> 1) & 1u)) return false;
