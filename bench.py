@@ -104,9 +104,49 @@ def max_over_ranks(vals, dist=None, device="cpu"):
     return t.tolist()
 
 
+def sum_over_ranks(vals, dist=None, device="cpu"):
+    """Element-wise sum of ``vals`` over all ranks."""
+    if dist is None:
+        return [float(v) for v in vals]
+    import torch
+
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return t.tolist()
+
+
 def job_gbs(world, bytes_per_rank, ms_per_step):
     """Whole-job throughput: every rank's bytes over the slowest rank's step time."""
     return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
+def rank_env():
+    """(world size, rank, local rank) from the launcher's environment (1, 0, 0 without one)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_workload(rank):
+    """Rank r's batch: replica r of the GQA batch-256 workload (same shapes and
+    distributions, its own seed), so the ranks share nothing (weak scaling)."""
+    import workloads
+
+    return workloads.build(CONFIG_ID, replica=rank)
+
+
+def _free_port():
+    import socket
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch_command(n, argv, script=None, port=None):
+    """The command that runs ``script`` (this file) as n ranks on this node, one per GPU."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+            "--master-addr=127.0.0.1", f"--master-port={port or _free_port()}",
+            script or os.path.abspath(__file__)] + list(argv)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -226,6 +266,67 @@ def _cpu_sample_bytes(wl, st, eval_seqs):
     return int(sum(int(st["seq_lens"][i]) for i in eval_seqs)) * wl.spec.kv_token_bytes
 
 
+def _oracle_worker(conn, replica, shard):
+    """One process of OraclePool: builds its shard's oracle state once (untimed), then runs
+    one oracle step over the shard per request and answers with its seconds."""
+    import workloads
+
+    wl = workloads.build(CONFIG_ID, replica=replica)
+    st = _oracle_state(wl, shard) if shard else None
+    conn.send(_cpu_sample_bytes(wl, st, shard) if shard else 0)
+    while conn.recv():
+        conn.send(_oracle_step(wl, st, shard) if shard else 0.0)
+    conn.close()
+
+
+class OraclePool:
+    """The oracle, as it stands, over the host's cores: the step's requests ``seqs`` dealt
+    round-robin to one process per core (started with spawn: this process may already hold
+    a CUDA context), each holding the oracle state of its own requests. A step runs every
+    shard at once; its time is the wall time until the last shard is done."""
+
+    THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+
+    def __init__(self, seqs, replica=0, workers=None):
+        import multiprocessing as mp
+
+        n = workers or len(os.sched_getaffinity(0))
+        self.workers = max(1, min(n, len(seqs)))
+        ctx = mp.get_context("spawn")
+        self.conns, self.procs = [], []
+        # one thread per process: the processes already cover the cores
+        saved = {k: os.environ.get(k) for k in self.THREAD_VARS}
+        os.environ.update({k: "1" for k in self.THREAD_VARS})
+        try:
+            for k in range(self.workers):
+                a, b = ctx.Pipe()
+                p = ctx.Process(target=_oracle_worker, args=(b, replica, list(seqs[k::self.workers])), daemon=True)
+                p.start()
+                self.conns.append(a)
+                self.procs.append(p)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        self.nbytes = sum(c.recv() for c in self.conns)  # also waits for every setup
+
+    def step(self):
+        """(wall seconds, summed per-shard CPU seconds) of one oracle step over all shards."""
+        t = time.perf_counter()
+        for c in self.conns:
+            c.send(True)
+        cpu = sum(c.recv() for c in self.conns)
+        return time.perf_counter() - t, cpu
+
+    def close(self):
+        for c in self.conns:
+            c.send(False)
+        for p in self.procs:
+            p.join(timeout=30)
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(a):
     import workloads
@@ -235,21 +336,23 @@ def run_reference(a):
         return 0
     wl = workloads.build(CONFIG_ID)
     sample = list(range(0, len(wl.step.batch), 8))  # 32 of the 256 requests per step
-    st = _oracle_state(wl, sample)
+    pool = OraclePool(sample)
     for _ in range(a.warmup):
-        _oracle_step(wl, st, sample)
-    secs = [_oracle_step(wl, st, sample) for _ in range(a.steps)]
+        pool.step()
+    secs = [pool.step()[0] for _ in range(a.steps)]
+    pool.close()
     total = sum(secs)
-    nbytes = _cpu_sample_bytes(wl, st, sample)
+    nbytes = pool.nbytes
     value = nbytes * a.steps / total / 1e9
-    desc = f"{len(sample)} of the 256 requests (every 8th) per step: their copies, KV writes and attention"
+    desc = (f"{len(sample)} of the 256 requests (every 8th) per step: their copies, KV writes and attention, "
+            f"dealt over {pool.workers} processes")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": a.gpus,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * total / a.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": _workload_config(wl, "CPU run (no L2 rule)"),
         "tokens_per_s": len(sample) * a.steps / total,
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": pool.workers, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -262,9 +365,7 @@ def run_ours(a):
     import numpy as np
     import torch
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -276,10 +377,9 @@ def run_ours(a):
     dev = torch.device("cuda", torch.cuda.current_device())
 
     import paged_kv_cache_161_gb300 as pa
-    import workloads
     from paged_kv_cache_161_gb300.device_workload import DeviceWorkload
 
-    wl = workloads.build(CONFIG_ID)
+    wl = rank_workload(rank)
     sp = wl.spec
     dw = DeviceWorkload(wl, device=dev, table_width=(8192 + 1 + 72 + 15) // 16)
     dw.run_setup()
@@ -332,7 +432,8 @@ def run_ours(a):
     step_ms = t_start.elapsed_time(t_end) / a.steps
     attn_ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / a.steps
     step_ms, attn_ms = max_over_ranks([step_ms, attn_ms], dist, dev)
-    value = job_gbs(world, kv_bytes, step_ms)
+    job_bytes = sum_over_ranks([kv_bytes], dist, dev)[0]  # every rank's own batch
+    value = job_bytes / (step_ms * 1e-3) / 1e9
 
     # ---- the same step as two calls (pa_kv_write, then pa_attention), for comparison
     for _ in range(a.warmup):
@@ -373,30 +474,33 @@ def run_ours(a):
 
     cpu = None
     if rank == 0 and not a.no_cpu_baseline and world == 1:
-        sample = list(range(n_req))
-        ost = _oracle_state(wl, sample)
-        passes = []  # whole passes of the step (idempotent) until about 10 s of CPU work
-        while sum(passes) < 10.0 and len(passes) < 10:
-            passes.append(_oracle_step(wl, ost, sample))
-        secs = sum(passes) / len(passes)
-        cpu = {"value": _cpu_sample_bytes(wl, ost, sample) / secs / 1e9, "unit": "GB/s", "cores": 1,
-               "kind": "oracle", "seconds": secs, "passes": len(passes), "total_seconds": sum(passes),
-               "sample": f"the whole step (all 256 requests: their KV writes and attention), {len(passes)} "
-                         "passes, mean per pass"}
+        pool = OraclePool(list(range(n_req)))
+        walls, cpus = [], []  # whole passes of the step (idempotent) until ~10 s of CPU work
+        while sum(cpus) < 10.0 and len(walls) < 10:
+            w, c = pool.step()
+            walls.append(w)
+            cpus.append(c)
+        pool.close()
+        secs = sum(walls) / len(walls)
+        cpu = {"value": pool.nbytes / secs / 1e9, "unit": "GB/s", "cores": pool.workers,
+               "kind": "oracle", "seconds": secs, "passes": len(walls), "cpu_seconds": sum(cpus),
+               "sample": f"the whole step (all 256 requests: their KV writes and attention) dealt over "
+                         f"{pool.workers} processes, {len(walls)} passes, mean wall time per pass"}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": _workload_config(wl, f"inputs ({kv_bytes / 1e9:.2f} GB of K/V per step) larger than the "
-                                            "129 MB L2; no flush"),
+            "config": dict(_workload_config(wl, f"inputs ({kv_bytes / 1e9:.2f} GB of K/V per step) larger than "
+                                                 "the 129 MB L2; no flush"),
+                           parallelism=f"replicas x{world} (rank r: its own batch, seed + 1000 r; no collective)"),
             "tokens_per_s": world * n_req / (step_ms * 1e-3),
-            "hbm_frac_of_measured": value / peak,
+            "hbm_frac_of_measured": value / (world * peak),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": a.steps * 2, "clocks": clk,
             "two_call_step": {"ms_per_step": u_step_ms, "attention_ms": u_attn_ms,
-                              "value": job_gbs(world, kv_bytes, u_step_ms), "unit": "GB/s",
+                              "value": job_bytes / (u_step_ms * 1e-3) / 1e9, "unit": "GB/s",
                               "calls": "pa_kv_write then pa_attention (3 launches), timed after the fused steps"},
         }
         print(json.dumps(line))
@@ -517,8 +621,8 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
     secs = max_over_ranks([secs], dist, dev)[0]
     if pa.read_device_errors(clear=True):
         raise RuntimeError("device error flags set during the end-to-end run")
-    mean_bytes = sum(kv_bytes_steps) / len(kv_bytes_steps)
-    return {"value": job_gbs(world, mean_bytes, secs * 1e3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+    mean_bytes = sum_over_ranks([sum(kv_bytes_steps) / len(kv_bytes_steps)], dist, dev)[0]
+    return {"value": mean_bytes / secs / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": secs * 1e3, "steps": steps, "warmup": warm,
             "includes": "host block accounting (pa_bm_append_batch, pa_bm_batch_tables) into pinned memory, one "
                         "H2D copy of q/k/v/slots/table/lens/query_start_loc, pa_write_attention storing out "
@@ -995,7 +1099,13 @@ def run_swap(a):
 
 
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
     a = _args(argv)
+    if a.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # started without a launcher: run this command again as a.gpus ranks, one per GPU
+        if a.workload != "gqa_decode":
+            raise SystemExit("--gpus > 1 runs the default workload (gqa_decode) only")
+        return subprocess.call(launch_command(a.gpus, argv))
     if a.impl == "reference":
         return run_reference(a)
     if a.workload == "mixed":

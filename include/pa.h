@@ -28,6 +28,12 @@
  *    would leave the buffers; such a skip sets a bit in a per-device error word that
  *    pa_read_device_errors() returns. Results are then unspecified but no memory outside
  *    the arguments is touched.
+ *  - Per-device state: the library looks up a few device addresses (the error word, the
+ *    fixed scratch of pa_attention_fixed_scratch) and creates a side stream with two
+ *    events once per device, on first use, and keeps them until exit. A process that
+ *    resets a device (cudaDeviceReset) or otherwise destroys its primary context must not
+ *    call the library for that device afterwards: the kept addresses and handles would be
+ *    stale.
  *
  * Sources (the pages this library restates):
  *  [docs]  "vLLM", docs.acceleratez.fun/llm/model-inference/vllm.html -- PagedAttention
@@ -137,13 +143,22 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
  * Softmax and accumulation in fp32; out is written in `dtype` (bf16 rounded to nearest
  * even). Requests with q_len == 1 run the split-K decode kernel; q_len >= 2 the prefill
  * kernel; q_len == 0 produces no rows. Requires q_len <= L.
- * With rows of both kinds (max_query_len >= 2, bf16) the two kernels run side by side: the
- * call forks an internal stream of the highest priority off `stream` (event record and
- * wait), runs the decode kernels there on 3/5 of the SMs and joins it back before
- * returning, so later work on `stream` is ordered after the whole call, as for one stream.
- * The first such call on a device creates that stream and two events (kept until exit);
- * make it before any stream capture. The decode rows' bits then come from a split over
- * fewer CTAs than in a decode-only call (same tolerance).
+ * With rows of both kinds (max_query_len >= 2) and the tensor-core kernels for both (bf16
+ * q, out and caches; head_dim 64 / 128; block size 8, 16, 32, 64 or 128; at most 4096
+ * requests) the two
+ * kernels run side by side: the call forks an internal stream of the highest priority off
+ * `stream` (event record and wait), runs the decode kernels there on 3/5 of the SMs and
+ * joins it back before returning -- also when a launch fails after the fork -- so later
+ * work on `stream` is ordered after the whole call, as for one stream. The first such call
+ * on a device creates that stream and two events (kept until exit). While `stream` is
+ * being captured into a CUDA graph the call keeps every kernel on `stream` instead (the
+ * internal stream is shared by all callers of the device and must not join a capture).
+ * The decode rows' bits differ between the two ways (a split over fewer CTAs beside the
+ * prefill kernel; same tolerance).
+ * Prefill kernels: the tensor-core kernel takes bf16 batches (q, out and caches) of at
+ * most 4096 requests with a block size of 8, 16, 32, 64 or 128; other prefill batches
+ * (fp32, E4M3 caches, block sizes 1, 2, 4 or above 128, more than 4096 requests) run a
+ * CUDA-core kernel with the same result within the tolerance, many times slower.
  * The result does not depend on which physical blocks hold the tokens: the reduction
  * order is fixed by positions only, so relabelling block ids gives identical bits.
  *

@@ -208,15 +208,53 @@ int prepare_attention(void* out, const void* q, const void* k_cache, const void*
   return PA_OK;
 }
 
-int run_attention(const pa::AttnArgs& a, int ctas, cudaStream_t s) {
-  if (a.max_query_len >= 2 && a.concurrent && pa::prefill_tc_supported(a)) {
+// Whether `s` is being captured into a CUDA graph (an error of the query counts as yes).
+bool stream_capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    cudaGetLastError();  // reset the error state the failed query set
+    return true;
+  }
+  return cs != cudaStreamCaptureStatusNone;
+}
+
+// A cache write to enqueue ahead of the attention kernels (pa_write_attention with prefill
+// rows), after the attention's own host-side preparation.
+struct KvWriteStep {
+  const void* k;
+  const void* v;
+  const int64_t* slot_mapping;
+  int64_t row_bytes;
+};
+
+int run_attention(const pa::AttnArgs& a, int ctas, cudaStream_t s, const KvWriteStep* write = nullptr) {
+  const bool prefill = a.max_query_len >= 2;
+  const bool tc = prefill && pa::prefill_tc_supported(a);
+  pa::PrefillTcPlan plan;
+  if (tc) {  // every host-side step of the prefill launches that can fail, before any launch
+    const cudaError_t e = pa::prepare_prefill_tc(a, &plan);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (write) {
+    const cudaError_t e = pa::launch_kv_write(write->k, write->v, const_cast<void*>(a.k_cache),
+                                              const_cast<void*>(a.v_cache), write->slot_mapping, a.num_tokens,
+                                              a.num_blocks * a.block_size, write->row_bytes, a.err, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  const int hg = pa::decode_hg(a.cache_dtype, a.head_dim, a.num_heads / a.num_kv_heads, a.num_kv_heads);
+  // Side by side only with the tensor-core decode kernel (its CTAs and the prefill kernel's
+  // cannot share an SM, which keeps the SM split below), and never while `s` is captured
+  // into a graph: the internal stream is shared by every caller of the device, and a
+  // capture would hold it until the capture ends.
+  if (tc && a.concurrent && pa::decode_mma_supported(a, hg) && !stream_capturing(s)) {
     // A batch with prefill rows: the decode kernels (HBM-bound) run on 3/5 of the SMs, on a
     // side stream of the highest priority, beside a first prefill launch (tensor-bound) of
     // as many CTAs as the other SMs on the caller's stream, so neither can take the other's
     // SMs whichever is dispatched first. A second prefill launch queued behind the decode
     // merge on the side stream takes the SMs the decode kernel leaves; both launches draw
     // the remaining pairs from one counter, zeroed before the fork. The caller's stream
-    // then waits for the side stream.
+    // then waits for the side stream -- on the error path too, once the fork is recorded,
+    // so nothing the call queued is left unordered against the caller's later work.
     pa::SideStream side;
     cudaError_t e;
     if (!pa::side_stream(&side, &e)) return cuda_fail(e);
@@ -227,19 +265,20 @@ int run_attention(const pa::AttnArgs& a, int ctas, cudaStream_t s) {
     std::lock_guard<std::mutex> lock(*side.mu);
     e = cudaMemsetAsync(a.prefill_sched, 0, sizeof(int), s);
     if (e == cudaSuccess) e = cudaEventRecord(side.fork, s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(side.stream, side.fork, 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaStreamWaitEvent(side.stream, side.fork, 0);
     if (e == cudaSuccess) e = pa::launch_decode(ad, dctas, side.stream);
-    if (e == cudaSuccess) e = pa::launch_prefill_tc(a, pctas, s, pa::PrefillLaunch{true, pctas, false});
-    if (e == cudaSuccess) e = pa::launch_prefill_tc(a, ctas, side.stream, pa::PrefillLaunch{false, pctas, false});
-    if (e == cudaSuccess) e = cudaEventRecord(side.join, side.stream);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, side.join, 0);
+    if (e == cudaSuccess) e = pa::launch_prefill_tc(a, plan, pctas, s, pa::PrefillLaunch{true, pctas, false});
+    if (e == cudaSuccess) e = pa::launch_prefill_tc(a, plan, ctas, side.stream, pa::PrefillLaunch{false, pctas, false});
+    cudaError_t j = cudaEventRecord(side.join, side.stream);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(s, side.join, 0);
+    if (e == cudaSuccess) e = j;
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
   }
   cudaError_t e = pa::launch_decode(a, ctas, s);
   if (e != cudaSuccess) return cuda_fail(e);
-  if (a.max_query_len >= 2) {
-    e = pa::prefill_tc_supported(a) ? pa::launch_prefill_tc(a, ctas, s, pa::PrefillLaunch{true, ctas, true})
-                                    : pa::launch_prefill(a, s);
+  if (prefill) {
+    e = tc ? pa::launch_prefill_tc(a, plan, ctas, s, pa::PrefillLaunch{true, ctas, true}) : pa::launch_prefill(a, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return PA_OK;
@@ -304,11 +343,8 @@ int pa_write_attention(void* out, const void* q, const void* k_new, const void* 
   if (max_query_len >= 2) {
     // prefill rows read their own new tokens from the cache through many CTAs: write every
     // new token first, then attend
-    const int64_t row_bytes = int64_t(num_kv_heads) * head_dim * elem_bytes(dtype);
-    cudaError_t e = pa::launch_kv_write(k_new, v_new, k_cache, v_cache, slot_mapping, num_tokens,
-                                        num_blocks * block_size, row_bytes, a.err, s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    return run_attention(a, ctas, s);
+    const KvWriteStep w{k_new, v_new, slot_mapping, int64_t(num_kv_heads) * head_dim * elem_bytes(dtype)};
+    return run_attention(a, ctas, s, &w);
   }
   a.k_new = k_new;  // a decode-only batch: the decode kernel writes each new token itself
   a.v_new = v_new;

@@ -1047,8 +1047,12 @@ cudaError_t run(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (!GROUPED) return launch_merge<__nv_bfloat16, D>(p, stream, a.merge_pdl);
   const int threads = 32 * (hg * p.group < 32 ? hg * p.group : 32);
-  return launch_pdl(decode_merge_grouped_kernel<__nv_bfloat16, D>, dim3(unsigned(int64_t(a.num_seqs) * p.num_hg)),
-                    dim3(threads), 0, stream, p);
+  const dim3 mgrid(unsigned(int64_t(a.num_seqs) * p.num_hg));
+  if (!a.merge_pdl) {  // plain stream order, as launch_merge
+    decode_merge_grouped_kernel<__nv_bfloat16, D><<<mgrid, dim3(threads), 0, stream>>>(p);
+    return cudaGetLastError();
+  }
+  return launch_pdl(decode_merge_grouped_kernel<__nv_bfloat16, D>, mgrid, dim3(threads), 0, stream, p);
 }
 
 template <typename KV, int D, int BT>

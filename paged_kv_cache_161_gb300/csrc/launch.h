@@ -2,6 +2,7 @@
 // caller (api.cpp); these only pick a kernel instantiation and enqueue it.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -133,6 +134,14 @@ struct PrefillLaunch {
   int ticket_base;
   bool zero_counter;
 };
-cudaError_t launch_prefill_tc(const AttnArgs& a, int num_ctas, cudaStream_t stream, const PrefillLaunch& how);
+// The host-side steps of a call's tensor-core prefill launches that can fail (the Q, K and
+// V tensor maps, the kernel's shared-memory attribute), done once per call before anything
+// of it is enqueued; every launch of the call then uses the plan.
+struct PrefillTcPlan {
+  CUtensorMap qm, km, vm;
+};
+cudaError_t prepare_prefill_tc(const AttnArgs& a, PrefillTcPlan* plan);
+cudaError_t launch_prefill_tc(const AttnArgs& a, const PrefillTcPlan& plan, int num_ctas, cudaStream_t stream,
+                              const PrefillLaunch& how);
 
 }  // namespace pa

@@ -668,13 +668,20 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_
 }
 
 template <int D, int G>
-cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream, const PrefillLaunch& how) {
-  CUtensorMap qm, km, vm;
+cudaError_t prepare(const AttnArgs& a, PrefillTcPlan* plan) {
   const int B = a.block_size;
-  if (!make_map(&qm, a.q, D, uint64_t(a.num_heads), uint64_t(a.num_tokens), G, kBM / G) ||
-      !make_map(&km, a.k_cache, D, uint64_t(a.num_kv_heads), uint64_t(a.num_blocks) * B, 1, B) ||
-      !make_map(&vm, a.v_cache, D, uint64_t(a.num_kv_heads), uint64_t(a.num_blocks) * B, 1, B))
+  if (!make_map(&plan->qm, a.q, D, uint64_t(a.num_heads), uint64_t(a.num_tokens), G, kBM / G) ||
+      !make_map(&plan->km, a.k_cache, D, uint64_t(a.num_kv_heads), uint64_t(a.num_blocks) * B, 1, B) ||
+      !make_map(&plan->vm, a.v_cache, D, uint64_t(a.num_kv_heads), uint64_t(a.num_blocks) * B, 1, B))
     return cudaErrorInvalidValue;
+  if (!a.prefill_sched) return cudaErrorInvalidValue;
+  return cudaFuncSetAttribute(prefill_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(Layout<D>::SMEM));
+}
+
+template <int D, int G>
+cudaError_t run(const AttnArgs& a, const PrefillTcPlan& plan, int num_ctas, cudaStream_t stream,
+                const PrefillLaunch& how) {
   PrefillParams p;
   p.out = a.out;
   p.block_table = a.block_table;
@@ -691,25 +698,34 @@ cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream, const Pref
   p.num_kv_heads = a.num_kv_heads;
   p.block_size = a.block_size;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  auto kern = prefill_tc_kernel<D, G>;
-  const size_t smem = Layout<D>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  if (e != cudaSuccess) return e;
   if (!p.sched || how.ticket_base < 0) return cudaErrorInvalidValue;
   if (how.zero_counter) {
-    e = cudaMemsetAsync(p.sched, 0, sizeof(int), stream);  // the pair counter starts at 0
+    const cudaError_t e = cudaMemsetAsync(p.sched, 0, sizeof(int), stream);  // the pair counter starts at 0
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(kern, dim3(num_ctas), dim3(kThreads), smem, stream, p, qm, km, vm);
+  return launch_pdl(prefill_tc_kernel<D, G>, dim3(num_ctas), dim3(kThreads), Layout<D>::SMEM, stream, p, plan.qm,
+                    plan.km, plan.vm);
 }
 
 template <int D>
-cudaError_t run_g(const AttnArgs& a, int G, int num_ctas, cudaStream_t stream, const PrefillLaunch& how) {
+cudaError_t prepare_g(const AttnArgs& a, int G, PrefillTcPlan* plan) {
   switch (G) {
-    case 1: return run<D, 1>(a, num_ctas, stream, how);
-    case 2: return run<D, 2>(a, num_ctas, stream, how);
-    case 4: return run<D, 4>(a, num_ctas, stream, how);
-    case 8: return run<D, 8>(a, num_ctas, stream, how);
+    case 1: return prepare<D, 1>(a, plan);
+    case 2: return prepare<D, 2>(a, plan);
+    case 4: return prepare<D, 4>(a, plan);
+    case 8: return prepare<D, 8>(a, plan);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <int D>
+cudaError_t run_g(const AttnArgs& a, const PrefillTcPlan& plan, int G, int num_ctas, cudaStream_t stream,
+                  const PrefillLaunch& how) {
+  switch (G) {
+    case 1: return run<D, 1>(a, plan, num_ctas, stream, how);
+    case 2: return run<D, 2>(a, plan, num_ctas, stream, how);
+    case 4: return run<D, 4>(a, plan, num_ctas, stream, how);
+    case 8: return run<D, 8>(a, plan, num_ctas, stream, how);
   }
   return cudaErrorInvalidValue;
 }
@@ -722,10 +738,17 @@ bool prefill_tc_supported(const AttnArgs& a) {
          a.num_seqs <= kMaxSeqs && encode_fn() != nullptr;
 }
 
-cudaError_t launch_prefill_tc(const AttnArgs& a, int num_ctas, cudaStream_t stream, const PrefillLaunch& how) {
+cudaError_t prepare_prefill_tc(const AttnArgs& a, PrefillTcPlan* plan) {
   const int G = a.num_heads / a.num_kv_heads;
-  if (a.head_dim == 64) return run_g<64>(a, G, num_ctas, stream, how);
-  return run_g<128>(a, G, num_ctas, stream, how);
+  if (a.head_dim == 64) return prepare_g<64>(a, G, plan);
+  return prepare_g<128>(a, G, plan);
+}
+
+cudaError_t launch_prefill_tc(const AttnArgs& a, const PrefillTcPlan& plan, int num_ctas, cudaStream_t stream,
+                              const PrefillLaunch& how) {
+  const int G = a.num_heads / a.num_kv_heads;
+  if (a.head_dim == 64) return run_g<64>(a, plan, G, num_ctas, stream, how);
+  return run_g<128>(a, plan, G, num_ctas, stream, how);
 }
 
 }  // namespace pa

@@ -1,13 +1,18 @@
 """CUDA path vs the float64 oracle, element by element, through the C ABI.
 
 Bars: cache writes, block copies, slot mappings and copy pairs bit-exact; attention
-max|err| <= 2e-5 for fp32 inputs, |err| <= 1.5e-2 + 1e-2 * |ref| for bf16 inputs.
+max|err| <= 2e-5 for fp32 inputs; for bf16 inputs the pass bar |err| <= 1.5e-2 + 1e-2 |ref|
+and, beside it, the diagnostic bound of tests/errmodel.py (the kernels' own rounding:
+|err| <= 2^-8 (1 + 2^-7) |ref| + 4 u sigma + 1e-5), which a dropped block or stage fails
+even at 8192 keys. At full size every request of the batch is evaluated, so a request cut
+between CTAs anywhere, the longest one and every chunked prefill are all covered.
 """
 import numpy as np
 import pytest
 import torch
 
 import workloads
+from errmodel import assert_close_bf16, batch_sigma
 from oracle import run_workload, to_f64
 
 pytestmark = pytest.mark.gpu
@@ -21,15 +26,25 @@ def pa():
     return m
 
 
-def _close(got, ref, dtype, what):
+def _close(got, ref, dtype, what, sigma=None):
     got = to_f64(got)
     err = np.abs(got - ref)
     if dtype == "f32":
         assert np.max(err) <= 2e-5, f"{what}: max err {np.max(err)}"
+    elif sigma is not None:
+        assert_close_bf16(got, ref, sigma, what)
     else:
         bound = 1.5e-2 + 1e-2 * np.abs(ref)
         bad = err > bound
         assert not bad.any(), f"{what}: {bad.sum()} elements out of tolerance, worst {np.max(err - bound)}"
+
+
+def _sigma(wl, ref, seqs=None):
+    """Error scale of the diagnostic bound for the evaluated rows (bf16 workloads)."""
+    if wl.spec.dtype != "bf16":
+        return None
+    seqs = range(len(ref.seq_lens)) if seqs is None else seqs
+    return batch_sigma(ref, seqs, wl.spec.scale, wl.spec.block_size)
 
 
 def _run(pa, wl, eval_seqs=None):
@@ -61,44 +76,20 @@ def test_small_workload_matches_oracle(pa, cfg):
     _check_accounting(dw, ref)
     assert np.array_equal(t2s(dw.k_cache), ref.k_cache)
     assert np.array_equal(t2s(dw.v_cache), ref.v_cache)
-    _close(out, ref.out, wl.spec.dtype, wl.name)
-
-
-def _sample(wl, k=10, seed=0):
-    """Batch indices to evaluate: first, last, longest, shortest and random ones."""
-    lens = np.array(wl.meta["final_lens"])
-    batch = wl.step.batch
-    idx = {0, len(batch) - 1, int(np.argmax(lens)), int(np.argmin(lens))}
-    qlens = [q for _, q in batch]
-    if max(qlens) > 1:
-        idx |= {i for i, q in enumerate(qlens) if q > 1}
-    rng = np.random.default_rng(seed)
-    idx |= set(int(i) for i in rng.choice(len(batch), size=min(k, len(batch)), replace=False))
-    return sorted(idx)
+    _close(out, ref.out, wl.spec.dtype, wl.name, _sigma(wl, ref))
 
 
 @pytest.mark.parametrize("cfg", [2, 3, 4, 5])
-def test_full_size_sampled_outputs(pa, cfg):
+def test_full_size_all_requests(pa, cfg):
+    """The workloads at full size (the bench's launch configuration for the GQA batch):
+    the whole caches bit-exact and every request's rows against the oracle."""
     wl = workloads.build(cfg)
-    pick = _sample(wl)
-    dw, st, out, ref, t2s = _run(pa, wl, eval_seqs=pick)
+    dw, st, out, ref, t2s = _run(pa, wl)
     _check_accounting(dw, ref)
     kc, vc = t2s(dw.k_cache), t2s(dw.v_cache)
-    B = wl.spec.block_size
-    for i in pick:  # every slot the evaluated requests read (other rows of a shared block may
-        # have been written in place by a request outside the sample)
-        table = ref.block_table[i]
-        for pos in range(int(ref.seq_lens[i])):
-            blk, off = int(table[pos // B]), pos % B
-            assert np.array_equal(kc[blk, off], ref.k_cache[blk][off]), (i, pos)
-            assert np.array_equal(vc[blk, off], ref.v_cache[blk][off]), (i, pos)
-    qsl = ref.query_start_loc
-    rows = np.concatenate([np.arange(qsl[i], qsl[i + 1]) for i in pick])
-    _close(out[rows], ref.out[rows], wl.spec.dtype, wl.name)
-    # every row: finite and inside the hull of V (a convex combination of V rows)
-    allf = to_f64(out)
-    assert np.isfinite(allf).all()
-    assert np.abs(allf).max() <= to_f64(vc).__abs__().max() + 1e-2
+    assert np.array_equal(kc, ref.k_cache)
+    assert np.array_equal(vc, ref.v_cache)
+    _close(out, ref.out, wl.spec.dtype, wl.name, _sigma(wl, ref))
 
 
 def test_output_bits_independent_of_physical_placement(pa):
@@ -147,7 +138,8 @@ def test_edge_cases(pa, name, spec, ctx, q_lens):
     qsl = ref.query_start_loc
     rows = np.concatenate([np.arange(qsl[i], qsl[i + 1]) for i in range(len(q_lens))])
     if len(rows):
-        _close(out[rows], ref.out[rows], spec.dtype, name)
+        sig = _sigma(wl, ref)
+        _close(out[rows], ref.out[rows], spec.dtype, name, None if sig is None else sig[rows])
 
 
 def test_kv_write_padding_and_bad_slots(pa):

@@ -5,7 +5,11 @@ workspace it uses a fixed scratch array inside the library.
 
 Checked through the C ABI against pa_attention (caller workspace) on the same inputs, on
 two calls in a row: the second call starts from whatever the first left in the shared
-scratch. This file is named to be collected last.
+scratch. Each call's output is also checked directly against the float64 oracle (the pass
+bar, and for bf16 the diagnostic bound of tests/errmodel.py): every request of the reduced
+workloads, and for the full-size GQA and mixed batches the longest request, every
+chunked-prefill request and a seeded sample of the rest. This file is named to be
+collected last.
 """
 import ctypes
 
@@ -14,7 +18,8 @@ import pytest
 import torch
 
 import workloads
-from oracle import to_f64
+from errmodel import assert_close_bf16, batch_sigma
+from oracle import run_workload, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -49,6 +54,18 @@ def test_matches_workspace_entry_point_on_two_calls(cfg, size):
     dw.run_step(st)  # pa_kv_write + pa_attention with a caller workspace
     torch.cuda.synchronize()
     ref = to_f64(torch_to_storage(st.out))
+    n = len(wl.step.batch)
+    if size == "full":
+        lens = wl.meta["final_lens"]
+        pick = {int(np.argmax(lens))} | {i for i, (_, q) in enumerate(wl.step.batch) if q != 1}
+        pick |= set(int(i) for i in np.random.default_rng(cfg).choice(n, 12, replace=False))
+        pick = sorted(pick)
+    else:
+        pick = list(range(n))
+    oref = run_workload(wl, eval_seqs=None if size != "full" else pick)
+    qsl = oref.query_start_loc
+    rows = np.concatenate([np.arange(qsl[i], qsl[i + 1]) for i in pick])
+    sig = batch_sigma(oref, pick, wl.spec.scale, wl.spec.block_size)[rows] if wl.spec.dtype == "bf16" else None
     f = _entry(pa)
     for _ in range(2):
         out = torch.full_like(st.q, float("nan"))
@@ -60,8 +77,10 @@ def test_matches_workspace_entry_point_on_two_calls(cfg, size):
         err = np.abs(got - ref)
         if wl.spec.dtype == "f32":
             assert err.max() <= 2e-5
+            assert np.abs(got[rows] - oref.out[rows]).max() <= 2e-5
         else:
             assert (err <= 1.5e-2 + 1e-2 * np.abs(ref)).all()
+            assert_close_bf16(got[rows], oref.out[rows], sig, f"fixed scratch vs oracle, {wl.name}")
     assert pa.read_device_errors(clear=True) == 0
 
 

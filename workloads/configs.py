@@ -44,6 +44,9 @@ from dataclasses import dataclass, field
 import numpy as np
 
 SEED_BASE = 161000
+# Replica r of a workload (one per rank when a benchmark runs on several GPUs) draws from
+# seed + REPLICA_STRIDE * r: same shapes and distributions, its own lengths and values.
+REPLICA_STRIDE = 1000
 _KIND_K, _KIND_V, _KIND_Q, _KIND_STRUCT = 1, 2, 3, 0
 
 
@@ -240,15 +243,15 @@ def _decode_workload(name, spec, seed, ctx, write_step, rng, pool=None, meta=Non
                     dict(meta or {}, final_lens=final))
 
 
-def _cfg1(size):
-    seed = SEED_BASE + 1
+def _cfg1(size, replica=0):
+    seed = SEED_BASE + 1 + REPLICA_STRIDE * replica
     spec = Spec("f32", 4, 4, 64, 4, 1.0 / 8)
     rng = _rng(seed)
     return _decode_workload("tiny_fp32_decode", spec, seed, [7, 16, 33], True, rng, pool=64)
 
 
-def _cfg2(size):
-    seed = SEED_BASE + 2 + (100 if size == "small" else 0)
+def _cfg2(size, replica=0):
+    seed = SEED_BASE + 2 + (100 if size == "small" else 0) + REPLICA_STRIDE * replica
     spec = Spec("bf16", 32, 32, 128, 16, 1.0 / math.sqrt(128))
     rng = _rng(seed)
     if size == "small":
@@ -258,8 +261,8 @@ def _cfg2(size):
     return _decode_workload("mha_bf16_decode" + ("_small" if size == "small" else ""), spec, seed, ctx, False, rng)
 
 
-def _cfg3(size):
-    seed = SEED_BASE + 3 + (100 if size == "small" else 0)
+def _cfg3(size, replica=0):
+    seed = SEED_BASE + 3 + (100 if size == "small" else 0) + REPLICA_STRIDE * replica
     spec = Spec("bf16", **GQA)
     rng = _rng(seed)
     if size == "small":
@@ -271,8 +274,8 @@ def _cfg3(size):
                             True, rng, meta=dict(lognormal_sigma=1.0, median=med, clip=(lo, hi)))
 
 
-def _cfg4(size):
-    seed = SEED_BASE + 4 + (100 if size == "small" else 0)
+def _cfg4(size, replica=0):
+    seed = SEED_BASE + 4 + (100 if size == "small" else 0) + REPLICA_STRIDE * replica
     spec = Spec("bf16", **GQA)
     rng = _rng(seed)
     if size == "small":
@@ -299,8 +302,8 @@ def _cfg4(size):
                     dict(prompts=P, prompt_len=prompt_len, samples=n_samp, tails=tails, final_lens=final))
 
 
-def _cfg5(size):
-    seed = SEED_BASE + 5 + (100 if size == "small" else 0)
+def _cfg5(size, replica=0):
+    seed = SEED_BASE + 5 + (100 if size == "small" else 0) + REPLICA_STRIDE * replica
     spec = Spec("bf16", **GQA)
     rng = _rng(seed)
     if size == "small":
@@ -413,11 +416,14 @@ def system_prompt(size: str = "full", caching: bool = True) -> Workload:
 CONFIGS = {1: _cfg1, 2: _cfg2, 3: _cfg3, 4: _cfg4, 5: _cfg5}
 
 
-def build(config: int, size: str = "full") -> Workload:
-    """Workload ``config`` (1..5) at ``size`` 'full' or 'small'."""
+def build(config: int, size: str = "full", replica: int = 0) -> Workload:
+    """Workload ``config`` (1..5) at ``size`` 'full' or 'small'; ``replica`` r > 0 gives an
+    independent draw of the same workload (seed + REPLICA_STRIDE * r)."""
     if size not in ("full", "small"):
         raise ValueError(size)
-    return CONFIGS[config](size)
+    if replica < 0:
+        raise ValueError(replica)
+    return CONFIGS[config](size, replica)
 
 
 def custom(spec: Spec, ctx, q_lens, seed: int = SEED_BASE + 999, pool: int | None = None,
