@@ -65,6 +65,7 @@ def _args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fp8", action="store_true", help="mixed / system_prompt workloads over an E4M3 cache")
     ap.add_argument("--workload", choices=["gqa_decode", "mixed", "mha_decode", "shared_prefix", "system_prompt",
                                            "gqa_decode_fp8", "swap"],
                     default="gqa_decode",
@@ -667,6 +668,8 @@ def run_mixed(a):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     wl = workloads.build(5)
+    if a.fp8:
+        wl = workloads.with_fp8_cache(wl)
     sp = wl.spec
     dw = DeviceWorkload(wl, device=dev)
     dw.run_setup()
@@ -678,8 +681,9 @@ def run_mixed(a):
     # algorithmic work: prefill flops (4 * D per query-key pair per query head), decode K/V bytes
     pf_flops = sum(4.0 * sp.head_dim * sp.num_heads * sum(lens[i] - qlens[i] + j + 1 for j in range(qlens[i]))
                    for i in range(C))
-    dec_bytes = sum(lens[i] for i in range(C, len(lens))) * sp.kv_token_bytes
-    pf_kv_bytes = sum(lens[i] for i in range(C)) * sp.kv_token_bytes
+    tok_bytes = sp.kv_token_bytes // 2 if a.fp8 else sp.kv_token_bytes  # E4M3: one byte an element
+    dec_bytes = sum(lens[i] for i in range(C, len(lens))) * tok_bytes
+    pf_kv_bytes = sum(lens[i] for i in range(C)) * tok_bytes
 
     def timed(fn, steps, warm):
         for _ in range(warm):
@@ -694,6 +698,11 @@ def run_mixed(a):
         return e0.elapsed_time(e1) / steps
 
     def attn(b):
+        if a.fp8:
+            return lambda: pa.attention_fp8(b["out"], b["q"], dw.k_cache, dw.v_cache, b["block_table"],
+                                            b["seq_lens"], b["query_start_loc"], max_query_len=b["max_query_len"],
+                                            max_seq_len=b["max_seq_len"], scale=sp.scale, k_scale=wl.k_scale,
+                                            v_scale=wl.v_scale, workspace=st.workspace, stream=stream)
         return lambda: pa.attention(b["out"], b["q"], dw.k_cache, dw.v_cache, b["block_table"], b["seq_lens"],
                                     b["query_start_loc"], max_query_len=b["max_query_len"],
                                     max_seq_len=b["max_seq_len"], scale=sp.scale, workspace=st.workspace,
@@ -720,19 +729,22 @@ def run_mixed(a):
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
     t_star = max(pf_flops / (tflops_peak * 1e12), (dec_bytes + pf_kv_bytes) / (hbm * 1e9)) * 1e3
     line = {
-        "metric": "mixed chunked-prefill + decode attention (8 x 512-query chunks + 248 decodes)",
+        "metric": "mixed chunked-prefill + decode attention (8 x 512-query chunks + 248 decodes)"
+                  + (" over an E4M3 cache" if a.fp8 else ""),
         "value": t_star / attn_ms, "unit": "fraction of max(flops / tensor peak, bytes / HBM peak) roofline time",
         "n_gpus": 1, "steps": steps, "warmup": a.warmup, "ms_per_step": step_ms, "higher_is_better": True,
-        "dtype": "bf16", "data": "synthetic",
+        "dtype": "e4m3 cache, f16 MMA operands" if a.fp8 else "bf16", "data": "synthetic",
         "config": {"workload": "mixed_prefill_decode_bf16: 8 chunks x 512 queries, prior context U[0, 4096]; "
-                               "248 decodes, L ~ U[256, 4096]; 32 q / 8 kv heads, head_dim 128, block 16",
+                               "248 decodes, L ~ U[256, 4096]; 32 q / 8 kv heads, head_dim 128, block 16"
+                               + ("; E4M3 K/V cache (scales 2^-6)" if a.fp8 else ""),
                    "prefill_gflop": pf_flops / 1e9, "decode_kv_bytes": dec_bytes, "seed": wl.seed},
         "attention_ms": attn_ms, "roofline_time_ms": t_star,
         "execution": "one pa_attention call: the decode kernels on 3/5 of the SMs on a side stream beside the "
                      "prefill kernel, whose CTAs also take the rest of the GPU once the decode CTAs are done; "
                      "the two parts below are the same call on each sub-batch alone",
         "prefill": {"ms": pre_ms, "tflops": pre_tf, "peak_tflops": tflops_peak, "frac": pre_tf / tflops_peak,
-                    "bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05)"},
+                    "bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05" +
+                    (", E4M3 codes converted to f16 tiles by the producer warps)" if a.fp8 else ")")},
         "decode": {"ms": dec_ms, "gbs": dec_gbs, "peak_gbs": hbm, "frac": dec_gbs / hbm, "bound": "hbm"},
         "peak_source": src, "clocks": clk,
     }

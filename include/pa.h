@@ -143,9 +143,8 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
  * Softmax and accumulation in fp32; out is written in `dtype` (bf16 rounded to nearest
  * even). Requests with q_len == 1 run the split-K decode kernel; q_len >= 2 the prefill
  * kernel; q_len == 0 produces no rows. Requires q_len <= L.
- * With rows of both kinds (max_query_len >= 2) and the tensor-core kernels for both (bf16
- * q, out and caches; head_dim 64 / 128; block size 8, 16, 32, 64 or 128; at most 4096
- * requests) the two
+ * With rows of both kinds (max_query_len >= 2) and the tensor-core kernels for both (see
+ * "Prefill kernels" below; block size 8, 16, 32, 64 or 128) the two
  * kernels run side by side: the call forks an internal stream of the highest priority off
  * `stream` (event record and wait), runs the decode kernels there on 3/5 of the SMs and
  * joins it back before returning -- also when a launch fails after the fork -- so later
@@ -155,10 +154,11 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
  * internal stream is shared by all callers of the device and must not join a capture).
  * The decode rows' bits differ between the two ways (a split over fewer CTAs beside the
  * prefill kernel; same tolerance).
- * Prefill kernels: the tensor-core kernel takes bf16 batches (q, out and caches) of at
- * most 4096 requests with a block size of 8, 16, 32, 64 or 128; other prefill batches
- * (fp32, E4M3 caches, block sizes 1, 2, 4 or above 128, more than 4096 requests) run a
- * CUDA-core kernel with the same result within the tolerance, many times slower.
+ * Prefill kernels: the tensor-core kernel takes bf16 q and out over bf16 caches (head_dim
+ * 64 / 128) or E4M3 caches (head_dim 128; see pa_attention_fp8), at most 4096 requests,
+ * block size 8, 16, 32, 64 or 128; other prefill batches (fp32, block sizes 1, 2, 4 or
+ * above 128, more than 4096 requests) run a CUDA-core kernel with the same result within
+ * the tolerance, many times slower.
  * The result does not depend on which physical blocks hold the tokens: the reduction
  * order is fixed by positions only, so relabelling block ids gives identical bits.
  *
@@ -274,7 +274,11 @@ int pa_attention_grouped(void* out, const void* q, const void* k_cache, const vo
  * pa_attention_fp8: pa_attention over E4M3 caches with bf16 q and out: K and V are
  * read as value(code) * scale (exact in fp32 up to the scale product), the rest is
  * pa_attention's arithmetic. The split-K decode kernel reads the 1-byte cache directly
- * (half the bytes of bf16); requests with q_len >= 2 run the CUDA-core prefill kernel.
+ * (half the bytes of bf16). Requests with q_len >= 2 run the tensor-core prefill kernel
+ * when head_dim is 128 and the block size is 8, 16, 32, 64 or 128 (at most 4096 requests):
+ * it converts each K/V tile of codes to f16 in shared memory (exact) and the pair's queries
+ * from bf16 to f16, so q must lie within f16's range (|q| < 65520; magnitudes below 2^-24
+ * become 0) and P is rounded to f16; other prefill shapes run the CUDA-core kernel.
  * Workspace from pa_attention_workspace_size. pa_copy_blocks takes PA_FP8_E4M3 caches
  * (byte copy), and pa_kv_write with dtype PA_FP8_E4M3 copies already-encoded rows.
  * --------------------------------------------------------------------------- */

@@ -175,6 +175,11 @@ int prepare_attention(void* out, const void* q, const void* k_cache, const void*
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
+  // Make the device's primary context current on this thread: the tensor maps are encoded
+  // by a driver call before any other CUDA call of the attention path, and in a thread that
+  // has made no CUDA call yet no context is current (the encoding then fails).
+  e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e);
   ctas = pa::decode_num_ctas(dev, &e);
   if (e != cudaSuccess) return cuda_fail(e);
   const size_t dneed = pa::decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, ctas, cache_dtype);

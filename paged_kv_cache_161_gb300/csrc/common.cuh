@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <utility>
 
 #include "pa.h"
@@ -223,6 +224,24 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 // Allow the next grid in the stream (launched with the PDL attribute) to be scheduled.
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Raises kernel Kern's dynamic shared-memory limit to at least `bytes` on the current
+// device, once per device (later calls only read a table). Host threads launching the same
+// kernel concurrently therefore never set its attribute while another thread launches it.
+template <auto Kern>
+static cudaError_t ensure_smem(size_t bytes) {
+  static std::mutex mu;
+  static size_t done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+  if (e == cudaSuccess) done[dev] = bytes;
+  return e;
 }
 
 // Launch with programmatic stream serialisation allowed: the kernel may start while the

@@ -599,7 +599,7 @@ cudaError_t run(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   const int warps = hg * QG;
   const size_t smem = SM::total(hg, warps);
   auto kern = decode_splitk_kernel<T, D, GW, KV>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  cudaError_t e = ensure_smem<decode_splitk_kernel<T, D, GW, KV>>(smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_ctas), dim3((warps + 1) * 32), smem, stream, p);
   if (e != cudaSuccess) return e;

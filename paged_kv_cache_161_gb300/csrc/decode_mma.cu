@@ -1041,7 +1041,7 @@ cudaError_t run(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream) {
   p.q_slot = int(q_slot);
   const size_t smem = C::total(hg, q_slot);
   auto kern = decode_mma_kernel<__nv_bfloat16, D, KV, BT, GROUPED>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  cudaError_t e = ensure_smem<decode_mma_kernel<__nv_bfloat16, D, KV, BT, GROUPED>>(smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_ctas), dim3((hg + 1) * 32), smem, stream, p, km, vm);
   if (e != cudaSuccess) return e;

@@ -183,7 +183,7 @@ cudaError_t run(const AttnArgs& a, cudaStream_t stream) {
   constexpr int kQT = kRows / G;
   const size_t smem = simple_smem_bytes<D>();
   auto kern = prefill_simple_kernel<T, D, G, KV>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  cudaError_t e = ensure_smem<prefill_simple_kernel<T, D, G, KV>>(smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.num_seqs, a.num_kv_heads, (a.max_query_len + kQT - 1) / kQT);
   kern<<<grid, kThreads, smem, stream>>>(a);

@@ -19,7 +19,9 @@
 //                  shared-memory operand), O in TMEM; issued in two halves of 4, keys
 //                  64..127 as soon as the softmax has stored their P, then keys 0..63
 // The two tiles ping-pong: while tile A's softmax runs, the tensor core does tile B's
-// P.V and next Q.K, and the other way round.
+// P.V and next Q.K, and the other way round. E4M3 caches (head_dim 128) take the same
+// path with f16 operands: the producer warps convert each step's codes, and the pair's
+// bf16 queries, to f16 tiles in shared memory.
 //
 // Roles (352 threads, one CTA per SM, persistent: pairs enumerated with the requests
 // longest first and each request's last tiles first; CTA c starts with pair c and then
@@ -32,7 +34,9 @@
 //                    warp's lanes one step ahead);
 //   warp 10          TMA: V (2-deep ring) the same way;
 //   warp 9           allocates the 512 TMEM columns (S_A, S_B, O_A, O_B) and one thread
-//                    issues the MMAs, tracking completion with tcgen05.commit.
+//                    issues the MMAs of both tiles, tracking completion with tcgen05.commit
+//                    (one thread for both keeps the tiles out of phase: a thread per tile
+//                    measured 205 us against 170 us on the mixed batch's prefill part).
 // Every wait is bounded; on a timeout the kernel sets an error bit and leaves after its
 // copies and MMAs in flight have landed, freeing TMEM.
 #include <cuda.h>
@@ -71,7 +75,8 @@ struct PrefillParams {
   int num_heads;
   int num_kv_heads;
   int block_size;
-  float scale_log2;
+  float scale_log2;  // softmax scale x log2(e) (x k_scale over an E4M3 cache)
+  float out_scale;   // 1, or v_scale over an E4M3 cache
 };
 
 template <int D>
@@ -83,10 +88,10 @@ struct Layout {
   static constexpr uint32_t PFX = V + 2 * NH * kHalf;   // int[kMaxSeqs + 8]
   static constexpr uint32_t ORD = PFX + (kMaxSeqs + 8) * 4;  // int[kMaxSeqs + 8], right after PFX
   static constexpr uint32_t BAR = ORD + (kMaxSeqs + 8) * 4;
-  static constexpr int NBAR = 26;
+  static constexpr int NBAR = 31;
   static constexpr uint32_t MISC = BAR + NBAR * 8;       // tmem base, abort flag
-  static constexpr uint32_t RING = MISC + 16;            // int[2]: the next pairs, for every role
-  static constexpr uint32_t BYTES = RING + 16;
+  static constexpr uint32_t RING = MISC + 16;            // RingSlot[2]: the next pairs, for every role
+  static constexpr uint32_t BYTES = RING + 128;
   static constexpr uint32_t SMEM = BYTES + 1024;         // + alignment slack
 };
 
@@ -95,11 +100,13 @@ enum : int {
   bQFull = 0, bQEmpty, bKFull0, bKFull1, bKEmpty0, bKEmpty1, bVFull0, bVFull1, bVEmpty0, bVEmpty1,
   bSFull0, bSFull1, bPFull0, bPFull1, bPVDone0, bPVDone1, bOEmpty0, bOEmpty1, bMmaDone,
   bPHalf0, bPHalf1,  // P of keys 64..127 is in TMEM (the first half of P.V may start)
-  bRingFull0, bRingFull1, bRingEmpty0, bRingEmpty1
+  bRingFull0, bRingFull1, bRingEmpty0, bRingEmpty1,
+  // E4M3 caches: the producer has converted the stage's codes (Q: its bf16 values) to f16
+  bQReady, bKReady0, bKReady1, bVReady0, bVReady1
 };
 // roles that take each pair from the ring: the V producer, the MMA thread, 8 softmax warps
 constexpr uint32_t kRingTakers = 10;
-static_assert(bRingEmpty1 < Layout<128>::NBAR && bRingEmpty1 < Layout<64>::NBAR,
+static_assert(bVReady1 < Layout<128>::NBAR && bVReady1 < Layout<64>::NBAR,
               "every barrier index needs a slot in the shared-memory layout");
 
 // A pair of consecutive query tiles of one (request, KV head); they share every K/V step.
@@ -107,6 +114,14 @@ struct Pair {
   int s, hk, qs, L, leff, nt;
   int q0[2], nq[2], pos0[2];
 };
+
+// A pair as the Q/K producer hands it to the other roles (its ticket t, -1 at the end, and
+// the pair's geometry, so no taker repeats the lookups).
+struct RingSlot {
+  int t;
+  Pair pr;
+};
+static_assert(2 * sizeof(RingSlot) <= 128, "two ring slots in the layout's ring bytes");
 
 // Pair t of the enumeration: the prefill requests in the order ord[0..P) (longest first),
 // each request's pairs with the KV head fastest and the query tiles from the last one back
@@ -145,7 +160,64 @@ __device__ __forceinline__ void pair_info(const PrefillParams& p, const int* pfx
   pr.nt = (q_len > L || pr.nq[0] <= 0) ? 0 : (leff + kBN - 1) / kBN;
 }
 
-template <int D, int G>
+// ---- E4M3 caches: the producer warps turn their operands into f16 tiles in shared memory
+// (every E4M3 value, and every bf16 query in f16's range, is exact in f16), so the MMAs
+// run as kind::f16 with f16 operands exactly as with bf16 caches.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& c01, uint32_t& c23) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(c01), "=r"(c23)
+      : "r"(x));
+}
+
+// One 128-key step of codes -> the step's f16 tile, in place. TMA stored key row r's 128
+// codes (head_dim 128), 128-byte swizzled, in the stage's second 64-dim half; dims 0..63
+// become row r of half 0 and dims 64..127 row r of half 1, swizzled the same way. Rows at
+// or past `valid` become zeros (stale rows of V must not be NaN: P is 0 there, and 0 * NaN
+// is not 0). Each iteration reads its 4 rows (8 lanes a row) before a __syncwarp and
+// stores after it, so a row's half-1 codes are read before they are overwritten; other
+// rows' codes are never written by the iteration.
+__device__ __forceinline__ void convert_kv_step(unsigned char* stage, int valid, int lane) {
+  const int rsub = lane >> 3, c = lane & 7;
+  const unsigned char* codes = stage + kHalf;
+#pragma unroll 4
+  for (int r0 = 0; r0 < kBN; r0 += 4) {
+    const int r = r0 + rsub, sw = r & 7;
+    const uint4 v = *reinterpret_cast<const uint4*>(codes + r * 128 + ((c ^ sw) << 4));
+    __syncwarp();
+    uint32_t h[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    if (r < valid) {
+      e4m3x4_to_f16x2x2(v.x, h[0], h[1]);
+      e4m3x4_to_f16x2x2(v.y, h[2], h[3]);
+      e4m3x4_to_f16x2x2(v.z, h[4], h[5]);
+      e4m3x4_to_f16x2x2(v.w, h[6], h[7]);
+    }
+    unsigned char* row = stage + (c >> 2) * kHalf + r * 128;
+    const int j0 = 2 * (c & 3);  // dims 16c .. 16c + 15 are 16-byte chunks j0, j0 + 1 of the half row
+    *reinterpret_cast<uint4*>(row + ((j0 ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(row + (((j0 + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+    __syncwarp();
+  }
+}
+
+// bf16 -> f16 in place over `bytes` of shared memory (the pair's two query tiles).
+__device__ __forceinline__ void convert_q_to_f16(unsigned char* q, uint32_t bytes, int lane) {
+  uint4* v = reinterpret_cast<uint4*>(q);
+  for (uint32_t i = lane; i < bytes / 16; i += 32) {
+    uint4 x = v[i];
+    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+      const __half2 h = __float22half2_rn(f);
+      w[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    v[i] = x;
+  }
+}
+
+// F8: E4M3 caches (head_dim 128): q and out bf16, K/V codes converted to f16 tiles by the
+// producer warps, MMAs and P in f16.
+template <int D, int G, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillParams p,
                                                                  const __grid_constant__ CUtensorMap qmap,
                                                                  const __grid_constant__ CUtensorMap kmap,
@@ -153,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   using LY = Layout<D>;
   constexpr int NH = LY::NH;
   constexpr int TOK = kBM / G;
+  static_assert(!F8 || D == 128, "E4M3 tiles: one 128-byte row of codes per key");
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1024-byte alignment
@@ -244,19 +317,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   // (dealt in enumeration order as CTAs run out of work; -1 when none is left). The Q/K
   // producer draws the tickets and passes each pair to the other roles through a two-slot
   // ring in shared memory.
-  volatile int* ring = reinterpret_cast<volatile int*>(sm + LY::RING);
-  auto ring_take = [&](int i, int& t) -> bool {  // one thread; false on a timeout
+  RingSlot* ring = reinterpret_cast<RingSlot*>(sm + LY::RING);
+  auto ring_take = [&](int i, int& t, Pair& pr) -> bool {  // one thread; false on a timeout
     if (!mbar_wait(bar(bRingFull0 + (i & 1)), uint32_t(i >> 1) & 1u)) return false;
-    t = ring[i & 1];
+    t = ring[i & 1].t;
+    if (t >= 0) pr = ring[i & 1].pr;
     mbar_arrive(bar(bRingEmpty0 + (i & 1)));
     return true;
   };
-  auto ring_take_warp = [&](int i, int& t) -> bool {  // a whole warp: lane 0 takes, all get it
-    int v = -1, okv = 1;
-    if (lane == 0) okv = ring_take(i, v) ? 1 : 0;
-    okv = __shfl_sync(0xffffffffu, okv, 0);
-    t = __shfl_sync(0xffffffffu, v, 0);
-    return okv != 0;
+  auto ring_take_warp = [&](int i, int& t, Pair& pr) -> bool {  // a whole warp; each lane reads the slot
+    if (!__all_sync(0xffffffffu, mbar_wait(bar(bRingFull0 + (i & 1)), uint32_t(i >> 1) & 1u))) return false;
+    t = ring[i & 1].t;
+    if (t >= 0) pr = ring[i & 1].pr;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(bRingEmpty0 + (i & 1)));
+    return true;
   };
 
   if (threadIdx.x == 0) {
@@ -295,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     bool ok = true;
     for (int i = 0; ok; ++i) {
       int t = -1;
-      if (is_k) {  // draw the CTA's i-th pair and publish it in ring slot i % 2
-        int rok = 1;
+      Pair pr;
+      if (is_k) {  // draw the CTA's i-th pair and publish it, with its geometry, in ring slot i % 2
         if (lane == 0) {
           if (i == 0 && p.first_static) {
             t = int(blockIdx.x);
@@ -304,21 +379,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             t = p.ticket_base + atomicAdd(p.sched, 1);
             if (t >= total) t = -1;
           }
+        }
+        t = __shfl_sync(0xffffffffu, t, 0);
+        if (t >= 0) pair_info<G>(p, pfx, P, t, pr);
+        int rok = 1;
+        if (lane == 0) {
           rok = mbar_wait(bar(bRingEmpty0 + (i & 1)), (uint32_t(i >> 1) & 1u) ^ 1u) ? 1 : 0;
           if (rok) {
-            ring[i & 1] = t;
+            ring[i & 1].t = t;
+            if (t >= 0) ring[i & 1].pr = pr;
             mbar_arrive(bar(bRingFull0 + (i & 1)));
           }
         }
-        t = __shfl_sync(0xffffffffu, t, 0);
         if (!__shfl_sync(0xffffffffu, rok, 0)) { ok = false; break; }
-      } else if (!ring_take_warp(i, t)) {
+      } else if (!ring_take_warp(i, t, pr)) {
         ok = false;
         break;
       }
       if (t < 0) break;
-      Pair pr;
-      pair_info<G>(p, pfx, P, t, pr);
       if (pr.nt == 0) continue;
       if (is_k) {
         int qok = 1;
@@ -354,14 +432,33 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         int wok = 1;
         if (lane == 0) {
           wok = mbar_wait(bar((is_k ? bKEmpty0 : bVEmpty0) + stage), ((n >> 1) & 1) ^ 1) ? 1 : 0;
-          if (wok) mbar_arrive_expect_tx(fb, uint32_t(nload * B * 128 * NH));
+          if (wok) mbar_arrive_expect_tx(fb, uint32_t(nload * B * 128 * (F8 ? 1 : NH)));
         }
         if (!__shfl_sync(0xffffffffu, wok, 0)) { ok = false; break; }
+        const uint32_t sbase = (is_k ? LY::K : LY::V) + uint32_t(stage * NH) * kHalf;
         if (good) {
-          const uint32_t dst = base + (is_k ? LY::K : LY::V) + uint32_t(stage * NH) * kHalf + uint32_t(lane * B * 128);
+          const uint32_t dst = base + sbase + uint32_t(lane * B * 128);
+          if constexpr (F8) {  // the codes of a key row: one 128-byte box row, in half 1
+            tc::tma_load_3d(dst + kHalf, map, 0, pr.hk, int(ent * B), fb);
+          } else {
 #pragma unroll
-          for (int h = 0; h < NH; ++h)
-            tc::tma_load_3d(dst + uint32_t(h) * kHalf, map, 64 * h, pr.hk, int(ent * B), fb);
+            for (int h = 0; h < NH; ++h)
+              tc::tma_load_3d(dst + uint32_t(h) * kHalf, map, 64 * h, pr.hk, int(ent * B), fb);
+          }
+        }
+        if constexpr (F8) {
+          if (is_k && kb == 0) {  // the pair's queries, bf16 -> f16, while K(0) is in flight
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bQFull), tt & 1))) { ok = false; break; }
+            convert_q_to_f16(sm + LY::Q, 2u * NH * kHalf, lane);
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bQReady));
+          }
+          if (!__all_sync(0xffffffffu, mbar_wait(fb, (n >> 1) & 1))) { ok = false; break; }
+          convert_kv_step(sm + sbase, min(kBN, pr.leff - kb * kBN), lane);
+          tc::fence_proxy_async_smem();  // generic-proxy stores -> the MMA's operand reads
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar((is_k ? bKReady0 : bVReady0) + stage));
         }
       }
       ++tt;
@@ -373,8 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     // in S's columns); P.V(B, n); Q.K(B, n + 1). Tile A's softmax overlaps tile B's MMAs
     // and the other way round.
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kBM, kBN, 0);
-      constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kBM, D, 1);
+      constexpr uint32_t idesc_qk = F8 ? tc::idesc_f16_f32(kBM, kBN, 0) : tc::idesc_bf16_f32(kBM, kBN, 0);
+      constexpr uint32_t idesc_pv = F8 ? tc::idesc_f16_f32(kBM, D, 1) : tc::idesc_bf16_f32(kBM, D, 1);
+      constexpr int kQ = F8 ? bQReady : bQFull, kK0 = F8 ? bKReady0 : bKFull0, kV0 = F8 ? bVReady0 : bVFull0;
       // Descriptors are built once per operand and advanced by the byte offset / 16 (the
       // start-address field counts 16-byte units; shared addresses stay below 256 KB, so
       // the 14-bit field never carries), keeping the issuing thread's work per MMA small.
@@ -411,14 +509,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       bool ok = true;
       for (int i = 0; ok; ++i) {
         int t = -1;
-        if (!ring_take(i, t)) { ok = false; break; }
-        if (t < 0) break;
         Pair pr;
-        pair_info<G>(p, pfx, P, t, pr);
+        if (!ring_take(i, t, pr)) { ok = false; break; }
+        if (t < 0) break;
         if (pr.nt == 0) continue;
         const int n0 = n;
-        if (!mbar_wait(bar(bQFull), tt & 1)) { ok = false; break; }
-        if (!mbar_wait(bar(bKFull0 + (n0 & 1)), (n0 >> 1) & 1)) { ok = false; break; }
+        if (!mbar_wait(bar(kQ), tt & 1)) { ok = false; break; }
+        if (!mbar_wait(bar(kK0 + (n0 & 1)), (n0 >> 1) & 1)) { ok = false; break; }
         if (n0 > 0 && (!mbar_wait(bar(bPVDone0), (n0 - 1) & 1) || !mbar_wait(bar(bPVDone1), (n0 - 1) & 1))) {
           ok = false;  // the previous pair's last P.V read P out of S
           break;
@@ -434,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           for (int x = 0; x < 2; ++x) {
             if (!mbar_wait(bar(bPHalf0 + x), n & 1)) { ok = false; break; }
             if (kb == 0 && !mbar_wait(bar(bOEmpty0 + x), (tt & 1) ^ 1)) { ok = false; break; }
-            if (x == 0 && !mbar_wait(bar(bVFull0 + (n & 1)), (n >> 1) & 1)) { ok = false; break; }
+            if (x == 0 && !mbar_wait(bar(kV0 + (n & 1)), (n >> 1) & 1)) { ok = false; break; }
             tc::fence_after_sync();
             pv_half(x, n, 1, kb == 0);
             if (!mbar_wait(bar(bPFull0 + x), n & 1)) { ok = false; break; }
@@ -444,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             if (x == 1) tc::mma_commit(bar(bVEmpty0 + (n & 1)));
             if (more) {
               if (!mbar_wait(bar(bPVDone0 + x), n & 1)) { ok = false; break; }
-              if (x == 0 && !mbar_wait(bar(bKFull0 + ((n + 1) & 1)), ((n + 1) >> 1) & 1)) { ok = false; break; }
+              if (x == 0 && !mbar_wait(bar(kK0 + ((n + 1) & 1)), ((n + 1) >> 1) & 1)) { ok = false; break; }
               tc::fence_after_sync();
               qk(x, n + 1);
               if (x == 1) {
@@ -473,10 +570,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     bool ok = true;
     for (int it = 0; ok; ++it) {
       int t = -1;
-      if (!ring_take_warp(it, t)) { ok = false; break; }
-      if (t < 0) break;
       Pair pr;
-      pair_info<G>(p, pfx, P, t, pr);
+      if (!ring_take_warp(it, t, pr)) { ok = false; break; }
+      if (t < 0) break;
       if (pr.nt == 0) continue;
       const int i = r / G, g = r % G;
       const int nq_x = x ? pr.nq[1] : pr.nq[0];  // selects, not a runtime index into the struct
@@ -548,8 +644,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           const float2 xv = ffma2v(make_float2(s[c], s[c + 1]), sc2, bias2);
           const float2 pp = make_float2(ex2_ftz(xv.x), ex2_ftz(xv.y));
           rs[(c >> 1) & 3] = fadd2(rs[(c >> 1) & 3], pp);
-          __nv_bfloat162 hh = __floats2bfloat162_rn(pp.x, pp.y);
-          pk[c / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&hh));
+          if constexpr (F8) {
+            __half2 hh = __floats2half2_rn(pp.x, pp.y);
+            pk[c / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&hh));
+          } else {
+            __nv_bfloat162 hh = __floats2bfloat162_rn(pp.x, pp.y);
+            pk[c / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&hh));
+          }
         };
         {
           float pk[32];
@@ -563,8 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tc::tmem_ld32(trow + scol + 32u, *reinterpret_cast<float(*)[32]>(s + 32));
         // last step: V rows past the keys the pair needs may hold stale or invalid data;
         // P is 0 there, but 0 * NaN is NaN in the MMA: tile A's threads zero them before
-        // any P.V of the step starts
-        if (x == 0 && kb == pr.nt - 1 && pr.leff - key0 < kBN) {
+        // any P.V of the step starts (E4M3 caches: the V converter writes zeros there)
+        if (!F8 && x == 0 && kb == pr.nt - 1 && pr.leff - key0 < kBN) {
           if (!mbar_wait(bar(bVFull0 + (n & 1)), (n >> 1) & 1)) { ok = false; break; }
           if (r >= pr.leff - key0) {
 #pragma unroll
@@ -604,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       // ---- epilogue: O / l -> out
       if (!mbar_wait(bar(bPVDone0 + x), (n - 1) & 1)) { ok = false; break; }
       tc::fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? p.out_scale / l : 0.f;
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
                            (int64_t(pr.qs + q0_x + i) * p.num_heads + pr.hk * G + g) * D;
       // two 32-column loads per wait (the score registers are free here)
@@ -654,32 +755,34 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D bf16 map over [d2][d1][d0] (d0 contiguous), box {64, b1, b2}, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1, uint32_t b2) {
+// 3-D map over [d2][d1][d0] (d0 contiguous) of bf16 (el 2) or 1-byte codes (el 1), box
+// {128 bytes of d0, b1, b2}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, int el, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1,
+              uint32_t b2) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
-  const cuuint32_t box[3] = {64, b1, b2};
+  const cuuint64_t strides[2] = {d0 * el, d0 * d1 * el};
+  const cuuint32_t box[3] = {cuuint32_t(128 / el), b1, b2};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, el == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 cudaError_t prepare(const AttnArgs& a, PrefillTcPlan* plan) {
   const int B = a.block_size;
-  if (!make_map(&plan->qm, a.q, D, uint64_t(a.num_heads), uint64_t(a.num_tokens), G, kBM / G) ||
-      !make_map(&plan->km, a.k_cache, D, uint64_t(a.num_kv_heads), uint64_t(a.num_blocks) * B, 1, B) ||
-      !make_map(&plan->vm, a.v_cache, D, uint64_t(a.num_kv_heads), uint64_t(a.num_blocks) * B, 1, B))
+  const int el = F8 ? 1 : 2;
+  if (!make_map(&plan->qm, a.q, 2, D, uint64_t(a.num_heads), uint64_t(a.num_tokens), G, kBM / G) ||
+      !make_map(&plan->km, a.k_cache, el, D, uint64_t(a.num_kv_heads), uint64_t(a.num_blocks) * B, 1, B) ||
+      !make_map(&plan->vm, a.v_cache, el, D, uint64_t(a.num_kv_heads), uint64_t(a.num_blocks) * B, 1, B))
     return cudaErrorInvalidValue;
   if (!a.prefill_sched) return cudaErrorInvalidValue;
-  return cudaFuncSetAttribute(prefill_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(Layout<D>::SMEM));
+  return ensure_smem<prefill_tc_kernel<D, G, F8>>(Layout<D>::SMEM);
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 cudaError_t run(const AttnArgs& a, const PrefillTcPlan& plan, int num_ctas, cudaStream_t stream,
                 const PrefillLaunch& how) {
   PrefillParams p;
@@ -697,35 +800,38 @@ cudaError_t run(const AttnArgs& a, const PrefillTcPlan& plan, int num_ctas, cuda
   p.num_heads = a.num_heads;
   p.num_kv_heads = a.num_kv_heads;
   p.block_size = a.block_size;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
+  // E4M3: a K code stands for value * k_scale (folded into the logit scale), a V code for
+  // value * v_scale (folded into the final 1 / l)
+  p.scale_log2 = a.scale * 1.4426950408889634f * (F8 ? a.k_scale : 1.f);
+  p.out_scale = F8 ? a.v_scale : 1.f;
   if (!p.sched || how.ticket_base < 0) return cudaErrorInvalidValue;
   if (how.zero_counter) {
     const cudaError_t e = cudaMemsetAsync(p.sched, 0, sizeof(int), stream);  // the pair counter starts at 0
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(prefill_tc_kernel<D, G>, dim3(num_ctas), dim3(kThreads), Layout<D>::SMEM, stream, p, plan.qm,
-                    plan.km, plan.vm);
+  return launch_pdl(prefill_tc_kernel<D, G, F8>, dim3(num_ctas), dim3(kThreads), Layout<D>::SMEM, stream, p,
+                    plan.qm, plan.km, plan.vm);
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t prepare_g(const AttnArgs& a, int G, PrefillTcPlan* plan) {
   switch (G) {
-    case 1: return prepare<D, 1>(a, plan);
-    case 2: return prepare<D, 2>(a, plan);
-    case 4: return prepare<D, 4>(a, plan);
-    case 8: return prepare<D, 8>(a, plan);
+    case 1: return prepare<D, 1, F8>(a, plan);
+    case 2: return prepare<D, 2, F8>(a, plan);
+    case 4: return prepare<D, 4, F8>(a, plan);
+    case 8: return prepare<D, 8, F8>(a, plan);
   }
   return cudaErrorInvalidValue;
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t run_g(const AttnArgs& a, const PrefillTcPlan& plan, int G, int num_ctas, cudaStream_t stream,
                   const PrefillLaunch& how) {
   switch (G) {
-    case 1: return run<D, 1>(a, plan, num_ctas, stream, how);
-    case 2: return run<D, 2>(a, plan, num_ctas, stream, how);
-    case 4: return run<D, 4>(a, plan, num_ctas, stream, how);
-    case 8: return run<D, 8>(a, plan, num_ctas, stream, how);
+    case 1: return run<D, 1, F8>(a, plan, num_ctas, stream, how);
+    case 2: return run<D, 2, F8>(a, plan, num_ctas, stream, how);
+    case 4: return run<D, 4, F8>(a, plan, num_ctas, stream, how);
+    case 8: return run<D, 8, F8>(a, plan, num_ctas, stream, how);
   }
   return cudaErrorInvalidValue;
 }
@@ -734,21 +840,25 @@ cudaError_t run_g(const AttnArgs& a, const PrefillTcPlan& plan, int G, int num_c
 
 bool prefill_tc_supported(const AttnArgs& a) {
   const int B = a.block_size;
-  return a.dtype == PA_BF16 && a.cache_dtype == PA_BF16 && (a.head_dim == 64 || a.head_dim == 128) && B >= 8 && B <= kBN && kBN % B == 0 &&
-         a.num_seqs <= kMaxSeqs && encode_fn() != nullptr;
+  const bool types = a.dtype == PA_BF16 &&
+                     ((a.cache_dtype == PA_BF16 && (a.head_dim == 64 || a.head_dim == 128)) ||
+                      (a.cache_dtype == PA_FP8_E4M3 && a.head_dim == 128));
+  return types && B >= 8 && B <= kBN && kBN % B == 0 && a.num_seqs <= kMaxSeqs && encode_fn() != nullptr;
 }
 
 cudaError_t prepare_prefill_tc(const AttnArgs& a, PrefillTcPlan* plan) {
   const int G = a.num_heads / a.num_kv_heads;
-  if (a.head_dim == 64) return prepare_g<64>(a, G, plan);
-  return prepare_g<128>(a, G, plan);
+  if (a.cache_dtype == PA_FP8_E4M3) return prepare_g<128, true>(a, G, plan);
+  if (a.head_dim == 64) return prepare_g<64, false>(a, G, plan);
+  return prepare_g<128, false>(a, G, plan);
 }
 
 cudaError_t launch_prefill_tc(const AttnArgs& a, const PrefillTcPlan& plan, int num_ctas, cudaStream_t stream,
                               const PrefillLaunch& how) {
   const int G = a.num_heads / a.num_kv_heads;
-  if (a.head_dim == 64) return run_g<64>(a, plan, G, num_ctas, stream, how);
-  return run_g<128>(a, plan, G, num_ctas, stream, how);
+  if (a.cache_dtype == PA_FP8_E4M3) return run_g<128, true>(a, plan, G, num_ctas, stream, how);
+  if (a.head_dim == 64) return run_g<64, false>(a, plan, G, num_ctas, stream, how);
+  return run_g<128, false>(a, plan, G, num_ctas, stream, how);
 }
 
 }  // namespace pa

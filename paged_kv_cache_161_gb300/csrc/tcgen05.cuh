@@ -67,6 +67,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_maj
          | (uint32_t(M >> 4) << 24);     // M / 16
 }
 
+// The same with A = B = f16 (kind::f16, atype = btype = 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int b_mn_major) {
+  return (1u << 4)                       // D format: f32
+         | (uint32_t(b_mn_major) << 16)  // B major
+         | (uint32_t(N >> 3) << 17)      // N / 8
+         | (uint32_t(M >> 4) << 24);     // M / 16
+}
+
 // Shared-memory matrix descriptor with 128-byte swizzling. lbo / sbo in bytes.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;

@@ -2,7 +2,10 @@
 
 Bars: the quantised cache bytes bit-exact (E4M3(x / scale), binary32 division, round to
 nearest even, saturation); attention over the cache |err| <= 1.5e-2 + 1e-2 * |ref|
-against the oracle's float64 attention over the dequantised values.
+against the oracle's float64 attention over the dequantised values. Chunked-prefill rows
+over an E4M3 cache run on the tensor cores (codes converted to f16 tiles in shared
+memory): the mixed batch at full size (every request), the system-prompt batches with and
+without prefix caching, and edge cases of group size, block size and context.
 """
 import numpy as np
 import pytest
@@ -139,3 +142,68 @@ def test_fp8_copy_blocks_and_argument_checks(pa):
         pa.kv_write_fp8(torch.zeros((1, H, D), dtype=torch.bfloat16, device="cuda"),
                         torch.zeros((1, H, D), dtype=torch.bfloat16, device="cuda"), kc, vc,
                         torch.zeros(1, dtype=torch.int64, device="cuda"), 0.0, 1.0)
+
+
+FP8_PREFILL_EDGE = [
+    # (name, spec, ctx, q_lens)
+    ("g4_b16_mixed", workloads.Spec("bf16", 32, 8, 128, 16, 0.088), [0, 100, 300, 7, 900], [200, 77, 5, 1, 1]),
+    ("g1_b64", workloads.Spec("bf16", 8, 8, 128, 64, 0.088), [50, 0], [130, 300]),
+    ("g2_b128", workloads.Spec("bf16", 8, 4, 128, 128, 0.088), [129, 0], [40, 256]),
+    ("g8_b8", workloads.Spec("bf16", 32, 4, 128, 8, 0.088), [17, 0], [60, 2]),
+    ("g4_b32_long_prior", workloads.Spec("bf16", 32, 8, 128, 32, 0.088), [3000], [300]),
+]
+
+
+@pytest.mark.parametrize("name,spec,ctx,q_lens", FP8_PREFILL_EDGE, ids=[e[0] for e in FP8_PREFILL_EDGE])
+def test_fp8_prefill_edge_cases(pa, name, spec, ctx, q_lens):
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload, torch_to_storage
+
+    wl = workloads.with_fp8_cache(workloads.custom(spec, ctx, q_lens, name=name), k_scale=2.0 ** -5,
+                                  v_scale=0.0173)
+    dw = DeviceWorkload(wl)
+    dw.run_setup()
+    st = dw.prepare_step()
+    dw.run_step(st)
+    torch.cuda.synchronize()
+    assert pa.read_device_errors(clear=True) == 0
+    ref = run_workload(wl)
+    assert np.array_equal(torch_to_storage(dw.k_cache), ref.k_cache)
+    _close(torch_to_storage(st.out), ref.out, name)
+
+
+def test_fp8_full_size_mixed_all_requests(pa):
+    """The mixed batch (8 chunks of 512 queries + 248 decodes) over an E4M3 cache: every
+    request's rows against the oracle."""
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload, torch_to_storage
+
+    wl = workloads.with_fp8_cache(workloads.build(5))
+    dw = DeviceWorkload(wl)
+    dw.run_setup()
+    st = dw.prepare_step()
+    dw.run_step(st)
+    torch.cuda.synchronize()
+    assert pa.read_device_errors(clear=True) == 0
+    ref = run_workload(wl)
+    assert np.array_equal(torch_to_storage(dw.k_cache), ref.k_cache)
+    _close(torch_to_storage(st.out), ref.out, wl.name)
+
+
+@pytest.mark.parametrize("size,caching", [("small", True), ("small", False), ("full", True)])
+def test_fp8_system_prompt(pa, size, caching):
+    """Requests reusing a cached system prompt (or computing it all) over an E4M3 cache."""
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload, torch_to_storage
+
+    wl = workloads.with_fp8_cache(workloads.system_prompt(size, caching=caching))
+    dw = DeviceWorkload(wl)
+    dw.run_setup()
+    st = dw.prepare_step()
+    dw.run_step(st)
+    torch.cuda.synchronize()
+    assert pa.read_device_errors(clear=True) == 0
+    n = wl.meta["requests"]
+    pick = list(range(n)) if size == "small" else [0, 17, 40, 63]
+    ref = run_workload(wl, eval_seqs=None if size == "small" else pick)
+    assert np.array_equal(st.query_start_loc.cpu().numpy(), ref.query_start_loc)
+    qsl = ref.query_start_loc
+    rows = np.concatenate([np.arange(qsl[i], qsl[i + 1]) for i in pick])
+    _close(torch_to_storage(st.out)[rows], ref.out[rows], wl.name)

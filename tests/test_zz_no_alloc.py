@@ -58,7 +58,7 @@ def test_matches_workspace_entry_point_on_two_calls(cfg, size):
     if size == "full":
         lens = wl.meta["final_lens"]
         pick = {int(np.argmax(lens))} | {i for i, (_, q) in enumerate(wl.step.batch) if q != 1}
-        pick |= set(int(i) for i in np.random.default_rng(cfg).choice(n, 12, replace=False))
+        pick |= set(int(i) for i in np.random.default_rng(cfg).choice(n, min(12, n), replace=False))
         pick = sorted(pick)
     else:
         pick = list(range(n))
