@@ -65,9 +65,11 @@ def _args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="leave out the other workloads' summary lines from the default run")
     ap.add_argument("--fp8", action="store_true", help="mixed / system_prompt workloads over an E4M3 cache")
-    ap.add_argument("--workload", choices=["gqa_decode", "mixed", "mha_decode", "shared_prefix", "system_prompt",
-                                           "gqa_decode_fp8", "swap"],
+    ap.add_argument("--workload", choices=["gqa_decode", "mixed", "prefill", "mha_decode", "shared_prefix",
+                                           "system_prompt", "gqa_decode_fp8", "swap"],
                     default="gqa_decode",
                     help="gqa_decode: the headline line (default); mixed: the chunked-prefill + decode "
                          "batch, timed whole and as its prefill-only and decode-only sub-batches; "
@@ -239,8 +241,9 @@ def _oracle_state(wl, eval_seqs):
             t0 += a[2]
     step_apps = wl.appends(wl.step, lens)
     step_vals = wl.kv_many(step_apps)
-    k_new = np.concatenate([v[0] for v in step_vals])
-    v_new = np.concatenate([v[1] for v in step_vals])
+    empty = np.zeros((0, sp.num_kv_heads, sp.head_dim), np.float32 if sp.dtype == "f32" else np.uint16)
+    k_new = np.concatenate([v[0] for v in step_vals]) if step_vals else empty  # (attention-only steps
+    v_new = np.concatenate([v[1] for v in step_vals]) if step_vals else empty  # write nothing)
     bt, seq_lens, qsl, seqs = batch_metadata(wl, alloc)
     q = np.concatenate([wl.q(s, a, n) for s, a, n in wl.step_queries()])
     return dict(kc=kc, vc=vc, k_new=k_new, v_new=v_new, slots=slots_pp[-1], copies=copies_pp[-1], bt=bt,
@@ -267,12 +270,12 @@ def _cpu_sample_bytes(wl, st, eval_seqs):
     return int(sum(int(st["seq_lens"][i]) for i in eval_seqs)) * wl.spec.kv_token_bytes
 
 
-def _oracle_worker(conn, replica, shard):
+def _oracle_worker(conn, replica, shard, config=CONFIG_ID):
     """One process of OraclePool: builds its shard's oracle state once (untimed), then runs
     one oracle step over the shard per request and answers with its seconds."""
     import workloads
 
-    wl = workloads.build(CONFIG_ID, replica=replica)
+    wl = workloads.build(config, replica=replica)
     st = _oracle_state(wl, shard) if shard else None
     conn.send(_cpu_sample_bytes(wl, st, shard) if shard else 0)
     while conn.recv():
@@ -288,7 +291,7 @@ class OraclePool:
 
     THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
 
-    def __init__(self, seqs, replica=0, workers=None):
+    def __init__(self, seqs, replica=0, workers=None, config=CONFIG_ID):
         import multiprocessing as mp
 
         n = workers or len(os.sched_getaffinity(0))
@@ -301,7 +304,8 @@ class OraclePool:
         try:
             for k in range(self.workers):
                 a, b = ctx.Pipe()
-                p = ctx.Process(target=_oracle_worker, args=(b, replica, list(seqs[k::self.workers])), daemon=True)
+                p = ctx.Process(target=_oracle_worker, args=(b, replica, list(seqs[k::self.workers]), config),
+                                daemon=True)
                 p.start()
                 self.conns.append(a)
                 self.procs.append(p)
@@ -326,6 +330,63 @@ class OraclePool:
             c.send(False)
         for p in self.procs:
             p.join(timeout=30)
+
+
+def _secondary(a):
+    """The other workloads at full size, summarised into the default line (one GPU): the
+    mixed chunked-prefill + decode batch, MHA decode, the shared-prefix batch (plain and
+    grouped decode), each with its roofline fraction and the oracle over the host's cores on
+    the same workload (one whole pass: a baseline, not a target)."""
+    import copy
+
+    out = {}
+    hbm, tflops, src = _peaks()
+    specs = [("mixed", "mixed", 5), ("mha_decode", "mha_decode", 2), ("shared_prefix", "shared_prefix", 4)]
+    for name, wname, cfg in specs:
+        b = copy.copy(a)
+        b.workload, b.fp8 = wname, False
+        b.steps = max(30, a.steps // 4)
+        try:
+            ln = mixed_line(b) if name == "mixed" else secondary_line(b)
+        except Exception as e:  # keep the headline line whatever happens here
+            out[name] = {"error": f"{type(e).__name__}: {e}"}
+            continue
+        if name == "mixed":
+            d = {"value": ln["value"], "unit": ln["unit"], "attention_ms": ln["attention_ms"],
+                 "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel (the batch's prefill part alone)",
+                              "achieved": ln["prefill"]["tflops"], "peak": tflops, "unit": "TFLOP/s",
+                              "frac": ln["prefill"]["frac"], "ms": ln["prefill"]["ms"]},
+                 "decode_part": {"bound": "hbm", "achieved": ln["decode"]["gbs"], "peak": hbm, "unit": "GB/s",
+                                 "frac": ln["decode"]["frac"], "ms": ln["decode"]["ms"]},
+                 "clocks": ln["clocks"]}
+        elif name == "mha_decode":
+            d = {"attention_ms": ln["attention_ms"],
+                 "roofline": {"bound": "hbm", "kernel": "decode_mma_kernel + merge (pa_attention)",
+                              "achieved": ln["attention_gbs_logical"], "peak": hbm, "unit": "GB/s",
+                              "frac": ln["frac_logical"]}, "clocks": ln["clocks"]}
+        else:
+            g = ln["grouped"]
+            d = {"attention_ms": ln["attention_ms"], "attention_gbs_logical": ln["attention_gbs_logical"],
+                 "frac_logical": ln["attention_gbs_logical"] / hbm, "frac_unique": ln["frac_unique"],
+                 "roofline": {"bound": "hbm", "kernel": "pa_attention_grouped (distinct blocks read once)",
+                              "achieved": g["gbs_unique"], "peak": hbm, "unit": "GB/s", "frac": g["frac_unique"],
+                              "ms": g["ms"]},
+                 "copy_blocks": ln["copy_blocks"], "kv_write": ln["kv_write"], "clocks": ln["clocks"]}
+        d["peak_source"] = src
+        try:
+            import workloads
+
+            wl = workloads.build(cfg)
+            pool = OraclePool(list(range(len(wl.step.batch))), config=cfg)
+            wall, cpu = pool.step()
+            pool.close()
+            d["cpu_baseline"] = {"value": pool.nbytes / wall / 1e9, "unit": "GB/s of K/V", "cores": pool.workers,
+                                 "kind": "oracle", "seconds": wall, "cpu_seconds": cpu,
+                                 "sample": "the whole step (every request's copies, writes and attention), one pass"}
+        except Exception as e:
+            d["cpu_baseline"] = {"error": f"{type(e).__name__}: {e}"}
+        out[name] = d
+    return out
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -460,6 +521,8 @@ def run_ours(a):
     e2e = None
     if not a.no_e2e:
         e2e = _e2e(a, pa, dw, st, wl, dev, stream, world, dist)
+        e2e_copy = _e2e(a, pa, dw, st, wl, dev, stream, world, dist, copy_rows=True)
+        e2e["rows_copied_variant"] = {k: e2e_copy[k] for k in ("value", "ms_per_step", "h2d_copied_bytes_per_step")}
 
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(peaks_path):
@@ -488,6 +551,10 @@ def run_ours(a):
                "sample": f"the whole step (all 256 requests: their KV writes and attention) dealt over "
                          f"{pool.workers} processes, {len(walls)} passes, mean wall time per pass"}
 
+    secondary = None
+    if rank == 0 and world == 1 and not a.no_secondary:
+        secondary = _secondary(a)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": a.steps,
@@ -504,20 +571,24 @@ def run_ours(a):
                               "value": job_bytes / (u_step_ms * 1e-3) / 1e9, "unit": "GB/s",
                               "calls": "pa_kv_write then pa_attention (3 launches), timed after the fused steps"},
         }
+        if secondary is not None:
+            line["secondary_workloads"] = secondary
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
     return 0
 
 
-def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
+def _e2e(a, pa, dw, st, wl, dev, stream, world, dist, copy_rows=False):
     """Decode steps as a serving loop runs them: host block accounting (C++, one batched
     append and one table fill per step) into a pinned staging buffer, one host->device copy
-    of the step's inputs, write + attention with `out` in pinned host memory (the kernels
-    store the result rows over the CPU-GPU link), the result waited for before the next step
-    is launched; host wall time per step. The accounting of step n + 1 does not depend on
-    step n's output (one token per request), so it runs while the GPU works on step n, into
-    the other of two staging buffers."""
+    of the step's metadata (slots, tables, lengths, query_start_loc), write + attention with
+    q / k / v and `out` in pinned host memory (the decode kernel reads the rows and stores
+    the results over the CPU-GPU link itself; with ``copy_rows`` the rows are copied to the
+    device with the metadata instead), the result waited for before the next step is
+    launched; host wall time per step. The accounting of step n + 1 does not depend on step
+    n's output (one token per request), so it runs while the GPU works on step n, into the
+    other of two staging buffers."""
     import numpy as np
     import torch
 
@@ -526,9 +597,10 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
     ones = np.ones(len(seqs), np.int64)
     S = len(seqs)
     width = int(st.block_table.shape[1])
-    # pinned buffers holding every input of a step (two, used in turn), and one device twin
-    parts = [("q", st.q.numel() * 2), ("k", st.k_new.numel() * 2), ("v", st.v_new.numel() * 2),
-             ("slots", S * 8), ("table", S * width * 4), ("lens", S * 4), ("qsl", (S + 1) * 4)]
+    # pinned buffers holding every input of a step (two, used in turn), and one device twin;
+    # the metadata first, so that its copy is one contiguous prefix
+    parts = [("slots", S * 8), ("table", S * width * 4), ("lens", S * 4), ("qsl", (S + 1) * 4),
+             ("q", st.q.numel() * 2), ("k", st.k_new.numel() * 2), ("v", st.v_new.numel() * 2)]
     off, offs = 0, {}
     for name, nbytes in parts:
         offs[name] = (off, nbytes)
@@ -547,9 +619,9 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
         view(h_buf, "qsl", torch.int32, (S + 1,)).copy_(torch.arange(S + 1, dtype=torch.int32))
     host = [(view(h, "slots", torch.int64, (S,)).numpy(), view(h, "table", torch.int32, (S, width)).numpy(),
              view(h, "lens", torch.int32, (S,)).numpy()) for h in h_bufs]
-    q_d = view(d_buf, "q", torch.bfloat16, st.q.shape)
-    k_d = view(d_buf, "k", torch.bfloat16, st.k_new.shape)
-    v_d = view(d_buf, "v", torch.bfloat16, st.v_new.shape)
+    meta = offs["q"][0]  # bytes of the metadata prefix
+    rows = [tuple(view(buf, n, torch.bfloat16, t.shape) for n, t in (("q", st.q), ("k", st.k_new), ("v", st.v_new)))
+            for buf in ([d_buf, d_buf] if copy_rows else h_bufs)]
     slots_d = view(d_buf, "slots", torch.int64, (S,))
     table_d = view(d_buf, "table", torch.int32, (S, width))
     lens_d = view(d_buf, "lens", torch.int32, (S,))
@@ -566,9 +638,11 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
         bm.batch_tables(seqs, width, table_out=table_h, lens_out=lens_h)
         return int(lens_h.max()), int(lens_h.astype(np.int64).sum()) * sp.kv_token_bytes
 
-    def enqueue(b, max_len, s):  # the step's copies and call on stream s
-        d_buf.copy_(h_bufs[b], non_blocking=True)
-        pa.write_attention(out_h, q_d, k_d, v_d, slots_d, dw.k_cache, dw.v_cache, table_d, lens_d, qsl_d,
+    def enqueue(b, max_len, s):  # the step's copy and call on stream s
+        n = off if copy_rows else meta
+        d_buf[:n].copy_(h_bufs[b][:n], non_blocking=True)
+        q_x, k_x, v_x = rows[b]
+        pa.write_attention(out_h, q_x, k_x, v_x, slots_d, dw.k_cache, dw.v_cache, table_d, lens_d, qsl_d,
                            max_query_len=1, max_seq_len=max_len, scale=sp.scale, workspace=st.workspace, stream=s)
 
     graphs = None  # after the warm-up: one CUDA graph per staging buffer (H2D, call, D2H)
@@ -625,10 +699,14 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist):
     mean_bytes = sum_over_ranks([sum(kv_bytes_steps) / len(kv_bytes_steps)], dist, dev)[0]
     return {"value": mean_bytes / secs / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": secs * 1e3, "steps": steps, "warmup": warm,
+            "h2d_copied_bytes_per_step": off if copy_rows else meta,
             "includes": "host block accounting (pa_bm_append_batch, pa_bm_batch_tables) into pinned memory, one "
-                        "H2D copy of q/k/v/slots/table/lens/query_start_loc, pa_write_attention storing out "
-                        "straight into pinned host memory (the D2H bytes), waited for before the next step is "
-                        "launched; the next step's accounting runs while the GPU works (two staging buffers)",
+                        "H2D copy of slots/table/lens/query_start_loc" +
+                        (" and q/k/v" if copy_rows else "; q/k/v read by the decode kernel straight from pinned "
+                         "host memory (the rest of the H2D bytes)") +
+                        ", pa_write_attention storing out straight into pinned host memory (the D2H bytes), "
+                        "waited for before the next step is launched; the next step's accounting runs while the "
+                        "GPU works (two staging buffers)",
             "launch": graph_note}
 
 
@@ -656,7 +734,7 @@ def _sub_batch(st, rows_of, idx, dev):
                 max_query_len=int(lens_q.max()), max_seq_len=int(st.seq_lens.index_select(0, idx_t).max()))
 
 
-def run_mixed(a):
+def mixed_line(a):
     """The mixed chunked-prefill + decode batch (8 chunks of 512 queries with prior context
     U[0, 4096] + 248 decodes with L ~ U[256, 4096]): whole step, and each part alone."""
     import torch
@@ -748,11 +826,100 @@ def run_mixed(a):
         "decode": {"ms": dec_ms, "gbs": dec_gbs, "peak_gbs": hbm, "frac": dec_gbs / hbm, "bound": "hbm"},
         "peak_source": src, "clocks": clk,
     }
+    return line
+
+
+def run_mixed(a):
+    print(json.dumps(mixed_line(a)))
+    return 0
+
+
+def run_prefill(a):
+    """The mixed batch's 8 chunked-prefill requests alone, as one prefill launch over all SMs
+    (pa_attention_fixed_scratch keeps every kernel on the caller's stream) and through
+    pa_attention (two prefill launches sharing one pair counter, the first on the SMs a
+    decode kernel would leave): the tensor-core kernel's own roofline fraction."""
+    import torch
+
+    import paged_kv_cache_161_gb300 as pa
+    import workloads
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    wl = workloads.build(5)
+    if a.fp8:
+        wl = workloads.with_fp8_cache(wl)
+    sp = wl.spec
+    dw = DeviceWorkload(wl, device=dev)
+    dw.run_setup()
+    st = dw.prepare_step()
+    dw.run_step(st)  # writes the chunks' own K/V
+    stream = torch.cuda.current_stream(dev)
+    C = wl.meta["chunks"]
+    b = _sub_batch(st, None, list(range(C)), dev)
+    lens = b["seq_lens"].cpu().tolist()
+    qlens = torch.diff(b["query_start_loc"].cpu()).tolist()
+    flops = sum(4.0 * sp.head_dim * sp.num_heads * sum(lens[i] - qlens[i] + j + 1 for j in range(qlens[i]))
+                for i in range(C))
+    kw = dict(max_query_len=b["max_query_len"], max_seq_len=b["max_seq_len"], scale=sp.scale, stream=stream)
+    if a.fp8:
+        one = lambda: pa.attention_fp8(b["out"], b["q"], dw.k_cache, dw.v_cache, b["block_table"], b["seq_lens"],  # noqa: E731
+                                       b["query_start_loc"], k_scale=wl.k_scale, v_scale=wl.v_scale,
+                                       workspace=st.workspace, **kw)
+        single = None
+    else:
+        one = lambda: pa.attention(b["out"], b["q"], dw.k_cache, dw.v_cache, b["block_table"], b["seq_lens"],  # noqa: E731
+                                   b["query_start_loc"], workspace=st.workspace, **kw)
+        single = lambda: pa.attention_fixed_scratch(b["out"], b["q"], dw.k_cache, dw.v_cache, b["block_table"],  # noqa: E731
+                                                    b["seq_lens"], b["query_start_loc"], **kw)
+
+    def timed(fn, steps, warm):
+        for _ in range(warm):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    steps = max(10, a.steps // 10)
+    pa.read_device_errors(clear=True)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    ms = timed(single if single is not None else one, steps, a.warmup)
+    ms_two = timed(one, steps, a.warmup) if single is not None else None
+    clk = clocks.stop()
+    if pa.read_device_errors(clear=True):
+        raise RuntimeError("device error flags set")
+    hbm, tflops_peak, src = _peaks()
+    tf = flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": "chunked-prefill attention (8 x 512-query chunks of the mixed batch), TFLOP/s"
+                  + (" over an E4M3 cache" if a.fp8 else ""),
+        "value": tf, "unit": "TFLOP/s", "n_gpus": 1, "steps": steps, "warmup": a.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "e4m3 cache, f16 MMA operands" if a.fp8 else "bf16", "data": "synthetic",
+        "config": {"workload": "the mixed batch's prefill part: 8 chunks x 512 queries, prior context U[0, 4096], "
+                               "32 q / 8 kv heads, head_dim 128, block 16", "gflop": flops / 1e9, "seed": wl.seed},
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": tflops_peak, "unit": "TFLOP/s",
+                     "frac": tf / tflops_peak, "peak_source": src,
+                     "kernel": "prefill_tc_kernel, one launch of one CTA per SM" if single is not None else
+                               "prefill_tc_kernel (pa_attention_fp8)"},
+        "clocks": clk,
+    }
+    if ms_two is not None:
+        line["through_pa_attention"] = {"ms": ms_two, "tflops": flops / (ms_two * 1e-3) / 1e12,
+                                        "frac": flops / (ms_two * 1e-3) / 1e12 / tflops_peak,
+                                        "launches": "two prefill launches sharing one pair counter"}
     print(json.dumps(line))
     return 0
 
 
-def run_secondary(a):
+def secondary_line(a):
     """MHA decode (attention only) or shared-prefix sampling (copy-on-write copies, write,
     attention): per-operation times and bytes on one GPU, device-resident inputs."""
     import torch
@@ -853,7 +1020,11 @@ def run_secondary(a):
     line["clocks"] = clocks.stop()
     if pa.read_device_errors(clear=True):
         raise RuntimeError("device error flags set")
-    print(json.dumps(line))
+    return line
+
+
+def run_secondary(a):
+    print(json.dumps(secondary_line(a)))
     return 0
 
 
@@ -1122,6 +1293,8 @@ def main(argv=None):
         return run_reference(a)
     if a.workload == "mixed":
         return run_mixed(a)
+    if a.workload == "prefill":
+        return run_prefill(a)
     if a.workload in ("mha_decode", "shared_prefix"):
         return run_secondary(a)
     if a.workload == "system_prompt":

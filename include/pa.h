@@ -166,7 +166,14 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
  *               may also be page-locked host memory mapped into the unified address
  *               space: the kernels then store the rows over the CPU-GPU link and the host
  *               sees them once the stream has been synchronised
- * q             device, [num_tokens, num_heads, head_dim], `dtype`
+ * q             device, [num_tokens, num_heads, head_dim], `dtype`; for a decode-only
+ *               batch (max_query_len <= 1) on the tensor-core decode kernel it may also be
+ *               page-locked host memory mapped into the unified address space: the kernel
+ *               then reads the rows over the CPU-GPU link (plain loads, no copy). q is
+ *               checked with cudaPointerGetAttributes: pageable host memory or another
+ *               device's memory gives PA_ERR_INVALID_ARG; host memory with prefill rows gives
+ *               PA_ERR_INVALID_ARG, and on a shape the tensor-core decode kernel does not take
+ *               PA_ERR_UNSUPPORTED (all before anything is enqueued)
  * block_table   device, int32 [num_seqs, max_blocks_per_seq] (entries past a request's
  *               ceil(L / block_size) blocks are never read)
  * seq_lens      device, int32 [num_seqs]
@@ -210,7 +217,8 @@ int pa_attention(void* out, const void* q, const void* k_cache, const void* v_ca
  *    new token costs one write and no separate kernel.
  *  - max_query_len >= 2: the cache write is a separate kernel ahead of the attention
  *    kernels (prefill rows read their new tokens through many CTAs).
- * k_new, v_new  device, [num_tokens, num_kv_heads, head_dim], `dtype`, 16-byte aligned
+ * k_new, v_new  device, [num_tokens, num_kv_heads, head_dim], `dtype`, 16-byte aligned;
+ *               like q, page-locked host memory for decode-only batches (read over the link)
  * slot_mapping  device, int64 [num_tokens], distinct non-negative slots
  * Other arguments, validation, workspace and errors as pa_kv_write and pa_attention;
  * validation happens before anything is enqueued.

@@ -60,6 +60,8 @@ _sig = {
     "pa_attention_fp8": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i64, _f, _f, _f,
                               _p, _sz, _p]),
     "pa_swap_blocks": (_i, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i, _i, _i, _i, _p]),
+    "pa_attention_fixed_scratch": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i64, _f,
+                                        _i, _p]),
     "pa_attention_grouped_workspace_size": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "pa_attention_grouped": (_i, [_p, _p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i64, _f, _i, _p, _p,
                                   _p, _i, _p, _sz, _p]),
@@ -227,6 +229,8 @@ def attention(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, 
     least attention_workspace_size(...) bytes (no initial contents needed); when None one is
     allocated with torch. ``out`` may be a pinned host tensor: the kernels then store the
     rows over the CPU-GPU link, and they are in place once the stream has synchronised.
+    For a decode-only batch (max_query_len <= 1) ``q`` may be a pinned host tensor too: the
+    decode kernel reads its rows over the link (no separate copy).
     """
     NB, B, Hkv, D = _cache_geometry(k_cache, v_cache)
     T, Hq = int(q.shape[0]), int(q.shape[1])
@@ -238,15 +242,40 @@ def attention(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, 
     if block_table.dim() != 2 or int(block_table.shape[0]) != S or tuple(query_start_loc.shape) != (S + 1,):
         raise ValueError("block_table [S, W], seq_lens [S], query_start_loc [S + 1]")
     if workspace is None:
-        workspace = torch.empty(attention_workspace_size(S, Hq, Hkv, D), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(attention_workspace_size(S, Hq, Hkv, D), dtype=torch.uint8, device=k_cache.device)
     ws_ptr = workspace.data_ptr() if workspace.numel() > 0 else 0
-    st = lib.pa_attention(_out(out), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+    st = lib.pa_attention(_out(out), _pool_ptr(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
                           _dev(block_table, "block_table", torch.int32, 2), int(block_table.shape[1]),
                           _dev(seq_lens, "seq_lens", torch.int32, 1),
                           _dev(query_start_loc, "query_start_loc", torch.int32, 1), S, T, int(max_query_len),
                           int(max_seq_len), Hq, Hkv, D, B, NB, float(scale), _dtype_code(q), ws_ptr,
-                          workspace.numel(), _stream(stream, q.device))
+                          workspace.numel(), _stream(stream, k_cache.device))
     _check(st, "pa_attention")
+    return out
+
+
+def attention_fixed_scratch(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, *,
+                            max_query_len: int, max_seq_len: int, scale: float, stream=None):
+    """pa_attention_fixed_scratch: attention() with the library's fixed scratch instead of a
+    workspace, every kernel on ``stream`` (a batch with prefill rows runs one prefill launch
+    over all SMs after the decode kernels). Calls that may overlap on the GPU race on the
+    shared scratch."""
+    NB, B, Hkv, D = _cache_geometry(k_cache, v_cache)
+    T, Hq = int(q.shape[0]), int(q.shape[1])
+    if q.dim() != 3 or tuple(out.shape) != tuple(q.shape) or int(q.shape[2]) != D:
+        raise ValueError("q and out must be [num_tokens, num_heads, head_dim]")
+    if q.dtype != k_cache.dtype or out.dtype != k_cache.dtype:
+        raise TypeError("q, out and the caches must share one dtype")
+    S = int(seq_lens.shape[0])
+    if block_table.dim() != 2 or int(block_table.shape[0]) != S or tuple(query_start_loc.shape) != (S + 1,):
+        raise ValueError("block_table [S, W], seq_lens [S], query_start_loc [S + 1]")
+    st = lib.pa_attention_fixed_scratch(_out(out), _pool_ptr(q, "q"), _dev(k_cache, "k_cache"),
+                                        _dev(v_cache, "v_cache"), _dev(block_table, "block_table", torch.int32, 2),
+                                        int(block_table.shape[1]), _dev(seq_lens, "seq_lens", torch.int32, 1),
+                                        _dev(query_start_loc, "query_start_loc", torch.int32, 1), S, T,
+                                        int(max_query_len), int(max_seq_len), Hq, Hkv, D, B, NB, float(scale),
+                                        _dtype_code(q), _stream(stream, k_cache.device))
+    _check(st, "pa_attention_fixed_scratch")
     return out
 
 
@@ -256,7 +285,8 @@ def write_attention(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_
     """pa_write_attention: kv_write(k_new, v_new, ..., slot_mapping) then attention(...), in one call.
 
     For a decode request (q_len 1, length L) slot_mapping of its token must be the slot of
-    position L - 1 in its block table; the decode kernel then writes it itself.
+    position L - 1 in its block table; the decode kernel then writes it itself. For a
+    decode-only batch, q, k_new and v_new may be pinned host tensors (read over the link).
     """
     NB, B, Hkv, D = _cache_geometry(k_cache, v_cache)
     T, Hq = int(q.shape[0]), int(q.shape[1])
@@ -273,15 +303,15 @@ def write_attention(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_
     if block_table.dim() != 2 or int(block_table.shape[0]) != S or tuple(query_start_loc.shape) != (S + 1,):
         raise ValueError("block_table [S, W], seq_lens [S], query_start_loc [S + 1]")
     if workspace is None:
-        workspace = torch.empty(attention_workspace_size(S, Hq, Hkv, D), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(attention_workspace_size(S, Hq, Hkv, D), dtype=torch.uint8, device=k_cache.device)
     ws_ptr = workspace.data_ptr() if workspace.numel() > 0 else 0
-    st = lib.pa_write_attention(_out(out), _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+    st = lib.pa_write_attention(_out(out), _pool_ptr(q, "q"), _pool_ptr(k_new, "k_new"), _pool_ptr(v_new, "v_new"),
                                 _dev(slot_mapping, "slot_mapping", torch.int64), _dev(k_cache, "k_cache"),
                                 _dev(v_cache, "v_cache"), _dev(block_table, "block_table", torch.int32, 2),
                                 int(block_table.shape[1]), _dev(seq_lens, "seq_lens", torch.int32, 1),
                                 _dev(query_start_loc, "query_start_loc", torch.int32, 1), S, T, int(max_query_len),
                                 int(max_seq_len), Hq, Hkv, D, B, NB, float(scale), _dtype_code(q), ws_ptr,
-                                workspace.numel(), _stream(stream, q.device))
+                                workspace.numel(), _stream(stream, k_cache.device))
     _check(st, "pa_write_attention")
     return out
 
@@ -319,14 +349,14 @@ def attention_fp8(out, q, k_cache, v_cache, block_table, seq_lens, query_start_l
     if block_table.dim() != 2 or int(block_table.shape[0]) != S or tuple(query_start_loc.shape) != (S + 1,):
         raise ValueError("block_table [S, W], seq_lens [S], query_start_loc [S + 1]")
     if workspace is None:
-        workspace = torch.empty(attention_workspace_size(S, Hq, Hkv, D), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(attention_workspace_size(S, Hq, Hkv, D), dtype=torch.uint8, device=k_cache.device)
     ws_ptr = workspace.data_ptr() if workspace.numel() > 0 else 0
-    st = lib.pa_attention_fp8(_out(out), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+    st = lib.pa_attention_fp8(_out(out), _pool_ptr(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
                               _dev(block_table, "block_table", torch.int32, 2), int(block_table.shape[1]),
                               _dev(seq_lens, "seq_lens", torch.int32, 1),
                               _dev(query_start_loc, "query_start_loc", torch.int32, 1), S, T, int(max_query_len),
                               int(max_seq_len), Hq, Hkv, D, B, NB, float(scale), float(k_scale), float(v_scale),
-                              ws_ptr, workspace.numel(), _stream(stream, q.device))
+                              ws_ptr, workspace.numel(), _stream(stream, k_cache.device))
     _check(st, "pa_attention_fp8")
     return out
 
@@ -356,16 +386,16 @@ def attention_grouped(out, q, k_cache, v_cache, block_table, seq_lens, query_sta
         raise ValueError("seq_group [S], group_range [num_groups, 2], shared_len [num_groups]")
     if workspace is None:
         workspace = torch.empty(attention_grouped_workspace_size(S, G, Hq, Hkv, D), dtype=torch.uint8,
-                                device=q.device)
+                                device=k_cache.device)
     grp = lambda t, n: _dev(t, n, torch.int32) if G > 0 else 0  # noqa: E731
-    st = lib.pa_attention_grouped(_out(out), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+    st = lib.pa_attention_grouped(_out(out), _pool_ptr(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
                                   _dev(block_table, "block_table", torch.int32, 2), int(block_table.shape[1]),
                                   _dev(seq_lens, "seq_lens", torch.int32, 1),
                                   _dev(query_start_loc, "query_start_loc", torch.int32, 1), S, T, int(max_seq_len),
                                   Hq, Hkv, D, B, NB, float(scale), _dtype_code(q), grp(seq_group, "seq_group"),
                                   grp(group_range, "group_range"), grp(shared_len, "shared_len"), G,
                                   workspace.data_ptr() if workspace.numel() else 0, workspace.numel(),
-                                  _stream(stream, q.device))
+                                  _stream(stream, k_cache.device))
     _check(st, "pa_attention_grouped")
     return out
 

@@ -139,6 +139,23 @@ int pa_attention_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
 
 namespace {
 
+// Where a row input of an attention call lives: 0 device memory (or managed) of the current
+// device, 1 page-locked host memory mapped at its own address, -1 anything else (pageable
+// host memory, another device's memory), which no kernel may dereference.
+int input_home(const void* p, int dev) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // reset the error state the failed query set
+    return -1;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice: return at.device == dev ? 0 : -1;
+    case cudaMemoryTypeManaged: return 0;
+    case cudaMemoryTypeHost: return at.devicePointer == p ? 1 : -1;
+    default: return -1;
+  }
+}
+
 // Validation and argument packing shared by pa_attention and pa_write_attention; nothing
 // is launched. On success `a` and `ctas` are ready for run_attention.
 int prepare_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -210,7 +227,19 @@ int prepare_attention(void* out, const void* q, const void* k_cache, const void*
   a.workspace = workspace;
   a.prefill_sched = reinterpret_cast<int*>(static_cast<unsigned char*>(workspace) + dneed);
   a.err = err;
+  const int qh = input_home(q, dev);
+  if (qh < 0) return PA_ERR_INVALID_ARG;
+  a.host_inputs = qh == 1;
   return PA_OK;
+}
+
+// Host-memory row inputs are read by the tensor-core decode kernel only (plain loads over
+// the CPU-GPU link): decode-only batches on that kernel.
+int check_host_inputs(const pa::AttnArgs& a) {
+  if (!a.host_inputs) return PA_OK;
+  if (a.max_query_len >= 2) return PA_ERR_INVALID_ARG;
+  const int hg = pa::decode_hg(a.cache_dtype, a.head_dim, a.num_heads / a.num_kv_heads, a.num_kv_heads);
+  return pa::decode_mma_supported(a, hg) ? PA_OK : PA_ERR_UNSUPPORTED;
 }
 
 // Whether `s` is being captured into a CUDA graph (an error of the query counts as yes).
@@ -307,6 +336,8 @@ int attention_entry(void* out, const void* q, const void* k_cache, const void* v
                                    workspace_bytes, a, ctas, nothing, dtype);
   if (st != PA_OK || nothing) return st;
   a.concurrent = concurrent;
+  const int hs = check_host_inputs(a);
+  if (hs != PA_OK) return hs;
   return run_attention(a, ctas, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -344,6 +375,15 @@ int pa_write_attention(void* out, const void* q, const void* k_new, const void* 
                                    num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace,
                                    workspace_bytes, a, ctas, nothing, dtype);
   if (st != PA_OK || nothing) return st;
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail(cudaGetLastError());
+    const int kh = input_home(k_new, dev), vh = input_home(v_new, dev);
+    if (kh < 0 || vh < 0) return PA_ERR_INVALID_ARG;
+    a.host_inputs = a.host_inputs || kh == 1 || vh == 1;
+    const int hs = check_host_inputs(a);
+    if (hs != PA_OK) return hs;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (max_query_len >= 2) {
     // prefill rows read their own new tokens from the cache through many CTAs: write every
@@ -395,6 +435,8 @@ int pa_attention_fp8(void* out, const void* q, const void* k_cache, const void* 
   if (st != PA_OK || nothing) return st;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
+  const int hs = check_host_inputs(a);
+  if (hs != PA_OK) return hs;
   return run_attention(a, ctas, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -498,6 +540,8 @@ int pa_attention_grouped(void* out, const void* q, const void* k_cache, const vo
   a.shared_len = shared_len;
   a.num_groups = num_groups;
   if (!pa::decode_mma_supported(a, hg)) return PA_ERR_UNSUPPORTED;
+  const int hs = check_host_inputs(a);
+  if (hs != PA_OK) return hs;
   const size_t need = pa::decode_grouped_workspace_bytes(num_seqs, num_groups, num_kv_heads, head_dim, hg, ctas);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
   const cudaError_t e = pa::launch_decode_mma(a, hg, ctas, reinterpret_cast<cudaStream_t>(stream));

@@ -1033,7 +1033,7 @@ cudaError_t run(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream) {
   // query slots when they fit beside the stages (bf16 caches; with E4M3 caches the slots,
   // which push shared memory to the next carveout, measured slower than global loads)
   uint32_t q_slot = 0;
-  if (C::EL == 2) {
+  if (C::EL == 2 && !a.host_inputs) {
     q_slot = uint32_t(hg * p.group * D * 2) + (p.k_new ? uint32_t(2 * hg * D * 2) : 0u);
     q_slot = (q_slot + 15) / 16 * 16;
     if (C::total(hg, q_slot) > uint32_t(kSmemLimit)) q_slot = 0;

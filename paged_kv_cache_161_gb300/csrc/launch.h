@@ -87,6 +87,9 @@ struct AttnArgs {
   // false: never run the prefill kernel on the side stream (callers that must not create
   // CUDA resources)
   bool concurrent = true;
+  // q (and k_new / v_new) are page-locked host memory: the decode kernel reads them with
+  // plain loads over the CPU-GPU link (never with bulk copies into shared memory)
+  bool host_inputs = false;
   // Fused KV write (decode requests only; all three null otherwise): row t of k_new / v_new
   // [num_tokens, num_kv_heads, head_dim] goes to cache slot slot_mapping[t].
   const void* k_new = nullptr;

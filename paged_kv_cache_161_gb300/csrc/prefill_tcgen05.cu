@@ -77,6 +77,7 @@ struct PrefillParams {
   int block_size;
   float scale_log2;  // softmax scale x log2(e) (x k_scale over an E4M3 cache)
   float out_scale;   // 1, or v_scale over an E4M3 cache
+  int out_v8;        // out is 32-byte aligned: the epilogue stores 32 bytes per instruction
 };
 
 template <int D>
@@ -88,7 +89,7 @@ struct Layout {
   static constexpr uint32_t PFX = V + 2 * NH * kHalf;   // int[kMaxSeqs + 8]
   static constexpr uint32_t ORD = PFX + (kMaxSeqs + 8) * 4;  // int[kMaxSeqs + 8], right after PFX
   static constexpr uint32_t BAR = ORD + (kMaxSeqs + 8) * 4;
-  static constexpr int NBAR = 31;
+  static constexpr int NBAR = 28;
   static constexpr uint32_t MISC = BAR + NBAR * 8;       // tmem base, abort flag
   static constexpr uint32_t RING = MISC + 16;            // RingSlot[2]: the next pairs, for every role
   static constexpr uint32_t BYTES = RING + 128;
@@ -97,8 +98,14 @@ struct Layout {
 
 // barrier indices (X = tile A or B: index + X)
 enum : int {
-  bQFull = 0, bQEmpty, bKFull0, bKFull1, bKEmpty0, bKEmpty1, bVFull0, bVFull1, bVEmpty0, bVEmpty1,
-  bSFull0, bSFull1, bPFull0, bPFull1, bPVDone0, bPVDone1, bOEmpty0, bOEmpty1, bMmaDone,
+  // K stage s released (both tiles' Q.K on it landed) -- tile B's Q.K is issued last on a
+  // stage, so the same completion tells tile B's softmax that S_B is ready and the Q/K
+  // producer that the pair's queries are free after its last step; V stage s released
+  // (both tiles' P.V landed) -- which also tells that P.V(B) is done. Tile A has its own
+  // S-ready and P.V-done barriers. One commit per signal: a commit issued before the
+  // previous one has retired stalls the issuing thread.
+  bQFull = 0, bKFull0, bKFull1, bKEmpty0, bKEmpty1, bVFull0, bVFull1, bVEmpty0, bVEmpty1,
+  bSFullA, bPFull0, bPFull1, bPVDoneA, bOEmpty0, bOEmpty1, bMmaDone,
   bPHalf0, bPHalf1,  // P of keys 64..127 is in TMEM (the first half of P.V may start)
   bRingFull0, bRingFull1, bRingEmpty0, bRingEmpty1,
   // E4M3 caches: the producer has converted the stage's codes (Q: its bf16 values) to f16
@@ -368,6 +375,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int nb = kBN / B;  // physical blocks per step (<= 16)
     int n = 0, tt = 0;
     bool ok = true;
+    // E4M3: step nn (the kb-th of its pair) from codes to f16 once its copy has landed
+    auto convert = [&](int nn, int kb, int leff) -> bool {
+      const int stage = nn & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar((is_k ? bKFull0 : bVFull0) + stage), (nn >> 1) & 1))) return false;
+      convert_kv_step(sm + (is_k ? LY::K : LY::V) + uint32_t(stage * NH) * kHalf, min(kBN, leff - kb * kBN), lane);
+      tc::fence_proxy_async_smem();  // generic-proxy stores -> the MMA's operand reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar((is_k ? bKReady0 : bVReady0) + stage));
+      return true;
+    };
     for (int i = 0; ok; ++i) {
       int t = -1;
       Pair pr;
@@ -401,7 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (is_k) {
         int qok = 1;
         if (lane == 0) {
-          qok = mbar_wait(bar(bQEmpty), (tt & 1) ^ 1) ? 1 : 0;
+          // the previous pair's queries are free once its last Q.K (step n - 1) has landed,
+          // which the release of that step's K stage tells
+          qok = (tt == 0 || mbar_wait(bar(bKEmpty0 + ((n - 1) & 1)), uint32_t((n - 1) >> 1) & 1u)) ? 1 : 0;
           if (qok) {
             mbar_arrive_expect_tx(bar(bQFull), uint32_t(2 * kBM * D * 2));
 #pragma unroll
@@ -454,12 +473,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(bQReady));
           }
-          if (!__all_sync(0xffffffffu, mbar_wait(fb, (n >> 1) & 1))) { ok = false; break; }
-          convert_kv_step(sm + sbase, min(kBN, pr.leff - kb * kBN), lane);
-          tc::fence_proxy_async_smem();  // generic-proxy stores -> the MMA's operand reads
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar((is_k ? bKReady0 : bVReady0) + stage));
+          // the previous step's codes: converted after this step's copy has been issued, so
+          // that the copy is in flight while they are converted
+          if (kb > 0 && !convert(n - 1, kb - 1, pr.leff)) { ok = false; break; }
         }
+      }
+      if constexpr (F8) {  // the pair's last step
+        if (ok && !convert(n - 1, pr.nt - 1, pr.leff)) ok = false;
       }
       ++tt;
     }
@@ -488,7 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           const uint32_t koff = uint32_t(k / 4) * kHalf + uint32_t(k % 4) * 32;
           tc::mma_f16(tmem + uint32_t(x * kBN), a0 + (koff >> 4), b0 + (koff >> 4), idesc_qk, k > 0 ? 1u : 0u);
         }
-        tc::mma_commit(bar(bSFull0 + x));
+        // tile A: S_A ready; tile B (issued last on this K stage): the stage's release, which
+        // is also S_B's ready signal (one commit where two would stall the issuing thread)
+        tc::mma_commit(x == 0 ? bar(bSFullA) : bar(bKEmpty0 + stage));
       };
       // O_x += P_x . V(nn) over keys 64 h .. 64 h + 63 (h = 1 first: the softmax stores
       // those first); `first`: the pair's first step, whose first MMA starts O afresh
@@ -516,15 +538,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int n0 = n;
         if (!mbar_wait(bar(kQ), tt & 1)) { ok = false; break; }
         if (!mbar_wait(bar(kK0 + (n0 & 1)), (n0 >> 1) & 1)) { ok = false; break; }
-        if (n0 > 0 && (!mbar_wait(bar(bPVDone0), (n0 - 1) & 1) || !mbar_wait(bar(bPVDone1), (n0 - 1) & 1))) {
+        if (n0 > 0 && (!mbar_wait(bar(bPVDoneA), (n0 - 1) & 1) ||
+                       !mbar_wait(bar(bVEmpty0 + ((n0 - 1) & 1)), uint32_t((n0 - 1) >> 1) & 1u))) {
           ok = false;  // the previous pair's last P.V read P out of S
           break;
         }
         tc::fence_after_sync();
         qk(0, n0);
         qk(1, n0);
-        tc::mma_commit(bar(bKEmpty0 + (n0 & 1)));
-        if (pr.nt == 1) tc::mma_commit(bar(bQEmpty));
+
         for (int kb = 0; kb < pr.nt && ok; ++kb, ++n) {
           const bool more = kb + 1 < pr.nt;
 #pragma unroll
@@ -537,17 +559,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             if (!mbar_wait(bar(bPFull0 + x), n & 1)) { ok = false; break; }
             tc::fence_after_sync();
             pv_half(x, n, 0, false);
-            tc::mma_commit(bar(bPVDone0 + x));
-            if (x == 1) tc::mma_commit(bar(bVEmpty0 + (n & 1)));
+            // tile A: P.V done; tile B (the step's last reader of V): the V stage's release,
+            // which also tells that P.V(B) has landed
+            tc::mma_commit(x == 0 ? bar(bPVDoneA) : bar(bVEmpty0 + (n & 1)));
             if (more) {
-              if (!mbar_wait(bar(bPVDone0 + x), n & 1)) { ok = false; break; }
+              if (!(x == 0 ? mbar_wait(bar(bPVDoneA), n & 1)
+                           : mbar_wait(bar(bVEmpty0 + (n & 1)), uint32_t(n >> 1) & 1u))) { ok = false; break; }
               if (x == 0 && !mbar_wait(bar(kK0 + ((n + 1) & 1)), ((n + 1) >> 1) & 1)) { ok = false; break; }
               tc::fence_after_sync();
               qk(x, n + 1);
-              if (x == 1) {
-                tc::mma_commit(bar(bKEmpty0 + ((n + 1) & 1)));
-                if (kb + 2 == pr.nt) tc::mma_commit(bar(bQEmpty));
-              }
+
             }
           }
         }
@@ -582,7 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const int mypos = active ? pos_lo + i : pr.leff - 1;
       float m_used = -INFINITY, l = 0.f;  // m in raw score units
       for (int kb = 0; kb < pr.nt; ++kb, ++n) {
-        if (!mbar_wait(bar(bSFull0 + x), n & 1)) { ok = false; break; }
+        if (!(x == 0 ? mbar_wait(bar(bSFullA), n & 1)
+                     : mbar_wait(bar(bKEmpty0 + (n & 1)), uint32_t(n >> 1) & 1u))) { ok = false; break; }
         tc::fence_after_sync();
         const int key0 = kb * kBN;
         const bool diag = key0 + kBN - 1 > pos_lo;
@@ -703,7 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       }
       if (!ok) break;
       // ---- epilogue: O / l -> out
-      if (!mbar_wait(bar(bPVDone0 + x), (n - 1) & 1)) { ok = false; break; }
+      if (!(x == 0 ? mbar_wait(bar(bPVDoneA), (n - 1) & 1)
+                   : mbar_wait(bar(bVEmpty0 + ((n - 1) & 1)), uint32_t((n - 1) >> 1) & 1u))) { ok = false; break; }
       tc::fence_after_sync();
       const float inv = l > 0.f ? p.out_scale / l : 0.f;
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
@@ -715,7 +738,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tc::tmem_ld32(trow + ocol + uint32_t(c * 32), *reinterpret_cast<float(*)[32]>(o2));
         tc::tmem_ld32(trow + ocol + uint32_t(c * 32 + 32), *reinterpret_cast<float(*)[32]>(o2 + 32));
         tc::tmem_wait_ld();
-        if (active) {
+        if (active && p.out_v8) {  // 32 bytes (16 dims) per store: half the store instructions
+#pragma unroll
+          for (int e = 0; e < 64; e += 16) {
+            float f[8], h[8];
+#pragma unroll
+            for (int xx = 0; xx < 8; ++xx) {
+              f[xx] = o2[e + xx] * inv;
+              h[xx] = o2[e + 8 + xx] * inv;
+            }
+            const uint4 u = Elem<__nv_bfloat16>::pack(f), w = Elem<__nv_bfloat16>::pack(h);
+            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(out + c * 32 + e),
+                         "r"(u.x), "r"(u.y), "r"(u.z), "r"(u.w), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w)
+                         : "memory");
+          }
+        } else if (active) {
 #pragma unroll
           for (int e = 0; e < 64; e += 8) {
             float f[8];
@@ -804,6 +841,7 @@ cudaError_t run(const AttnArgs& a, const PrefillTcPlan& plan, int num_ctas, cuda
   // value * v_scale (folded into the final 1 / l)
   p.scale_log2 = a.scale * 1.4426950408889634f * (F8 ? a.k_scale : 1.f);
   p.out_scale = F8 ? a.v_scale : 1.f;
+  p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) % 32 == 0) ? 1 : 0;
   if (!p.sched || how.ticket_base < 0) return cudaErrorInvalidValue;
   if (how.zero_counter) {
     const cudaError_t e = cudaMemsetAsync(p.sched, 0, sizeof(int), stream);  // the pair counter starts at 0

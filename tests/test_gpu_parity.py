@@ -142,6 +142,29 @@ def test_edge_cases(pa, name, spec, ctx, q_lens):
         _close(out[rows], ref.out[rows], spec.dtype, name, None if sig is None else sig[rows])
 
 
+def test_prefill_output_only_16_byte_aligned(pa):
+    """An output buffer that is 16- but not 32-byte aligned (the ABI's minimum) takes the
+    prefill epilogue's 16-byte stores; the bits equal those written to an aligned buffer."""
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload
+
+    wl = workloads.custom(workloads.Spec("bf16", 32, 8, 128, 16, 0.088), [0, 300, 40], [200, 70, 1], name="a16")
+    dw = DeviceWorkload(wl)
+    dw.run_setup()
+    st = dw.prepare_step()
+    dw.run_step(st)
+    torch.cuda.synchronize()
+    T, H, D = st.q.shape
+    flat = torch.full((T * H * D + 8,), float("nan"), dtype=torch.bfloat16, device=st.q.device)
+    out16 = flat[8:].view(T, H, D)  # 16 bytes past a 256-byte aligned allocation
+    assert out16.data_ptr() % 32 == 16
+    pa.attention(out16, st.q, dw.k_cache, dw.v_cache, st.block_table, st.seq_lens, st.query_start_loc,
+                 max_query_len=st.max_query_len, max_seq_len=st.max_seq_len, scale=wl.spec.scale,
+                 workspace=st.workspace)
+    torch.cuda.synchronize()
+    assert pa.read_device_errors(clear=True) == 0
+    assert torch.equal(out16, st.out)
+
+
 def test_kv_write_padding_and_bad_slots(pa):
     dev = "cuda"
     NB, B, H, D = 8, 16, 8, 128

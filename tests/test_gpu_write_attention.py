@@ -304,3 +304,46 @@ def test_mixed_calls_from_two_host_threads(pa):
     assert pa.read_device_errors(clear=True) == 0
     for out in outs:
         assert torch.equal(out, ref)
+
+
+def test_decode_rows_in_pinned_host_memory(pa, monkeypatch):
+    """q, k_new and v_new in pinned host memory (decode-only batch): the decode kernel reads
+    them over the CPU-GPU link; the cache and the output bits equal the device-input call's.
+    Pageable host memory, and host rows with a prefill row in the batch, are refused before
+    anything is enqueued."""
+    from paged_kv_cache_161_gb300.device_workload import DeviceWorkload
+
+    outs, caches = [], []
+    for host in (False, True):
+        wl = workloads.build(3, "small")
+        dw = DeviceWorkload(wl)
+        dw.run_setup()
+        st = dw.prepare_step()
+        q, k, v = st.q, st.k_new, st.v_new
+        if host:
+            q, k, v = (t.cpu().pin_memory() for t in (q, k, v))
+        out = torch.full_like(st.q, float("nan"))
+        pa.write_attention(out, q, k, v, st.slot_mapping, dw.k_cache, dw.v_cache, st.block_table, st.seq_lens,
+                           st.query_start_loc, max_query_len=1, max_seq_len=st.max_seq_len, scale=wl.spec.scale,
+                           workspace=st.workspace)
+        out2 = torch.full_like(st.q, float("nan"))
+        pa.attention(out2, q, dw.k_cache, dw.v_cache, st.block_table, st.seq_lens, st.query_start_loc,
+                     max_query_len=1, max_seq_len=st.max_seq_len, scale=wl.spec.scale, workspace=st.workspace)
+        torch.cuda.synchronize()
+        assert pa.read_device_errors(clear=True) == 0
+        assert torch.equal(out, out2)
+        outs.append(out)
+        caches.append((dw.k_cache.clone(), dw.v_cache.clone()))
+        if host:
+            # the library's own check (past the binding's): pageable host memory is refused
+            monkeypatch.setattr(pa, "_pool_ptr", lambda t, name: t.data_ptr())
+            with pytest.raises(pa.PAError):
+                pa.attention(torch.empty_like(st.q), st.q.cpu(), dw.k_cache, dw.v_cache, st.block_table,
+                             st.seq_lens, st.query_start_loc, max_query_len=1, max_seq_len=st.max_seq_len,
+                             scale=wl.spec.scale, workspace=st.workspace)
+            with pytest.raises(pa.PAError):  # host rows with max_query_len >= 2: refused
+                pa.attention(torch.empty_like(st.q), q, dw.k_cache, dw.v_cache, st.block_table, st.seq_lens,
+                             st.query_start_loc, max_query_len=2, max_seq_len=st.max_seq_len,
+                             scale=wl.spec.scale, workspace=st.workspace)
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(caches[0][0], caches[1][0]) and torch.equal(caches[0][1], caches[1][1])
