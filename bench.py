@@ -37,10 +37,10 @@ METRIC = "paged decode attention: K/V GB/s (% of GB300 HBM peak) and tokens/s, b
 # from one ncu capture (the first timed step's two launches) of
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum \
 #       --clock-control none --csv --log-file launches.csv \
-#       python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-e2e
+#       python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-e2e --no-secondary
 # It holds only for the kernel sources it was measured on (their SHA-256 below); any
 # change to them makes the reported traffic null until it is measured again.
-DECODE_TRAFFIC = {"sources_sha256": "98e9193d9cd3500b321ca5ed99c1c9204cc5876661b230b28c1c993e369fee10", "bytes": 1653689600}
+DECODE_TRAFFIC = {"sources_sha256": "b80a7110390d94a1ceed383e7372531f2b82755e32b074d2066fbbbc3da977c9", "bytes": 1653198336}
 DECODE_SOURCES = ["paged_kv_cache_161_gb300/csrc/decode_attention.cu", "paged_kv_cache_161_gb300/csrc/decode_mma.cu",
                   "paged_kv_cache_161_gb300/csrc/decode_common.cuh", "paged_kv_cache_161_gb300/csrc/common.cuh"]
 
@@ -54,6 +54,10 @@ def _decode_traffic():
             h.update(fh.read())
     return DECODE_TRAFFIC["bytes"] if h.hexdigest() == DECODE_TRAFFIC["sources_sha256"] else None
 FALLBACK_HBM_GBS = 6800.0
+# End-to-end loops append one real token per request and step: two loops (rows read from
+# host memory, rows copied) of at most 8 warm-up + 2 graph-check + 64 timed steps.
+E2E_STEPS, E2E_WARMUP = 64, 8
+E2E_TABLE_WIDTH = (8192 + 1 + 2 * (E2E_STEPS + E2E_WARMUP + 2) + 15) // 16
 CONFIG_ID = 3
 
 
@@ -443,7 +447,7 @@ def run_ours(a):
 
     wl = rank_workload(rank)
     sp = wl.spec
-    dw = DeviceWorkload(wl, device=dev, table_width=(8192 + 1 + 72 + 15) // 16)
+    dw = DeviceWorkload(wl, device=dev, table_width=E2E_TABLE_WIDTH)
     dw.run_setup()
     st = dw.prepare_step()
     torch.cuda.synchronize()
@@ -669,7 +673,7 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist, copy_rows=False):
 
     # each end-to-end step appends a real token to every request: cap the count so the
     # requests stay inside the workload's block pool (1.25x the blocks of the batch)
-    steps, warm = min(a.steps, 64), min(a.warmup, 8)
+    steps, warm = min(a.steps, E2E_STEPS), min(a.warmup, E2E_WARMUP)
     run(warm)
     # Capture the launch side as a serving loop would (the table capacity as max_seq_len:
     # it only bounds the lengths the kernels read from the device).
@@ -1174,7 +1178,7 @@ def run_fp8_decode(a):
     time.sleep(0.3)
     for name, wl in (("fp8", workloads.with_fp8_cache(workloads.build(CONFIG_ID))), ("bf16", workloads.build(CONFIG_ID))):
         sp = wl.spec
-        dw = DeviceWorkload(wl, device=dev, table_width=(8192 + 1 + 72 + 15) // 16)
+        dw = DeviceWorkload(wl, device=dev, table_width=E2E_TABLE_WIDTH)
         dw.run_setup()
         st = dw.prepare_step()
         pa.read_device_errors(clear=True)

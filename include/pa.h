@@ -68,7 +68,7 @@ typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 /* caches only: see pa_k
 typedef enum {
   PA_OK = 0,
   PA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, misaligned pointer, bad shape */
-  PA_ERR_UNSUPPORTED = 2,  /* a valid shape this build has no kernel for */
+  PA_ERR_UNSUPPORTED = 2,  /* a valid shape the library has no kernel for */
   PA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than pa_attention_workspace_size */
   PA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
   PA_ERR_NO_BLOCKS = 5,    /* block manager: not enough free blocks now */

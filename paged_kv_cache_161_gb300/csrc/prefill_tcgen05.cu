@@ -375,16 +375,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int nb = kBN / B;  // physical blocks per step (<= 16)
     int n = 0, tt = 0;
     bool ok = true;
-    // E4M3: step nn (the kb-th of its pair) from codes to f16 once its copy has landed
-    auto convert = [&](int nn, int kb, int leff) -> bool {
-      const int stage = nn & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar((is_k ? bKFull0 : bVFull0) + stage), (nn >> 1) & 1))) return false;
-      convert_kv_step(sm + (is_k ? LY::K : LY::V) + uint32_t(stage * NH) * kHalf, min(kBN, leff - kb * kBN), lane);
-      tc::fence_proxy_async_smem();  // generic-proxy stores -> the MMA's operand reads
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar((is_k ? bKReady0 : bVReady0) + stage));
-      return true;
-    };
     for (int i = 0; ok; ++i) {
       int t = -1;
       Pair pr;
@@ -473,13 +463,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(bQReady));
           }
-          // the previous step's codes: converted after this step's copy has been issued, so
-          // that the copy is in flight while they are converted
-          if (kb > 0 && !convert(n - 1, kb - 1, pr.leff)) { ok = false; break; }
+          // this step's codes to f16 once they have landed, while the MMAs of the previous
+          // step run (converting step n - 1 after issuing step n's copy would wait, through
+          // the 2-deep ring, for the MMAs of step n - 2, and serialise conversion and MMA)
+          if (!__all_sync(0xffffffffu, mbar_wait(fb, (n >> 1) & 1))) { ok = false; break; }
+          convert_kv_step(sm + sbase, min(kBN, pr.leff - kb * kBN), lane);
+          tc::fence_proxy_async_smem();  // generic-proxy stores -> the MMA's operand reads
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar((is_k ? bKReady0 : bVReady0) + stage));
         }
-      }
-      if constexpr (F8) {  // the pair's last step
-        if (ok && !convert(n - 1, pr.nt - 1, pr.leff)) ok = false;
       }
       ++tt;
     }

@@ -29,7 +29,7 @@ while one dropped block, one dropped tail stage, one dropped 128-key prefill ste
 dropped CTA range of the longest request of the GQA batch fails the bound on most
 elements of the affected rows.
 
-The pass criterion stays the spec bar; tests assert both.
+The pass criterion stays the pass bar; tests assert both.
 """
 from __future__ import annotations
 
@@ -104,7 +104,7 @@ def northstar_failures(got, ref):
 
 
 def assert_close_bf16(got, ref, sigma, what):
-    """Both bars on bf16 outputs: the spec pass bar and the diagnostic bound."""
+    """Both bars on bf16 outputs: the pass bar and the diagnostic bound."""
     got = to_f64(got) if got.dtype != np.float64 else got
     bad = northstar_failures(got, ref)
     assert not bad.any(), f"{what}: {bad.sum()} elements outside the pass bar"

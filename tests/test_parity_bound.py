@@ -8,7 +8,7 @@
    the way a faulty kernel would leave them out -- one physical block, the request's last
    16-token stage, one 128-key prefill step of one KV head, one CTA's range of the
    split-K partition -- fails the bound, while the unmutated output rounded to bf16 and
-   the rounding model pass it. At these lengths the spec pass bar alone does not
+   the rounding model pass it. At these lengths the pass bar alone does not
    see the dropped block, which is why the GPU parity tests assert both.
 
 The oracle is the reference throughout; the mutants and the rounding model are test-side
