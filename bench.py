@@ -589,10 +589,11 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist, copy_rows=False):
     of the step's metadata (slots, tables, lengths, query_start_loc), write + attention with
     q / k / v and `out` in pinned host memory (the decode kernel reads the rows and stores
     the results over the CPU-GPU link itself; with ``copy_rows`` the rows are copied to the
-    device with the metadata instead), the result waited for before the next step is
-    launched; host wall time per step. The accounting of step n + 1 does not depend on step
-    n's output (one token per request), so it runs while the GPU works on step n, into the
-    other of two staging buffers."""
+    device at the start of the step instead), the result waited for before the next step is
+    launched; host wall time per step. The metadata of step n + 1 does not depend on step
+    n's output (one token per request), so its accounting and its copy (on a side stream,
+    into the other of two device buffers) run while the GPU works on step n; the rows do
+    depend on it in a serving loop, and are not fetched ahead."""
     import numpy as np
     import torch
 
@@ -610,7 +611,7 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist, copy_rows=False):
         offs[name] = (off, nbytes)
         off += (nbytes + 255) // 256 * 256
     h_bufs = [torch.empty(off, dtype=torch.uint8).pin_memory() for _ in range(2)]
-    d_buf = torch.empty(off, dtype=torch.uint8, device=dev)
+    d_bufs = [torch.empty(off, dtype=torch.uint8, device=dev) for _ in range(2)]
 
     def view(buf, name, dtype, shape):
         o, nb = offs[name]
@@ -625,11 +626,11 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist, copy_rows=False):
              view(h, "lens", torch.int32, (S,)).numpy()) for h in h_bufs]
     meta = offs["q"][0]  # bytes of the metadata prefix
     rows = [tuple(view(buf, n, torch.bfloat16, t.shape) for n, t in (("q", st.q), ("k", st.k_new), ("v", st.v_new)))
-            for buf in ([d_buf, d_buf] if copy_rows else h_bufs)]
-    slots_d = view(d_buf, "slots", torch.int64, (S,))
-    table_d = view(d_buf, "table", torch.int32, (S, width))
-    lens_d = view(d_buf, "lens", torch.int32, (S,))
-    qsl_d = view(d_buf, "qsl", torch.int32, (S + 1,))
+            for buf in (d_bufs if copy_rows else h_bufs)]
+    meta_d = [(view(d, "slots", torch.int64, (S,)), view(d, "table", torch.int32, (S, width)),
+               view(d, "lens", torch.int32, (S,)), view(d, "qsl", torch.int32, (S + 1,))) for d in d_bufs]
+    copy_stream = torch.cuda.Stream(device=dev)
+    meta_ready = [torch.cuda.Event() for _ in range(2)]
     out_h = torch.empty_like(st.q, device="cpu").pin_memory()  # written by the kernels themselves
     h2d = off
     d2h = out_h.numel() * out_h.element_size()
@@ -642,24 +643,33 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist, copy_rows=False):
         bm.batch_tables(seqs, width, table_out=table_h, lens_out=lens_h)
         return int(lens_h.max()), int(lens_h.astype(np.int64).sum()) * sp.kv_token_bytes
 
-    def enqueue(b, max_len, s):  # the step's copy and call on stream s
-        n = off if copy_rows else meta
-        d_buf[:n].copy_(h_bufs[b][:n], non_blocking=True)
+    def fetch_meta(b):  # staging buffer b's metadata to device buffer b, on the side stream
+        with torch.cuda.stream(copy_stream):
+            d_bufs[b][:meta].copy_(h_bufs[b][:meta], non_blocking=True)
+            meta_ready[b].record(copy_stream)
+
+    def enqueue(b, max_len, s):  # the step's row copy (copy_rows) and call on stream s
+        if copy_rows:
+            d_bufs[b][meta:].copy_(h_bufs[b][meta:], non_blocking=True)
         q_x, k_x, v_x = rows[b]
+        slots_d, table_d, lens_d, qsl_d = meta_d[b]
         pa.write_attention(out_h, q_x, k_x, v_x, slots_d, dw.k_cache, dw.v_cache, table_d, lens_d, qsl_d,
                            max_query_len=1, max_seq_len=max_len, scale=sp.scale, workspace=st.workspace, stream=s)
 
-    graphs = None  # after the warm-up: one CUDA graph per staging buffer (H2D, call, D2H)
+    graphs = None  # after the warm-up: one CUDA graph per buffer pair (row copy, call)
 
     def run(n):
-        """n steps; returns the K/V bytes of each. Staging buffer b is refilled only after
-        the step that copied from it has completed (its result was waited for)."""
+        """n steps; returns the K/V bytes of each. Buffer pair b (staging and device) is
+        refilled only after the step that used it has completed (its result was waited
+        for)."""
         kv = []
         nxt = account(0)
+        fetch_meta(0)
         for i in range(n):
             b = i % 2
             max_len, kv_bytes = nxt
             with torch.cuda.stream(stream):
+                stream.wait_event(meta_ready[b])
                 if graphs is not None:
                     graphs[b].replay()
                 else:
@@ -667,6 +677,7 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist, copy_rows=False):
                 done.record(stream)
             if i + 1 < n:
                 nxt = account(1 - b)  # overlaps the GPU's step i
+                fetch_meta(1 - b)
             done.synchronize()  # step i's output is on the host
             kv.append(kv_bytes)
         return kv
@@ -677,7 +688,8 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist, copy_rows=False):
     run(warm)
     # Capture the launch side as a serving loop would (the table capacity as max_seq_len:
     # it only bounds the lengths the kernels read from the device).
-    graph_note = "CUDA graph per staging buffer (H2D copy, pa_write_attention), replayed each step"
+    graph_note = ("CUDA graph per buffer pair (" + ("row H2D copy, " if copy_rows else "") +
+                  "pa_write_attention), replayed each step after the side stream's metadata copy")
     try:
         torch.cuda.synchronize()
         captured = []
@@ -704,13 +716,14 @@ def _e2e(a, pa, dw, st, wl, dev, stream, world, dist, copy_rows=False):
     return {"value": mean_bytes / secs / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": secs * 1e3, "steps": steps, "warmup": warm,
             "h2d_copied_bytes_per_step": off if copy_rows else meta,
-            "includes": "host block accounting (pa_bm_append_batch, pa_bm_batch_tables) into pinned memory, one "
-                        "H2D copy of slots/table/lens/query_start_loc" +
-                        (" and q/k/v" if copy_rows else "; q/k/v read by the decode kernel straight from pinned "
-                         "host memory (the rest of the H2D bytes)") +
-                        ", pa_write_attention storing out straight into pinned host memory (the D2H bytes), "
-                        "waited for before the next step is launched; the next step's accounting runs while the "
-                        "GPU works (two staging buffers)",
+            "includes": "host block accounting (pa_bm_append_batch, pa_bm_batch_tables) into pinned memory and "
+                        "one H2D copy of slots/table/lens/query_start_loc, both for step n + 1 while the GPU works "
+                        "on step n (two staging and two device buffers; the copy on a side stream)" +
+                        ("; one H2D copy of q/k/v at the start of the step" if copy_rows else
+                         "; q/k/v read by the decode kernel straight from pinned host memory (the rest of the "
+                         "H2D bytes)") +
+                        "; pa_write_attention storing out straight into pinned host memory (the D2H bytes), "
+                        "waited for before the next step is launched",
             "launch": graph_note}
 
 
