@@ -80,6 +80,23 @@ def test_grouped_full_size_all_requests(pa):
     _close(out, to_f64(t2s(plain)), "grouped vs pa_attention", k=2.0)
 
 
+@pytest.mark.parametrize("P,prompt_len,tail_hi,seed", [(2, 200, 300, 161041), (5, 33, 70, 161042)])
+def test_grouped_long_member_tails(pa, P, prompt_len, tail_hi, seed):
+    """Members whose own chunks outnumber the shared ones, in a batch smaller than the
+    grid: a group's segment (its shared chunks, then each member's own) spreads over many
+    CTAs, some of them with empty ranges, and a member's result merges dozens of pieces."""
+    wl = workloads.shared_prefix(P, prompt_len, 4, tail_hi, seed)
+    dw, st, plain, t2s = _step(pa, wl)
+    seqs = [s for s, _ in wl.step.batch]
+    sg, gr, sl = dw.bm.batch_groups(seqs, 4)
+    assert len(gr) == P
+    out = t2s(_grouped(pa, dw, st, wl, sg, gr, sl))
+    ref = run_workload(wl)
+    sig = batch_sigma(ref, range(len(ref.seq_lens)), wl.spec.scale, wl.spec.block_size)
+    assert_close_bf16(to_f64(out), ref.out, sig, "grouped vs oracle")
+    _close(out, to_f64(t2s(plain)), "grouped vs pa_attention", k=2.0)
+
+
 def test_grouped_degenerate_groups_match_plain(pa):
     """No groups; a member whose seq_group disagrees with its range (it runs on its own);
     groups too wide for 16 matrix rows (G = 8 x 4 members: they run ungrouped)."""

@@ -21,6 +21,7 @@ from .configs import (  # noqa: F401
     custom,
     relevant_seqs,
     preemption,
+    shared_prefix,
     system_prompt,
     with_fp8_cache,
 )

@@ -276,12 +276,18 @@ def _cfg3(size, replica=0):
 
 def _cfg4(size, replica=0):
     seed = SEED_BASE + 4 + (100 if size == "small" else 0) + REPLICA_STRIDE * replica
+    if size == "small":
+        return shared_prefix(3, 40, 4, 20, seed, "shared_prefix_bf16_small")
+    return shared_prefix(64, 1000, 4, 256, seed, "shared_prefix_bf16")
+
+
+def shared_prefix(P: int, prompt_len: int, n_samp: int, tail_hi: int, seed: int,
+                  name: str = "shared_prefix_custom") -> Workload:
+    """P prompts of prompt_len tokens, n_samp samples forked from each (the prompt's blocks
+    shared, the partial last block copied on write), tails U[0, tail_hi] appended to every
+    sample, then one decode token per sample; GQA 32 q / 8 kv heads, head_dim 128, block 16."""
     spec = Spec("bf16", **GQA)
     rng = _rng(seed)
-    if size == "small":
-        P, prompt_len, n_samp, tail_hi = 3, 40, 4, 20
-    else:
-        P, prompt_len, n_samp, tail_hi = 64, 1000, 4, 256
     B = spec.block_size
     tails = rng.integers(0, tail_hi, size=(P, n_samp), endpoint=True)
     seq = lambda p, i: p * n_samp + i  # noqa: E731
@@ -297,8 +303,7 @@ def _cfg4(size, replica=0):
         needed += shared_full + sum(-(-(prompt_len + int(t) + 1) // B) - shared_full for t in tails[p])
     pool = _pool(needed)
     final = [prompt_len + int(tails[p, i]) + 1 for p in range(P) for i in range(n_samp)]
-    return Workload("shared_prefix_bf16" + ("_small" if size == "small" else ""), spec, seed, pool,
-                    rng.permutation(pool).astype(np.int32), [prompt, fork, tail], step, S,
+    return Workload(name, spec, seed, pool, rng.permutation(pool).astype(np.int32), [prompt, fork, tail], step, S,
                     dict(prompts=P, prompt_len=prompt_len, samples=n_samp, tails=tails, final_lens=final))
 
 
