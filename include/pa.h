@@ -144,11 +144,11 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
  * even). Requests with q_len == 1 run the split-K decode kernel; q_len >= 2 the prefill
  * kernel; q_len == 0 produces no rows. Requires q_len <= L.
  * With rows of both kinds (max_query_len >= 2) and the tensor-core kernels for both (see
- * "Prefill kernels" below; block size 8, 16, 32, 64 or 128) the two
- * kernels run side by side: the call forks an internal stream of the highest priority off
- * `stream` (event record and wait), runs the decode kernels there on 3/5 of the SMs and
- * joins it back before returning -- also when a launch fails after the fork -- so later
- * work on `stream` is ordered after the whole call, as for one stream. The first such call
+ * "Prefill kernels" below; block size 8, 16, 32, 64 or 128) the two kernels run side by
+ * side: the call forks an internal stream of the highest priority off `stream` (event
+ * record and wait), runs the decode kernels there on 3/5 of the SMs (1/2 with E4M3
+ * caches) and joins it back before returning -- also when a launch fails after the fork --
+ * so later work on `stream` is ordered after the whole call, as for one stream. The first such call
  * on a device creates that stream and two events (kept until exit). While `stream` is
  * being captured into a CUDA graph the call keeps every kernel on `stream` instead (the
  * internal stream is shared by all callers of the device and must not join a capture).

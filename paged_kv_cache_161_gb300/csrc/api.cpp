@@ -281,9 +281,11 @@ int run_attention(const pa::AttnArgs& a, int ctas, cudaStream_t s, const KvWrite
   // into a graph: the internal stream is shared by every caller of the device, and a
   // capture would hold it until the capture ends.
   if (tc && a.concurrent && pa::decode_mma_supported(a, hg) && !stream_capturing(s)) {
-    // A batch with prefill rows: the decode kernels (HBM-bound) run on 3/5 of the SMs, on a
-    // side stream of the highest priority, beside a first prefill launch (tensor-bound) of
-    // as many CTAs as the other SMs on the caller's stream, so neither can take the other's
+    // A batch with prefill rows: the decode kernels (HBM-bound) run on 3/5 of the SMs (1/2
+    // over an E4M3 cache, whose prefill steps cost more: the best of 1/2 .. 3/4 measured on
+    // the mixed chunked-prefill batch for each cache type), on a side stream of the
+    // highest priority, beside a first prefill launch (tensor-bound) of as many CTAs as
+    // the other SMs on the caller's stream, so neither can take the other's
     // SMs whichever is dispatched first. A second prefill launch queued behind the decode
     // merge on the side stream takes the SMs the decode kernel leaves; both launches draw
     // the remaining pairs from one counter, zeroed before the fork. The caller's stream
@@ -294,7 +296,7 @@ int run_attention(const pa::AttnArgs& a, int ctas, cudaStream_t s, const KvWrite
     if (!pa::side_stream(&side, &e)) return cuda_fail(e);
     pa::AttnArgs ad = a;
     ad.merge_pdl = false;  // the merge's CTAs must not hold SMs while the decode kernel runs
-    const int dctas = ctas > 1 ? ctas * 3 / 5 : 1;
+    const int dctas = ctas > 1 ? (a.cache_dtype == PA_FP8_E4M3 ? ctas / 2 : ctas * 3 / 5) : 1;
     const int pctas = ctas - dctas > 0 ? ctas - dctas : 1;
     std::lock_guard<std::mutex> lock(*side.mu);
     e = cudaMemsetAsync(a.prefill_sched, 0, sizeof(int), s);

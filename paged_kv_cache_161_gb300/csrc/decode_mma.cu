@@ -664,16 +664,19 @@ __global__ void __launch_bounds__(9 * 32, 1)
       }
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    const float mnew0 = fmaxf(mrun0, mx0);
+    // The reference max moves only when a score exceeds it by more than 8 (log2 units; the
+    // first finite score always moves it): numerators stay below 2^8, and O and l are
+    // rescaled only on those steps (alpha is exactly 1 otherwise).
+    const float mnew0 = (mx0 > mrun0 + 8.f) ? mx0 : mrun0;
     const float ms0 = (mnew0 == -INFINITY) ? 0.f : mnew0;
-    const float alpha0 = ex2_ftz(mrun0 - ms0);
+    const float alpha0 = (mnew0 == mrun0) ? 1.f : ex2_ftz(mrun0 - ms0);
     float alpha1 = 1.f, ms1 = 0.f;
     if constexpr (GROUPED) {
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mnew1 = fmaxf(mrun1, mx1);
+      const float mnew1 = (mx1 > mrun1 + 8.f) ? mx1 : mrun1;
       ms1 = (mnew1 == -INFINITY) ? 0.f : mnew1;
-      alpha1 = ex2_ftz(mrun1 - ms1);
+      alpha1 = (mnew1 == mrun1) ? 1.f : ex2_ftz(mrun1 - ms1);
       mrun1 = mnew1;
     }
     float pv[2][4];
