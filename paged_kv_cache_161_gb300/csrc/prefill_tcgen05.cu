@@ -54,6 +54,11 @@ constexpr int kBN = 128;             // keys per step
 constexpr int kMaxSeqs = 4096;       // requests per call this kernel accepts
 constexpr int kThreads = 11 * 32;    // 8 softmax warps (4 per tile), Q/K TMA, MMA, V TMA
 constexpr int kWarpQK = 8, kWarpMMA = 9, kWarpV = 10;
+// E4M3 caches: one more warp converts half of each step's codes (and half the queries) to
+// f16 beside the two producers (384 threads x 168 registers fit the SM's 65536)
+constexpr int kWarpCvt = 11;
+template <bool F8>
+__host__ __device__ constexpr int threads_of() { return F8 ? kThreads + 32 : kThreads; }
 constexpr uint32_t kTmemCols = 512;  // S_A, S_B, O_A, O_B: 128 columns each
 constexpr uint32_t kHalf = 128 * 128;  // bytes of a 128-row x 64-element bf16 half tile
 
@@ -112,6 +117,7 @@ enum : int {
   bQReady, bKReady0, bKReady1, bVReady0, bVReady1
 };
 // roles that take each pair from the ring: the V producer, the MMA thread, 8 softmax warps
+// (and, E4M3 caches, the converter warp)
 constexpr uint32_t kRingTakers = 10;
 static_assert(bVReady1 < Layout<128>::NBAR && bVReady1 < Layout<64>::NBAR,
               "every barrier index needs a slot in the shared-memory layout");
@@ -176,18 +182,19 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& c01, uin
       : "r"(x));
 }
 
-// One 128-key step of codes -> the step's f16 tile, in place. TMA stored key row r's 128
-// codes (head_dim 128), 128-byte swizzled, in the stage's second 64-dim half; dims 0..63
-// become row r of half 0 and dims 64..127 row r of half 1, swizzled the same way. Rows at
-// or past `valid` become zeros (stale rows of V must not be NaN: P is 0 there, and 0 * NaN
-// is not 0). Each iteration reads its 4 rows (8 lanes a row) before a __syncwarp and
-// stores after it, so a row's half-1 codes are read before they are overwritten; other
-// rows' codes are never written by the iteration.
-__device__ __forceinline__ void convert_kv_step(unsigned char* stage, int valid, int lane) {
+// Rows [r_begin, r_end) (multiples of 4) of one 128-key step of codes -> the step's f16
+// tile, in place. TMA stored key row r's 128 codes (head_dim 128), 128-byte swizzled, in
+// the stage's second 64-dim half; dims 0..63 become row r of half 0 and dims 64..127 row r
+// of half 1, swizzled the same way. Rows at or past `valid` become zeros (stale rows of V
+// must not be NaN: P is 0 there, and 0 * NaN is not 0). Each iteration reads its 4 rows
+// (8 lanes a row) before a __syncwarp and stores after it, so a row's half-1 codes are read
+// before they are overwritten; no row's codes are written but by the warp converting that
+// row, so two warps may convert disjoint row ranges of one stage.
+__device__ __forceinline__ void convert_kv_step(unsigned char* stage, int valid, int lane, int r_begin, int r_end) {
   const int rsub = lane >> 3, c = lane & 7;
   const unsigned char* codes = stage + kHalf;
 #pragma unroll 4
-  for (int r0 = 0; r0 < kBN; r0 += 4) {
+  for (int r0 = r_begin; r0 < r_end; r0 += 4) {
     const int r = r0 + rsub, sw = r & 7;
     const uint4 v = *reinterpret_cast<const uint4*>(codes + r * 128 + ((c ^ sw) << 4));
     __syncwarp();
@@ -225,7 +232,7 @@ __device__ __forceinline__ void convert_q_to_f16(unsigned char* q, uint32_t byte
 // F8: E4M3 caches (head_dim 128): q and out bf16, K/V codes converted to f16 tiles by the
 // producer warps, MMAs and P in f16.
 template <int D, int G, bool F8>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillParams p,
+__global__ void __launch_bounds__(threads_of<F8>(), 1) prefill_tc_kernel(const __grid_constant__ PrefillParams p,
                                                                  const __grid_constant__ CUtensorMap qmap,
                                                                  const __grid_constant__ CUtensorMap kmap,
                                                                  const __grid_constant__ CUtensorMap vmap) {
@@ -253,7 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   // most one per thread; else batch order): the costliest pairs start first and the cheap
   // ones at the end fill the CTAs that finish early.
   int* ord = reinterpret_cast<int*>(sm + LY::ORD);
-  __shared__ int wsum[kThreads / 32];
+  constexpr int NT = threads_of<F8>();
+  __shared__ int wsum[NT / 32];
   // Block-wide exclusive scan of x (thread order); returns it, the total in *tot.
   auto block_scan = [&](int x, int* tot) {
     int inc = x;
@@ -266,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     __syncthreads();
     int off = 0, t = 0;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < NT / 32; ++w) {
       if (w < warp) off += wsum[w];
       t += wsum[w];
     }
@@ -276,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   };
   const int cap = p.max_blocks_per_seq * p.block_size;
   int P = 0;  // compact: ord[i] = the i-th prefill request, pfx[i] = its length (the key)
-  for (int b0 = 0; b0 < S; b0 += kThreads) {
+  for (int b0 = 0; b0 < S; b0 += NT) {
     const int s = b0 + threadIdx.x;
     const int flag = (s < S && __ldg(p.qsl + s + 1) - __ldg(p.qsl + s) >= 2) ? 1 : 0;
     int tot;
@@ -288,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     P += tot;
   }
   __syncthreads();
-  if (P <= kThreads) {  // rank: longer first, then batch order
+  if (P <= NT) {  // rank: longer first, then batch order
     int my_s = 0, my_key = 0, rank = 0;
     if (int(threadIdx.x) < P) {
       my_s = ord[threadIdx.x];
@@ -303,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     __syncthreads();
   }
   int run = 0;  // pfx[i]: pairs of ord[0..i); pfx[P] = total
-  for (int b0 = 0; b0 <= P; b0 += kThreads) {
+  for (int b0 = 0; b0 <= P; b0 += NT) {
     const int i = b0 + threadIdx.x;
     int cnt = 0;
     if (i < P) {
@@ -345,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     for (int i = 0; i < LY::NBAR; ++i) {
       uint32_t cnt = 1;
       if (i == bPFull0 || i == bPFull1 || i == bOEmpty0 || i == bOEmpty1 || i == bPHalf0 || i == bPHalf1) cnt = 4;
-      if (i == bRingEmpty0 || i == bRingEmpty1) cnt = kRingTakers;
+      if (i == bRingEmpty0 || i == bRingEmpty1) cnt = kRingTakers + (F8 ? 1 : 0);
+      if (i == bQReady || i == bKReady0 || i == bKReady1 || i == bVReady0 || i == bVReady1) cnt = 2;  // E4M3 only
       mbar_init(bar(i), cnt);
     }
     fence_mbar_init();
@@ -456,9 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           }
         }
         if constexpr (F8) {
-          if (is_k && kb == 0) {  // the pair's queries, bf16 -> f16, while K(0) is in flight
+          if (is_k && kb == 0) {  // tile A's queries, bf16 -> f16, while K(0) is in flight
             if (!__all_sync(0xffffffffu, mbar_wait(bar(bQFull), tt & 1))) { ok = false; break; }
-            convert_q_to_f16(sm + LY::Q, 2u * NH * kHalf, lane);
+            convert_q_to_f16(sm + LY::Q, uint32_t(NH) * kHalf, lane);
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(bQReady));
@@ -467,10 +476,45 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           // step run (converting step n - 1 after issuing step n's copy would wait, through
           // the 2-deep ring, for the MMAs of step n - 2, and serialise conversion and MMA)
           if (!__all_sync(0xffffffffu, mbar_wait(fb, (n >> 1) & 1))) { ok = false; break; }
-          convert_kv_step(sm + sbase, min(kBN, pr.leff - kb * kBN), lane);
+          convert_kv_step(sm + sbase, min(kBN, pr.leff - kb * kBN), lane, 0, kBN / 2);  // the converter warp: the rest
           tc::fence_proxy_async_smem();  // generic-proxy stores -> the MMA's operand reads
           __syncwarp();
           if (lane == 0) mbar_arrive(bar((is_k ? bKReady0 : bVReady0) + stage));
+        }
+      }
+      ++tt;
+    }
+    if (!ok && lane == 0) fail();
+  } else if (F8 && warp == kWarpCvt) {
+    // =========================== E4M3 converter ===========================
+    // Tile B's queries and rows 64..127 of every K and V step, beside the producers (which
+    // convert tile A's queries and rows 0..63); the Ready barriers take both arrivals.
+    int n = 0, tt = 0;
+    bool ok = true;
+    auto convert = [&](int full0, int ready0, uint32_t off, int kb, int leff) -> bool {
+      const int stage = n & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(full0 + stage), (n >> 1) & 1))) return false;
+      convert_kv_step(sm + off + uint32_t(stage * NH) * kHalf, min(kBN, leff - kb * kBN), lane, kBN / 2, kBN);
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(ready0 + stage));
+      return true;
+    };
+    for (int i = 0; ok; ++i) {
+      int t = -1;
+      Pair pr;
+      if (!ring_take_warp(i, t, pr)) { ok = false; break; }
+      if (t < 0) break;
+      if (pr.nt == 0) continue;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(bQFull), tt & 1))) { ok = false; break; }
+      convert_q_to_f16(sm + LY::Q + uint32_t(NH) * kHalf, uint32_t(NH) * kHalf, lane);
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(bQReady));
+      for (int kb = 0; kb < pr.nt; ++kb, ++n) {
+        if (!convert(bKFull0, bKReady0, LY::K, kb, pr.leff) || !convert(bVFull0, bVReady0, LY::V, kb, pr.leff)) {
+          ok = false;
+          break;
         }
       }
       ++tt;
@@ -839,7 +883,7 @@ cudaError_t run(const AttnArgs& a, const PrefillTcPlan& plan, int num_ctas, cuda
     const cudaError_t e = cudaMemsetAsync(p.sched, 0, sizeof(int), stream);  // the pair counter starts at 0
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(prefill_tc_kernel<D, G, F8>, dim3(num_ctas), dim3(kThreads), Layout<D>::SMEM, stream, p,
+  return launch_pdl(prefill_tc_kernel<D, G, F8>, dim3(num_ctas), dim3(threads_of<F8>()), Layout<D>::SMEM, stream, p,
                     plan.qm, plan.km, plan.vm);
 }
 
