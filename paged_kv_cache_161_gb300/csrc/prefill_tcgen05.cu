@@ -57,6 +57,11 @@ constexpr int kWarpQK = 8, kWarpMMA = 9, kWarpV = 10;
 // E4M3 caches: one more warp converts half of each step's codes (and half the queries) to
 // f16 beside the two producers (384 threads x 168 registers fit the SM's 65536)
 constexpr int kWarpCvt = 11;
+// rows [0, kCvtSplit) of a step: the producer of that operand, which also issues its
+// copies and waits for them (and converts tile A's queries); [kCvtSplit, 128): the
+// converter warp, for both operands. Mixed-batch E4M3 prefill by split: 48: 259.0 us,
+// 56: 241.9, 64: 228.9, 72: 230.2, 84: 244.0 (same box; bit-identical).
+constexpr int kCvtSplit = 64;
 template <bool F8>
 __host__ __device__ constexpr int threads_of() { return F8 ? kThreads + 32 : kThreads; }
 constexpr uint32_t kTmemCols = 512;  // S_A, S_B, O_A, O_B: 128 columns each
@@ -476,7 +481,7 @@ __global__ void __launch_bounds__(threads_of<F8>(), 1) prefill_tc_kernel(const _
           // step run (converting step n - 1 after issuing step n's copy would wait, through
           // the 2-deep ring, for the MMAs of step n - 2, and serialise conversion and MMA)
           if (!__all_sync(0xffffffffu, mbar_wait(fb, (n >> 1) & 1))) { ok = false; break; }
-          convert_kv_step(sm + sbase, min(kBN, pr.leff - kb * kBN), lane, 0, kBN / 2);  // the converter warp: the rest
+          convert_kv_step(sm + sbase, min(kBN, pr.leff - kb * kBN), lane, 0, kCvtSplit);  // the converter warp: the rest
           tc::fence_proxy_async_smem();  // generic-proxy stores -> the MMA's operand reads
           __syncwarp();
           if (lane == 0) mbar_arrive(bar((is_k ? bKReady0 : bVReady0) + stage));
@@ -487,14 +492,15 @@ __global__ void __launch_bounds__(threads_of<F8>(), 1) prefill_tc_kernel(const _
     if (!ok && lane == 0) fail();
   } else if (F8 && warp == kWarpCvt) {
     // =========================== E4M3 converter ===========================
-    // Tile B's queries and rows 64..127 of every K and V step, beside the producers (which
-    // convert tile A's queries and rows 0..63); the Ready barriers take both arrivals.
+    // Tile B's queries and rows kCvtSplit..127 of every K and V step, beside the producers
+    // (which convert tile A's queries and the rows below); the Ready barriers take both
+    // arrivals.
     int n = 0, tt = 0;
     bool ok = true;
     auto convert = [&](int full0, int ready0, uint32_t off, int kb, int leff) -> bool {
       const int stage = n & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(full0 + stage), (n >> 1) & 1))) return false;
-      convert_kv_step(sm + off + uint32_t(stage * NH) * kHalf, min(kBN, leff - kb * kBN), lane, kBN / 2, kBN);
+      convert_kv_step(sm + off + uint32_t(stage * NH) * kHalf, min(kBN, leff - kb * kBN), lane, kCvtSplit, kBN);
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(ready0 + stage));
