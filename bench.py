@@ -40,7 +40,7 @@ METRIC = "paged decode attention: K/V GB/s (% of GB300 HBM peak) and tokens/s, b
 #       python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-e2e --no-secondary
 # It holds only for the kernel sources it was measured on (their SHA-256 below); any
 # change to them makes the reported traffic null until it is measured again.
-DECODE_TRAFFIC = {"sources_sha256": "b80a7110390d94a1ceed383e7372531f2b82755e32b074d2066fbbbc3da977c9", "bytes": 1653198336}
+DECODE_TRAFFIC = {"sources_sha256": "a0d3427b367055138ad69d6f11db3268e913d2aa91bb125ebba446e14a85da6b", "bytes": 1653172224}
 DECODE_SOURCES = ["paged_kv_cache_161_gb300/csrc/decode_attention.cu", "paged_kv_cache_161_gb300/csrc/decode_mma.cu",
                   "paged_kv_cache_161_gb300/csrc/decode_common.cuh", "paged_kv_cache_161_gb300/csrc/common.cuh"]
 
