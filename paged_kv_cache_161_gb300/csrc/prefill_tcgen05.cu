@@ -20,12 +20,13 @@
 //                  64..127 as soon as the softmax has stored their P, then keys 0..63
 // The two tiles ping-pong: while tile A's softmax runs, the tensor core does tile B's
 // P.V and next Q.K, and the other way round. E4M3 caches (head_dim 128) take the same
-// path with f16 operands: the producer warps convert each step's codes, and the pair's
-// bf16 queries, to f16 tiles in shared memory.
+// path with f16 operands: the producer warps and a converter warp turn each step's codes,
+// and the pair's bf16 queries, into f16 tiles in shared memory.
 //
-// Roles (352 threads, one CTA per SM, persistent: pairs enumerated with the requests
-// longest first and each request's last tiles first; CTA c starts with pair c and then
-// draws the next unclaimed pair from a grid-wide counter whenever it needs one):
+// Roles (352 threads, 384 with E4M3 caches; one CTA per SM, persistent: pairs enumerated
+// with the requests longest first and each request's last tiles first; CTA c starts with
+// pair c and then draws the next unclaimed pair from a grid-wide counter whenever it needs
+// one):
 //   warps 0-3 / 4-7  softmax + epilogue of tile A / tile B (thread = row = TMEM lane);
 //   warp 8           draws the pairs (ring of two slots in shared memory, read by every
 //                    other role); TMA: both Q tiles once per pair (3-D box {64 dims, G heads, 128 / G
@@ -36,7 +37,9 @@
 //   warp 9           allocates the 512 TMEM columns (S_A, S_B, O_A, O_B) and one thread
 //                    issues the MMAs of both tiles, tracking completion with tcgen05.commit
 //                    (one thread for both keeps the tiles out of phase: a thread per tile
-//                    measured 205 us against 170 us on the mixed batch's prefill part).
+//                    measured 205 us against 170 us on the mixed batch's prefill part);
+//   warp 11          E4M3 caches only: converts rows 64..127 of every K and V step and
+//                    tile B's queries (warps 8 and 10 convert the rest of their operand).
 // Every wait is bounded; on a timeout the kernel sets an error bit and leaves after its
 // copies and MMAs in flight have landed, freeing TMEM.
 #include <cuda.h>
