@@ -1049,7 +1049,10 @@ cudaError_t run(const AttnArgs& a, int hg, int num_ctas, cudaStream_t stream) {
   e = launch_pdl(kern, dim3(num_ctas), dim3((hg + 1) * 32), smem, stream, p, km, vm);
   if (e != cudaSuccess) return e;
   if (!GROUPED) return launch_merge<__nv_bfloat16, D>(p, stream, a.merge_pdl);
-  const int threads = 32 * (hg * p.group < 32 ? hg * p.group : 32);
+  // 16 warps (a warp per head, looping): the kernel's 64 registers a thread let two such
+  // CTAs share an SM, so every member's merge runs in one wave (1024 threads: two waves;
+  // shared-prefix batch 89.0 -> 86.9 us, bit-identical)
+  const int threads = 32 * (hg * p.group < 16 ? hg * p.group : 16);
   const dim3 mgrid(unsigned(int64_t(a.num_seqs) * p.num_hg));
   if (!a.merge_pdl) {  // plain stream order, as launch_merge
     decode_merge_grouped_kernel<__nv_bfloat16, D><<<mgrid, dim3(threads), 0, stream>>>(p);
