@@ -202,18 +202,26 @@ __device__ int seg_units(const DecodeParams& p, int k) {
   return max(units_of(decode_len(p, s)) - own_skip(p, s), 0);
 }
 
-// The CTA's range over the segment-major numbering (as plan_range over requests).
+// The CTA's range over the segment-major numbering (as plan_range over requests). `cache`
+// (`cap` ints of shared memory the pipeline has not started on yet) keeps each segment's
+// unit count from the first pass for the later ones (each thread rereads the entries it
+// wrote; the start segment's is read after the scan's barriers): a grouped request's count
+// is a chain of dependent loads (its group, the group's span, the members' lengths).
 template <typename T, int D>
-__device__ bool plan_segments(const DecodeParams& p, int* red, Plan& pl) {
+__device__ bool plan_segments(const DecodeParams& p, int* red, Plan& pl, int* cache, int cap) {
   const int S = p.num_seqs, NS = p.num_groups + S;
   int my_units = 0;
-  for (int k = threadIdx.x; k < NS; k += blockDim.x) my_units += seg_units(p, k);
+  for (int k = threadIdx.x; k < NS; k += blockDim.x) {
+    const int n = seg_units(p, k);
+    if (k < cap) cache[k] = n;
+    my_units += n;
+  }
   pl.units_per_hg = block_sum(my_units, red);
   const int64_t U = int64_t(pl.units_per_hg) * p.num_hg;
   const int64_t c = blockIdx.x, C_ = gridDim.x;
   if (c == 0) {
     for (int k = threadIdx.x; k < NS; k += blockDim.x) {
-      if (seg_units(p, k) > 0) continue;
+      if ((k < cap ? cache[k] : seg_units(p, k)) > 0) continue;
       for (int hg = 0; hg < p.num_hg; ++hg) p.ws_meta[int64_t(k) * p.num_hg + hg] = make_int4(-1, -1, 0, 0);
       if (k < p.num_groups) continue;
       const int s = k - p.num_groups;
@@ -232,7 +240,7 @@ __device__ bool plan_segments(const DecodeParams& p, int* red, Plan& pl) {
   int64_t run = 0;
   for (int base = 0; base < NS; base += blockDim.x) {
     const int k = base + threadIdx.x;
-    const int us = k < NS ? seg_units(p, k) * p.num_hg : 0;
+    const int us = k < NS ? (k < cap ? cache[k] : seg_units(p, k)) * p.num_hg : 0;
     int total;
     const int ex = block_exclusive_scan(us, red, &total);
     if (us > 0 && run + ex <= rem && rem < run + ex + us) {
@@ -244,7 +252,7 @@ __device__ bool plan_segments(const DecodeParams& p, int* red, Plan& pl) {
     if (run > rem) break;
   }
   pl.start_s = red[34];  // a segment here
-  const int start_us = seg_units(p, pl.start_s);
+  const int start_us = pl.start_s < cap ? cache[pl.start_s] : seg_units(p, pl.start_s);
   pl.start_hg = red[35] / start_us;
   pl.start_j = red[35] % start_us;
   return true;
@@ -282,7 +290,9 @@ __global__ void __launch_bounds__(9 * 32, 1)
   griddep_launch_dependents();
 
   Plan pl;
-  if (!plan_segments<T, D>(p, red, pl)) return;
+  // the stages' shared memory caches the plan's counts (no copy lands there before the
+  // barrier below)
+  if (!plan_segments<T, D>(p, red, pl, reinterpret_cast<int*>(smem), int(C::desc_off(HG) / 4))) return;
   const int64_t u_begin = pl.u_begin, u_end = pl.u_end, c = blockIdx.x;
 
   if (threadIdx.x == 0) {
