@@ -40,7 +40,7 @@ METRIC = "paged decode attention: K/V GB/s (% of GB300 HBM peak) and tokens/s, b
 #       python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-e2e --no-secondary
 # It holds only for the kernel sources it was measured on (their SHA-256 below); any
 # change to them makes the reported traffic null until it is measured again.
-DECODE_TRAFFIC = {"sources_sha256": "30a1c997052cdab84e1ec67ce325bd62be5de2b7bc8bf9f3f595eeeb1ae414cd", "bytes": 1653508864}
+DECODE_TRAFFIC = {"sources_sha256": "e29717f03a8df0cfaa62284ccd1132765bfba070981a6dbeeb0bdddb150e47e8", "bytes": 1653156096}
 DECODE_SOURCES = ["paged_kv_cache_161_gb300/csrc/decode_attention.cu", "paged_kv_cache_161_gb300/csrc/decode_mma.cu",
                   "paged_kv_cache_161_gb300/csrc/decode_common.cuh", "paged_kv_cache_161_gb300/csrc/common.cuh"]
 
