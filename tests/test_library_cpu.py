@@ -200,3 +200,31 @@ def test_batched_append_stops_at_first_failure():
         bm.append_batch([0, 1, 2], [8, 8, 1])  # the second needs 2 blocks, only 2 left -> ok; third fails
     assert e.value.status == 5 and "after 2 entries" in str(e.value)
     assert bm.seq_len(0) == 8 and bm.seq_len(1) == 8 and bm.seq_len(2) == 0
+
+
+def test_end_to_end_loops_fit_the_tables_and_the_pool():
+    """bench.py's end-to-end loops append one token to each of the GQA batch's 256 requests
+    per step (two loops of warm-up, graph check and timed steps): the host block manager,
+    replaying the workload's script, must still give every request a table within the
+    tables' width and find free blocks for every append."""
+    import bench
+
+    wl = workloads.build(3)
+    bm = pa.BlockManager(wl.num_blocks, wl.spec.block_size, wl.free_order)
+    for ph in list(wl.setup) + [wl.step]:
+        for op in ph.ops:
+            assert op[0] in ("add", "append"), op[0]
+            if op[0] == "add":
+                bm.add_seq(op[1])
+            else:
+                bm.append(op[1], op[2])
+        bm.take_copies()
+    seqs = np.asarray([s for s, _ in wl.step.batch], np.int64)
+    ones = np.ones(len(seqs), np.int64)
+    slots = np.empty(len(seqs), np.int64)
+    steps = 2 * (bench.E2E_STEPS + bench.E2E_WARMUP + 2)
+    for _ in range(steps):
+        bm.append_batch(seqs, ones, out=slots)
+        table, lens = bm.batch_tables(seqs, bench.E2E_TABLE_WIDTH)
+    assert int(lens.max()) <= bench.E2E_TABLE_WIDTH * wl.spec.block_size
+    assert bm.num_free() >= 0
