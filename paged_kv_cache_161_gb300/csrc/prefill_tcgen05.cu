@@ -38,7 +38,7 @@
 //                    issues the MMAs of both tiles, tracking completion with tcgen05.commit
 //                    (one thread for both keeps the tiles out of phase: a thread per tile
 //                    measured 205 us against 170 us on the mixed batch's prefill part);
-//   warp 11          E4M3 caches only: converts rows 64..127 of every K and V step and
+//   warp 11          E4M3 caches only: converts the last rows of every K and V step and
 //                    tile B's queries (warps 8 and 10 convert the rest of their operand).
 // Every wait is bounded; on a timeout the kernel sets an error bit and leaves after its
 // copies and MMAs in flight have landed, freeing TMEM.
@@ -60,11 +60,13 @@ constexpr int kWarpQK = 8, kWarpMMA = 9, kWarpV = 10;
 // E4M3 caches: one more warp converts half of each step's codes (and half the queries) to
 // f16 beside the two producers (384 threads x 168 registers fit the SM's 65536)
 constexpr int kWarpCvt = 11;
-// rows [0, kCvtSplit) of a step: the producer of that operand, which also issues its
-// copies and waits for them (and converts tile A's queries); [kCvtSplit, 128): the
-// converter warp, for both operands. Mixed-batch E4M3 prefill by split: 48: 259.0 us,
-// 56: 241.9, 64: 228.9, 72: 230.2, 84: 244.0 (same box; bit-identical).
-constexpr int kCvtSplit = 64;
+// rows [0, kCvtSplitK) of a K step and [0, kCvtSplitV) of a V step: the producer of that
+// operand, which also issues its copies and waits for them (the K producer also converts
+// tile A's queries); the rest: the converter warp, for both operands. Mixed-batch E4M3
+// prefill by split (same box, bit-identical): K/V 48/48: 259.0 us, 56/56: 241.9, 64/64:
+// 228.9, 72/72: 230.2, 84/84: 244.0; 64/72: 226.4, 64/76: 230.2, 64/80: 233.2, 68/72:
+// 230.4, 56/72: 231.3, 56/64: 235.0.
+constexpr int kCvtSplitK = 64, kCvtSplitV = 72;
 template <bool F8>
 __host__ __device__ constexpr int threads_of() { return F8 ? kThreads + 32 : kThreads; }
 constexpr uint32_t kTmemCols = 512;  // S_A, S_B, O_A, O_B: 128 columns each
@@ -484,7 +486,7 @@ __global__ void __launch_bounds__(threads_of<F8>(), 1) prefill_tc_kernel(const _
           // step run (converting step n - 1 after issuing step n's copy would wait, through
           // the 2-deep ring, for the MMAs of step n - 2, and serialise conversion and MMA)
           if (!__all_sync(0xffffffffu, mbar_wait(fb, (n >> 1) & 1))) { ok = false; break; }
-          convert_kv_step(sm + sbase, min(kBN, pr.leff - kb * kBN), lane, 0, kCvtSplit);  // the converter warp: the rest
+          convert_kv_step(sm + sbase, min(kBN, pr.leff - kb * kBN), lane, 0, is_k ? kCvtSplitK : kCvtSplitV);  // the converter warp: the rest
           tc::fence_proxy_async_smem();  // generic-proxy stores -> the MMA's operand reads
           __syncwarp();
           if (lane == 0) mbar_arrive(bar((is_k ? bKReady0 : bVReady0) + stage));
@@ -495,15 +497,15 @@ __global__ void __launch_bounds__(threads_of<F8>(), 1) prefill_tc_kernel(const _
     if (!ok && lane == 0) fail();
   } else if (F8 && warp == kWarpCvt) {
     // =========================== E4M3 converter ===========================
-    // Tile B's queries and rows kCvtSplit..127 of every K and V step, beside the producers
-    // (which convert tile A's queries and the rows below); the Ready barriers take both
-    // arrivals.
+    // Tile B's queries and rows kCvtSplitK..127 of every K step and kCvtSplitV..127 of every
+    // V step, beside the producers (which convert tile A's queries and the rows below); the
+    // Ready barriers take both arrivals.
     int n = 0, tt = 0;
     bool ok = true;
-    auto convert = [&](int full0, int ready0, uint32_t off, int kb, int leff) -> bool {
+    auto convert = [&](int full0, int ready0, uint32_t off, int kb, int leff, int r0) -> bool {
       const int stage = n & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(full0 + stage), (n >> 1) & 1))) return false;
-      convert_kv_step(sm + off + uint32_t(stage * NH) * kHalf, min(kBN, leff - kb * kBN), lane, kCvtSplit, kBN);
+      convert_kv_step(sm + off + uint32_t(stage * NH) * kHalf, min(kBN, leff - kb * kBN), lane, r0, kBN);
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(ready0 + stage));
@@ -521,7 +523,8 @@ __global__ void __launch_bounds__(threads_of<F8>(), 1) prefill_tc_kernel(const _
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(bQReady));
       for (int kb = 0; kb < pr.nt; ++kb, ++n) {
-        if (!convert(bKFull0, bKReady0, LY::K, kb, pr.leff) || !convert(bVFull0, bVReady0, LY::V, kb, pr.leff)) {
+        if (!convert(bKFull0, bKReady0, LY::K, kb, pr.leff, kCvtSplitK) ||
+            !convert(bVFull0, bVReady0, LY::V, kb, pr.leff, kCvtSplitV)) {
           ok = false;
           break;
         }
